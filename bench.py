@@ -1,0 +1,580 @@
+"""Benchmark of the row-reduction hot path on GB300.
+
+One step = one pass of every hot-path operation over its synthetic workload:
+  block tier    8192 x 8192 fp32 sum / max / min, int32 sum
+  warp tier     1,048,576 x 32 fp32 sum / max / min
+  tiled tier    1,048,576 x 8 fp32 sum / max / min
+  split-K tier  16 x 16,777,216 fp32 sum / max (cluster size picked by the
+                library, 8 on a 152-SM GB300)
+  softmax       32768 x 4096 bf16 -> fp32
+  layernorm     16384 x 8192 bf16 -> mean, rstd
+  combine       P = 2, 4, 8 partials of 131072 x 128 fp32 -> bf16
+Every operation has its own input buffer (its own seed), so within a step no
+buffer is read twice and between two reads of a buffer the step moves about
+5.6 GB, far more than the 129 MB L2.
+
+value = algorithmic HBM bytes of all ranks' steps / max-over-ranks time
+(GB/s, 1e9 bytes).  Algorithmic bytes per operation: input bytes read once
+plus output bytes written once.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the method has no other reference implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (fraction of GB300 peak) per reduce tier and split-K combine"
+WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx32 f32 "
+            "sum/max/min; tiled 1Mx8 f32 sum/max/min; split-K 16x16M f32 sum/max; softmax "
+            "32768x4096 bf16->f32; layernorm stats 16384x8192 bf16; split-K combine "
+            "P=2,4,8 x 131072x128")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by operation name,
+# valid only while the kernel source hashes to `src_sha`.  The capture and
+# its command are summarised in profiles/.
+NCU_TRAFFIC = {}
+
+
+def op_specs():
+    """(name, tier label, builder) for each operation of one step.  A builder
+    returns (inputs, run, bytes_in, bytes_out, host_run)."""
+    return [
+        ("block_sum_f32", "block", dict(kind="reduce", rows=8192, cols=8192, dt="f32", op="sum", cfg=1, opi=0)),
+        ("block_max_f32", "block", dict(kind="reduce", rows=8192, cols=8192, dt="f32", op="max", cfg=1, opi=1)),
+        ("block_min_f32", "block", dict(kind="reduce", rows=8192, cols=8192, dt="f32", op="min", cfg=1, opi=2)),
+        ("block_sum_i32", "block", dict(kind="reduce", rows=8192, cols=8192, dt="i32", op="sum", cfg=1, opi=3)),
+        ("warp_sum_f32", "warp", dict(kind="reduce", rows=1 << 20, cols=32, dt="f32", op="sum", cfg=1, opi=4)),
+        ("warp_max_f32", "warp", dict(kind="reduce", rows=1 << 20, cols=32, dt="f32", op="max", cfg=1, opi=5)),
+        ("warp_min_f32", "warp", dict(kind="reduce", rows=1 << 20, cols=32, dt="f32", op="min", cfg=1, opi=6)),
+        ("tiled_sum_f32", "tiled", dict(kind="reduce", rows=1 << 20, cols=8, dt="f32", op="sum", cfg=1, opi=7)),
+        ("tiled_max_f32", "tiled", dict(kind="reduce", rows=1 << 20, cols=8, dt="f32", op="max", cfg=1, opi=8)),
+        ("tiled_min_f32", "tiled", dict(kind="reduce", rows=1 << 20, cols=8, dt="f32", op="min", cfg=1, opi=9)),
+        ("splitk_sum_f32", "splitk", dict(kind="reduce", rows=16, cols=1 << 24, dt="f32", op="sum", cfg=2, opi=0)),
+        ("splitk_max_f32", "splitk", dict(kind="reduce", rows=16, cols=1 << 24, dt="f32", op="max", cfg=2, opi=1)),
+        ("softmax_bf16", "softmax", dict(kind="softmax", rows=32768, cols=4096, cfg=3, opi=0)),
+        ("layernorm_bf16", "layernorm", dict(kind="lnstats", rows=16384, cols=8192, cfg=3, opi=1)),
+        ("combine_p2", "combine", dict(kind="combine", P=2, rows=131072, D=128, cfg=4, opi=2)),
+        ("combine_p4", "combine", dict(kind="combine", P=4, rows=131072, D=128, cfg=4, opi=4)),
+        ("combine_p8", "combine", dict(kind="combine", P=8, rows=131072, D=128, cfg=4, opi=8)),
+    ]
+
+
+def algorithmic_bytes(spec) -> tuple:
+    k = spec["kind"]
+    if k == "reduce":
+        return spec["rows"] * spec["cols"] * 4, spec["rows"] * 4
+    if k == "softmax":
+        return spec["rows"] * spec["cols"] * 2, spec["rows"] * spec["cols"] * 4
+    if k == "lnstats":
+        return spec["rows"] * spec["cols"] * 2, spec["rows"] * 8
+    if k == "combine":
+        P, R, D = spec["P"], spec["rows"], spec["D"]
+        return P * R * (D * 4 + 8), R * D * 2
+    raise ValueError(k)
+
+
+def make_inputs(spec, device):
+    import torch
+    from cluster_reductions_gb300 import inputs
+    seed = inputs.seed_for(spec["cfg"], spec["opi"])
+    k = spec["kind"]
+    if k == "reduce":
+        if spec["dt"] == "i32":
+            return [inputs.uniform_i32(spec["rows"], spec["cols"], seed, device)]
+        return [inputs.normal_f32(spec["rows"], spec["cols"], seed, device)]
+    if k == "softmax":
+        return [inputs.normal_bf16(spec["rows"], spec["cols"], seed, device, 3.0)]
+    if k == "lnstats":
+        return [inputs.normal_bf16(spec["rows"], spec["cols"], seed, device, 1.0)]
+    if k == "combine":
+        O, m, l, s = inputs.combine_partials(spec["P"], spec["rows"], spec["D"], seed, device)
+        return [O, m, l, torch.tensor(s)]
+    raise ValueError(k)
+
+
+def make_outputs(spec, ins, device):
+    import torch
+    k = spec["kind"]
+    if k == "reduce":
+        return [torch.empty(spec["rows"], dtype=ins[0].dtype, device=device)]
+    if k == "softmax":
+        return [torch.empty((spec["rows"], spec["cols"]), dtype=torch.float32, device=device)]
+    if k == "lnstats":
+        return [torch.empty(spec["rows"], dtype=torch.float32, device=device),
+                torch.empty(spec["rows"], dtype=torch.float32, device=device)]
+    if k == "combine":
+        return [torch.empty((spec["rows"], spec["D"]), dtype=torch.bfloat16, device=device)]
+    raise ValueError(k)
+
+
+def run_op(rr, spec, ins, outs):
+    k = spec["kind"]
+    if k == "reduce":
+        return rr.reduce(ins[0], spec["op"], out=outs[0])
+    if k == "softmax":
+        return rr.softmax(ins[0], out=outs[0])
+    if k == "lnstats":
+        return rr.layernorm_stats(ins[0], 1e-5, mean=outs[0], rstd=outs[1])
+    if k == "combine":
+        return rr.splitk_combine(ins[0], ins[1], ins[2], float(ins[3]), out=outs[0])
+    raise ValueError(k)
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- helpers
+
+def read_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "cluster_reductions_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_plan(scale: float):
+    """Samples of each operation for the oracle, `scale` of its elements:
+    `scale` of the rows, or, where that is under one row (the 16-row
+    split-K workload), one row cut to `scale` of the elements."""
+    plan = []
+    for name, tier, spec in op_specs():
+        s = dict(spec)
+        r = spec["rows"] * scale
+        if r >= 1 or spec["kind"] == "combine":
+            s["rows"] = max(1, int(round(r)))
+        else:
+            s["rows"] = 1
+            s["cols"] = max(1, int(round(spec["cols"] * r)))
+        plan.append((name, tier, spec, s))
+    return plan
+
+
+def oracle_inputs(plan):
+    """Host inputs of the sampled rows (same generators, CPU)."""
+    import numpy as np
+    import torch
+    from cluster_reductions_gb300 import inputs
+    out = []
+    for name, tier, full, s in plan:
+        seed = inputs.seed_for(s["cfg"], s["opi"])
+        k = s["kind"]
+        if k == "reduce":
+            x = (inputs.uniform_i32(s["rows"], s["cols"], seed) if s["dt"] == "i32"
+                 else inputs.normal_f32(s["rows"], s["cols"], seed)).numpy()
+            out.append((k, s, [x]))
+        elif k in ("softmax", "lnstats"):
+            x = inputs.normal_bf16(s["rows"], s["cols"], seed, "cpu",
+                                   3.0 if k == "softmax" else 1.0)
+            out.append((k, s, [x.view(torch.int16).numpy().view(np.uint16)]))
+        else:
+            O, m, l, sc = inputs.combine_partials(s["P"], s["rows"], s["D"], seed)
+            out.append((k, s, [O.numpy(), m.numpy(), l.numpy(), sc]))
+    return out
+
+
+def run_oracle_step(data, threads: int):
+    """One pass of the oracle over the sampled rows, row chunks spread over
+    `threads` host threads (the oracle releases the GIL inside its C code)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    def chunks(n):
+        t = max(1, min(threads, n))
+        b = [n * i // t for i in range(t + 1)]
+        return [(b[i], b[i + 1]) for i in range(t) if b[i + 1] > b[i]]
+
+    jobs = []
+    for k, s, arrs in data:
+        if k == "reduce":
+            x = arrs[0]
+            jobs += [(lambda a=a, b=b, x=x, op=s["op"]: oracle.reduce_rows(x[a:b], op))
+                     for a, b in chunks(x.shape[0])]
+        elif k == "softmax":
+            x = arrs[0]
+            jobs += [(lambda a=a, b=b, x=x: oracle.softmax(x[a:b])) for a, b in chunks(x.shape[0])]
+        elif k == "lnstats":
+            x = arrs[0]
+            jobs += [(lambda a=a, b=b, x=x: oracle.layernorm_stats(x[a:b], 1e-5))
+                     for a, b in chunks(x.shape[0])]
+        else:
+            O, m, l, sc = arrs
+            jobs += [(lambda a=a, b=b, O=O, m=m, l=l, sc=sc:
+                      oracle.splitk_combine(O[:, a:b], m[:, a:b], l[:, a:b], sc))
+                     for a, b in chunks(O.shape[1])]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for f in [ex.submit(j) for j in jobs]:
+            f.result()
+
+
+def sample_bytes(data):
+    tot = 0
+    for k, s, _ in data:
+        bi, bo = algorithmic_bytes(s)
+        tot += bi + bo
+    return tot
+
+
+def calibrate_oracle(target_s: float, threads: int):
+    """Pick the sample fraction whose oracle pass takes about target_s."""
+    import oracle
+    oracle.build()
+    scale = 1.0 / 8192
+    for _ in range(2):
+        data = oracle_inputs(oracle_sample_plan(scale))
+        t0 = time.perf_counter()
+        run_oracle_step(data, threads)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        scale = min(1.0, scale * target_s / dt)
+    return scale
+
+
+def cpu_baseline(target_s: float):
+    threads = os.cpu_count() or 1
+    scale = calibrate_oracle(target_s, threads)
+    plan = oracle_sample_plan(scale)
+    data = oracle_inputs(plan)
+    t0 = time.perf_counter()
+    run_oracle_step(data, threads)
+    dt = time.perf_counter() - t0
+    b = sample_bytes(data)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"every operation of the step on {scale:.2e} of its rows "
+                      f"({b / 1e6:.1f} MB algorithmic), fp64 C oracle, {threads} host threads, "
+                      f"{dt:.2f} s"}
+
+
+# --------------------------------------------------------------------- our arm
+
+def bench_ours(args):
+    import torch
+    import cluster_reductions_gb300 as rr
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rr.load()
+    specs = op_specs()
+    data = []
+    for name, tier, spec in specs:
+        ins = make_inputs(spec, dev)
+        outs = make_outputs(spec, ins, dev)
+        data.append((name, tier, spec, ins, outs))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for name, tier, spec, ins, outs in data:
+            run_op(rr, spec, ins, outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: whole steps bracketed by barrier + synchronize; inner
+    # events give each operation's average launch duration
+    nops = len(data)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nops)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_start.record(stream)
+        for s in range(args.steps):
+            for i, (name, tier, spec, ins, outs) in enumerate(data):
+                ev[s][i][0].record(stream)
+                run_op(rr, spec, ins, outs)
+                ev[s][i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    op_ms = [statistics.fmean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+             for i in range(nops)]
+
+    step_bytes = sum(sum(algorithmic_bytes(spec)) for _, _, spec, _, _ in data)
+    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    peak, peak_kind = read_peak()
+
+    tiers = {}
+    for i, (name, tier, spec, ins, outs) in enumerate(data):
+        bi, bo = algorithmic_bytes(spec)
+        gbs = (bi + bo) / (op_ms[i] / 1e3) / 1e9
+        tiers[name] = {"gbs": round(gbs, 1), "ms": round(op_ms[i], 4),
+                       "frac_measured": round(gbs / peak, 4),
+                       "frac_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                       "rows_per_s": round(spec["rows"] / (op_ms[i] / 1e3), 1)}
+    # dominant kernel: largest share of the step time
+    dom = max(range(nops), key=lambda i: op_ms[i])
+    dname, _, dspec, _, _ = data[dom]
+    dbytes = sum(algorithmic_bytes(dspec))
+    achieved = dbytes / (op_ms[dom] / 1e3) / 1e9
+    sha = kernel_src_sha()
+    tr = NCU_TRAFFIC.get(dname)
+    traffic = tr["bytes"] if (tr and tr.get("src_sha") == sha) else None
+    roofline = {"bound": "hbm", "kernel": dname, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
+                "traffic": traffic, "algorithmic_bytes": dbytes}
+
+    # splitk tier at every cluster size (same input, outside the step)
+    splitk_c = {}
+    x_sk = next(ins[0] for name, _, _, ins, _ in data if name == "splitk_sum_f32")
+    out_sk = torch.empty(16, dtype=torch.float32, device=dev)
+    for C in (2, 4, 8, 16):
+        try:
+            for _ in range(3):
+                rr.reduce(x_sk, "sum", tier="splitk", cluster_size=C, out=out_sk)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 20
+            a.record(stream)
+            for _ in range(reps):
+                rr.reduce(x_sk, "sum", tier="splitk", cluster_size=C, out=out_sk)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            g = (16 * (1 << 24) * 4 + 64) / (ms / 1e3) / 1e9
+            splitk_c[str(C)] = {"gbs": round(g, 1), "frac_measured": round(g / peak, 4)}
+        except rr.RRError as e:
+            splitk_c[str(C)] = {"unsupported": str(e)}
+
+    e2e = bench_e2e(args, rr, data, dev, stream, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD,
+                   "l2": "inputs larger than L2: every operation reads its own buffer once "
+                         "per step; a step moves %.2f GB" % (step_bytes / 1e9),
+                   "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
+        "tiers": tiers, "splitk_by_cluster": splitk_c, "roofline": roofline,
+        "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_e2e(args, rr, data, dev, stream, world):
+    """Same step through the public API from pinned host buffers: every
+    step copies each operation's inputs host -> device and its results
+    device -> host inside the timed region."""
+    import torch
+    host_in, h2d, d2h = [], 0, 0
+    for name, tier, spec, ins, outs in data:
+        hi = []
+        for t in ins:
+            if t.dim() == 0:
+                hi.append(t)
+                continue
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            hi.append(h)
+            h2d += t.numel() * t.element_size()
+        for o in outs:
+            d2h += o.numel() * o.element_size()
+        host_in.append(hi)
+    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+                for (_, _, _, _, outs) in data]
+    dev_in = [[t for t in ins] for (_, _, _, ins, _) in data]
+
+    def step():
+        for i, (name, tier, spec, ins, outs) in enumerate(data):
+            for h, d in zip(host_in[i], dev_in[i]):
+                if h.dim():
+                    d.copy_(h, non_blocking=True)
+            run_op(rr, spec, dev_in[i], outs)
+            for h, o in zip(host_out[i], outs):
+                h.copy_(o, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    step_bytes = sum(sum(algorithmic_bytes(spec)) for _, _, spec, _, _ in data)
+    return {"value": round(world * step_bytes * steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+# --------------------------------------------------------------------- reference arm
+
+def bench_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    budget = max(0.02, min(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    scale = calibrate_oracle(budget, threads)
+    plan = oracle_sample_plan(scale)
+    data = oracle_inputs(plan)
+    for _ in range(args.warmup):
+        run_oracle_step(data, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(data, threads)
+    dt = time.perf_counter() - t0
+    b = sample_bytes(data)
+    value = b * args.steps / dt / 1e9
+    sample = (f"every operation of the step on {scale:.2e} of its rows ({b / 1e6:.2f} MB "
+              f"algorithmic per step), fp64 C oracle, {threads} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""cluster_reductions_gb300 -- deterministic row-wise monoid reductions on
+NVIDIA GB300 (sm_103a), behind the C ABI of librr.so (include/rr.h).
+
+Python names mirror the C entry points.  Tensors are torch tensors used only
+as device memory (and their current CUDA stream); every computation runs in
+the library's CUDA kernels.  Passing CPU tensors stages them through device
+memory (host -> device copy, kernel, device -> host copy) on the current
+stream, which is what an end-to-end call from host buffers costs.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import (RR_BF16, RR_F32, RR_I32, RR_OP_MAX, RR_OP_MIN, RR_OP_SUM,  # noqa: F401
+                   RR_TIER_AUTO, RR_TIER_BLOCK, RR_TIER_SPLITK, RR_TIER_TILED,
+                   RR_TIER_WARP, RRError, TIER_NAMES, check, load)
+
+_OPS = {"sum": RR_OP_SUM, "max": RR_OP_MAX, "min": RR_OP_MIN}
+_TIERS = {None: RR_TIER_AUTO, "auto": RR_TIER_AUTO, "warp": RR_TIER_WARP,
+          "tiled": RR_TIER_TILED, "serial": RR_TIER_TILED, "block": RR_TIER_BLOCK,
+          "splitk": RR_TIER_SPLITK}
+_DT = {torch.float32: RR_F32, torch.int32: RR_I32, torch.bfloat16: RR_BF16}
+
+
+def _op(op) -> int:
+    return _OPS[op] if isinstance(op, str) else int(op)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _as_2d(x: torch.Tensor) -> torch.Tensor:
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dim() != 2:
+        raise ValueError(f"expected a 2-D [rows, cols] tensor, got shape {tuple(x.shape)}")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous (row-major) tensor")
+    return x
+
+
+def _device_of(x: torch.Tensor) -> torch.device:
+    if x.is_cuda:
+        return x.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _to_device(x: torch.Tensor) -> torch.Tensor:
+    return x if x.is_cuda else x.to(_device_of(x), non_blocking=True)
+
+
+def _to_host(y: torch.Tensor, like: torch.Tensor) -> torch.Tensor:
+    if like.is_cuda:
+        return y
+    h = torch.empty(y.shape, dtype=y.dtype, pin_memory=like.is_pinned())
+    h.copy_(y, non_blocking=like.is_pinned())
+    return h
+
+
+def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tier=None,
+           cluster_size: int = 0, emit_tile_width: int = 0,
+           rank_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_reduce / rr_reduce_ex: reduce every row of a [rows, cols] fp32 or
+    int32 tensor with sum, max or min.  Returns [rows] of the same dtype."""
+    x = _as_2d(x)
+    xd = _to_device(x)
+    rows, cols = xd.shape
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_F32, RR_I32):
+        raise TypeError(f"reduce: dtype {xd.dtype} not supported (float32, int32)")
+    o = out if (out is not None and out.is_cuda) else torch.empty(rows, dtype=xd.dtype,
+                                                                  device=xd.device)
+    lib = load()
+    if tier is None and cluster_size == 0 and emit_tile_width == 0 and rank_out is None:
+        st = lib.rr_reduce(_ptr(xd), rows, cols, _op(op), dt, _ptr(o), _stream())
+    else:
+        opts = _lib.rr_reduce_opts(_TIERS[tier] if not isinstance(tier, int) else tier,
+                                   int(cluster_size), 0, int(emit_tile_width), _ptr(rank_out))
+        st = lib.rr_reduce_ex(_ptr(xd), rows, cols, _op(op), dt, _ptr(o), _stream(),
+                              ctypes.byref(opts))
+    check(st, "rr_reduce")
+    if out is not None and not out.is_cuda:
+        out.copy_(o)
+        return out
+    return _to_host(o, x)
+
+
+def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_softmax: row softmax of a bf16 or fp32 [rows, cols] tensor, fp32 out."""
+    x = _as_2d(x)
+    xd = _to_device(x)
+    rows, cols = xd.shape
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_BF16, RR_F32):
+        raise TypeError(f"softmax: dtype {xd.dtype} not supported (bfloat16, float32)")
+    o = out if out is not None else torch.empty((rows, cols), dtype=torch.float32,
+                                                device=xd.device)
+    check(load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream()), "rr_softmax")
+    return _to_host(o, x)
+
+
+def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
+                    mean: Optional[torch.Tensor] = None,
+                    rstd: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """rr_layernorm_stats: per-row mean and 1/sqrt(var + eps), fp32."""
+    x = _as_2d(x)
+    xd = _to_device(x)
+    rows, cols = xd.shape
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_BF16, RR_F32):
+        raise TypeError(f"layernorm_stats: dtype {xd.dtype} not supported")
+    mu = mean if mean is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
+    rs = rstd if rstd is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
+    check(load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
+                                    _stream()), "rr_layernorm_stats")
+    return _to_host(mu, x), _to_host(rs, x)
+
+
+def cluster_allreduce(vals: torch.Tensor, op="sum", *, two_slot: bool = False,
+                      skew_cycles: int = 0, res: Optional[torch.Tensor] = None,
+                      mismatches: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_cluster_allreduce: vals is [iters, clusters, C, W] fp32 or int32 on
+    the device; returns res of the same shape (each rank's combined copy).
+    `mismatches` (int64 [1] on the device) accumulates per-thread bit
+    differences from the rank-order fold."""
+    if vals.dim() != 4 or not vals.is_contiguous() or not vals.is_cuda:
+        raise ValueError("vals must be a contiguous CUDA tensor [iters, clusters, C, W]")
+    iters, clusters, C, W = vals.shape
+    dt = _DT.get(vals.dtype)
+    if dt not in (RR_F32, RR_I32):
+        raise TypeError("cluster_allreduce: float32 or int32 values")
+    r = res if res is not None else torch.empty_like(vals)
+    check(load().rr_cluster_allreduce(_ptr(vals), clusters, C, W, _op(op), dt, iters,
+                                      1 if two_slot else 0, int(skew_cycles), _ptr(r),
+                                      _ptr(mismatches), _stream()), "rr_cluster_allreduce")
+    return r
+
+
+def cluster_allreduce_selftest(cluster_size: int, width: int = 1, op="sum",
+                               dtype: torch.dtype = torch.float32, iters: int = 1000,
+                               two_slot: bool = True, seed: int = 1) -> int:
+    """rr_cluster_allreduce_selftest (blocking): number of values that differ
+    from the rank-order fold (0 on success)."""
+    n = ctypes.c_int64(-1)
+    st = load().rr_cluster_allreduce_selftest(int(cluster_size), int(width), _op(op),
+                                              _DT[dtype], int(iters), 1 if two_slot else 0,
+                                              int(seed), _stream(), ctypes.byref(n))
+    if st not in (_lib.RR_OK, _lib.RR_ERR_MISMATCH):
+        check(st, "rr_cluster_allreduce_selftest")
+    return int(n.value)
+
+
+def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2e: float, *,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_splitk_combine: O [P, rows, D], m and l [P, rows] fp32 -> bf16 [rows, D]."""
+    if O.dim() != 3 or m.dim() != 2 or l.dim() != 2:
+        raise ValueError("O must be [P, rows, D], m and l [P, rows]")
+    P, rows, D = O.shape
+    if tuple(m.shape) != (P, rows) or tuple(l.shape) != (P, rows):
+        raise ValueError("m and l must be [P, rows]")
+    for t in (O, m, l):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError("O, m, l must be contiguous float32")
+    Od, md, ld = _to_device(O), _to_device(m), _to_device(l)
+    o = out if out is not None else torch.empty((rows, D), dtype=torch.bfloat16,
+                                                device=Od.device)
+    check(load().rr_splitk_combine(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
+                                   float(scale_log2e), _ptr(o), _stream()),
+          "rr_splitk_combine")
+    return _to_host(o, O)
+
+
+def device_status() -> int:
+    """rr_device_status on the current stream (RR_OK or RR_ERR_TIMEOUT)."""
+    return int(load().rr_device_status(_stream()))
+
+
+def last_tier() -> Tuple[str, int]:
+    v = int(load().rr_last_tier())
+    return TIER_NAMES.get(v & 0xff, "?"), v >> 8
+
+
+def plan_reduce(rows: int, cols: int, sm_count: int, max_cluster: int) -> Tuple[str, int]:
+    """rr_plan_reduce (host only): the tier and cluster size rr_reduce picks."""
+    t, c = ctypes.c_int(), ctypes.c_int()
+    check(load().rr_plan_reduce(int(rows), int(cols), int(sm_count), int(max_cluster),
+                                ctypes.byref(t), ctypes.byref(c)), "rr_plan_reduce")
+    return TIER_NAMES[t.value], c.value
+
+
+def test_wait_timeout(budget_iters: int = 64) -> None:
+    """rr_test_wait_timeout: enqueue the bounded-wait probe (see rr.h)."""
+    check(load().rr_test_wait_timeout(int(budget_iters), _stream()), "rr_test_wait_timeout")

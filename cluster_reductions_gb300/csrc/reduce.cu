@@ -1,0 +1,474 @@
+// reduce.cu -- row-wise monoid reduction in four tiers (the "reduce" page,
+// algorithm/gpu/rowwise, tier semantics): warp, tiled/serial, block and
+// split-K.  The split-K tier spreads one row over the CTAs of a thread-block
+// cluster and combines the CTA partials with cluster_allreduce (the
+// "cluster_allreduce" page).
+//
+// Every tier folds each row in a fixed order that depends only on the shape,
+// the tier's compile-time geometry and the row's address alignment, so the
+// same call gives the same bits on every run.
+#include <cstdio>
+
+#include "rr.h"
+#include "rr_device.cuh"
+#include "rr_internal.h"
+
+namespace rr {
+namespace {
+
+// Geometry of the tiers.
+constexpr int kBlockThreads = 256, kBlockUnroll = 8;
+constexpr int kSplitThreads = 512, kSplitUnroll = 8;
+constexpr int kWarpBlock = 256, kWarpUnroll = 8;
+constexpr int kTiledBlock = 256;
+// Tiled tier: groups of rows each thread keeps in flight, so that a thread
+// holds about 8 vectors (NV vectors per row, EWT rows per group).
+__host__ __device__ constexpr int tiled_unroll(int nv, int ewt) {
+  return 8 / (nv * ewt) < 1 ? 1 : (8 / (nv * ewt) > 4 ? 4 : 8 / (nv * ewt));
+}
+
+// ---------------------------------------------------------------------------
+// Fold elements [begin, end) of one row, as one thread of a THREADS-wide CTA.
+// Scalar head up to the first 16-byte boundary, 128-bit streaming loads over
+// the aligned body (UNROLL independent loads and accumulators per thread per
+// step, so UNROLL * 16 bytes are in flight per thread), scalar tail.  The
+// block tier folds whole rows with it; the split-K tier folds one slice.
+// Returns this thread's partial (to be combined by block_reduce).
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int UNROLL>
+__device__ __forceinline__ typename Op::T fold_range(const typename Op::T *__restrict__ p,
+                                                     int64_t begin, int64_t end) {
+  using T = typename Op::T;
+  using V = typename Vec4<T>::type;
+  const int tid = threadIdx.x;
+  T acc[UNROLL];
+#pragma unroll
+  for (int u = 0; u < UNROLL; ++u) acc[u] = Op::id();
+  const int64_t n = end - begin;
+  if (n > 0) {
+    const T *s = p + begin;
+    int64_t head = (int64_t)(((16u - ((uint32_t)(uintptr_t)s & 15u)) & 15u) / sizeof(T));
+    if (head > n) head = n;
+    if (tid < head) acc[0] = Op::f(acc[0], __ldg(s + tid));
+    const V *q = reinterpret_cast<const V *>(s + head);
+    const int64_t nv = (n - head) >> 2;
+    int64_t i = tid;
+    for (; i + (int64_t)(UNROLL - 1) * THREADS < nv; i += (int64_t)UNROLL * THREADS) {
+      V v[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) v[u] = ld_stream(q + i + (int64_t)u * THREADS);
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) acc[u] = fold4<Op>(acc[u], v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL - 1; ++u) {
+      const int64_t k = i + (int64_t)u * THREADS;
+      if (k < nv) acc[u] = fold4<Op>(acc[u], ld_stream(q + k));
+    }
+    const int64_t t0 = head + (nv << 2);
+    if (tid < n - t0) acc[UNROLL - 1] = Op::f(acc[UNROLL - 1], __ldg(s + t0 + tid));
+  }
+  T a = acc[0];
+#pragma unroll
+  for (int u = 1; u < UNROLL; ++u) a = Op::f(a, acc[u]);
+  return a;
+}
+
+// ---------------------------------------------------------------------------
+// Block tier: one CTA per row, persistent grid-stride over rows.
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int UNROLL>
+__global__ void __launch_bounds__(THREADS)
+k_block(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
+        typename Op::T *__restrict__ out) {
+  using T = typename Op::T;
+  __shared__ T red[THREADS / 32];
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    T a = fold_range<Op, THREADS, UNROLL>(x + row * cols, 0, cols);
+    a = block_reduce<Op, THREADS>(a, red);
+    if (threadIdx.x == 0) out[row] = Op::finalize(a);
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warp tier, vector form: cols = 4 * LPR with LPR in {1, 2, 4, 8} and a
+// 16-byte aligned base.  A warp covers 32 / LPR rows per 512-byte load (a
+// segment of LPR lanes per row, one 128-bit vector per lane), folds the
+// vector serially, then combines the segment with an xor butterfly of
+// log2(LPR) steps.  U independent loads per lane are in flight.
+// ---------------------------------------------------------------------------
+template <class Op, int LPR, int U>
+__global__ void __launch_bounds__(kWarpBlock)
+k_warp_vec(const typename Op::T *__restrict__ x, int64_t rows,
+           typename Op::T *__restrict__ out) {
+  using T = typename Op::T;
+  using V = typename Vec4<T>::type;
+  constexpr int RPW = 32 / LPR;
+  const int lane = threadIdx.x & 31, seg = lane / LPR, sub = lane % LPR;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const V *q = reinterpret_cast<const V *>(x);
+  for (int64_t r0 = warp * (RPW * U); r0 < rows; r0 += nwarps * (RPW * U)) {
+    V v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = r0 + u * RPW + seg;
+      if (row < rows) {
+        v[u] = ld_stream(q + row * LPR + sub);
+      } else {
+        const T e = Op::id();
+        v[u].x = e; v[u].y = e; v[u].z = e; v[u].w = e;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      T a = fold4<Op>(Op::id(), v[u]);
+      a = warp_allreduce<Op, LPR>(a);
+      const int64_t row = r0 + u * RPW + seg;
+      if (sub == 0 && row < rows) out[row] = Op::finalize(a);
+    }
+  }
+}
+
+// Warp tier, scalar form (the page's literal reading): lane i loads element
+// i of the row (any alignment, cols <= 32), then a 5-step xor butterfly.
+template <class Op, int U>
+__global__ void __launch_bounds__(kWarpBlock)
+k_warp_scalar(const typename Op::T *__restrict__ x, int64_t rows, int cols,
+              typename Op::T *__restrict__ out) {
+  using T = typename Op::T;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r0 = warp * U; r0 < rows; r0 += nwarps * U) {
+    T v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = r0 + u;
+      v[u] = (row < rows && lane < cols) ? __ldg(x + row * cols + lane) : Op::id();
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const T a = warp_allreduce<Op, 32>(v[u]);
+      if (lane == 0 && r0 + u < rows) out[r0 + u] = Op::finalize(a);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tiled tier: a thread owns EWT adjacent rows and folds them on its own (no
+// cross-thread combine).  Vector form: cols = 4 * NV, 16-byte aligned base;
+// with V8 (NV even, 32-byte aligned base) each row is read with 256-bit
+// loads, so a warp instruction covers 32 * 32 contiguous bytes.
+// ---------------------------------------------------------------------------
+template <class Op, int NV, int EWT, bool V8, int U>
+__global__ void __launch_bounds__(kTiledBlock)
+k_tiled_vec(const typename Op::T *__restrict__ x, int64_t rows,
+            typename Op::T *__restrict__ out) {
+  using T = typename Op::T;
+  using V = typename Vec4<T>::type;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+  const int64_t groups = (rows + EWT - 1) / EWT;
+  const V *q = reinterpret_cast<const V *>(x);
+  for (int64_t g0 = tid; g0 < groups; g0 += nth * U) {
+    V v[U][EWT][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + (int64_t)u * nth;
+#pragma unroll
+      for (int e = 0; e < EWT; ++e) {
+        const int64_t row = g * EWT + e;
+        const bool ok = (g < groups) && (row < rows);
+        if (V8) {
+#pragma unroll
+          for (int k = 0; k < NV; k += 2) {
+            if (ok) {
+              uint32_t r8[8];
+              ld_stream_v8(q + row * NV + k, r8);
+              v[u][e][k].x = from_bits<T>(r8[0]); v[u][e][k].y = from_bits<T>(r8[1]);
+              v[u][e][k].z = from_bits<T>(r8[2]); v[u][e][k].w = from_bits<T>(r8[3]);
+              v[u][e][k + 1].x = from_bits<T>(r8[4]); v[u][e][k + 1].y = from_bits<T>(r8[5]);
+              v[u][e][k + 1].z = from_bits<T>(r8[6]); v[u][e][k + 1].w = from_bits<T>(r8[7]);
+            } else {
+              const T i0 = Op::id();
+              v[u][e][k].x = i0; v[u][e][k].y = i0; v[u][e][k].z = i0; v[u][e][k].w = i0;
+              v[u][e][k + 1] = v[u][e][k];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            if (ok) {
+              v[u][e][k] = ld_stream(q + row * NV + k);
+            } else {
+              const T i0 = Op::id();
+              v[u][e][k].x = i0; v[u][e][k].y = i0; v[u][e][k].z = i0; v[u][e][k].w = i0;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + (int64_t)u * nth;
+#pragma unroll
+      for (int e = 0; e < EWT; ++e) {
+        const int64_t row = g * EWT + e;
+        T a = Op::id();
+#pragma unroll
+        for (int k = 0; k < NV; ++k) a = fold4<Op>(a, v[u][e][k]);
+        if (g < groups && row < rows) out[row] = Op::finalize(a);
+      }
+    }
+  }
+}
+
+// Tiled / serial tier, scalar form: any cols, any alignment; a thread folds
+// its EWT rows element by element.
+template <class Op, int EWT>
+__global__ void __launch_bounds__(kTiledBlock)
+k_tiled_scalar(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
+               typename Op::T *__restrict__ out) {
+  using T = typename Op::T;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+  const int64_t groups = (rows + EWT - 1) / EWT;
+  for (int64_t g = tid; g < groups; g += nth) {
+#pragma unroll
+    for (int e = 0; e < EWT; ++e) {
+      const int64_t row = g * EWT + e;
+      if (row < rows) {
+        T a = Op::id();
+        const T *p = x + row * cols;
+        for (int64_t i = 0; i < cols; ++i) a = Op::f(a, __ldg(p + i));
+        out[row] = Op::finalize(a);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K tier ("reduce" page, split-K tier; "cluster_allreduce" page).
+// A cluster of C CTAs per row; CTA rank r folds slice r of the row.  Slices
+// are ceil(cols / C) elements rounded up to a multiple of 4 and shifted down
+// by the row's misalignment, so every slice but the first starts on a
+// 16-byte boundary; the last slice takes the remainder.  The CTA partials
+// are combined with cluster_allreduce: every CTA gathers every peer and
+// folds in rank order, so all C copies of the result are bit-identical.
+// Rank 0 writes out[row]; rank_out (optional) receives every rank's copy.
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int UNROLL>
+__global__ void __launch_bounds__(THREADS)
+k_splitk(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
+         typename Op::T *__restrict__ out, typename Op::T *__restrict__ rank_out) {
+  using T = typename Op::T;
+  __shared__ T red[THREADS / 32];
+  __shared__ T slot[2];
+  const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
+  const int64_t row = cluster_id_x();
+  const T *p = x + row * cols;
+  const int64_t chunk = ((cols + C - 1) / C + 3) & ~int64_t(3);
+  const int64_t mis = (int64_t)(((uint32_t)(uintptr_t)p & 15u) / sizeof(T));
+  auto bound = [&](int64_t k) -> int64_t {
+    if (k == 0) return 0;
+    if (k >= (int64_t)C) return cols;
+    const int64_t b = k * chunk - mis;
+    return b < 0 ? 0 : (b > cols ? cols : b);
+  };
+  T a = fold_range<Op, THREADS, UNROLL>(p, bound(r), bound(r + 1));
+  a = block_reduce<Op, THREADS>(a, red);
+  const T v[1] = {a};
+  T res[1];
+  cluster_allreduce<Op, 1>(slot, v, C, /*tail_sync=*/true, res);
+  if (threadIdx.x == 0) {
+    const T fin = Op::finalize(res[0]);
+    if (r == 0) out[row] = fin;
+    if (rank_out) rank_out[row * C + r] = fin;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+template <class K>
+int grid_for(K kernel, int threads, int64_t work_blocks, const DevInfo &d, int smem = 0) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess || nb < 1)
+    nb = 1;
+  const int64_t cap = (int64_t)nb * d.sm_count;
+  int64_t g = work_blocks < cap ? work_blocks : cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+template <class Op>
+int launch_splitk_kernel(const void *x, int64_t rows, int64_t cols, void *out,
+                         void *rank_out, int C, cudaStream_t s) {
+  using T = typename Op::T;
+  auto kern = k_splitk<Op, kSplitThreads, kSplitUnroll>;
+  if (C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const T *)x, rows, cols, (T *)out,
+                                        (T *)rank_out));
+}
+
+template <class Op>
+int max_cluster_for(int want, const DevInfo &d) {
+  auto kern = k_splitk<Op, kSplitThreads, kSplitUnroll>;
+  for (int C = 16; C >= 1; C >>= 1) {
+    if (C > want) continue;
+    if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (C == 1) return 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) return C;
+    cudaGetLastError();
+  }
+  return 0;
+}
+
+template <class Op>
+int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStream_t s,
+                int tier, int C, int ewt, void *rank_out, const DevInfo &d) {
+  using T = typename Op::T;
+  const T *x = (const T *)xv;
+  T *out = (T *)outv;
+  const uintptr_t a = (uintptr_t)xv;
+  switch (tier) {
+    case RR_TIER_BLOCK: {
+      auto k = k_block<Op, kBlockThreads, kBlockUnroll>;
+      const int g = grid_for(k, kBlockThreads, rows, d);
+      k<<<g, kBlockThreads, 0, s>>>(x, rows, cols, out);
+      return cuda_status(cudaGetLastError());
+    }
+    case RR_TIER_WARP: {
+      const bool vec = (cols % 4 == 0) && cols >= 4 && (a % 16 == 0) &&
+                       (cols == 4 || cols == 8 || cols == 16 || cols == 32);
+      if (vec) {
+        const int lpr = (int)(cols / 4);
+        const int64_t rows_per_block = (int64_t)(kWarpBlock / 32) * (32 / lpr) * kWarpUnroll;
+        const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+#define RR_WARP_VEC(L)                                                         \
+  {                                                                            \
+    auto k = k_warp_vec<Op, L, kWarpUnroll>;                                   \
+    const int g = grid_for(k, kWarpBlock, blocks, d);                          \
+    k<<<g, kWarpBlock, 0, s>>>(x, rows, out);                                  \
+    break;                                                                     \
+  }
+        switch (lpr) {
+          case 1: RR_WARP_VEC(1)
+          case 2: RR_WARP_VEC(2)
+          case 4: RR_WARP_VEC(4)
+          default: RR_WARP_VEC(8)
+        }
+#undef RR_WARP_VEC
+      } else {
+        auto k = k_warp_scalar<Op, kWarpUnroll>;
+        const int64_t rows_per_block = (int64_t)(kWarpBlock / 32) * kWarpUnroll;
+        const int g = grid_for(k, kWarpBlock, (rows + rows_per_block - 1) / rows_per_block, d);
+        k<<<g, kWarpBlock, 0, s>>>(x, rows, (int)cols, out);
+      }
+      return cuda_status(cudaGetLastError());
+    }
+    case RR_TIER_TILED: {
+      const int e = (ewt == 2 || ewt == 4) ? ewt : 1;
+      const int64_t groups = (rows + e - 1) / e;
+      const bool vec = cols >= 4 && cols <= 16 && cols % 4 == 0 && (a % 16 == 0);
+      if (vec) {
+        const int nv = (int)(cols / 4);
+        const bool v8 = (nv % 2 == 0) && (a % 32 == 0);
+        const int64_t blocks = (groups + kTiledBlock - 1) / kTiledBlock;
+#define RR_TILED_VEC(NV, E, V8)                                                \
+  {                                                                            \
+    auto k = k_tiled_vec<Op, NV, E, V8, tiled_unroll(NV, E)>;                  \
+    const int g = grid_for(k, kTiledBlock, blocks, d);                         \
+    k<<<g, kTiledBlock, 0, s>>>(x, rows, out);                                 \
+  }
+#define RR_TILED_E(NV, V8)                                                     \
+  {                                                                            \
+    if (e == 1) RR_TILED_VEC(NV, 1, V8)                                        \
+    else if (e == 2) RR_TILED_VEC(NV, 2, V8)                                   \
+    else RR_TILED_VEC(NV, 4, V8)                                               \
+  }
+        if (nv == 1) RR_TILED_E(1, false)
+        else if (nv == 2) { if (v8) RR_TILED_E(2, true) else RR_TILED_E(2, false) }
+        else if (nv == 3) RR_TILED_E(3, false)
+        else { if (v8) RR_TILED_E(4, true) else RR_TILED_E(4, false) }
+#undef RR_TILED_E
+#undef RR_TILED_VEC
+      } else {
+        const int64_t blocks = (groups + kTiledBlock - 1) / kTiledBlock;
+        if (e == 1) {
+          auto k = k_tiled_scalar<Op, 1>;
+          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+        } else if (e == 2) {
+          auto k = k_tiled_scalar<Op, 2>;
+          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+        } else {
+          auto k = k_tiled_scalar<Op, 4>;
+          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+        }
+      }
+      return cuda_status(cudaGetLastError());
+    }
+    case RR_TIER_SPLITK:
+      return launch_splitk_kernel<Op>(xv, rows, cols, outv, rank_out, C, s);
+    default:
+      return RR_ERR_INVALID;
+  }
+}
+
+}  // namespace
+
+int splitk_max_cluster(int op, int dtype, int want, const DevInfo &d) {
+  (void)d;
+  if (dtype == RR_F32) {
+    if (op == RR_OP_SUM) return max_cluster_for<SumF32>(want, d);
+    if (op == RR_OP_MAX) return max_cluster_for<MaxF32>(want, d);
+    return max_cluster_for<MinF32>(want, d);
+  }
+  if (op == RR_OP_SUM) return max_cluster_for<SumI32>(want, d);
+  if (op == RR_OP_MAX) return max_cluster_for<MaxI32>(want, d);
+  return max_cluster_for<MinI32>(want, d);
+}
+
+int launch_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype, void *out,
+                  cudaStream_t s, int tier, int C, int ewt, void *rank_out, const DevInfo &d) {
+  if (dtype == RR_F32) {
+    if (op == RR_OP_SUM) return launch_tier<SumF32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+    if (op == RR_OP_MAX) return launch_tier<MaxF32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+    return launch_tier<MinF32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+  }
+  if (op == RR_OP_SUM) return launch_tier<SumI32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+  if (op == RR_OP_MAX) return launch_tier<MaxI32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+  return launch_tier<MinI32>(x, rows, cols, out, s, tier, C, ewt, rank_out, d);
+}
+
+}  // namespace rr

@@ -1,0 +1,55 @@
+// rr_internal.h -- host-side interface between the C-ABI layer (api.cu) and
+// the per-family launchers (reduce.cu, rowwise.cu, combine.cu, cluster.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rr {
+
+struct DevInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;     // bytes of shared memory a CTA may opt into
+  int cluster_launch = 0;     // device supports cluster launch
+  int *err_word = nullptr;    // device error word (4 bytes), zeroed
+};
+
+// Returns the cached info of the current device (creating the error word on
+// first use), or nullptr with *status set on failure.
+const DevInfo *current_device(int *status);
+
+// ---- reduce (reduce.cu)
+// Largest cluster size in {16, 8, 4, 2, 1} <= `want` that the split-K kernel
+// for (op, dtype) can co-schedule on this device (0 if not even 1).
+int splitk_max_cluster(int op, int dtype, int want, const DevInfo &d);
+int launch_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype,
+                  void *out, cudaStream_t s, int tier, int C, int ewt,
+                  void *rank_out, const DevInfo &d);
+
+// ---- softmax / layernorm statistics (rowwise.cu)
+int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype,
+                   float *out, cudaStream_t s, const DevInfo &d, int *tier_out);
+int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols,
+                           int in_dtype, float eps, float *mean, float *rstd,
+                           cudaStream_t s, const DevInfo &d, int *tier_out);
+
+// ---- split-K combine (combine.cu)
+int launch_combine(const float *O, const float *m, const float *l, int P,
+                   int64_t rows, int D, float scale_log2e, uint16_t *out,
+                   cudaStream_t s, const DevInfo &d);
+
+// ---- cluster all-reduce primitive (cluster.cu)
+int launch_cluster_allreduce(const void *vals, int clusters, int C, int width,
+                             int op, int dtype, int iters, int two_slot,
+                             int64_t skew_cycles, void *res,
+                             int64_t *mismatches, cudaStream_t s,
+                             const DevInfo &d);
+int launch_fill_selftest_values(void *vals, int64_t n, int dtype,
+                                uint64_t seed, cudaStream_t s);
+int launch_wait_timeout_probe(int64_t budget, cudaStream_t s, const DevInfo &d);
+
+// Maps a CUDA error to an rr_status, remembering the message.
+int cuda_status(cudaError_t e);
+
+}  // namespace rr

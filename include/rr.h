@@ -1,0 +1,237 @@
+/*
+ * rr.h -- C ABI of librr.so: deterministic row-wise monoid reductions on
+ * NVIDIA GB300 (sm_103a), the cluster all-reduce they are built on, and the
+ * split-K attention-output combine.
+ *
+ * Sources (Mojo API documentation pages; cited by title and section):
+ *   [CA] "cluster_allreduce" (max/gpu/primitives/cluster): description,
+ *        parameters combine_fn / cluster_size / need_tail_sync, arg slot.
+ *   [RW] "reduce" (algorithm/gpu/rowwise): tier semantics (warp, block,
+ *        tiled, serial, split-K), the stateless and the state-carrying
+ *        overloads, pjoin.
+ *   [FA] "fa4_splitk_reduce_scatter_write" (kernels/nn/attention/gpu/nvidia/
+ *        sm100/softmax_warp): split-K pass 2, band per partition, stage,
+ *        publish, combine, bf16 store, terminal cluster sync.
+ *
+ * Conventions for every entry point
+ *   - Pointers named x, out, O, m, l, mean, rstd, vals, res are DEVICE
+ *     pointers owned by the caller; tensors are dense row-major (C order).
+ *     The library never frees or retains them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work and return, unless stated otherwise.
+ *   - Return value: an rr_status.  Arguments are validated on the host
+ *     before anything is enqueued; an invalid call enqueues nothing.  No
+ *     exception crosses this ABI.
+ *   - rows == 0 is a no-op returning RR_OK.
+ *   - The library allocates only a 4-byte device error word per device
+ *     (on first use) and caches device properties; rr_cluster_allreduce_
+ *     selftest also allocates and frees its own scratch.
+ *   - Results are deterministic: the same inputs, shapes, pointer
+ *     alignments and options give the same bits on every run (no float
+ *     atomics, no occupancy-dependent partitioning of a row).
+ */
+#ifndef RR_H_
+#define RR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RR_OK = 0,
+    RR_ERR_INVALID = 1,     /* bad argument: null pointer, negative size,
+                               unsupported (op, dtype), bad P / D, aliasing */
+    RR_ERR_UNSUPPORTED = 2, /* valid request the device cannot run, e.g. no
+                               active cluster of the requested size */
+    RR_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+    RR_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+    RR_ERR_MISMATCH = 5     /* a self-test found a result that differs */
+} rr_status;
+
+typedef enum { RR_OP_SUM = 0, RR_OP_MAX = 1, RR_OP_MIN = 2 } rr_op;
+
+typedef enum { RR_F32 = 0, RR_I32 = 1, RR_BF16 = 2 } rr_dtype;
+
+/* Reduction tiers of [RW] "tier semantics". */
+typedef enum {
+    RR_TIER_AUTO = 0,
+    RR_TIER_WARP = 1,    /* axis <= 32: a warp (or a warp segment) per row */
+    RR_TIER_TILED = 2,   /* a thread owns emit_tile_width adjacent rows; no
+                            cross-thread combine ([RW] tiled and serial tiers:
+                            emit_tile_width 1 is the serial tier) */
+    RR_TIER_BLOCK = 3,   /* a CTA per row, threads stride the axis */
+    RR_TIER_SPLITK = 4   /* a cluster of C CTAs per row, combined through
+                            distributed shared memory ([CA]) */
+} rr_tier;
+
+/*
+ * Options of rr_reduce_ex.  Zero-initialise and set what you need.
+ *   tier            RR_TIER_AUTO or a forced tier.
+ *   cluster_size    split-K: 0 = automatic, else 1, 2, 4, 8 or 16.
+ *   two_slot        reserved for multi-combine kernels (ignored by reduce,
+ *                   which combines once per row).
+ *   emit_tile_width tiled tier: rows per thread, 0 = automatic, else 1, 2, 4.
+ *   rank_out        split-K only, optional device pointer to rows * C
+ *                   elements of the output type: rank r of the cluster of
+ *                   row i writes its copy of the combined result to
+ *                   rank_out[i * C + r].  Every copy is bit-identical ([CA]
+ *                   description); this exposes it for checking.
+ */
+typedef struct {
+    int tier;
+    int cluster_size;
+    int two_slot;
+    int emit_tile_width;
+    void *rank_out;
+} rr_reduce_opts;
+
+/*
+ * rr_reduce -- out[i] = x[i,0] (+) x[i,1] (+) ... (+) x[i,cols-1] for each
+ * of `rows` rows ([RW] state-carrying overload: every tile of the row is
+ * folded into one monoid state, then pjoin combines across threads / CTAs).
+ *   x      device, rows x cols, dtype RR_F32 or RR_I32, element-aligned
+ *          (any 4-byte alignment; 16-byte alignment enables vector loads).
+ *   op     RR_OP_SUM, RR_OP_MAX or RR_OP_MIN.
+ *   out    device, rows elements of the same dtype as x; must not overlap x.
+ * fp32 sum is accumulated in fp32 in a fixed order (result within the
+ * usual fp32 summation error); int32 sum wraps modulo 2^32; max / min are
+ * exact, with max(+0,-0) = +0, min(+0,-0) = -0 and NaN propagating as the
+ * quiet NaN 0x7fc00000.  cols == 0 writes the identity (0, -inf / INT_MIN,
+ * +inf / INT_MAX).  The tier is picked from rows, cols and the SM count:
+ * cols <= 16 tiled; cols <= 32 warp; rows < SMs and cols >= 4096 split-K
+ * with C the largest power of two <= min(16, SMs / rows) that the device
+ * can co-schedule; otherwise block.
+ * Errors: RR_ERR_INVALID (null pointer with rows > 0, negative sizes, bad
+ * op / dtype, overlap), RR_ERR_UNSUPPORTED, RR_ERR_CUDA.
+ */
+int rr_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype,
+              void *out, void *stream);
+
+/* rr_reduce with options (forced tier, cluster size, tile width, per-rank
+ * output).  opts may be NULL (same as rr_reduce).  A forced cluster size
+ * the device cannot co-schedule returns RR_ERR_UNSUPPORTED. */
+int rr_reduce_ex(const void *x, int64_t rows, int64_t cols, int op, int dtype,
+                 void *out, void *stream, const rr_reduce_opts *opts);
+
+/*
+ * rr_softmax -- out[i,:] = exp(x[i,:] - m_i) / s_i with m_i = max_j x[i,j],
+ * s_i = sum_j exp(x[i,j] - m_i) ([RW]: pass 1 reduces the (max, sum)
+ * monoid, pass 2 is a stateless map over the row).  The row is read from
+ * HBM once when it fits on chip.
+ *   x      device, rows x cols, in_dtype RR_BF16 or RR_F32.
+ *   out    device fp32, rows x cols; must not overlap x.
+ *   cols must be >= 1 (RR_ERR_INVALID otherwise).
+ */
+int rr_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype,
+               float *out, void *stream);
+
+/*
+ * rr_layernorm_stats -- per row mean = sum x / cols, population variance
+ * var = sum (x - mean)^2 / cols taken about the mean in a second pass over
+ * the on-chip row, rstd = 1 / sqrt(var + eps) ([RW]: the statistics reduce
+ * that precedes the layernorm rewrite).
+ *   x      device, rows x cols, in_dtype RR_BF16 or RR_F32; cols >= 1.
+ *   mean, rstd  device fp32, rows elements each.
+ */
+int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
+                       float eps, float *mean, float *rstd, void *stream);
+
+/*
+ * rr_cluster_allreduce -- the [CA] primitive, run `iters` times back to back
+ * by `clusters` clusters of `cluster_size` CTAs.  For iteration t, cluster
+ * c, rank r, the CTA's block-reduced vector is vals[((t*clusters + c)*C
+ * + r)*width + j] (loaded by thread 0 only).  Every CTA gathers every peer's
+ * vector through distributed shared memory and folds it in rank order
+ * 0..C-1, so all CTAs hold the same bits; res receives each rank's result
+ * in the same layout.  two_slot = 0 retires the slot with a trailing
+ * cluster barrier after every combine (need_tail_sync = True); two_slot = 1
+ * drops it and alternates between two slots ([CA] need_tail_sync).
+ * skew_cycles > 0 makes each rank spin a pseudo-random multiple (0..7) of
+ * skew_cycles clock cycles before each combine, so that CTAs race ahead.
+ * Every thread of every CTA also re-folds the inputs of its iteration from
+ * global memory in rank order and compares bits with its own result;
+ * *mismatches (device int64, optional) is incremented per differing value.
+ *   cluster_size 1..16 (16 needs the device's non-portable cluster size),
+ *   width 1, 2, 4 or 8, dtype RR_F32 or RR_I32; iters >= 0 (0 is a no-op);
+ *   skew_cycles 0..2^20.
+ */
+int rr_cluster_allreduce(const void *vals, int clusters, int cluster_size,
+                         int width, int op, int dtype, int iters, int two_slot,
+                         int64_t skew_cycles, void *res,
+                         int64_t *mismatches, void *stream);
+
+/*
+ * rr_cluster_allreduce_selftest -- BLOCKING self-test of the [CA]
+ * primitive: draws seeded per-rank vectors on the device (a counter-based
+ * hash of seed, iteration, cluster, rank, element), runs
+ * rr_cluster_allreduce with 2 clusters of `cluster_size` CTAs and a rank
+ * skew, synchronises, and writes to *mismatches_out (host pointer) the
+ * number of values, over all threads and iterations, that differ in bits
+ * from the rank-order fold.  Returns RR_OK, or RR_ERR_MISMATCH when the
+ * count is non-zero.  Allocates and frees its own device scratch.
+ */
+int rr_cluster_allreduce_selftest(int cluster_size, int width, int op,
+                                  int dtype, int iters, int two_slot,
+                                  uint64_t seed, void *stream,
+                                  int64_t *mismatches_out);
+
+/*
+ * rr_splitk_combine -- split-K attention-output combine ([FA]).
+ *   O       device fp32 [P][rows][D] partial outputs (unnormalised).
+ *   m, l    device fp32 [P][rows] per-partition row max (raw scores) and
+ *           row sum of exp.
+ *   out_bf16 device [rows][D] bf16 bit patterns.
+ * Per row: M = max_p m_p, w_p = exp2((m_p - M) * scale_log2e),
+ * L = sum_p w_p l_p (rank order), out = bf16_rn(sum_p w_p O_p / L); rows
+ * with M = -inf or L = 0 are written as +0.  A cluster of P CTAs handles a
+ * tile of rows: CTA p stages its own partial into its shared memory,
+ * publishes it with a cluster barrier, then folds the P partials of its
+ * column band [p*D/P, (p+1)*D/P) in rank order through distributed shared
+ * memory and stores that band.  A partition whose band is empty (D < P)
+ * only stages and publishes.
+ *   P in 1..16 (16 needs the non-portable cluster size), D in 1..1024.
+ * Errors: RR_ERR_INVALID, RR_ERR_UNSUPPORTED (cluster of P CTAs cannot be
+ * co-scheduled), RR_ERR_CUDA.  A staging copy that does not land within the
+ * device wait budget sets the device error word (see rr_device_status).
+ */
+int rr_splitk_combine(const float *O, const float *m, const float *l, int P,
+                      int64_t rows, int D, float scale_log2e,
+                      uint16_t *out_bf16, void *stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word: RR_OK, or RR_ERR_TIMEOUT if a bounded device wait gave up since the
+ * last call.  RR_ERR_CUDA if the synchronisation itself failed. */
+int rr_device_status(void *stream);
+
+/* Tier and cluster size of the last reduce / softmax / layernorm call made
+ * by this process: (cluster_size << 8) | tier. */
+int rr_last_tier(void);
+
+/* Static English name of a status code. */
+const char *rr_status_string(int status);
+
+/*
+ * rr_plan_reduce -- the host-only tier choice of rr_reduce for a device
+ * with `sm_count` SMs whose largest co-schedulable cluster is
+ * `max_cluster` CTAs: writes the tier and cluster size rr_reduce would use.
+ * Touches no GPU.  Returns RR_ERR_INVALID on negative sizes.
+ */
+int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster,
+                   int *tier_out, int *cluster_out);
+
+/*
+ * rr_test_wait_timeout -- failure-detection hook: launches one CTA that
+ * waits on a shared-memory mbarrier that nothing completes, with a budget
+ * of `budget_iters` polls.  The wait gives up, sets the device error word
+ * and the kernel returns normally, so a following rr_device_status
+ * reports RR_ERR_TIMEOUT and the context stays usable.
+ */
+int rr_test_wait_timeout(int64_t budget_iters, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RR_H_ */

@@ -1,0 +1,78 @@
+"""GPU checks of the cluster all-reduce primitive: every rank's result equal
+in bits to the oracle's rank-order fold, with and without the tail sync
+(two-slot alternation), with ranks skewed so that CTAs race ahead; the
+blocking self-test; and the bounded-wait failure path."""
+import numpy as np
+import pytest
+import torch
+
+from _util import to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import cluster_reductions_gb300 as rr
+    rr.load()
+    return rr
+
+
+def _vals(iters, clusters, C, W, dtype, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    if dtype == torch.int32:
+        return torch.randint(-2**31, 2**31, (iters, clusters, C, W), generator=g,
+                             device="cuda", dtype=torch.int64).to(torch.int32)
+    mant = torch.rand((iters, clusters, C, W), generator=g, device="cuda") * 2 - 1
+    ex = torch.randint(-20, 21, (iters, clusters, C, W), generator=g, device="cuda")
+    return torch.ldexp(mant, ex).to(torch.float32)
+
+
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("two_slot", [False, True], ids=["tail", "twoslot"])
+def test_cluster_allreduce_matches_rank_order_fold(rr, oracle_mod, C, two_slot):
+    iters, clusters = 64, 3
+    for W in (1, 2, 8):
+        for dtype in (torch.float32, torch.int32):
+            for op in ("sum", "max", "min"):
+                v = _vals(iters, clusters, C, W, dtype, C * 100 + W)
+                mism = torch.zeros(1, dtype=torch.int64, device="cuda")
+                try:
+                    res = rr.cluster_allreduce(v, op, two_slot=two_slot, skew_cycles=500,
+                                               mismatches=mism)
+                except rr.RRError as e:
+                    if C == 16 and e.status == 2:
+                        pytest.skip("cluster of 16 not schedulable")
+                    raise
+                assert int(mism.item()) == 0
+                vh, rh = to_np(v), to_np(res)
+                # all ranks hold the same bits
+                assert (rh.view(np.uint32) == rh[:, :, :1, :].view(np.uint32)).all()
+                for t in (0, iters // 2, iters - 1):
+                    for c in range(clusters):
+                        ref = oracle_mod.cluster_fold(vh[t, c], op)
+                        assert (rh[t, c, 0].view(np.uint32) == ref.view(np.uint32)).all()
+
+
+@pytest.mark.parametrize("C", [2, 4, 8])
+def test_selftest_stress(rr, C):
+    for two_slot in (True, False):
+        assert rr.cluster_allreduce_selftest(C, width=2, op="sum", iters=2000,
+                                             two_slot=two_slot, seed=C) == 0
+
+
+def test_single_cta_cluster_is_broadcast(rr):
+    v = _vals(5, 4, 1, 4, torch.float32, 3)
+    res = rr.cluster_allreduce(v, "sum")
+    assert torch.equal(res.view(torch.int32), v.view(torch.int32))
+
+
+def test_bounded_wait_reports_timeout(rr):
+    assert rr.device_status() == 0
+    rr.test_wait_timeout(64)
+    assert rr.device_status() == 4          # RR_ERR_TIMEOUT, context still usable
+    assert rr.device_status() == 0          # cleared by the read
+    x = torch.ones((4, 100), device="cuda")
+    assert torch.equal(rr.reduce(x, "sum").cpu(), torch.full((4,), 100.0))

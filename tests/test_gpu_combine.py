@@ -1,0 +1,88 @@
+"""GPU parity of rr_splitk_combine against the fp64 oracle: every output
+within 1 bf16 ulp of the oracle's correctly rounded bf16 value."""
+import numpy as np
+import pytest
+import torch
+
+from _util import assert_bf16_ulp, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import cluster_reductions_gb300 as rr
+    rr.load()
+    return rr
+
+
+def run(rr, oracle_mod, P, rows, D, seed):
+    from cluster_reductions_gb300 import inputs
+    O, m, l, s = inputs.combine_partials(P, rows, D, seed, "cuda")
+    try:
+        out = rr.splitk_combine(O, m, l, s)
+    except rr.RRError as e:
+        if P > 8 and e.status == 2:
+            pytest.skip(f"cluster of {P} CTAs not schedulable")
+        raise
+    _, ref = oracle_mod.splitk_combine(to_np(O), to_np(m), to_np(l), s)
+    assert_bf16_ulp(to_np(out), ref)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("D", [128, 64, 16, 12, 7, 3])
+def test_combine_small(rr, oracle_mod, P, D):
+    for rows in (1, 5, 33, 130):
+        run(rr, oracle_mod, P, rows, D, 400 + P * 7 + D + rows)
+
+
+@pytest.mark.parametrize("P", [2, 4, 8])
+def test_combine_workload_full_size(rr, oracle_mod, P):
+    # rows = 32 batch x 32 heads x 128 queries = 131072, D = 128; the oracle
+    # checks a strided sample of rows
+    from cluster_reductions_gb300 import inputs
+    rows, D = 131072, 128
+    O, m, l, s = inputs.combine_partials(P, rows, D, inputs.seed_for(4, P), "cuda")
+    out = rr.splitk_combine(O, m, l, s)
+    idx = torch.arange(0, rows, 97, device="cuda")
+    _, ref = oracle_mod.splitk_combine(to_np(O[:, idx]), to_np(m[:, idx]), to_np(l[:, idx]), s)
+    assert_bf16_ulp(to_np(out[idx]), ref)
+
+
+def test_combine_special_cases(rr, oracle_mod):
+    P, rows, D = 4, 40, 128
+    from cluster_reductions_gb300 import inputs
+    O, m, l, s = inputs.combine_partials(P, rows, D, 9, "cuda")
+    m[:, 0] = float("-inf")            # every partition empty -> 0
+    l[:, 1] = 0.0                      # zero mass -> 0
+    m[2, 2] += 1000.0                  # one dominant partition -> its O / l
+    m[:, 3] = m[0, 3]                  # equal maxima -> sum O / sum l
+    out = rr.splitk_combine(O, m, l, s)
+    got = to_np(out)
+    assert (got[0] == 0).all() and (got[1] == 0).all()
+    _, ref = oracle_mod.splitk_combine(to_np(O), to_np(m), to_np(l), s)
+    assert_bf16_ulp(got, ref)
+    # P = 1: O / l
+    out1 = rr.splitk_combine(O[:1].contiguous(), m[:1].contiguous(), l[:1].contiguous(), s)
+    _, ref1 = oracle_mod.splitk_combine(to_np(O[:1]), to_np(m[:1]), to_np(l[:1]), s)
+    assert_bf16_ulp(to_np(out1)[2:], ref1[2:])
+
+
+def test_combine_deterministic(rr):
+    from cluster_reductions_gb300 import inputs
+    O, m, l, s = inputs.combine_partials(8, 4096, 128, 11, "cuda")
+    a = rr.splitk_combine(O, m, l, s).clone()
+    for _ in range(20):
+        assert torch.equal(rr.splitk_combine(O, m, l, s).view(torch.int16), a.view(torch.int16))
+
+
+def test_combine_argument_errors(rr):
+    O = torch.zeros((2, 4, 8), device="cuda")
+    m = torch.zeros((2, 4), device="cuda")
+    with pytest.raises(rr.RRError):
+        rr.splitk_combine(torch.zeros((17, 4, 8), device="cuda"), torch.zeros((17, 4), device="cuda"),
+                          torch.zeros((17, 4), device="cuda"), 1.0)
+    with pytest.raises(rr.RRError):
+        rr.splitk_combine(O, m, m.clone(), float("nan"))

@@ -1,0 +1,201 @@
+"""GPU parity of rr_reduce in every tier against the CPU oracle.
+
+Bars: int32 sum and every max / min bit-exact; fp32 sum within
+1e-5 * max(|ref|, ||x_row||_2) of the fp64 oracle.  Small shapes span several
+tiles, ragged tails and misaligned rows; the full workload sizes are checked
+on every row the oracle can afford (all rows for the warp, tiled and split-K
+workloads, sampled rows for 8192 x 8192)."""
+import numpy as np
+import pytest
+import torch
+
+from _util import assert_bits_equal, assert_sum_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+TIERS = ["warp", "tiled", "block", "splitk"]
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import cluster_reductions_gb300 as rr
+    rr.load()
+    return rr
+
+
+def check(rr, oracle_mod, x: torch.Tensor, op: str, **kw):
+    got = to_np(rr.reduce(x, op, **kw))
+    xh = to_np(x)
+    ref = oracle_mod.reduce_rows(xh, op)
+    if op == "sum" and xh.dtype == np.float32:
+        assert_sum_close(got, ref, xh)
+    else:
+        assert_bits_equal(got, ref.astype(xh.dtype) if xh.dtype == np.int32 else ref)
+
+
+def gen(rows, cols, dtype, seed, offset=0):
+    """Seeded input; `offset` elements of padding in front make the rows
+    start off 16-byte boundaries."""
+    from cluster_reductions_gb300 import inputs
+    if dtype == torch.int32:
+        base = inputs.uniform_i32(1, rows * cols + offset, seed, "cuda")
+    else:
+        base = inputs.normal_f32(1, rows * cols + offset, seed, "cuda")
+    return base.view(-1)[offset:].view(rows, cols)
+
+
+SHAPES = [(1, 1), (3, 3), (5, 4), (7, 5), (9, 8), (4, 13), (6, 16), (5, 17), (33, 31),
+          (65, 32), (3, 33), (2, 100), (9, 1000), (4, 4099), (3, 8192)]
+
+
+@pytest.mark.parametrize("tier", TIERS)
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int32], ids=["f32", "i32"])
+def test_forced_tiers_small(rr, oracle_mod, tier, op, dtype):
+    for i, (rows, cols) in enumerate(SHAPES):
+        if tier == "warp" and cols > 32:
+            continue
+        for offset in (0, 1, 3):
+            x = gen(rows, cols, dtype, 100 + i, offset)
+            kw = {"tier": tier}
+            if tier == "splitk":
+                for C in (1, 2, 4):
+                    check(rr, oracle_mod, x, op, tier=tier, cluster_size=C)
+                continue
+            if tier == "tiled":
+                for e in (1, 2, 4):
+                    check(rr, oracle_mod, x, op, tier=tier, emit_tile_width=e)
+                continue
+            check(rr, oracle_mod, x, op, **kw)
+
+
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+def test_auto_tier_and_empty(rr, oracle_mod, op):
+    for rows, cols in [(0, 5), (4, 0), (1, 0)]:
+        x = torch.zeros((rows, cols), device="cuda")
+        got = to_np(rr.reduce(x, op))
+        ref = oracle_mod.reduce_rows(to_np(x), op)
+        assert_bits_equal(got, ref)
+    for rows, cols in [(1000, 7), (1000, 24), (300, 2000), (3, 70000)]:
+        check(rr, oracle_mod, gen(rows, cols, torch.float32, 7), op)
+
+
+def test_signed_zero_nan_all_tiers(rr, oracle_mod):
+    rows = [[0.0, -0.0, -0.0, 0.0], [-0.0, -0.0, -0.0, -0.0], [0.0, 0.0, 0.0, 0.0],
+            [1.0, float("nan"), 2.0, -3.0], [-1.0, -2.0, -0.0, float("nan")]]
+    x = torch.tensor(rows, dtype=torch.float32, device="cuda")
+    for tier in TIERS:
+        for op in ("max", "min"):
+            got = to_np(rr.reduce(x, op, tier=tier,
+                                  **({"cluster_size": 2} if tier == "splitk" else {})))
+            ref = oracle_mod.reduce_rows(to_np(x), op)
+            assert_bits_equal(got[:3], ref[:3])
+            assert np.isnan(got[3:]).all()
+            assert (to_np(torch.from_numpy(got[3:]).view(torch.int32)) == 0x7fc00000).all()
+
+
+def test_small_splitk_workload(rr, oracle_mod):
+    # 64 x 4096, x ~ U[-1, 1], sum / max / min, plus int32 sum; cluster 1 and 2
+    from cluster_reductions_gb300 import inputs
+    for oi, op in enumerate(["sum", "max", "min"]):
+        x = inputs.uniform_f32(64, 4096, inputs.seed_for(0, oi), "cuda")
+        for C in (1, 2):
+            check(rr, oracle_mod, x, op, tier="splitk", cluster_size=C)
+        check(rr, oracle_mod, x, op)
+        assert rr.last_tier() == ("splitk", 2)
+    xi = inputs.uniform_i32(64, 4096, inputs.seed_for(0, 3), "cuda")
+    for C in (1, 2):
+        check(rr, oracle_mod, xi, "sum", tier="splitk", cluster_size=C)
+
+
+def test_block_workload_full_size(rr, oracle_mod):
+    # 8192 x 8192; the kernel runs on the whole matrix, the oracle checks
+    # every 64th row plus the last one
+    from cluster_reductions_gb300 import inputs
+    idx = np.r_[np.arange(0, 8192, 64), 8191]
+    for oi, op in enumerate(["sum", "max", "min"]):
+        x = inputs.normal_f32(8192, 8192, inputs.seed_for(1, oi), "cuda")
+        got = to_np(rr.reduce(x, op))
+        assert rr.last_tier() == ("block", 1)
+        xs = to_np(x[torch.from_numpy(idx).cuda()])
+        ref = oracle_mod.reduce_rows(xs, op)
+        if op == "sum":
+            assert_sum_close(got[idx], ref, xs)
+        else:
+            assert_bits_equal(got[idx], ref)
+        del x
+    xi = inputs.uniform_i32(8192, 8192, inputs.seed_for(1, 3), "cuda")
+    got = to_np(rr.reduce(xi, "sum"))
+    # every row: int64 sums of |x| <= 2^15 over 8192 columns cannot wrap
+    assert_bits_equal(got, xi.to(torch.int64).sum(dim=1).to(torch.int32).cpu().numpy())
+    xs = to_np(xi[torch.from_numpy(idx).cuda()])
+    assert_bits_equal(got[idx], oracle_mod.reduce_rows(xs, "sum"))
+
+
+@pytest.mark.parametrize("cols,tier", [(32, "warp"), (8, "tiled")])
+def test_narrow_workloads_full_size(rr, oracle_mod, cols, tier):
+    from cluster_reductions_gb300 import inputs
+    rows = 1 << 20
+    for oi, op in enumerate(["sum", "max", "min"]):
+        x = inputs.normal_f32(rows, cols, inputs.seed_for(1, 4 + oi), "cuda")
+        got = to_np(rr.reduce(x, op))
+        assert rr.last_tier() == (tier, 1)
+        xh = to_np(x)
+        ref = oracle_mod.reduce_rows(xh, op)
+        if op == "sum":
+            assert_sum_close(got, ref, xh)
+        else:
+            assert_bits_equal(got, ref)
+
+
+def test_splitk_workload_full_size(rr, oracle_mod):
+    # 16 x 16,777,216 fp32, sum and max, cluster 2 / 4 / 8 / 16; all 16 rows
+    # against the oracle, every rank's copy bit-identical
+    from cluster_reductions_gb300 import inputs
+    rows, cols = 16, 1 << 24
+    x = inputs.normal_f32(rows, cols, inputs.seed_for(2, 0), "cuda")
+    xh = to_np(x)
+    for op in ("sum", "max"):
+        ref = oracle_mod.reduce_rows(xh, op)
+        for C in (2, 4, 8, 16):
+            rank_out = torch.empty(rows * C, dtype=torch.float32, device="cuda")
+            try:
+                got = to_np(rr.reduce(x, op, tier="splitk", cluster_size=C, rank_out=rank_out))
+            except rr.RRError as e:
+                if C == 16 and e.status == 2:
+                    continue   # cluster of 16 not schedulable on this device
+                raise
+            if op == "sum":
+                assert_sum_close(got, ref, xh)
+            else:
+                assert_bits_equal(got, ref)
+            ro = to_np(rank_out).reshape(rows, C)
+            assert (ro.view(np.uint32) == got.view(np.uint32)[:, None]).all()
+    got = rr.reduce(x, "sum")
+    assert rr.last_tier()[0] == "splitk"
+
+
+def test_splitk_bit_identical_100_runs(rr):
+    from cluster_reductions_gb300 import inputs
+    x = inputs.normal_f32(16, 1 << 22, inputs.seed_for(2, 1), "cuda")
+    for C in (2, 8):
+        first = rr.reduce(x, "sum", tier="splitk", cluster_size=C).clone()
+        outs = torch.empty((100, 16), dtype=torch.float32, device="cuda")
+        for i in range(100):
+            rr.reduce(x, "sum", tier="splitk", cluster_size=C, out=outs[i])
+        assert (outs.view(torch.int32) == first.view(torch.int32)).all()
+
+
+def test_argument_errors(rr):
+    x = torch.zeros((4, 8), device="cuda")
+    with pytest.raises(rr.RRError) as e:
+        rr.reduce(x, "sum", tier="warp", out=None, emit_tile_width=3)
+    assert e.value.status == 1
+    with pytest.raises(rr.RRError):
+        rr.reduce(torch.zeros((4, 64), device="cuda"), "sum", tier="warp")
+    with pytest.raises(rr.RRError):
+        rr.reduce(x, "sum", out=x.view(-1)[:4])   # out overlaps x
+    with pytest.raises(TypeError):
+        rr.reduce(torch.zeros((4, 8), device="cuda", dtype=torch.float64), "sum")

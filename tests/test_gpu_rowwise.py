@@ -1,0 +1,114 @@
+"""GPU parity of rr_softmax and rr_layernorm_stats against the fp64 oracle.
+
+Bars: softmax per element within relative 1e-5 (elements >= 1e-30); each
+row's sum within 1e-5 of 1; layernorm mean within 1e-5 * max(|mean|,
+||x_row||_2 / N), rstd within relative 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+from _util import assert_rel_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import cluster_reductions_gb300 as rr
+    rr.load()
+    return rr
+
+
+def _x(rows, cols, dtype, seed, std, offset=0):
+    from cluster_reductions_gb300 import inputs
+    base = inputs.normal_f32(1, rows * cols + offset, seed, "cuda", std).to(dtype)
+    return base.view(-1)[offset:].view(rows, cols)
+
+
+def check_softmax(rr, oracle_mod, x):
+    y = to_np(rr.softmax(x))
+    ref = oracle_mod.softmax(to_np(x))
+    assert_rel_close(y, ref, 1e-5, floor=1e-30, what="softmax")
+    np.testing.assert_allclose(y.astype(np.float64).sum(axis=1), 1.0, rtol=0, atol=1e-5)
+
+
+def check_lnstats(rr, oracle_mod, x, eps=1e-5):
+    mean, rstd = rr.layernorm_stats(x, eps)
+    xh = to_np(x)
+    rm, rv, rr_ = oracle_mod.layernorm_stats(xh, eps)
+    xf = x.to(torch.float64).cpu().numpy()
+    n = xf.shape[1]
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / n)
+    err = np.abs(to_np(mean).astype(np.float64) - rm)
+    assert (err <= bound).all(), f"mean: max err {err.max()} bound {bound[err.argmax()]}"
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="rstd")
+
+
+SHAPES = [(1, 1), (3, 7), (5, 8), (4, 64), (7, 100), (3, 1000), (2, 4096), (9, 4104),
+          (2, 16384), (2, 20000), (1, 70001)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_softmax_small(rr, oracle_mod, dtype):
+    for i, (rows, cols) in enumerate(SHAPES):
+        for offset in (0, 1):
+            check_softmax(rr, oracle_mod, _x(rows, cols, dtype, 200 + i, 3.0, offset))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_layernorm_small(rr, oracle_mod, dtype):
+    for i, (rows, cols) in enumerate(SHAPES):
+        for offset in (0, 3):
+            check_lnstats(rr, oracle_mod, _x(rows, cols, dtype, 300 + i, 1.0, offset))
+
+
+def test_special_rows(rr, oracle_mod):
+    x = torch.full((2, 4096), 3.25, dtype=torch.bfloat16, device="cuda")
+    y = to_np(rr.softmax(x))
+    np.testing.assert_allclose(y, 1.0 / 4096, rtol=1e-6)
+    a = 1.75
+    x = torch.tensor([a, -a] * 4096, dtype=torch.bfloat16, device="cuda").view(1, -1)
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    assert abs(float(mean[0])) <= 1e-6
+    assert abs(float(rstd[0]) - 1.0 / np.sqrt(a * a + 1e-5)) <= 1e-5 / a
+    x = torch.full((1, 8192), 2.5, dtype=torch.bfloat16, device="cuda")
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    assert float(mean[0]) == 2.5
+    assert abs(float(rstd[0]) - 1.0 / np.sqrt(1e-5)) <= 1e-5 / np.sqrt(1e-5)
+
+
+def test_softmax_workload_full_size(rr, oracle_mod):
+    # 32768 x 4096 bf16 = bf16_rn(3 * N(0,1)); sampled rows against the oracle,
+    # every row's sum against 1
+    from cluster_reductions_gb300 import inputs
+    x = inputs.normal_bf16(32768, 4096, inputs.seed_for(3, 0), "cuda", 3.0)
+    y = rr.softmax(x)
+    idx = torch.tensor(np.r_[np.arange(0, 32768, 256), 32767], device="cuda")
+    ref = oracle_mod.softmax(to_np(x[idx]))
+    assert_rel_close(to_np(y[idx]), ref, 1e-5, floor=1e-30, what="softmax")
+    s = y.to(torch.float64).sum(dim=1).cpu().numpy()
+    np.testing.assert_allclose(s, 1.0, rtol=0, atol=1e-5)
+
+
+def test_layernorm_workload_full_size(rr, oracle_mod):
+    from cluster_reductions_gb300 import inputs
+    x = inputs.normal_bf16(16384, 8192, inputs.seed_for(3, 1), "cuda")
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    idx = np.r_[np.arange(0, 16384, 128), 16383]
+    xs = x[torch.from_numpy(idx).cuda()]
+    rm, rv, rr_ = oracle_mod.layernorm_stats(to_np(xs), 1e-5)
+    xf = xs.to(torch.float64).cpu().numpy()
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / 8192)
+    assert (np.abs(to_np(mean)[idx] - rm) <= bound).all()
+    assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what="rstd")
+
+
+def test_argument_errors(rr):
+    with pytest.raises(rr.RRError):
+        rr.softmax(torch.zeros((3, 0), device="cuda"))
+    with pytest.raises(rr.RRError):
+        rr.layernorm_stats(torch.zeros((3, 0), device="cuda"))
+    with pytest.raises(rr.RRError):
+        rr.layernorm_stats(torch.zeros((3, 4), device="cuda"), eps=-1.0)
