@@ -34,15 +34,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link librr.so if any source is newer; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_lib: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile and link librr.so if any source is newer; returns its path.
+    `extra_flags` are added to every nvcc compile; `out_lib` / `build_dir`
+    place a variant build elsewhere."""
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "rr.h"))
     objs, procs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
             cmd = [nvcc()] + NVCC_FLAGS + list(extra_flags) + ["-c", s, "-o", o]
@@ -60,12 +63,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    if force or procs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or procs or _stale(out_lib, objs):
+        tmp = out_lib + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         subprocess.check_call(cmd)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <climits>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -34,6 +35,14 @@ cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 }  // namespace
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? RR_OK : RR_ERR_CUDA; }
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("RR_LOG");
+    return v && *v && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
 
 const DevInfo *current_device(int *status) {
   int dev = -1;
@@ -111,15 +120,13 @@ int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster, in
   } else if (cols <= 32) {
     tier = RR_TIER_WARP;
   } else if (rows >= 1 && rows < sm_count && cols >= 4096 && max_cluster >= 2) {
-    int64_t cap = sm_count / rows;
-    if (cap > 16) cap = 16;
-    if (cap > max_cluster) cap = max_cluster;
-    int c = 1;
-    while ((int64_t)c * 2 <= cap) c *= 2;
-    if (c >= 2) {
-      tier = RR_TIER_SPLITK;
-      C = c;
-    }
+    // the smallest power of two that puts at least one CTA on every SM,
+    // capped by 16 and by what the device can co-schedule
+    const int cap = max_cluster < 16 ? max_cluster : 16;
+    int c = 2;
+    while (c < cap && (int64_t)c * rows < sm_count) c *= 2;
+    tier = RR_TIER_SPLITK;
+    C = c;
   }
   *tier_out = tier;
   *cluster_out = C;
@@ -159,10 +166,9 @@ int rr_reduce_ex(const void *x, int64_t rows, int64_t cols, int op, int dtype, v
   if (tier == RR_TIER_SPLITK) {
     if (C == 0) {
       const int maxc = max_cluster_cached(op, dtype, *d);
-      int64_t cap = d->sm_count / (rows > 0 ? rows : 1);
-      if (cap > maxc) cap = maxc;
+      const int cap = maxc < 16 ? maxc : 16;
       C = 1;
-      while ((int64_t)C * 2 <= cap) C *= 2;
+      while (C < cap && (int64_t)C * rows < d->sm_count) C *= 2;
     }
     if (C > 1 && (!d->cluster_launch || max_cluster_cached(op, dtype, *d) < C))
       return RR_ERR_UNSUPPORTED;

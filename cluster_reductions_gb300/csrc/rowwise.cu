@@ -193,6 +193,8 @@ k_softmax_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols,
 // Layernorm statistics, register-resident row: mean = sum / cols (block
 // sum), var = sum (x - mean)^2 / cols (second block sum over the registers),
 // rstd = 1 / sqrt(var + eps).  Requires cols % EPV == 0 and x 16-byte aligned.
+// The next row's raw vectors are loaded as soon as the current row is
+// unpacked, so the loads stay in flight across the two block reductions.
 // ---------------------------------------------------------------------------
 template <int THREADS, int NV, class In>
 __global__ void __launch_bounds__(THREADS)
@@ -203,19 +205,29 @@ k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, floa
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
   const float inv_n = 1.0f / (float)cols;
+  uint4 raw[NV];
+  auto fetch = [&](int64_t r) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(x + r * (int64_t)cols);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx < nvec) raw[k] = ld_stream_u4(q + idx);
+    }
+  };
+  if ((int64_t)blockIdx.x < rows) fetch(blockIdx.x);
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const uint4 *q = reinterpret_cast<const uint4 *>(x + row * (int64_t)cols);
     float v[NV][EPV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int idx = k * THREADS + tid;
       if (idx < nvec) {
-        In::unpack(ld_stream_u4(q + idx), v[k]);
+        In::unpack(raw[k], v[k]);
       } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
       }
     }
+    if (row + gridDim.x < rows) fetch(row + gridDim.x);
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < NV; ++k)

@@ -18,8 +18,23 @@ constexpr int kErrTimeout = 1;
 //
 // max / min on fp32 are made independent of the fold order down to the bits:
 // max(+0,-0) = +0 and min(+0,-0) = -0 in either order, and a NaN operand
-// makes the result NaN (canonicalised to 0x7fc00000 by finalize()).
+// makes the result NaN (canonicalised to 0x7fc00000 by finalize()).  The
+// PTX max.NaN / min.NaN instructions have exactly these semantics on
+// sm_103a (checked on the device for every pair of +-0, +-1, +-inf and
+// NaNs, and by the signed-zero / NaN GPU tests), so each fold step is one
+// instruction.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 struct SumF32 {
   using T = float;
   static __device__ __forceinline__ T id() { return 0.0f; }
@@ -30,12 +45,7 @@ struct SumF32 {
 struct MaxF32 {
   using T = float;
   static __device__ __forceinline__ T id() { return __int_as_float(0xff800000); }
-  static __device__ __forceinline__ T f(T a, T b) {
-    T r = (a > b) ? a : b;
-    if (a == b) r = __int_as_float(__float_as_int(a) & __float_as_int(b));
-    if (a != a) r = a;
-    return r;
-  }
+  static __device__ __forceinline__ T f(T a, T b) { return max_nan(a, b); }
   static __device__ __forceinline__ T finalize(T a) {
     return (a != a) ? __int_as_float(0x7fc00000) : a;
   }
@@ -44,12 +54,7 @@ struct MaxF32 {
 struct MinF32 {
   using T = float;
   static __device__ __forceinline__ T id() { return __int_as_float(0x7f800000); }
-  static __device__ __forceinline__ T f(T a, T b) {
-    T r = (a < b) ? a : b;
-    if (a == b) r = __int_as_float(__float_as_int(a) | __float_as_int(b));
-    if (a != a) r = a;
-    return r;
-  }
+  static __device__ __forceinline__ T f(T a, T b) { return min_nan(a, b); }
   static __device__ __forceinline__ T finalize(T a) {
     return (a != a) ? __int_as_float(0x7fc00000) : a;
   }
@@ -347,6 +352,52 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src,
       : "memory");
 }
 
+// Arrive (release, cluster scope) on the mbarrier at `bar`'s offset in the
+// shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
+  const uint32_t a = map_peer(smem_u32(bar), rank);
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a)
+               : "memory");
+}
+// Relaxed remote arrive: orders nothing, only counts.  For signals whose
+// payload is already guaranteed by data dependences (e.g. "my loads of your
+// buffer have returned").
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint64_t *bar, uint32_t rank) {
+  const uint32_t a = map_peer(smem_u32(bar), rank);
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(a)
+               : "memory");
+}
+// Wait (acquire, cluster scope) for phase `parity` of a local mbarrier whose
+// arrivals come from peer CTAs.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded waits that give up at once after the CTA's first timeout (`dead`,
+// a shared flag), so that a broken protocol costs one budget, not one per
+// wait.
+__device__ __forceinline__ bool mbar_wait_or_die(uint64_t *bar, uint32_t parity, int64_t budget,
+                                                 volatile int *dead, bool cluster_scope) {
+  for (int64_t i = 0; i < budget; ++i) {
+    if (cluster_scope ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity))
+      return true;
+    if (*dead) return false;
+  }
+  *dead = 1;
+  return false;
+}
+// Barrier over the first `n` threads of the CTA (named barrier `id`, 1..15).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void set_error(int *err, int code) {
   if (err) atomicOr(err, code);
 }
@@ -354,6 +405,6 @@ __device__ __forceinline__ void set_error(int *err, int code) {
 // Polls of a bounded mbarrier wait before it gives up.  Each poll is a
 // try_wait that may itself suspend for a short, hardware-defined time, so
 // the budget is of the order of a second.
-constexpr int64_t kWaitBudget = int64_t(1) << 22;
+constexpr int64_t kWaitBudget = int64_t(1) << 20;
 
 }  // namespace rr

@@ -49,7 +49,11 @@ int launch_fill_selftest_values(void *vals, int64_t n, int dtype,
                                 uint64_t seed, cudaStream_t s);
 int launch_wait_timeout_probe(int64_t budget, cudaStream_t s, const DevInfo &d);
 
-// Maps a CUDA error to an rr_status, remembering the message.
+// Maps a CUDA error to an rr_status.
 int cuda_status(cudaError_t e);
+
+// True when the environment variable RR_LOG is set to a non-zero value:
+// launchers then print their tier and launch configuration to stderr.
+bool log_enabled();
 
 }  // namespace rr

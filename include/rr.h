@@ -101,8 +101,9 @@ typedef struct {
  * quiet NaN 0x7fc00000.  cols == 0 writes the identity (0, -inf / INT_MIN,
  * +inf / INT_MAX).  The tier is picked from rows, cols and the SM count:
  * cols <= 16 tiled; cols <= 32 warp; rows < SMs and cols >= 4096 split-K
- * with C the largest power of two <= min(16, SMs / rows) that the device
- * can co-schedule; otherwise block.
+ * with C the smallest power of two >= 2 such that rows * C >= SMs, capped
+ * at 16 and at the largest cluster the device can co-schedule; otherwise
+ * block.
  * Errors: RR_ERR_INVALID (null pointer with rows > 0, negative sizes, bad
  * op / dtype, overlap), RR_ERR_UNSUPPORTED, RR_ERR_CUDA.
  */

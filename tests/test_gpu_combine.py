@@ -1,10 +1,13 @@
 """GPU parity of rr_splitk_combine against the fp64 oracle: every output
-within 1 bf16 ulp of the oracle's correctly rounded bf16 value."""
+within 1 bf16 ulp of the oracle's correctly rounded bf16 value, except where
+sum_p w_p O_p cancels far below its summands; there the bound is one ulp
+plus the fp32 rounding bound of the weighted sum (see _util.combine_fp32_bound),
+and such outputs must stay rare."""
 import numpy as np
 import pytest
 import torch
 
-from _util import assert_bf16_ulp, to_np
+from _util import assert_bf16_ulp, assert_combine_close, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +30,9 @@ def run(rr, oracle_mod, P, rows, D, seed):
         if P > 8 and e.status == 2:
             pytest.skip(f"cluster of {P} CTAs not schedulable")
         raise
-    _, ref = oracle_mod.splitk_combine(to_np(O), to_np(m), to_np(l), s)
-    assert_bf16_ulp(to_np(out), ref)
+    Oh, mh, lh = to_np(O), to_np(m), to_np(l)
+    ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
+    assert_combine_close(to_np(out), ref64, ref, Oh, mh, lh, s)
 
 
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
@@ -47,8 +51,9 @@ def test_combine_workload_full_size(rr, oracle_mod, P):
     O, m, l, s = inputs.combine_partials(P, rows, D, inputs.seed_for(4, P), "cuda")
     out = rr.splitk_combine(O, m, l, s)
     idx = torch.arange(0, rows, 97, device="cuda")
-    _, ref = oracle_mod.splitk_combine(to_np(O[:, idx]), to_np(m[:, idx]), to_np(l[:, idx]), s)
-    assert_bf16_ulp(to_np(out[idx]), ref)
+    Oh, mh, lh = to_np(O[:, idx]), to_np(m[:, idx]), to_np(l[:, idx])
+    ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
+    assert_combine_close(to_np(out[idx]), ref64, ref, Oh, mh, lh, s)
 
 
 def test_combine_special_cases(rr, oracle_mod):
@@ -62,11 +67,12 @@ def test_combine_special_cases(rr, oracle_mod):
     out = rr.splitk_combine(O, m, l, s)
     got = to_np(out)
     assert (got[0] == 0).all() and (got[1] == 0).all()
-    _, ref = oracle_mod.splitk_combine(to_np(O), to_np(m), to_np(l), s)
-    assert_bf16_ulp(got, ref)
-    # P = 1: O / l
+    Oh, mh, lh = to_np(O), to_np(m), to_np(l)
+    ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
+    assert_combine_close(got, ref64, ref, Oh, mh, lh, s)
+    # P = 1: O / l, one fp32 division: within 1 ulp everywhere
     out1 = rr.splitk_combine(O[:1].contiguous(), m[:1].contiguous(), l[:1].contiguous(), s)
-    _, ref1 = oracle_mod.splitk_combine(to_np(O[:1]), to_np(m[:1]), to_np(l[:1]), s)
+    _, ref1 = oracle_mod.splitk_combine(Oh[:1], mh[:1], lh[:1], s)
     assert_bf16_ulp(to_np(out1)[2:], ref1[2:])
 
 
