@@ -235,13 +235,22 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_gbs(step_bytes: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank runs the full step (replicas, weak
+    scaling), so the job moves world * step_bytes * steps bytes in the
+    slowest rank's time."""
+    return world * step_bytes * steps / (max_ms / 1e3) / 1e9
 
 
 # --------------------------------------------------------------------- CPU oracle timing
@@ -407,7 +416,7 @@ def bench_ours(args):
              for i in range(nops)]
 
     step_bytes = sum(sum(algorithmic_bytes(spec)) for _, _, spec, _, _ in data)
-    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    value = job_gbs(step_bytes, args.steps, world, elapsed_ms)
     peak, peak_kind = read_peak()
 
     tiers = {}
@@ -520,7 +529,7 @@ def bench_e2e(args, rr, data, dev, stream, world):
     barrier(world)
     ms = max_over_ranks(a.elapsed_time(b), world)
     step_bytes = sum(sum(algorithmic_bytes(spec)) for _, _, spec, _, _ in data)
-    return {"value": round(world * step_bytes * steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(job_gbs(step_bytes, steps, world, ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(ms / steps, 3)}
 

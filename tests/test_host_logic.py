@@ -1,0 +1,136 @@
+"""Host-side checks that need no GPU: the C ABI exports every entry point
+include/rr.h declares, arguments are rejected before anything touches a
+device, the tier dispatch picks what the header documents, and the
+multi-rank timing of bench.py aggregates correctly over two gloo ranks."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from cluster_reductions_gb300 import build
+    build.build()
+    import cluster_reductions_gb300 as rr
+    return rr.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "rr.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int)\s*(rr_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("rr_reduce", "rr_reduce_ex", "rr_softmax", "rr_layernorm_stats",
+                 "rr_cluster_allreduce_selftest", "rr_splitk_combine", "rr_device_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from cluster_reductions_gb300._lib import SIGNATURES
+    for name in declared_functions():
+        assert hasattr(lib, name), f"librr.so does not export {name}"
+        assert name in SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_arguments_rejected_on_the_host(lib):
+    INVALID = 1
+    null = None
+    assert lib.rr_reduce(null, -1, 4, 0, 0, null, null) == INVALID
+    assert lib.rr_reduce(null, 4, -1, 0, 0, null, null) == INVALID
+    assert lib.rr_reduce(null, 4, 4, 7, 0, null, null) == INVALID      # bad op
+    assert lib.rr_reduce(null, 4, 4, 0, 2, null, null) == INVALID      # bf16 not reducible
+    assert lib.rr_reduce(null, 4, 4, 0, 0, null, null) == INVALID      # null pointers
+    assert lib.rr_reduce(null, 0, 4, 0, 0, null, null) == 0            # empty: no-op
+    buf = (ctypes.c_float * 64)()
+    p = ctypes.addressof(buf)
+    assert lib.rr_reduce(p, 4, 8, 0, 0, p + 16, null) == INVALID       # out overlaps x
+    from cluster_reductions_gb300._lib import rr_reduce_opts
+    bad = rr_reduce_opts(1, 0, 0, 0, None)                             # warp tier, 64 cols
+    assert lib.rr_reduce_ex(p, 1, 64, 0, 0, p, null, ctypes.byref(bad)) == INVALID
+    bad = rr_reduce_opts(4, 3, 0, 0, None)                             # cluster size 3
+    assert lib.rr_reduce_ex(p, 1, 8, 0, 0, p + 64, null, ctypes.byref(bad)) == INVALID
+    assert lib.rr_softmax(p, 2, 0, 2, p, null) == INVALID              # cols == 0
+    assert lib.rr_softmax(p, 2, 4, 0, p, null) == INVALID              # out overlaps x
+    assert lib.rr_layernorm_stats(p, 2, 4, 2, ctypes.c_float(-1.0), p, p, null) == INVALID
+    assert lib.rr_splitk_combine(p, p, p, 17, 4, 8, ctypes.c_float(1.0), p, null) == INVALID
+    assert lib.rr_splitk_combine(p, p, p, 2, 4, 0, ctypes.c_float(1.0), p, null) == INVALID
+    assert lib.rr_splitk_combine(p, p, p, 2, 4, 8, ctypes.c_float(float("inf")), p, null) == INVALID
+    assert lib.rr_cluster_allreduce(p, 1, 2, 3, 0, 0, 4, 0, 0, p, null, null) == INVALID
+    n = ctypes.c_int64(-1)
+    assert lib.rr_cluster_allreduce_selftest(2, 1, 0, 0, 0, 0, 1, null, ctypes.byref(n)) == INVALID
+    assert n.value == -1
+    assert lib.rr_test_wait_timeout(-1, null) == INVALID
+
+
+def test_status_strings(lib):
+    import cluster_reductions_gb300 as rr
+    assert rr._lib.status_string(0) == "ok"
+    assert rr._lib.status_string(4) == "device wait timed out"
+    assert rr._lib.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("rows,cols,sms,maxc,expect", [
+    (1 << 20, 8, 152, 16, ("tiled", 1)),
+    (1 << 20, 16, 152, 16, ("tiled", 1)),
+    (5, 0, 152, 16, ("tiled", 1)),
+    (1 << 20, 17, 152, 16, ("warp", 1)),
+    (1 << 20, 32, 152, 16, ("warp", 1)),
+    (8192, 8192, 152, 16, ("block", 1)),
+    (16, 1 << 24, 152, 16, ("splitk", 16)),
+    (16, 1 << 24, 152, 8, ("splitk", 8)),
+    (64, 4096, 152, 16, ("splitk", 4)),
+    (100, 5000, 152, 16, ("splitk", 2)),
+    (151, 4096, 152, 16, ("splitk", 2)),
+    (152, 4096, 152, 16, ("block", 1)),
+    (16, 4095, 152, 16, ("block", 1)),
+    (16, 1 << 24, 152, 1, ("block", 1)),   # no clusters: block tier
+    (1, 1 << 20, 148, 16, ("splitk", 16)),
+])
+def test_tier_dispatch(lib, rows, cols, sms, maxc, expect):
+    import cluster_reductions_gb300 as rr
+    assert rr.plan_reduce(rows, cols, sms, maxc) == expect
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    ms = [12.5, 20.0][rank]              # rank 1 is the slow one
+    slowest = bench.max_over_ranks(ms, world)
+    bench.barrier(world)
+    q.put((rank, slowest, bench.job_gbs(1_000_000_000, 10, world, slowest)))
+    dist.destroy_process_group()
+
+
+def test_two_rank_replica_timing_gloo():
+    import socket
+
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, slowest, gbs in got:
+        assert slowest == 20.0
+        # both replicas' bytes over the slowest rank's time: 2 * 10 GB / 20 ms
+        assert abs(gbs - 2 * 10 / 0.020) < 1e-9
