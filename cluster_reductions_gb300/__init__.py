@@ -159,6 +159,23 @@ def cluster_allreduce_selftest(cluster_size: int, width: int = 1, op="sum",
     return int(n.value)
 
 
+def cluster_allreduce_selftest_noalloc(cluster_size: int, width: int = 1, op="sum",
+                                       dtype: torch.dtype = torch.float32, iters: int = 1000,
+                                       two_slot: bool = True, seed: int = 1) -> int:
+    """rr_cluster_allreduce_selftest_noalloc (blocking): the same self-test as
+    cluster_allreduce_selftest, run out of the library's fixed device array
+    instead of freshly allocated memory, for callers that cannot allocate.
+    iters * 2 * cluster_size * width must be at most 262144."""
+    n = ctypes.c_int64(-1)
+    st = load().rr_cluster_allreduce_selftest_noalloc(int(cluster_size), int(width), _op(op),
+                                                      _DT[dtype], int(iters),
+                                                      1 if two_slot else 0, int(seed),
+                                                      _stream(), ctypes.byref(n))
+    if st not in (_lib.RR_OK, _lib.RR_ERR_MISMATCH):
+        check(st, "rr_cluster_allreduce_selftest_noalloc")
+    return int(n.value)
+
+
 def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2e: float, *,
                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """rr_splitk_combine: O [P, rows, D], m and l [P, rows] fp32 -> bf16 [rows, D]."""

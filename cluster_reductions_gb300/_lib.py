@@ -40,6 +40,9 @@ SIGNATURES = {
     "rr_cluster_allreduce_selftest": (_int, [_int, _int, _int, _int, _int, _int,
                                              ctypes.c_uint64, _vp,
                                              ctypes.POINTER(ctypes.c_int64)]),
+    "rr_cluster_allreduce_selftest_noalloc": (_int, [_int, _int, _int, _int, _int, _int,
+                                                     ctypes.c_uint64, _vp,
+                                                     ctypes.POINTER(ctypes.c_int64)]),
     "rr_splitk_combine": (_int, [_vp, _vp, _vp, _int, _i64, _int, _f32, _vp, _vp]),
     "rr_device_status": (_int, [_vp]),
     "rr_last_tier": (_int, []),

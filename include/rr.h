@@ -179,6 +179,32 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op,
                                   int64_t *mismatches_out);
 
 /*
+ * rr_cluster_allreduce_selftest_noalloc -- the same blocking self-test as
+ * rr_cluster_allreduce_selftest (same arguments, same checks, same result),
+ * but it allocates no device memory: no cudaMalloc, no cudaFree, no
+ * allocating library call.  The pages have no counterpart of this entry
+ * point; it exists for callers that cannot allocate, such as a serving
+ * process whose memory pool already holds the whole device, or one that
+ * must not risk the implicit device synchronisation of cudaMalloc/cudaFree
+ * between its own kernels.
+ *   Scratch: a fixed device array inside librr.so, 2 * 2^18 32-bit values
+ *   plus a counter (about 2 MiB).  Every GPU that loads the library holds it
+ *   until the process exits.  iters * 2 * cluster_size * width must not
+ *   exceed 2^18 (262144); larger requests return RR_ERR_INVALID.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.  Each call resets the counter it needs; the array keeps
+ *   the last call's other contents.  All calls share the one array, so calls
+ *   that overlap on the GPU (other streams, other host threads) race.
+ * Returns RR_OK, RR_ERR_MISMATCH, RR_ERR_INVALID, RR_ERR_UNSUPPORTED or
+ * RR_ERR_CUDA.
+ */
+int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width, int op,
+                                          int dtype, int iters, int two_slot,
+                                          uint64_t seed, void *stream,
+                                          int64_t *mismatches_out);
+
+/*
  * rr_splitk_combine -- split-K attention-output combine ([FA]).
  *   O       device fp32 [P][rows][D] partial outputs (unnormalised).
  *   m, l    device fp32 [P][rows] per-partition row max (raw scores) and

@@ -66,6 +66,8 @@ def test_arguments_rejected_on_the_host(lib):
     assert lib.rr_cluster_allreduce(p, 1, 2, 3, 0, 0, 4, 0, 0, p, null, null) == INVALID
     n = ctypes.c_int64(-1)
     assert lib.rr_cluster_allreduce_selftest(2, 1, 0, 0, 0, 0, 1, null, ctypes.byref(n)) == INVALID
+    assert lib.rr_cluster_allreduce_selftest_noalloc(16, 8, 0, 0, 1025, 1, 1, null,
+                                                     ctypes.byref(n)) == INVALID
     assert n.value == -1
     assert lib.rr_test_wait_timeout(-1, null) == INVALID
 
