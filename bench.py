@@ -352,18 +352,25 @@ def calibrate_oracle(target_s: float, threads: int):
 
 
 def cpu_baseline(target_s: float):
+    """Oracle throughput on a bounded sample: `scale` of every operation's
+    rows, repeated until about target_s seconds of CPU work have run (one
+    pass of the whole workload is faster than that on a many-core host)."""
     threads = os.cpu_count() or 1
     scale = calibrate_oracle(target_s, threads)
     plan = oracle_sample_plan(scale)
     data = oracle_inputs(plan)
+    passes, dt = 0, 0.0
     t0 = time.perf_counter()
-    run_oracle_step(data, threads)
-    dt = time.perf_counter() - t0
+    while passes == 0 or dt < target_s:
+        run_oracle_step(data, threads)
+        passes += 1
+        dt = time.perf_counter() - t0
     b = sample_bytes(data)
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    return {"value": round(b * passes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
             "sample": f"every operation of the step on {scale:.2e} of its rows "
-                      f"({b / 1e6:.1f} MB algorithmic), fp64 C oracle, {threads} host threads, "
-                      f"{dt:.2f} s"}
+                      f"({b / 1e6:.1f} MB algorithmic per pass), {passes} passes, fp64 C oracle, "
+                      f"{threads} host threads, {dt:.2f} s"}
 
 
 # --------------------------------------------------------------------- our arm

@@ -176,9 +176,14 @@ def cluster_allreduce_selftest_noalloc(cluster_size: int, width: int = 1, op="su
     return int(n.value)
 
 
+COMBINE_MODES = {None: 0, "auto": 0, "pull": 1, "push": 2, "generic": 3, "direct": 4}
+
+
 def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2e: float, *,
-                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """rr_splitk_combine: O [P, rows, D], m and l [P, rows] fp32 -> bf16 [rows, D]."""
+                   out: Optional[torch.Tensor] = None, mode=None) -> torch.Tensor:
+    """rr_splitk_combine / rr_splitk_combine_ex: O [P, rows, D], m and l
+    [P, rows] fp32 -> bf16 [rows, D].  mode: None/"auto", "pull", "push" or
+    "generic" (see rr_combine_mode in rr.h)."""
     if O.dim() != 3 or m.dim() != 2 or l.dim() != 2:
         raise ValueError("O must be [P, rows, D], m and l [P, rows]")
     P, rows, D = O.shape
@@ -190,9 +195,14 @@ def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2
     Od, md, ld = _to_device(O), _to_device(m), _to_device(l)
     o = out if out is not None else torch.empty((rows, D), dtype=torch.bfloat16,
                                                 device=Od.device)
-    check(load().rr_splitk_combine(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
-                                   float(scale_log2e), _ptr(o), _stream()),
-          "rr_splitk_combine")
+    if mode is None:
+        st = load().rr_splitk_combine(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
+                                      float(scale_log2e), _ptr(o), _stream())
+    else:
+        st = load().rr_splitk_combine_ex(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
+                                         float(scale_log2e), _ptr(o), _stream(),
+                                         COMBINE_MODES[mode])
+    check(st, "rr_splitk_combine")
     return _to_host(o, O)
 
 

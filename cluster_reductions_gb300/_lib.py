@@ -44,6 +44,7 @@ SIGNATURES = {
                                                      ctypes.c_uint64, _vp,
                                                      ctypes.POINTER(ctypes.c_int64)]),
     "rr_splitk_combine": (_int, [_vp, _vp, _vp, _int, _i64, _int, _f32, _vp, _vp]),
+    "rr_splitk_combine_ex": (_int, [_vp, _vp, _vp, _int, _i64, _int, _f32, _vp, _vp, _int]),
     "rr_device_status": (_int, [_vp]),
     "rr_last_tier": (_int, []),
     "rr_status_string": (ctypes.c_char_p, [_int]),

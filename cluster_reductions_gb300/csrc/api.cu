@@ -301,7 +301,14 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op, int dtype
 
 int rr_splitk_combine(const float *O, const float *m, const float *l, int P, int64_t rows, int D,
                       float scale_log2e, uint16_t *out_bf16, void *stream) {
+  return rr_splitk_combine_ex(O, m, l, P, rows, D, scale_log2e, out_bf16, stream,
+                              RR_COMBINE_AUTO);
+}
+
+int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P, int64_t rows,
+                         int D, float scale_log2e, uint16_t *out_bf16, void *stream, int mode) {
   if (P < 1 || P > 16 || rows < 0 || D < 1 || D > 1024) return RR_ERR_INVALID;
+  if (mode < RR_COMBINE_AUTO || mode > RR_COMBINE_DIRECT) return RR_ERR_INVALID;
   if (!std::isfinite(scale_log2e)) return RR_ERR_INVALID;
   if (rows == 0) return RR_OK;
   if (!O || !m || !l || !out_bf16) return RR_ERR_INVALID;
@@ -317,7 +324,7 @@ int rr_splitk_combine(const float *O, const float *m, const float *l, int P, int
   const DevInfo *d = current_device(&st);
   if (!d) return st;
   if (P > 1 && !d->cluster_launch) return RR_ERR_UNSUPPORTED;
-  return launch_combine(O, m, l, P, rows, D, scale_log2e, out_bf16, as_stream(stream), *d);
+  return launch_combine(O, m, l, P, rows, D, scale_log2e, out_bf16, as_stream(stream), *d, mode);
 }
 
 int rr_device_status(void *stream) {

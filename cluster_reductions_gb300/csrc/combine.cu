@@ -47,7 +47,7 @@ constexpr int kCombThreads = 128;  // generic path
 #define RR_COMBINE_CONSUMERS 128
 #endif
 constexpr int kTileBytes = RR_COMBINE_TILE_BYTES;  // staged O bytes per CTA and slot
-constexpr int kStages = RR_COMBINE_STAGES;         // staging slots per CTA
+constexpr int kStages = RR_COMBINE_STAGES;         // staging slots per CTA (cluster variants)
 constexpr int kCons = RR_COMBINE_CONSUMERS;        // consumer threads (the first warps)
 constexpr int kPipeThreads = kCons + 64;           // + producer warp + publisher warp
 
@@ -239,6 +239,301 @@ k_combine_pipe(const float *__restrict__ O, const float *__restrict__ m,
   cluster_sync();
 }
 
+// ---------------------------------------------------------------------------
+// Push variant of the fast path: the reduce-scatter is done by the bulk copy
+// engine instead of per-thread DSMEM loads, and the scatter is along rows
+// (the slice of a row-major tile that a peer owns is then contiguous).
+// CTA p owns rows [p*TS, (p+1)*TS) of every tile, TS = TR / P.  Per tile:
+//   producer  stages O_p[tile, :] and the (m, l) of all P partitions
+//             (full[s]);
+//   pusher    once full[s] completes, copies slice q of its staged tile into
+//             CTA q's receive area recv[s][p] for every q (itself included),
+//             each copy completing on CTA q's rfull[s] (P arrivals + bytes);
+//   consumers once rfull[s] completes, fold their TS rows over the P
+//             received partials from local shared memory in rank order,
+//             store bf16, then tell every sender (relaxed remote arrive on
+//             its cons[s]) that its slice has been used.
+// cons[s] completing at a CTA means every destination has received and used
+// what it pushed from slot s, so both its staged tile and the peers'
+// receive areas for slot s may be refilled.
+// Slot layout: stage TR*D | recv P*TS*D | m_all P*TRp | l_all P*TRp.
+template <int P>
+__global__ void __launch_bounds__(kPipeThreads)
+k_combine_push(const float *__restrict__ O, const float *__restrict__ m,
+               const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
+               uint16_t *__restrict__ out, int ml_bulk, int *err) {
+  extern __shared__ __align__(128) float dyn[];
+  __shared__ __align__(8) uint64_t full[kStages], rfull[kStages], cons[kStages];
+  __shared__ int dead;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t p = cluster_ctarank();
+  const int64_t cl = cluster_id_x(), ncl = cluster_nid_x();
+  const int64_t ntiles = (rows + TR - 1) / TR;
+  const int TS = TR / P;
+  const int TRp = (TR + 3) & ~3;
+  const int slot_floats = 2 * TR * D + 2 * P * TRp;
+  float *sw = dyn + kStages * slot_floats;  // [TS][P]
+  float *sinv = sw + TS * P;                // [TS]
+  if (tid == 0) {
+    dead = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&rfull[s], P);
+      mbar_init(&cons[s], P);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync();  // every peer's barriers exist before any remote operation
+
+  const int64_t K = (cl < ntiles) ? (ntiles - 1 - cl) / ncl + 1 : 0;
+  auto tile_rows_of = [&](int64_t k) {
+    const int64_t row0 = (cl + k * ncl) * TR;
+    return (int)((rows - row0) < TR ? (rows - row0) : TR);
+  };
+  auto slice_rows = [&](int nr, int q) {
+    const int a = q * TS, b = a + TS < nr ? a + TS : nr;
+    return b > a ? b - a : 0;
+  };
+  if (tid >= kCons + 32) {
+    // ---- pusher warp (lane q serves destination q)
+    for (int64_t k = 0; k < K; ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t par = (uint32_t)(k / kStages) & 1u;
+      const int nr = tile_rows_of(k);
+      float *stage = dyn + s * slot_floats;
+      float *recv = stage + TR * D;
+      if (!mbar_wait_or_die(&full[s], par, kWaitBudget, &dead, false)) set_error(err, kErrTimeout);
+      __syncwarp();
+      if (lane < P) {
+        const int q = lane;
+        const uint32_t bytes = (uint32_t)slice_rows(nr, q) * (uint32_t)D * 4u;
+        mbar_arrive_expect_tx_remote(&rfull[s], (uint32_t)q, bytes);
+        if (bytes)
+          bulk_s2peer(recv + p * TS * D, stage + q * TS * D, bytes, &rfull[s], (uint32_t)q);
+      }
+      __syncwarp();
+    }
+  } else if (tid >= kCons) {
+    // ---- producer warp
+    for (int64_t k = 0; k < K; ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t r = (uint32_t)(k / kStages);
+      const int64_t row0 = (cl + k * ncl) * TR;
+      const int nr = tile_rows_of(k);
+      float *stage = dyn + s * slot_floats;
+      float *mall = stage + 2 * TR * D, *lall = mall + P * TRp;
+      if (k >= kStages && !mbar_wait_or_die(&cons[s], (r - 1) & 1u, kWaitBudget, &dead, true))
+        set_error(err, kErrTimeout);
+      if (!ml_bulk) {
+        for (int j = lane; j < P * nr; j += 32) {
+          const int q = j / nr, i = j - q * nr;
+          mall[q * TRp + i] = __ldg(m + (int64_t)q * rows + row0 + i);
+          lall[q * TRp + i] = __ldg(l + (int64_t)q * rows + row0 + i);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        const uint32_t ob = (uint32_t)nr * (uint32_t)D * 4u;
+        const uint32_t mb = ml_bulk ? (uint32_t)nr * 4u : 0u;
+        mbar_arrive_expect_tx(&full[s], ob + 2u * P * mb);
+        bulk_g2s(stage, O + ((int64_t)p * rows + row0) * D, ob, &full[s]);
+        if (ml_bulk) {
+          for (int q = 0; q < P; ++q) {
+            bulk_g2s(mall + q * TRp, m + (int64_t)q * rows + row0, mb, &full[s]);
+            bulk_g2s(lall + q * TRp, l + (int64_t)q * rows + row0, mb, &full[s]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---- consumers: this CTA's TS rows of each tile
+    for (int64_t k = 0; k < K; ++k) {
+      const int s = (int)(k % kStages);
+      const uint32_t par = (uint32_t)(k / kStages) & 1u;
+      const int64_t row0 = (cl + k * ncl) * TR;
+      const int nr = tile_rows_of(k);
+      const int ns = slice_rows(nr, (int)p);
+      const float *stage = dyn + s * slot_floats;
+      const float *recv = stage + TR * D;
+      const float *mall = stage + 2 * TR * D, *lall = mall + P * TRp;
+      // rfull[s] includes this CTA's own push, issued after its full[s]
+      // completed, so the staged (m, l) are covered too
+      if (!mbar_wait_or_die(&rfull[s], par, kWaitBudget, &dead, true)) set_error(err, kErrTimeout);
+      const int i0 = (int)p * TS;
+      for (int i = tid; i < ns; i += kCons) {
+        float mq[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q) mq[q] = mall[q * TRp + i0 + i];
+        float M = mq[0];
+#pragma unroll
+        for (int q = 1; q < P; ++q) M = fmaxf(M, mq[q]);
+        float L = 0.0f;
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const float w = (M == -INFINITY) ? 0.0f : ex2f_approx((mq[q] - M) * scale_log2e);
+          sw[i * P + q] = w;
+          L = fmaf(w, lall[q * TRp + i0 + i], L);
+        }
+        sinv[i] = (M == -INFINITY || L == 0.0f) ? 0.0f : 1.0f / L;
+      }
+      named_sync(1, kCons);
+      const int cpr = D >> 2;
+      for (int c = tid; c < ns * cpr; c += kCons) {
+        const int i = c / cpr, col = 4 * (c - i * cpr);
+        float4 v[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q)
+          v[q] = *reinterpret_cast<const float4 *>(recv + (q * TS + i) * D + col);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const float w = sw[i * P + q];
+          acc.x = fmaf(w, v[q].x, acc.x);
+          acc.y = fmaf(w, v[q].y, acc.y);
+          acc.z = fmaf(w, v[q].z, acc.z);
+          acc.w = fmaf(w, v[q].w, acc.w);
+        }
+        const float inv = sinv[i];
+        uint2 pk = make_uint2(0u, 0u);
+        if (inv != 0.0f) {
+          pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        }
+        *reinterpret_cast<uint2 *>(out + (row0 + i0 + i) * D + col) = pk;
+      }
+      named_sync(1, kCons);
+      if (tid < P) mbar_arrive_remote_relaxed(&cons[s], (uint32_t)tid);
+    }
+  }
+  __syncthreads();
+  cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// Direct variant: no exchange between CTAs at all.  Each CTA streams tiles
+// of TR rows, staging the rows of all P partitions (P contiguous 1-D bulk
+// copies; the (m, l) by the producer warp) through a ring of S slots,
+// then folds every row over the P partials in rank order from local shared
+// memory.  DRAM traffic is the same as the cluster variants' (each partial
+// byte is read once); what it drops is the per-tile cluster synchronisation.
+// Slot layout: O_all P*TR*D | m_all P*TRp | l_all P*TRp.
+//   full[s]  (local, 1 arrival + tx)  the slot's copies and loads landed;
+//   free[s]  (local, 1 arrival)       the consumers are done with the slot.
+template <int P, int S>
+__global__ void __launch_bounds__(kPipeThreads)
+k_combine_direct(const float *__restrict__ O, const float *__restrict__ m,
+                 const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
+                 uint16_t *__restrict__ out, int *err) {
+  extern __shared__ __align__(128) float dyn[];
+  __shared__ __align__(8) uint64_t full[S], freed[S];
+  __shared__ int dead;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t ntiles = (rows + TR - 1) / TR;
+  const int TRp = (TR + 3) & ~3;
+  const int slot_floats = P * TR * D + 2 * P * TRp;
+  float *sw = dyn + S * slot_floats;  // [TR][P]
+  float *sinv = sw + TR * P;                // [TR]
+  if (tid == 0) {
+    dead = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&freed[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t K = ((int64_t)blockIdx.x < ntiles) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (tid >= kCons + 32) {
+    // idle warp (keeps the block shape of the cluster variants)
+  } else if (tid >= kCons) {
+    // ---- producer warp
+    for (int64_t k = 0; k < K; ++k) {
+      const int s = (int)(k % S);
+      const uint32_t r = (uint32_t)(k / S);
+      const int64_t row0 = ((int64_t)blockIdx.x + k * gridDim.x) * TR;
+      const int nr = (int)((rows - row0) < TR ? (rows - row0) : TR);
+      float *so = dyn + s * slot_floats;
+      float *mall = so + P * TR * D, *lall = mall + P * TRp;
+      if (k >= S &&
+          !mbar_wait_or_die(&freed[s], (r - 1) & 1u, kWaitBudget, &dead, false))
+        set_error(err, kErrTimeout);
+      // arm the byte count and start the big copies first, then fetch the
+      // (m, l) while they fly; the arrival releases the (m, l) stores
+      if (lane == 0) {
+        const uint32_t ob = (uint32_t)nr * (uint32_t)D * 4u;
+        mbar_expect_tx(&full[s], ob * P);
+        for (int q = 0; q < P; ++q)
+          bulk_g2s(so + q * TR * D, O + ((int64_t)q * rows + row0) * D, ob, &full[s]);
+      }
+      for (int j = lane; j < P * nr; j += 32) {
+        const int q = j / nr, i = j - q * nr;
+        mall[q * TRp + i] = __ldg(m + (int64_t)q * rows + row0 + i);
+        lall[q * TRp + i] = __ldg(l + (int64_t)q * rows + row0 + i);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+      __syncwarp();
+    }
+  } else {
+    // ---- consumers
+    for (int64_t k = 0; k < K; ++k) {
+      const int s = (int)(k % S);
+      const uint32_t par = (uint32_t)(k / S) & 1u;
+      const int64_t row0 = ((int64_t)blockIdx.x + k * gridDim.x) * TR;
+      const int nr = (int)((rows - row0) < TR ? (rows - row0) : TR);
+      const float *so = dyn + s * slot_floats;
+      const float *mall = so + P * TR * D, *lall = mall + P * TRp;
+      if (!mbar_wait_or_die(&full[s], par, kWaitBudget, &dead, false)) set_error(err, kErrTimeout);
+      for (int i = tid; i < nr; i += kCons) {
+        float mq[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q) mq[q] = mall[q * TRp + i];
+        float M = mq[0];
+#pragma unroll
+        for (int q = 1; q < P; ++q) M = fmaxf(M, mq[q]);
+        float L = 0.0f;
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const float w = (M == -INFINITY) ? 0.0f : ex2f_approx((mq[q] - M) * scale_log2e);
+          sw[i * P + q] = w;
+          L = fmaf(w, lall[q * TRp + i], L);
+        }
+        sinv[i] = (M == -INFINITY || L == 0.0f) ? 0.0f : 1.0f / L;
+      }
+      named_sync(1, kCons);
+      const int cpr = D >> 2;
+      for (int c = tid; c < nr * cpr; c += kCons) {
+        const int i = c / cpr, col = 4 * (c - i * cpr);
+        float4 v[P];
+#pragma unroll
+        for (int q = 0; q < P; ++q)
+          v[q] = *reinterpret_cast<const float4 *>(so + (q * TR + i) * D + col);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const float w = sw[i * P + q];
+          acc.x = fmaf(w, v[q].x, acc.x);
+          acc.y = fmaf(w, v[q].y, acc.y);
+          acc.z = fmaf(w, v[q].z, acc.z);
+          acc.w = fmaf(w, v[q].w, acc.w);
+        }
+        const float inv = sinv[i];
+        uint2 pk = make_uint2(0u, 0u);
+        if (inv != 0.0f) {
+          pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        }
+        *reinterpret_cast<uint2 *>(out + (row0 + i) * D + col) = pk;
+      }
+      named_sync(1, kCons);
+      if (tid == 0) mbar_arrive(&freed[s]);
+    }
+  }
+  __syncthreads();
+}
+
 // Generic path: one tile per cluster, plain loads, per-element bands.
 __global__ void __launch_bounds__(kCombThreads)
 k_combine_generic(const float *__restrict__ O, const float *__restrict__ m,
@@ -365,6 +660,84 @@ int launch_pipe(const float *O, const float *m, const float *l, int64_t rows, in
                                         ml_bulk, d.err_word));
 }
 
+template <int P>
+int launch_push(const float *O, const float *m, const float *l, int64_t rows, int D,
+                float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d) {
+  // tile rows: a multiple of max(P, 4), at least P (a tile may overrun rows)
+  const int unit = P > 4 ? P : 4;
+  int TR = kTileBytes / (D * 4);
+  TR = (TR / unit) * unit;
+  if (TR < unit) TR = unit;
+  const int TS = TR / P;
+  const size_t TRp = ((size_t)TR + 3) & ~(size_t)3;
+  const size_t smem = sizeof(float) * ((size_t)kStages * (2 * (size_t)TR * D + 2 * P * TRp) +
+                                       (size_t)TS * P + (size_t)TS);
+  auto kern = k_combine_push<P>;
+  int st = prepare(kern, P, smem);
+  if (st != RR_OK) return st;
+  const int64_t ntiles = (rows + TR - 1) / TR;
+  cudaLaunchAttribute attr[1];
+  int clusters = 1;
+  {
+    cudaLaunchConfig_t q = cluster_cfg(1, P, smem, s, attr, kPipeThreads);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
+      cudaGetLastError();
+      return RR_ERR_UNSUPPORTED;
+    }
+    if (n < 1) return RR_ERR_UNSUPPORTED;
+    clusters = n;
+  }
+  if ((int64_t)clusters > ntiles) clusters = (int)ntiles;
+  const int ml_bulk = (rows % 4 == 0) && ((uintptr_t)m % 16 == 0) && ((uintptr_t)l % 16 == 0);
+  if (log_enabled())
+    std::fprintf(stderr, "rr: combine push P=%d D=%d TR=%d stages=%d clusters=%d smem=%zu ml_bulk=%d\n",
+                 P, D, TR, kStages, clusters, smem, ml_bulk);
+  cudaLaunchConfig_t cfg = cluster_cfg(clusters, P, smem, s, attr, kPipeThreads);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, O, m, l, rows, D, TR, scale_log2e, out,
+                                        ml_bulk, d.err_word));
+}
+
+// Direct variant geometry per P, from a sweep on GB300 (131072 x 128 rows):
+// one slot of 16 KiB per CTA (overlap comes from the other CTAs on the SM)
+// up to P = 8, two slots of 32 KiB for P = 16.
+template <int P> struct DirectGeom {
+  static constexpr int S = (P <= 8) ? 1 : 2;
+  static constexpr int bytes = (P <= 8) ? 16384 : 32768;
+};
+
+template <int P>
+int launch_direct(const float *O, const float *m, const float *l, int64_t rows, int D,
+                  float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d) {
+  constexpr int S = DirectGeom<P>::S;
+  int TR = DirectGeom<P>::bytes / (P * D * 4);
+  if (TR < 1) TR = 1;
+  if ((int64_t)TR > rows) TR = (int)rows;
+  const size_t TRp = ((size_t)TR + 3) & ~(size_t)3;
+  const size_t smem = sizeof(float) * ((size_t)S * ((size_t)P * TR * D + 2 * P * TRp) +
+                                       (size_t)TR * P + (size_t)TR);
+  auto kern = k_combine_direct<P, S>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kPipeThreads, smem) != cudaSuccess ||
+      nb < 1) {
+    cudaGetLastError();
+    return RR_ERR_UNSUPPORTED;
+  }
+  const int64_t ntiles = (rows + TR - 1) / TR;
+  int64_t grid = (int64_t)nb * d.sm_count;
+  if (grid > ntiles) grid = ntiles;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: combine direct P=%d D=%d TR=%d stages=%d ctas=%lld smem=%zu\n", P, D,
+                 TR, S, (long long)grid, smem);
+  kern<<<(unsigned)grid, kPipeThreads, smem, s>>>(O, m, l, rows, D, TR, scale_log2e, out,
+                                                  d.err_word);
+  return cuda_status(cudaGetLastError());
+}
+
 int launch_generic(const float *O, const float *m, const float *l, int P, int64_t rows, int D,
                    float scale_log2e, uint16_t *out, cudaStream_t s) {
   const int TR = tile_rows(rows, D);
@@ -393,10 +766,37 @@ int launch_generic(const float *O, const float *m, const float *l, int P, int64_
 }  // namespace
 
 int launch_combine(const float *O, const float *m, const float *l, int P, int64_t rows, int D,
-                   float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d) {
-  const bool fast = (P == 1 || P == 2 || P == 4 || P == 8 || P == 16) && D % (4 * P) == 0 &&
-                    ((uintptr_t)O % 16 == 0) && ((uintptr_t)out % 8 == 0);
-  if (fast) {
+                   float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d, int mode) {
+  const bool pow2 = (P == 1 || P == 2 || P == 4 || P == 8 || P == 16);
+  const bool aligned = ((uintptr_t)O % 16 == 0) && ((uintptr_t)out % 8 == 0);
+  const bool pull_ok = pow2 && D % (4 * P) == 0 && aligned;
+  const bool push_ok = pow2 && D % 4 == 0 && aligned && D <= 256;
+  const bool direct_ok = pow2 && D % 4 == 0 && aligned && (size_t)2 * P * D * 4 <= (size_t)96 * 1024;
+  if (mode == RR_COMBINE_AUTO)
+    mode = direct_ok ? RR_COMBINE_DIRECT
+                     : (push_ok ? RR_COMBINE_PUSH : (pull_ok ? RR_COMBINE_PULL : RR_COMBINE_GENERIC));
+  if (mode == RR_COMBINE_DIRECT) {
+    if (!direct_ok) return RR_ERR_UNSUPPORTED;
+    switch (P) {
+      case 1: return launch_direct<1>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 2: return launch_direct<2>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 4: return launch_direct<4>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 8: return launch_direct<8>(O, m, l, rows, D, scale_log2e, out, s, d);
+      default: return launch_direct<16>(O, m, l, rows, D, scale_log2e, out, s, d);
+    }
+  }
+  if (mode == RR_COMBINE_PUSH) {
+    if (!push_ok) return RR_ERR_UNSUPPORTED;
+    switch (P) {
+      case 1: return launch_push<1>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 2: return launch_push<2>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 4: return launch_push<4>(O, m, l, rows, D, scale_log2e, out, s, d);
+      case 8: return launch_push<8>(O, m, l, rows, D, scale_log2e, out, s, d);
+      default: return launch_push<16>(O, m, l, rows, D, scale_log2e, out, s, d);
+    }
+  }
+  if (mode == RR_COMBINE_PULL) {
+    if (!pull_ok) return RR_ERR_UNSUPPORTED;
     switch (P) {
       case 1: return launch_pipe<1>(O, m, l, rows, D, scale_log2e, out, s, d);
       case 2: return launch_pipe<2>(O, m, l, rows, D, scale_log2e, out, s, d);

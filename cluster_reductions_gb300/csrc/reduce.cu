@@ -16,15 +16,36 @@
 namespace rr {
 namespace {
 
-// Geometry of the tiers.
-constexpr int kBlockThreads = 256, kBlockUnroll = 8;
+// Geometry of the tiers (each can be overridden at build time).
+#ifndef RR_BLOCK_THREADS
+#define RR_BLOCK_THREADS 256
+#endif
+#ifndef RR_BLOCK_UNROLL
+#define RR_BLOCK_UNROLL 8
+#endif
+#ifndef RR_WARP_UNROLL
+#define RR_WARP_UNROLL 8
+#endif
+#ifndef RR_TILED_VECS
+#define RR_TILED_VECS 8
+#endif
+#ifndef RR_TILED_UNROLL_MAX
+#define RR_TILED_UNROLL_MAX 4
+#endif
+#ifndef RR_GRID_CAP
+#define RR_GRID_CAP 1
+#endif
+constexpr int kBlockThreads = RR_BLOCK_THREADS, kBlockUnroll = RR_BLOCK_UNROLL;
 constexpr int kSplitThreads = 512, kSplitUnroll = 8;
-constexpr int kWarpBlock = 256, kWarpUnroll = 8;
+constexpr int kWarpBlock = 256, kWarpUnroll = RR_WARP_UNROLL;
 constexpr int kTiledBlock = 256;
 // Tiled tier: groups of rows each thread keeps in flight, so that a thread
-// holds about 8 vectors (NV vectors per row, EWT rows per group).
+// holds about RR_TILED_VECS vectors (NV vectors per row, EWT rows per group).
 __host__ __device__ constexpr int tiled_unroll(int nv, int ewt) {
-  return 8 / (nv * ewt) < 1 ? 1 : (8 / (nv * ewt) > 4 ? 4 : 8 / (nv * ewt));
+  return RR_TILED_VECS / (nv * ewt) < 1
+             ? 1
+             : (RR_TILED_VECS / (nv * ewt) > RR_TILED_UNROLL_MAX ? RR_TILED_UNROLL_MAX
+                                                                : RR_TILED_VECS / (nv * ewt));
 }
 
 // ---------------------------------------------------------------------------
@@ -294,11 +315,16 @@ k_splitk(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
 // ---------------------------------------------------------------------------
 template <class K>
 int grid_for(K kernel, int threads, int64_t work_blocks, const DevInfo &d, int smem = 0) {
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess || nb < 1)
-    nb = 1;
-  const int64_t cap = (int64_t)nb * d.sm_count;
-  int64_t g = work_blocks < cap ? work_blocks : cap;
+  int64_t g = work_blocks;
+  if (RR_GRID_CAP) {  // persistent: at most one wave of resident CTAs
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess ||
+        nb < 1)
+      nb = 1;
+    const int64_t cap = (int64_t)nb * d.sm_count;
+    if (g > cap) g = cap;
+  }
+  if (g > 0x7fffffffLL) g = 0x7fffffffLL;
   return (int)(g < 1 ? 1 : g);
 }
 

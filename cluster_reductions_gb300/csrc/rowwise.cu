@@ -14,7 +14,10 @@
 namespace rr {
 namespace {
 
-constexpr int kRowThreads = 256;
+#ifndef RR_ROW_THREADS
+#define RR_ROW_THREADS 256
+#endif
+constexpr int kRowThreads = RR_ROW_THREADS;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -321,6 +321,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Raise the expected transaction count of the current phase without
+// arriving (the arrival comes later, e.g. after plain stores it must
+// release).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -358,6 +366,28 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank)
   const uint32_t a = map_peer(smem_u32(bar), rank);
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a)
                : "memory");
+}
+// Relaxed remote arrive that also raises the expected transaction count of
+// the peer's mbarrier by `bytes` (the bytes a bulk copy will deliver there).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint64_t *bar, uint32_t rank,
+                                                             uint32_t bytes) {
+  const uint32_t a = map_peer(smem_u32(bar), rank);
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(a),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk copy from this CTA's shared memory into the shared memory of CTA
+// `rank` of the cluster (same offsets as `dst_local` / `bar_local` here);
+// completion is counted on that CTA's mbarrier.  bytes % 16 == 0.
+__device__ __forceinline__ void bulk_s2peer(void *dst_local, const void *src, uint32_t bytes,
+                                            uint64_t *bar_local, uint32_t rank) {
+  const uint32_t d = map_peer(smem_u32(dst_local), rank);
+  const uint32_t b = map_peer(smem_u32(bar_local), rank);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(d),
+      "r"(smem_u32(src)), "r"(bytes), "r"(b)
+      : "memory");
 }
 // Relaxed remote arrive: orders nothing, only counts.  For signals whose
 // payload is already guaranteed by data dependences (e.g. "my loads of your

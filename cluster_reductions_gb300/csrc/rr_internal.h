@@ -37,7 +37,7 @@ int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols,
 // ---- split-K combine (combine.cu)
 int launch_combine(const float *O, const float *m, const float *l, int P,
                    int64_t rows, int D, float scale_log2e, uint16_t *out,
-                   cudaStream_t s, const DevInfo &d);
+                   cudaStream_t s, const DevInfo &d, int mode);
 
 // ---- cluster all-reduce primitive (cluster.cu)
 int launch_cluster_allreduce(const void *vals, int clusters, int C, int width,

@@ -227,6 +227,38 @@ int rr_splitk_combine(const float *O, const float *m, const float *l, int P,
                       int64_t rows, int D, float scale_log2e,
                       uint16_t *out_bf16, void *stream);
 
+/* Combine variants (all compute the same result; see rr_splitk_combine_ex). */
+typedef enum {
+    RR_COMBINE_AUTO = 0,    /* the fastest variant the arguments allow:
+                               direct, else push, else pull, else generic */
+    RR_COMBINE_PULL = 1,    /* each CTA reads its depth band of every peer's
+                               staged tile through DSMEM ([FA] as printed);
+                               P in {1,2,4,8,16}, D % 4P == 0 */
+    RR_COMBINE_PUSH = 2,    /* each CTA bulk-copies every peer's row slice of
+                               its staged tile into that peer's shared memory
+                               (the scatter rides the copy engine); P in
+                               {1,2,4,8,16}, D % 4 == 0, D <= 256 */
+    RR_COMBINE_GENERIC = 3, /* one tile per cluster, plain loads, any P <= 16
+                               and D <= 1024, unequal or empty bands */
+    RR_COMBINE_DIRECT = 4   /* no cluster: each CTA stages the rows of all P
+                               partitions itself and folds them locally;
+                               same DRAM traffic, no exchange between CTAs;
+                               P in {1,2,4,8,16}, D % 4 == 0, 3*P*D*4 <= 160 KiB */
+} rr_combine_mode;
+
+/*
+ * rr_splitk_combine_ex -- rr_splitk_combine with an explicit variant.
+ * Every variant stages, publishes across the cluster of P CTAs, folds the P
+ * partials in rank order 0..P-1 and stores bf16; they differ in how the
+ * partials move between CTAs.  A variant whose conditions the arguments do
+ * not meet returns RR_ERR_UNSUPPORTED (AUTO never does for valid
+ * arguments).  16-byte aligned O and 8-byte aligned out are required by
+ * PULL and PUSH.
+ */
+int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
+                         int64_t rows, int D, float scale_log2e,
+                         uint16_t *out_bf16, void *stream, int mode);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word: RR_OK, or RR_ERR_TIMEOUT if a bounded device wait gave up since the
  * last call.  RR_ERR_CUDA if the synchronisation itself failed. */

@@ -21,35 +21,57 @@ def rr():
     return rr
 
 
-def run(rr, oracle_mod, P, rows, D, seed):
+def run(rr, oracle_mod, P, rows, D, seed, mode=None):
     from cluster_reductions_gb300 import inputs
     O, m, l, s = inputs.combine_partials(P, rows, D, seed, "cuda")
     try:
-        out = rr.splitk_combine(O, m, l, s)
+        out = rr.splitk_combine(O, m, l, s, mode=mode)
     except rr.RRError as e:
-        if P > 8 and e.status == 2:
-            pytest.skip(f"cluster of {P} CTAs not schedulable")
+        if e.status == 2 and (P > 8 or mode is not None):
+            return   # variant or cluster size not available for this shape
         raise
     Oh, mh, lh = to_np(O), to_np(m), to_np(l)
     ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
     assert_combine_close(to_np(out), ref64, ref, Oh, mh, lh, s)
 
 
+MODES = [None, "pull", "push", "generic", "direct"]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m or "auto")
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
-@pytest.mark.parametrize("D", [128, 64, 16, 12, 7, 3])
-def test_combine_small(rr, oracle_mod, P, D):
-    for rows in (1, 5, 33, 130):
-        run(rr, oracle_mod, P, rows, D, 400 + P * 7 + D + rows)
+@pytest.mark.parametrize("D", [256, 128, 64, 16, 12, 7, 3])
+def test_combine_small(rr, oracle_mod, P, D, mode):
+    for rows in (1, 5, 33, 130, 257):
+        run(rr, oracle_mod, P, rows, D, 400 + P * 7 + D + rows, mode)
 
 
+def test_combine_modes_agree_bitwise(rr):
+    # every variant folds in rank order with the same fp32 operations per
+    # output, so they agree bit for bit
+    from cluster_reductions_gb300 import inputs
+    for P, rows, D in ((2, 1000, 128), (8, 517, 128), (4, 64, 64), (16, 96, 128)):
+        O, m, l, s = inputs.combine_partials(P, rows, D, 77 + P, "cuda")
+        outs = {}
+        for mode in ("pull", "push", "direct", "generic"):
+            try:
+                outs[mode] = rr.splitk_combine(O, m, l, s, mode=mode).view(torch.int16)
+            except rr.RRError as e:
+                assert e.status == 2
+        ref = outs.pop("generic")
+        for mode, o in outs.items():
+            assert torch.equal(o, ref), (P, rows, D, mode)
+
+
+@pytest.mark.parametrize("mode", [None, "pull", "push", "direct"], ids=lambda m: m or "auto")
 @pytest.mark.parametrize("P", [2, 4, 8])
-def test_combine_workload_full_size(rr, oracle_mod, P):
+def test_combine_workload_full_size(rr, oracle_mod, P, mode):
     # rows = 32 batch x 32 heads x 128 queries = 131072, D = 128; the oracle
     # checks a strided sample of rows
     from cluster_reductions_gb300 import inputs
     rows, D = 131072, 128
     O, m, l, s = inputs.combine_partials(P, rows, D, inputs.seed_for(4, P), "cuda")
-    out = rr.splitk_combine(O, m, l, s)
+    out = rr.splitk_combine(O, m, l, s, mode=mode)
     idx = torch.arange(0, rows, 97, device="cuda")
     Oh, mh, lh = to_np(O[:, idx]), to_np(m[:, idx]), to_np(l[:, idx])
     ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
