@@ -44,11 +44,27 @@ WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by operation name,
-# valid only while the kernel source hashes to `src_sha`.  The capture and
-# its command are summarised in profiles/.
-NCU_TRAFFIC = {}
+# DRAM bytes per full-size launch from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum of one launch of `bench.py --case <op>`, scaled by
+# the units the full workload has over the captured case), keyed by
+# operation name, valid only while the kernel sources hash to `src_sha`.
+# The captures and their commands are summarised in profiles/.  Softmax's
+# figure is low because half of its output was still in L2 when the single
+# captured launch ended.
+NCU_TRAFFIC = {
+    "splitk_sum_f32": {"bytes": 1085112320, "src_sha": "00c668af13b6dccf",
+                       "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 575927296, "src_sha": "00c668af13b6dccf",
+                   "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+    "softmax_bf16": {"bytes": 562920448, "src_sha": "00c668af13b6dccf",
+                     "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271528192, "src_sha": "00c668af13b6dccf",
+                      "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271471616, "src_sha": "00c668af13b6dccf",
+                       "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137712640, "src_sha": "00c668af13b6dccf",
+                     "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+}
 
 
 def op_specs():
@@ -445,30 +461,47 @@ def bench_ours(args):
     roofline = {"bound": "hbm", "kernel": dname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
-                "traffic": traffic, "algorithmic_bytes": dbytes}
+                "traffic": traffic, "algorithmic_bytes": dbytes,
+                "traffic_source": tr["profile"] if traffic is not None else None}
 
-    # splitk tier at every cluster size (same input, outside the step)
-    splitk_c = {}
-    x_sk = next(ins[0] for name, _, _, ins, _ in data if name == "splitk_sum_f32")
-    out_sk = torch.empty(16, dtype=torch.float32, device=dev)
-    for C in (2, 4, 8, 16):
-        try:
+    splitk_c, combine_v, e2e = {}, {}, None
+    if not args.no_extras:
+        def timed(fn, nbytes, reps=20):
             for _ in range(3):
-                rr.reduce(x_sk, "sum", tier="splitk", cluster_size=C, out=out_sk)
+                fn()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 20
             a.record(stream)
             for _ in range(reps):
-                rr.reduce(x_sk, "sum", tier="splitk", cluster_size=C, out=out_sk)
+                fn()
             b.record(stream)
             torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / reps
-            g = (16 * (1 << 24) * 4 + 64) / (ms / 1e3) / 1e9
-            splitk_c[str(C)] = {"gbs": round(g, 1), "frac_measured": round(g / peak, 4)}
-        except rr.RRError as e:
-            splitk_c[str(C)] = {"unsupported": str(e)}
+            g = nbytes / (a.elapsed_time(b) / reps / 1e3) / 1e9
+            return {"gbs": round(g, 1), "frac_measured": round(g / peak, 4)}
 
-    e2e = bench_e2e(args, rr, data, dev, stream, world)
+        # split-K tier at every cluster size (same input, outside the step)
+        x_sk = next(ins[0] for name, _, _, ins, _ in data if name == "splitk_sum_f32")
+        out_sk = torch.empty(16, dtype=torch.float32, device=dev)
+        for C in (2, 4, 8, 16):
+            try:
+                splitk_c[str(C)] = timed(lambda: rr.reduce(x_sk, "sum", tier="splitk",
+                                                           cluster_size=C, out=out_sk),
+                                         16 * (1 << 24) * 4 + 64)
+            except rr.RRError as e:
+                splitk_c[str(C)] = {"unsupported": str(e)}
+        # every combine variant on the step's inputs: the cluster ones (pull:
+        # DSMEM loads as on the page; push: copy-engine scatter) and direct
+        for name, _, spec, ins, outs in data:
+            if spec["kind"] != "combine":
+                continue
+            nbytes = sum(algorithmic_bytes(spec))
+            for mode in ("pull", "push", "direct"):
+                try:
+                    combine_v[f"{name}_{mode}"] = timed(
+                        lambda: rr.splitk_combine(ins[0], ins[1], ins[2], float(ins[3]),
+                                                  out=outs[0], mode=mode), nbytes)
+                except rr.RRError as e:
+                    combine_v[f"{name}_{mode}"] = {"unsupported": str(e)}
+        e2e = bench_e2e(args, rr, data, dev, stream, world)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -479,7 +512,8 @@ def bench_ours(args):
                    "l2": "inputs larger than L2: every operation reads its own buffer once "
                          "per step; a step moves %.2f GB" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
-        "tiers": tiers, "splitk_by_cluster": splitk_c, "roofline": roofline,
+        "tiers": tiers, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
+        "roofline": roofline,
         "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -574,6 +608,47 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# Workloads for ncu captures: the step's operation with fewer rows (or
+# columns) where the full one is large, every input still larger than L2
+# except the tiled tier's, which is the full workload.  `scale` = full-size
+# units / case units, to scale a captured per-launch DRAM traffic.
+PROFILE_CASES = {
+    "block_sum_f32": ({}, None, 1.0),
+    "warp_sum_f32": ({}, None, 1.0),
+    "tiled_sum_f32": ({}, None, 1.0),
+    "splitk_sum_f32": ({"cols": 1 << 22}, None, 4.0),
+    "softmax_bf16": ({"rows": 8192}, None, 4.0),
+    "layernorm_bf16": ({}, None, 1.0),
+    "combine_p8": ({"rows": 32768}, None, 4.0),
+    "combine_p8_pull": ({"rows": 32768}, "pull", 4.0),
+    "combine_p8_push": ({"rows": 32768}, "push", 4.0),
+}
+
+
+def run_case(args):
+    import torch
+    import cluster_reductions_gb300 as rr
+    torch.cuda.set_device(0)
+    rr.load()
+    over, mode, scale = PROFILE_CASES[args.case]
+    base = args.case.replace("_pull", "").replace("_push", "")
+    spec = dict(next(s for n, _, s in op_specs() if n == base))
+    spec.update(over)
+    dev = torch.device("cuda", 0)
+    ins = make_inputs(spec, dev)
+    outs = make_outputs(spec, ins, dev)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        if mode:
+            rr.splitk_combine(ins[0], ins[1], ins[2], float(ins[3]), out=outs[0], mode=mode)
+        else:
+            run_op(rr, spec, ins, outs)
+    torch.cuda.synchronize()
+    bi, bo = algorithmic_bytes(spec)
+    print(json.dumps({"case": args.case, "launches": args.steps, "algorithmic_bytes": bi + bo,
+                      "scale_to_full": scale, "status": rr.device_status()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,7 +658,18 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the steps (no per-cluster-size, per-variant or e2e passes), "
+                         "e.g. for an ncu launch list of exactly the step's kernels")
+    ap.add_argument("--case", default=None,
+                    help="run one operation of the step on a workload sized for an ncu capture "
+                         "(larger than L2, a few hundred MB) --steps times, and exit; one of "
+                         + ", ".join(PROFILE_CASES))
     args = ap.parse_args()
+    if args.case:
+        if args.case not in PROFILE_CASES:
+            ap.error(f"--case must be one of {', '.join(PROFILE_CASES)}")
+        return run_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
