@@ -464,7 +464,7 @@ def bench_ours(args):
                 "traffic": traffic, "algorithmic_bytes": dbytes,
                 "traffic_source": tr["profile"] if traffic is not None else None}
 
-    splitk_c, combine_v, e2e = {}, {}, None
+    splitk_c, combine_v, callreduce_us, rowwise_sk, e2e = {}, {}, {}, {}, None
     if not args.no_extras:
         def timed(fn, nbytes, reps=20):
             for _ in range(3):
@@ -501,6 +501,34 @@ def bench_ours(args):
                                                   out=outs[0], mode=mode), nbytes)
                 except rr.RRError as e:
                     combine_v[f"{name}_{mode}"] = {"unsupported": str(e)}
+        # split-K tier of the two-pass row ops (a few very long rows)
+        from cluster_reductions_gb300 import inputs as _inp
+        xs = _inp.normal_bf16(16, 1 << 20, 777, dev, 3.0)
+        ys = torch.empty((16, 1 << 20), dtype=torch.float32, device=dev)
+        rowwise_sk["softmax_16x1M_bf16"] = timed(lambda: rr.softmax(xs, out=ys), 16 * (1 << 20) * 6)
+        mu, rs = torch.empty(16, device=dev), torch.empty(16, device=dev)
+        rowwise_sk["layernorm_16x1M_bf16"] = timed(
+            lambda: rr.layernorm_stats(xs, 1e-5, mean=mu, rstd=rs), 16 * (1 << 20) * 2 + 128)
+        rowwise_sk["tier"] = "splitk C=%d" % rr.last_tier()[1]
+        del xs, ys
+        # the cluster all-reduce primitive alone: one cluster, 4096 back-to-back
+        # combines of one fp32 per CTA, with the tail sync and with two slots
+        for C in (2, 4, 8, 16):
+            vals = torch.randn((4096, 1, C, 1), device=dev)
+            res = torch.empty_like(vals)
+            for two in (False, True):
+                key = f"C{C}_{'two_slot' if two else 'tail_sync'}_us"
+                try:
+                    for _ in range(2):
+                        rr.cluster_allreduce(vals, "sum", two_slot=two, res=res)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    rr.cluster_allreduce(vals, "sum", two_slot=two, res=res)
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    callreduce_us[key] = round(a.elapsed_time(b) * 1e3 / 4096, 3)
+                except rr.RRError as e:
+                    callreduce_us[key] = str(e)
         e2e = bench_e2e(args, rr, data, dev, stream, world)
 
     line = {
@@ -513,6 +541,7 @@ def bench_ours(args):
                          "per step; a step moves %.2f GB" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
         "tiers": tiers, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
+        "cluster_allreduce_latency": callreduce_us, "rowwise_splitk": rowwise_sk,
         "roofline": roofline,
         "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
     }

@@ -94,8 +94,17 @@ def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tie
     return _to_host(o, x)
 
 
-def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """rr_softmax: row softmax of a bf16 or fp32 [rows, cols] tensor, fp32 out."""
+def _rowwise_opts(tier, cluster_size):
+    if tier is None and not cluster_size:
+        return None
+    return ctypes.byref(_lib.rr_rowwise_opts(_TIERS[tier] if not isinstance(tier, int) else tier,
+                                             int(cluster_size)))
+
+
+def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
+            cluster_size: int = 0) -> torch.Tensor:
+    """rr_softmax / rr_softmax_ex: row softmax of a bf16 or fp32 [rows, cols]
+    tensor, fp32 out.  tier: None/"auto", "block" or "splitk"."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -104,14 +113,21 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None) -> torch.Ten
         raise TypeError(f"softmax: dtype {xd.dtype} not supported (bfloat16, float32)")
     o = out if out is not None else torch.empty((rows, cols), dtype=torch.float32,
                                                 device=xd.device)
-    check(load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream()), "rr_softmax")
+    opts = _rowwise_opts(tier, cluster_size)
+    if opts is None:
+        st = load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream())
+    else:
+        st = load().rr_softmax_ex(_ptr(xd), rows, cols, dt, _ptr(o), _stream(), opts)
+    check(st, "rr_softmax")
     return _to_host(o, x)
 
 
 def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
                     mean: Optional[torch.Tensor] = None,
-                    rstd: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """rr_layernorm_stats: per-row mean and 1/sqrt(var + eps), fp32."""
+                    rstd: Optional[torch.Tensor] = None, tier=None,
+                    cluster_size: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """rr_layernorm_stats / rr_layernorm_stats_ex: per-row mean and
+    1/sqrt(var + eps), fp32.  tier: None/"auto", "block" or "splitk"."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -120,8 +136,14 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
         raise TypeError(f"layernorm_stats: dtype {xd.dtype} not supported")
     mu = mean if mean is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
     rs = rstd if rstd is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
-    check(load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
-                                    _stream()), "rr_layernorm_stats")
+    opts = _rowwise_opts(tier, cluster_size)
+    if opts is None:
+        st = load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
+                                       _stream())
+    else:
+        st = load().rr_layernorm_stats_ex(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu),
+                                          _ptr(rs), _stream(), opts)
+    check(st, "rr_layernorm_stats")
     return _to_host(mu, x), _to_host(rs, x)
 
 

@@ -27,6 +27,10 @@ class rr_reduce_opts(ctypes.Structure):
                 ("rank_out", ctypes.c_void_p)]
 
 
+class rr_rowwise_opts(ctypes.Structure):
+    _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int)]
+
+
 # name -> (restype, argtypes), mirroring include/rr.h
 _i64, _int, _vp, _f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
 SIGNATURES = {
@@ -35,6 +39,9 @@ SIGNATURES = {
                             ctypes.POINTER(rr_reduce_opts)]),
     "rr_softmax": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
     "rr_layernorm_stats": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp]),
+    "rr_softmax_ex": (_int, [_vp, _i64, _i64, _int, _vp, _vp, ctypes.POINTER(rr_rowwise_opts)]),
+    "rr_layernorm_stats_ex": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp,
+                                     ctypes.POINTER(rr_rowwise_opts)]),
     "rr_cluster_allreduce": (_int, [_vp, _int, _int, _int, _int, _int, _int, _int, _i64,
                                     _vp, _vp, _vp]),
     "rr_cluster_allreduce_selftest": (_int, [_int, _int, _int, _int, _int, _int,

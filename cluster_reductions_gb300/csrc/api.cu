@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "rr.h"
 #include "rr_internal.h"
@@ -35,6 +36,72 @@ cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 }  // namespace
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? RR_OK : RR_ERR_CUDA; }
+
+namespace {
+struct OccKey {
+  const void *func;
+  int threads, cluster, device;
+  size_t smem;
+  bool operator==(const OccKey &o) const {
+    return func == o.func && threads == o.threads && cluster == o.cluster && device == o.device &&
+           smem == o.smem;
+  }
+};
+struct OccHash {
+  size_t operator()(const OccKey &k) const {
+    return std::hash<const void *>()(k.func) ^ ((size_t)k.threads << 20) ^
+           ((size_t)k.cluster << 40) ^ ((size_t)k.device << 48) ^ (k.smem * 2654435761u);
+  }
+};
+std::mutex g_occ_mu;
+std::unordered_map<OccKey, int, OccHash> g_occ;
+}  // namespace
+
+int occupancy_blocks(const void *func, int threads, size_t smem, int device) {
+  const OccKey key{func, threads, 0, device, smem};
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    nb = 0;
+  }
+  if (nb < 1) nb = 1;
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  g_occ[key] = nb;
+  return nb;
+}
+
+int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, int device) {
+  const OccKey key{func, threads, cluster, device, smem};
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  g_occ[key] = n;
+  return n;
+}
 
 bool log_enabled() {
   static const bool on = [] {
@@ -189,8 +256,22 @@ int rr_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype, void
   return rr_reduce_ex(x, rows, cols, op, dtype, out, stream, nullptr);
 }
 
+static bool rowwise_opts_ok(const rr_rowwise_opts *o) {
+  if (!o) return true;
+  if (!(o->tier == RR_TIER_AUTO || o->tier == RR_TIER_BLOCK || o->tier == RR_TIER_SPLITK))
+    return false;
+  return o->cluster_size == 0 || o->cluster_size == 1 || o->cluster_size == 2 ||
+         o->cluster_size == 4 || o->cluster_size == 8 || o->cluster_size == 16;
+}
+
 int rr_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
                void *stream) {
+  return rr_softmax_ex(x, rows, cols, in_dtype, out, stream, nullptr);
+}
+
+int rr_softmax_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
+                  void *stream, const rr_rowwise_opts *opts) {
+  if (!rowwise_opts_ok(opts)) return RR_ERR_INVALID;
   if (rows < 0 || cols < 0) return RR_ERR_INVALID;
   if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
   if (rows == 0) return RR_OK;
@@ -203,13 +284,20 @@ int rr_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *o
   const DevInfo *d = current_device(&st);
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
-  st = launch_softmax(x, rows, cols, in_dtype, out, as_stream(stream), *d, &tier);
-  if (st == RR_OK) g_last_tier.store((1 << 8) | tier);
+  st = launch_softmax(x, rows, cols, in_dtype, out, as_stream(stream), *d, &tier,
+                      opts ? opts->tier : RR_TIER_AUTO, opts ? opts->cluster_size : 0);
+  if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
 
 int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                        float *mean, float *rstd, void *stream) {
+  return rr_layernorm_stats_ex(x, rows, cols, in_dtype, eps, mean, rstd, stream, nullptr);
+}
+
+int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
+                          float *mean, float *rstd, void *stream, const rr_rowwise_opts *opts) {
+  if (!rowwise_opts_ok(opts)) return RR_ERR_INVALID;
   if (rows < 0 || cols < 0) return RR_ERR_INVALID;
   if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
   if (!(eps >= 0.0f) || std::isinf(eps)) return RR_ERR_INVALID;
@@ -226,8 +314,9 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype, 
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
   st = launch_layernorm_stats(x, rows, cols, in_dtype, eps, mean, rstd, as_stream(stream), *d,
-                              &tier);
-  if (st == RR_OK) g_last_tier.store((1 << 8) | tier);
+                              &tier, opts ? opts->tier : RR_TIER_AUTO,
+                              opts ? opts->cluster_size : 0);
+  if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
 

@@ -51,11 +51,13 @@ k_cluster_allreduce(const typename Op::T *__restrict__ vals, typename Op::T *__r
 #pragma unroll
       for (int j = 0; j < W; ++j) res[base + r * W + j] = o[j];
     }
+    if (mismatches) {  // without a counter the kernel only times the combines
 #pragma unroll
-    for (int j = 0; j < W; ++j) {
-      T e = __ldg(vin + j);
-      for (uint32_t q = 1; q < C; ++q) e = Op::f(e, __ldg(vin + q * W + j));
-      if (to_bits<T>(e) != to_bits<T>(o[j])) ++bad;
+      for (int j = 0; j < W; ++j) {
+        T e = __ldg(vin + j);
+        for (uint32_t q = 1; q < C; ++q) e = Op::f(e, __ldg(vin + q * W + j));
+        if (to_bits<T>(e) != to_bits<T>(o[j])) ++bad;
+      }
     }
   }
   // Without the per-combine tail sync a CTA must not exit while a peer may

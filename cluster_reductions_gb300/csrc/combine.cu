@@ -640,12 +640,7 @@ int launch_pipe(const float *O, const float *m, const float *l, int64_t rows, in
   cudaLaunchAttribute attr[1];
   int clusters = 1;
   {
-    cudaLaunchConfig_t q = cluster_cfg(1, P, smem, s, attr, kPipeThreads);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
-      cudaGetLastError();
-      return RR_ERR_UNSUPPORTED;
-    }
+    const int n = occupancy_clusters((const void *)kern, kPipeThreads, smem, P, d.device);
     if (n < 1) return RR_ERR_UNSUPPORTED;
     clusters = n;
   }
@@ -679,12 +674,7 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
   cudaLaunchAttribute attr[1];
   int clusters = 1;
   {
-    cudaLaunchConfig_t q = cluster_cfg(1, P, smem, s, attr, kPipeThreads);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
-      cudaGetLastError();
-      return RR_ERR_UNSUPPORTED;
-    }
+    const int n = occupancy_clusters((const void *)kern, kPipeThreads, smem, P, d.device);
     if (n < 1) return RR_ERR_UNSUPPORTED;
     clusters = n;
   }
@@ -721,12 +711,7 @@ int launch_direct(const float *O, const float *m, const float *l, int64_t rows, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kPipeThreads, smem) != cudaSuccess ||
-      nb < 1) {
-    cudaGetLastError();
-    return RR_ERR_UNSUPPORTED;
-  }
+  const int nb = occupancy_blocks((const void *)kern, kPipeThreads, smem, d.device);
   const int64_t ntiles = (rows + TR - 1) / TR;
   int64_t grid = (int64_t)nb * d.sm_count;
   if (grid > ntiles) grid = ntiles;

@@ -317,10 +317,7 @@ template <class K>
 int grid_for(K kernel, int threads, int64_t work_blocks, const DevInfo &d, int smem = 0) {
   int64_t g = work_blocks;
   if (RR_GRID_CAP) {  // persistent: at most one wave of resident CTAs
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess ||
-        nb < 1)
-      nb = 1;
+    const int nb = occupancy_blocks((const void *)kernel, threads, (size_t)smem, d.device);
     const int64_t cap = (int64_t)nb * d.sm_count;
     if (g > cap) g = cap;
   }

@@ -7,6 +7,8 @@
 // Fast path: one CTA per row with the whole row held in registers, so the
 // row is read from HBM exactly once.  Generic path (any width, any
 // alignment): the row is streamed from global memory once per pass.
+#include <cstdio>
+
 #include "rr.h"
 #include "rr_device.cuh"
 #include "rr_internal.h"
@@ -41,6 +43,7 @@ struct InBF16 {
   static __device__ __forceinline__ float load1(const S *p) {
     return __uint_as_float(((uint32_t)__ldg(p)) << 16);
   }
+  static __device__ __forceinline__ float cvt(S v) { return __uint_as_float(((uint32_t)v) << 16); }
 };
 struct InF32 {
   using S = float;
@@ -50,6 +53,7 @@ struct InF32 {
     o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
   }
   static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
+  static __device__ __forceinline__ float cvt(S v) { return v; }
 };
 
 // ---------------------------------------------------------------------------
@@ -284,9 +288,7 @@ k_lnstats_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, 
 
 template <class K>
 int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d) {
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess || nb < 1)
-    nb = 1;
+  const int nb = occupancy_blocks((const void *)kernel, threads, 0, d.device);
   const int64_t cap = (int64_t)nb * d.sm_count;
   return (int)(rows < cap ? rows : cap);
 }
@@ -299,17 +301,206 @@ inline int pick_nv(int64_t nvec) {
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Split-K tier of the two-pass row operations ("reduce" page, split-K tier;
+// "cluster_allreduce" page, two-slot mode).  A cluster of C CTAs per row;
+// CTA r owns slice r of the row (a multiple of 8 elements, shifted like the
+// reduce tier's so that every slice but the first starts 16-byte aligned).
+// The slice is staged once into shared memory (one 1-D bulk copy when it is
+// 16-byte granular, plain loads otherwise) when it fits, else it is re-read.
+// Each row needs two cluster combines, done back to back on two slots with
+// no tail sync in between and one terminal cluster sync:
+//   softmax:   CTA (max, sum) pair -> combine max -> M;
+//              rescale the CTA sum to M -> combine sum -> S;
+//              y = e^(x - M) / S over the slice.
+//   layernorm: CTA sum -> combine sum -> mean;
+//              CTA sum of (x - mean)^2 -> combine sum -> var; rstd.
+// Every CTA folds the partials in rank order, so every CTA holds the same
+// M, S (mean, var) bits.
+// ---------------------------------------------------------------------------
+template <int THREADS, class In, bool SOFTMAX>
+__global__ void __launch_bounds__(THREADS)
+k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
+                 float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
+                 int64_t stage_cap, int *err) {
+  using S = typename In::S;
+  extern __shared__ __align__(128) unsigned char dyn_raw[];
+  S *st = reinterpret_cast<S *>(dyn_raw);
+  __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
+  __shared__ float slot[2][2];
+  __shared__ __align__(8) uint64_t bar;
+  const int tid = threadIdx.x;
+  const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
+  const int64_t row = cluster_id_x();
+  const S *p = x + row * cols;
+  const int64_t chunk = ((cols + C - 1) / C + 7) & ~int64_t(7);
+  const int64_t mis = (int64_t)((16u - ((uint32_t)(uintptr_t)p & 15u)) & 15u) / (int64_t)sizeof(S);
+  auto bound = [&](int64_t k) -> int64_t {
+    if (k == 0) return 0;
+    if (k >= (int64_t)C) return cols;
+    const int64_t b = k * chunk + mis - (mis ? 8 : 0);
+    return b < 0 ? 0 : (b > cols ? cols : b);
+  };
+  const int64_t b0 = bound(r), b1 = bound(r + 1);
+  const int64_t n = b1 > b0 ? b1 - b0 : 0;
+  const S *ps = p + b0;
+  const bool staged = n > 0 && n <= stage_cap;
+
+  // ---- stage the slice on chip
+  if (staged) {
+    const bool bulk = ((uintptr_t)ps % 16 == 0) && ((n * (int64_t)sizeof(S)) % 16 == 0);
+    if (bulk) {
+      if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+      }
+      __syncthreads();
+      if (tid == 0) {
+        const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
+        mbar_arrive_expect_tx(&bar, bytes);
+        bulk_g2s(st, ps, bytes, &bar);
+      }
+      if (!mbar_wait_bounded(&bar, 0, kWaitBudget)) set_error(err, kErrTimeout);
+    } else {
+      for (int64_t i = tid; i < n; i += THREADS) st[i] = ps[i];
+      __syncthreads();
+    }
+  }
+  auto val = [&](int64_t i) -> float { return staged ? In::cvt(st[i]) : In::load1(ps + i); };
+
+  if (SOFTMAX) {
+    // per-thread online (max, sum) over the slice, then the CTA pair
+    float m = -INFINITY, s = 0.0f;
+    for (int64_t i = tid; i < n; i += THREADS) ms_combine(m, s, val(i), 1.0f);
+    ms_block_allreduce<THREADS>(m, s, red_m, red_s);
+    // combine 1 (slot 0, no tail sync): the row max
+    float v1[1] = {m}, M[1];
+    cluster_allreduce<MaxF32, 1>(slot[0], v1, C, /*tail_sync=*/false, M);
+    // combine 2 (slot 1, no tail sync): the CTA sums rescaled to that max
+    float v2[1] = {(m == -INFINITY) ? 0.0f : s * ex2_approx((m - M[0]) * kLog2e)}, Ssum[1];
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, Ssum);
+    const float inv = 1.0f / Ssum[0];
+    const float mb = M[0] * kLog2e;
+    float *yr = y + row * cols + b0;
+    for (int64_t i = tid; i < n; i += THREADS)
+      yr[i] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(val(i), kLog2e, -mb)) * inv;
+  } else {
+    float acc = 0.0f;
+    for (int64_t i = tid; i < n; i += THREADS) acc += val(i);
+    acc = block_reduce<SumF32, THREADS>(acc, red_s);
+    float v1[1] = {acc}, tot[1];
+    cluster_allreduce<SumF32, 1>(slot[0], v1, C, /*tail_sync=*/false, tot);
+    const float mu = tot[0] / (float)cols;
+    float q = 0.0f;
+    for (int64_t i = tid; i < n; i += THREADS) {
+      const float d = val(i) - mu;
+      q = fmaf(d, d, q);
+    }
+    __syncthreads();  // red_s is reused
+    q = block_reduce<SumF32, THREADS>(q, red_s);
+    float v2[1] = {q}, tq[1];
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, tq);
+    if (r == 0 && tid == 0) {
+      mean[row] = mu;
+      rstd[row] = 1.0f / sqrtf(tq[0] / (float)cols + eps);
+    }
+  }
+  // the second combine dropped its tail sync: retire both slots before exit
+  cluster_sync();
+}
+
+template <class In, bool SOFTMAX>
+int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps, float *y,
+                          float *mean, float *rstd, int C, cudaStream_t s, const DevInfo &d) {
+  using S = typename In::S;
+  constexpr int T = 512;
+  auto kern = k_rowwise_splitk<T, In, SOFTMAX>;
+  // stage the slice when it fits in shared memory (one slice per CTA)
+  const int64_t chunk = ((cols + C - 1) / C + 7) & ~int64_t(7);
+  const int64_t slice_max = chunk + 8;
+  const int64_t cap_bytes = (int64_t)d.max_smem_optin - 4096;
+  int64_t stage_cap = 0;
+  size_t smem = 0;
+  if (slice_max * (int64_t)sizeof(S) <= cap_bytes) {
+    stage_cap = slice_max;
+    smem = (size_t)(slice_max * (int64_t)sizeof(S) + 15) & ~(size_t)15;
+  }
+  cudaError_t e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (C > 1 && occupancy_clusters((const void *)kern, T, smem, C, d.device) < 1) {
+    // not schedulable with this much shared memory: stream the slice twice
+    stage_cap = 0;
+    smem = 0;
+    if (occupancy_clusters((const void *)kern, T, 0, C, d.device) < 1) return RR_ERR_UNSUPPORTED;
+  }
+  if (rows * C > 0x7fffffffLL) return RR_ERR_INVALID;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
+  cfg.blockDim = dim3(T, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: %s split-K rows=%lld cols=%lld C=%d stage=%lld smem=%zu\n",
+                 SOFTMAX ? "softmax" : "layernorm", (long long)rows, (long long)cols, C,
+                 (long long)stage_cap, smem);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const S *)xv, rows, cols, eps, y, mean, rstd,
+                                        stage_cap, d.err_word));
+}
+
+// Split-K cluster size for a two-pass row op: a staged slice fills most of
+// an SM's shared memory, so one CTA per SM: the largest power of two (2..16)
+// with rows * C <= SMs; 0 when the tier does not apply (then the block tier
+// runs).
+inline int rowwise_splitk_cluster(int64_t rows, int64_t cols, const DevInfo &d) {
+  if (!d.cluster_launch || rows < 1 || 2 * rows > d.sm_count || cols < 16384) return 0;
+  int c = 2;
+  while (c < 16 && (int64_t)(2 * c) * rows <= d.sm_count) c *= 2;
+  return c;
+}
+
+// Tier of a two-pass row op: forced (tier, C) or automatic.  Returns the
+// cluster size for the split-K tier, 0 for the block tier, -1 if a forced
+// split-K cluster size cannot run.
+inline int rowwise_pick(int64_t rows, int64_t cols, int tier, int C, const DevInfo &d) {
+  if (tier == RR_TIER_BLOCK) return 0;
+  if (tier == RR_TIER_SPLITK) {
+    if (C == 0) C = rowwise_splitk_cluster(rows, cols, d);
+    if (C == 0) C = 2;
+    if (C > 1 && !d.cluster_launch) return -1;
+    return C;
+  }
+  return rowwise_splitk_cluster(rows, cols, d);
+}
+
 template <class In>
 int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStream_t s,
-                 const DevInfo &d, int *tier_out) {
+                 const DevInfo &d, int *tier_out, int tier, int C) {
   using S = typename In::S;
   const S *x = (const S *)xv;
+  const int c = rowwise_pick(rows, cols, tier, C, d);
+  if (c < 0) return RR_ERR_UNSUPPORTED;
+  if (c > 0) {
+    *tier_out = RR_TIER_SPLITK | (c << 8);
+    return launch_rowwise_splitk<In, true>(xv, rows, cols, 0.0f, y, nullptr, nullptr, c, s, d);
+  }
   const uintptr_t ax = (uintptr_t)xv, ay = (uintptr_t)y;
   const int64_t nvec = cols / In::EPV;
   const bool reg = (cols % In::EPV == 0) && ax % 16 == 0 &&
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0) && pick_nv(nvec) > 0;
   if (reg) {
-    *tier_out = RR_TIER_BLOCK;
+    *tier_out = RR_TIER_BLOCK | (1 << 8);
 #define RR_SM_REG(NV)                                                          \
   {                                                                            \
     auto k = k_softmax_reg<kRowThreads, NV, In>;                               \
@@ -323,7 +514,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
     }
 #undef RR_SM_REG
   } else {
-    *tier_out = RR_TIER_BLOCK;
+    *tier_out = RR_TIER_BLOCK | (1 << 8);
     auto k = k_softmax_gen<kRowThreads, In>;
     k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, cols, y);
   }
@@ -332,12 +523,18 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
 
 template <class In>
 int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *mean,
-                 float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out) {
+                 float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
   using S = typename In::S;
   const S *x = (const S *)xv;
+  const int c = rowwise_pick(rows, cols, tier, C, d);
+  if (c < 0) return RR_ERR_UNSUPPORTED;
+  if (c > 0) {
+    *tier_out = RR_TIER_SPLITK | (c << 8);
+    return launch_rowwise_splitk<In, false>(xv, rows, cols, eps, nullptr, mean, rstd, c, s, d);
+  }
   const int64_t nvec = cols / In::EPV;
   const bool reg = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) && pick_nv(nvec) > 0;
-  *tier_out = RR_TIER_BLOCK;
+  *tier_out = RR_TIER_BLOCK | (1 << 8);
   if (reg) {
 #define RR_LN_REG(NV)                                                          \
   {                                                                            \
@@ -361,17 +558,18 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
 }  // namespace
 
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
-                   cudaStream_t s, const DevInfo &d, int *tier_out) {
-  if (in_dtype == RR_BF16) return softmax_impl<InBF16>(x, rows, cols, out, s, d, tier_out);
-  return softmax_impl<InF32>(x, rows, cols, out, s, d, tier_out);
+                   cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
+  if (in_dtype == RR_BF16)
+    return softmax_impl<InBF16>(x, rows, cols, out, s, d, tier_out, tier, C);
+  return softmax_impl<InF32>(x, rows, cols, out, s, d, tier_out, tier, C);
 }
 
 int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                            float *mean, float *rstd, cudaStream_t s, const DevInfo &d,
-                           int *tier_out) {
+                           int *tier_out, int tier, int C) {
   if (in_dtype == RR_BF16)
-    return lnstats_impl<InBF16>(x, rows, cols, eps, mean, rstd, s, d, tier_out);
-  return lnstats_impl<InF32>(x, rows, cols, eps, mean, rstd, s, d, tier_out);
+    return lnstats_impl<InBF16>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C);
+  return lnstats_impl<InF32>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C);
 }
 
 }  // namespace rr

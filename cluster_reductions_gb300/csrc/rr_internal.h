@@ -28,11 +28,15 @@ int launch_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype,
                   void *rank_out, const DevInfo &d);
 
 // ---- softmax / layernorm statistics (rowwise.cu)
+// tier: RR_TIER_AUTO, RR_TIER_BLOCK or RR_TIER_SPLITK; C: split-K cluster
+// size (0 = automatic).  *tier_out receives (C << 8) | tier.
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype,
-                   float *out, cudaStream_t s, const DevInfo &d, int *tier_out);
+                   float *out, cudaStream_t s, const DevInfo &d, int *tier_out,
+                   int tier, int C);
 int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols,
                            int in_dtype, float eps, float *mean, float *rstd,
-                           cudaStream_t s, const DevInfo &d, int *tier_out);
+                           cudaStream_t s, const DevInfo &d, int *tier_out,
+                           int tier, int C);
 
 // ---- split-K combine (combine.cu)
 int launch_combine(const float *O, const float *m, const float *l, int P,
@@ -51,6 +55,15 @@ int launch_wait_timeout_probe(int64_t budget, cudaStream_t s, const DevInfo &d);
 
 // Maps a CUDA error to an rr_status.
 int cuda_status(cudaError_t e);
+
+// Resident CTAs per SM of `func` with `threads` threads and `smem` bytes of
+// dynamic shared memory on `device`, cached (the occupancy query costs
+// microseconds per launch otherwise).  At least 1.
+int occupancy_blocks(const void *func, int threads, size_t smem, int device);
+
+// Largest number of co-resident clusters of `cluster` CTAs of `func`
+// (cudaOccupancyMaxActiveClusters), cached; 0 if none can run.
+int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, int device);
 
 // True when the environment variable RR_LOG is set to a non-zero value:
 // launchers then print their tier and launch configuration to stderr.

@@ -140,6 +140,36 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
                        float eps, float *mean, float *rstd, void *stream);
 
 /*
+ * Options of rr_softmax_ex / rr_layernorm_stats_ex ([RW] tier semantics for
+ * the two-pass row operations).  Zero-initialise and set what you need.
+ *   tier          RR_TIER_AUTO, RR_TIER_BLOCK (a CTA per row, the row on
+ *                 chip) or RR_TIER_SPLITK (a cluster of C CTAs per row).
+ *   cluster_size  split-K: 0 = automatic, else 1, 2, 4, 8 or 16.
+ * Split-K: CTA r stages slice r of the row in its shared memory when it fits
+ * (one 1-D bulk copy), and the row takes two cluster combines ([CA]) on two
+ * slots without a tail sync between them: softmax combines the CTA maxima,
+ * then the CTA sums rescaled to the row max; layernorm combines the sums,
+ * then the squared deviations about the mean.  Every CTA folds in rank
+ * order, so every CTA holds the same row statistics.  AUTO picks split-K
+ * when 2 * rows <= SMs and cols >= 16384, with C the largest power of two
+ * (2..16) such that rows * C <= SMs.
+ */
+typedef struct {
+    int tier;
+    int cluster_size;
+} rr_rowwise_opts;
+
+/* rr_softmax with options; opts may be NULL.  RR_ERR_UNSUPPORTED if a
+ * forced cluster size cannot be co-scheduled. */
+int rr_softmax_ex(const void *x, int64_t rows, int64_t cols, int in_dtype,
+                  float *out, void *stream, const rr_rowwise_opts *opts);
+
+/* rr_layernorm_stats with options; opts may be NULL. */
+int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols,
+                          int in_dtype, float eps, float *mean, float *rstd,
+                          void *stream, const rr_rowwise_opts *opts);
+
+/*
  * rr_cluster_allreduce -- the [CA] primitive, run `iters` times back to back
  * by `clusters` clusters of `cluster_size` CTAs.  For iteration t, cluster
  * c, rank r, the CTA's block-reduced vector is vals[((t*clusters + c)*C
@@ -151,9 +181,10 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * drops it and alternates between two slots ([CA] need_tail_sync).
  * skew_cycles > 0 makes each rank spin a pseudo-random multiple (0..7) of
  * skew_cycles clock cycles before each combine, so that CTAs race ahead.
- * Every thread of every CTA also re-folds the inputs of its iteration from
- * global memory in rank order and compares bits with its own result;
- * *mismatches (device int64, optional) is incremented per differing value.
+ * When `mismatches` (device int64) is given, every thread of every CTA also
+ * re-folds the inputs of its iteration from global memory in rank order,
+ * compares bits with its own result and adds the number of differing values
+ * to *mismatches; with NULL the kernel only runs the combines (for timing).
  *   cluster_size 1..16 (16 needs the device's non-portable cluster size),
  *   width 1, 2, 4 or 8, dtype RR_F32 or RR_I32; iters >= 0 (0 is a no-op);
  *   skew_cycles 0..2^20.

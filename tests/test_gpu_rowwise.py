@@ -105,6 +105,78 @@ def test_layernorm_workload_full_size(rr, oracle_mod):
     assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what="rstd")
 
 
+SPLITK_SHAPES = [(1, 1000), (3, 16387), (2, 20000), (1, 65536), (4, 100003)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+def test_softmax_splitk_forced(rr, oracle_mod, dtype, C):
+    for i, (rows, cols) in enumerate(SPLITK_SHAPES):
+        for offset in (0, 1):
+            x = _x(rows, cols, dtype, 500 + i, 3.0, offset)
+            try:
+                y = to_np(rr.softmax(x, tier="splitk", cluster_size=C))
+            except rr.RRError as e:
+                if C == 16 and e.status == 2:
+                    pytest.skip("cluster of 16 not schedulable")
+                raise
+            assert rr.last_tier() == ("splitk", C)
+            ref = oracle_mod.softmax(to_np(x))
+            assert_rel_close(y, ref, 1e-5, floor=1e-30, what=f"softmax splitk {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+def test_layernorm_splitk_forced(rr, oracle_mod, dtype, C):
+    for i, (rows, cols) in enumerate(SPLITK_SHAPES):
+        for offset in (0, 3):
+            x = _x(rows, cols, dtype, 600 + i, 1.0, offset)
+            try:
+                check_lnstats_tier(rr, oracle_mod, x, C)
+            except rr.RRError as e:
+                if C == 16 and e.status == 2:
+                    pytest.skip("cluster of 16 not schedulable")
+                raise
+
+
+def check_lnstats_tier(rr, oracle_mod, x, C, eps=1e-5):
+    mean, rstd = rr.layernorm_stats(x, eps, tier="splitk", cluster_size=C)
+    assert rr.last_tier() == ("splitk", C)
+    rm, rv, rr_ = oracle_mod.layernorm_stats(to_np(x), eps)
+    xf = x.to(torch.float64).cpu().numpy()
+    n = xf.shape[1]
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / n)
+    err = np.abs(to_np(mean).astype(np.float64) - rm)
+    assert (err <= bound).all(), f"mean: max err {err.max()}"
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="rstd splitk")
+
+
+def test_splitk_rowwise_long_rows_auto(rr, oracle_mod):
+    # a few very long rows: the automatic choice is split-K; every row is
+    # checked against the oracle and repeated runs give the same bits
+    from cluster_reductions_gb300 import inputs
+    x = inputs.normal_bf16(16, 1 << 20, 4242, "cuda", 3.0)
+    y = rr.softmax(x)
+    assert rr.last_tier()[0] == "splitk"
+    ref = oracle_mod.softmax(to_np(x))
+    assert_rel_close(to_np(y), ref, 1e-5, floor=1e-30, what="softmax 16x1M")
+    y2 = rr.softmax(x)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    xl = inputs.normal_bf16(16, 1 << 20, 4243, "cuda", 1.0)
+    mean, rstd = rr.layernorm_stats(xl, 1e-5)
+    assert rr.last_tier()[0] == "splitk"
+    rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xl), 1e-5)
+    xf = xl.to(torch.float64).cpu().numpy()
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / xf.shape[1])
+    assert (np.abs(to_np(mean) - rm) <= bound).all()
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="rstd 16x1M")
+    # fp32 rows too long to stage on chip: the slice is streamed twice
+    xf32 = inputs.normal_f32(4, 1 << 21, 4244, "cuda", 2.0)
+    yf = rr.softmax(xf32, tier="splitk", cluster_size=2)
+    assert_rel_close(to_np(yf), oracle_mod.softmax(to_np(xf32)), 1e-5, floor=1e-30,
+                     what="softmax fp32 unstaged")
+
+
 def test_argument_errors(rr):
     with pytest.raises(rr.RRError):
         rr.softmax(torch.zeros((3, 0), device="cuda"))
