@@ -58,6 +58,9 @@ def _load():
                                                vp, vp, vp]
         lib.oracle_splitk_combine.argtypes = [vp, vp, vp, i32, i64, i32,
                                               ctypes.c_float, vp, vp]
+        lib.oracle_layernorm.argtypes = [vp, i32, i64, i64, ctypes.c_double, vp, vp,
+                                         vp, vp, vp, vp]
+        lib.oracle_layernorm.restype = None
         lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         for f in (lib.oracle_reduce_f32, lib.oracle_reduce_i32,
@@ -143,6 +146,25 @@ def layernorm_stats(x: np.ndarray, eps: float = 1e-5):
     _load().oracle_layernorm_stats(_ptr(x), _x_dtype(x), rows, cols, float(eps),
                                    _ptr(mean), _ptr(var), _ptr(rstd))
     return mean, var, rstd
+
+
+def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float = 1e-5):
+    """Layernorm rewrite ("reduce" page: the map pass after the statistics):
+    y = (x - mean) * rstd * gamma + beta per row, fp64, then rounded once to
+    bf16.  x float32 or uint16 (bf16 bits) [rows, cols]; gamma, beta float32
+    [cols].  Returns (y_f64, y_bf16_bits, mean, rstd)."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    b = np.ascontiguousarray(beta, dtype=np.float32)
+    assert g.shape == (cols,) and b.shape == (cols,)
+    y64 = np.empty((rows, cols), np.float64)
+    y16 = np.empty((rows, cols), np.uint16)
+    mean = np.empty(rows, np.float64)
+    rstd = np.empty(rows, np.float64)
+    _load().oracle_layernorm(_ptr(x), _x_dtype(x), rows, cols, float(eps), _ptr(g), _ptr(b),
+                             _ptr(y64), _ptr(y16), _ptr(mean), _ptr(rstd))
+    return y64, y16, mean, rstd
 
 
 def splitk_combine(O: np.ndarray, m: np.ndarray, l: np.ndarray,

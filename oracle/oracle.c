@@ -247,6 +247,35 @@ void oracle_layernorm_stats(const void *x, int x_dtype, int64_t rows,
     }
 }
 
+/*
+ * Layernorm rewrite ("reduce" page: the second, map-style pass after the
+ * statistics reduce): y[r,i] = (x[r,i] - mean_r) * rstd_r * gamma[i] + beta[i]
+ * in fp64 with the fp64 statistics above, then rounded once to bf16
+ * (nearest-even).  y_f64 (optional) receives the unrounded values; mean and
+ * rstd (optional) the statistics.
+ */
+void oracle_layernorm(const void *x, int x_dtype, int64_t rows, int64_t cols,
+                      double eps, const float *gamma, const float *beta,
+                      double *y_f64, uint16_t *y_bf16, double *mean,
+                      double *rstd)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        double mu, va, rs;
+        const char *row = (const char *)x + r * cols * (x_dtype == 2 ? 2 : 4);
+        oracle_layernorm_stats(row, x_dtype, 1, cols, eps, &mu, &va, &rs);
+        for (int64_t i = 0; i < cols; ++i) {
+            double v = (x_dtype == 2)
+                ? bf16_to_f64(((const uint16_t *)row)[i])
+                : (double)((const float *)row)[i];
+            double yv = (v - mu) * rs * (double)gamma[i] + (double)beta[i];
+            if (y_f64) y_f64[r * cols + i] = yv;
+            if (y_bf16) y_bf16[r * cols + i] = oracle_f64_to_bf16(yv);
+        }
+        if (mean) mean[r] = mu;
+        if (rstd) rstd[r] = rs;
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* split-K attention-output combine ("fa4_splitk_reduce_scatter_write" */
 /* page: partials O_p with statistics (m_p, l_p) are rescaled by       */

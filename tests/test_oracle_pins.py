@@ -239,6 +239,48 @@ def test_layernorm_matches_numpy(oracle_mod):
     np.testing.assert_allclose(rstd, 1.0 / np.sqrt(xf.var(axis=1) + 1e-5), rtol=1e-12)
 
 
+def test_layernorm_rewrite_closed_forms(oracle_mod):
+    rng = np.random.default_rng(12)
+    cols = 96
+    # constant row: x - mean = 0, so y = beta exactly
+    x = np.full((2, cols), 1.25, np.float32)
+    g = rng.standard_normal(cols).astype(np.float32)
+    b = rng.standard_normal(cols).astype(np.float32)
+    y64, y16, mean, rstd = oracle_mod.layernorm(x, g, b, 1e-5)
+    np.testing.assert_array_equal(y64, np.broadcast_to(b.astype(np.float64), (2, cols)))
+    # +-a alternating, gamma = 1, beta = 0: y = +-a / sqrt(a^2 + eps)
+    a = 2.0
+    x = np.tile(np.array([a, -a], np.float32), cols // 2)[None, :]
+    ones, zeros = np.ones(cols, np.float32), np.zeros(cols, np.float32)
+    y64, _, _, _ = oracle_mod.layernorm(x, ones, zeros, 1e-5)
+    expect = np.tile([a, -a], cols // 2) / np.sqrt(a * a + 1e-5)
+    np.testing.assert_allclose(y64[0], expect, rtol=1e-14)
+    # gamma scales and beta shifts column-wise: index, not row, dependent
+    x = rng.standard_normal((3, cols)).astype(np.float32)
+    y1, _, m1, r1 = oracle_mod.layernorm(x, ones, zeros, 1e-5)
+    y2, _, _, _ = oracle_mod.layernorm(x, g, b, 1e-5)
+    np.testing.assert_allclose(y2, y1 * g.astype(np.float64) + b.astype(np.float64), rtol=1e-13,
+                               atol=1e-13)
+
+
+def test_layernorm_rewrite_matches_numpy_and_rounds_once(oracle_mod):
+    import torch
+    gen = torch.Generator().manual_seed(13)
+    xb = torch.randn(5, 700, generator=gen).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    xf = xb.to(torch.float64).numpy()
+    rng = np.random.default_rng(14)
+    g = rng.standard_normal(700).astype(np.float32)
+    b = rng.standard_normal(700).astype(np.float32)
+    y64, y16, mean, rstd = oracle_mod.layernorm(bits, g, b, 1e-5)
+    mu = xf.mean(axis=1, keepdims=True)
+    ref = (xf - mu) / np.sqrt(xf.var(axis=1, keepdims=True) + 1e-5) * g + b
+    np.testing.assert_allclose(y64, ref, rtol=1e-12, atol=1e-12)
+    # y_bf16 is the single rounding of y_f64
+    for i in range(0, 700, 37):
+        assert y16[2, i] == oracle_mod.f64_to_bf16_bits(y64[2, i])
+
+
 # ---------------------------------------------------------------- combine
 
 def _golden_combine_cases():
