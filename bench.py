@@ -510,7 +510,19 @@ def bench_ours(args):
         rowwise_sk["layernorm_16x1M_bf16"] = timed(
             lambda: rr.layernorm_stats(xs, 1e-5, mean=mu, rstd=rs), 16 * (1 << 20) * 2 + 128)
         rowwise_sk["tier"] = "splitk C=%d" % rr.last_tier()[1]
-        del xs, ys
+        g16, b16 = _inp.layernorm_params(1 << 20, 778, dev)
+        yb = torch.empty((16, 1 << 20), dtype=torch.bfloat16, device=dev)
+        rowwise_sk["layernorm_rewrite_16x1M_bf16"] = timed(
+            lambda: rr.layernorm(xs, g16, b16, 1e-5, out=yb), 16 * (1 << 20) * 4 + (1 << 20) * 8)
+        del xs, ys, yb
+        # the layernorm rewrite (statistics + y = (x - mean) rstd gamma + beta,
+        # bf16 out) on the layernorm workload, block tier
+        xl = _inp.normal_bf16(16384, 8192, 779, dev)
+        gl, bl = _inp.layernorm_params(8192, 780, dev)
+        yl = torch.empty((16384, 8192), dtype=torch.bfloat16, device=dev)
+        rowwise_sk["layernorm_rewrite_16384x8192_bf16"] = timed(
+            lambda: rr.layernorm(xl, gl, bl, 1e-5, out=yl), 16384 * 8192 * 4 + 8192 * 8)
+        del xl, yl
         # the cluster all-reduce primitive alone: one cluster, 4096 back-to-back
         # combines of one fp32 per CTA, with the tail sync and with two slots
         for C in (2, 4, 8, 16):

@@ -147,6 +147,34 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
     return _to_host(mu, x), _to_host(rs, x)
 
 
+def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
+              out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
+              rstd: Optional[torch.Tensor] = None, tier=None,
+              cluster_size: int = 0) -> torch.Tensor:
+    """rr_layernorm / rr_layernorm_ex: bf16 (x - mean) * rstd * gamma + beta per
+    row of a bf16 or fp32 [rows, cols] tensor; gamma, beta fp32 [cols].
+    mean / rstd (fp32 [rows]) are filled when given."""
+    x = _as_2d(x)
+    xd = _to_device(x)
+    rows, cols = xd.shape
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_BF16, RR_F32):
+        raise TypeError(f"layernorm: dtype {xd.dtype} not supported")
+    if gamma.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("gamma and beta must be float32")
+    if gamma.numel() != cols or beta.numel() != cols:
+        raise ValueError("gamma and beta must have cols elements")
+    gd, bd = _to_device(gamma.contiguous()), _to_device(beta.contiguous())
+    o = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16,
+                                                device=xd.device)
+    opts = _rowwise_opts(tier, cluster_size)
+    args = (_ptr(xd), rows, cols, dt, float(eps), _ptr(gd), _ptr(bd), _ptr(o), _ptr(mean),
+            _ptr(rstd), _stream())
+    st = load().rr_layernorm(*args) if opts is None else load().rr_layernorm_ex(*args, opts)
+    check(st, "rr_layernorm")
+    return _to_host(o, x)
+
+
 def cluster_allreduce(vals: torch.Tensor, op="sum", *, two_slot: bool = False,
                       skew_cycles: int = 0, res: Optional[torch.Tensor] = None,
                       mismatches: Optional[torch.Tensor] = None) -> torch.Tensor:

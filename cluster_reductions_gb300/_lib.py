@@ -42,6 +42,9 @@ SIGNATURES = {
     "rr_softmax_ex": (_int, [_vp, _i64, _i64, _int, _vp, _vp, ctypes.POINTER(rr_rowwise_opts)]),
     "rr_layernorm_stats_ex": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp,
                                      ctypes.POINTER(rr_rowwise_opts)]),
+    "rr_layernorm": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "rr_layernorm_ex": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
+                               ctypes.POINTER(rr_rowwise_opts)]),
     "rr_cluster_allreduce": (_int, [_vp, _int, _int, _int, _int, _int, _int, _int, _i64,
                                     _vp, _vp, _vp]),
     "rr_cluster_allreduce_selftest": (_int, [_int, _int, _int, _int, _int, _int,

@@ -320,6 +320,47 @@ int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols, int in_dtyp
   return st;
 }
 
+int rr_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
+                 const float *gamma, const float *beta, uint16_t *out_bf16, float *mean,
+                 float *rstd, void *stream) {
+  return rr_layernorm_ex(x, rows, cols, in_dtype, eps, gamma, beta, out_bf16, mean, rstd, stream,
+                         nullptr);
+}
+
+int rr_layernorm_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
+                    const float *gamma, const float *beta, uint16_t *out_bf16, float *mean,
+                    float *rstd, void *stream, const rr_rowwise_opts *opts) {
+  if (!rowwise_opts_ok(opts)) return RR_ERR_INVALID;
+  if (rows < 0 || cols < 0) return RR_ERR_INVALID;
+  if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
+  if (!(eps >= 0.0f) || std::isinf(eps)) return RR_ERR_INVALID;
+  if (rows == 0) return RR_OK;
+  if (cols == 0 || !x || !gamma || !beta || !out_bf16) return RR_ERR_INVALID;
+  if (mul_overflows(rows, cols, INT64_MAX / 4)) return RR_ERR_INVALID;
+  const size_t es = in_dtype == RR_BF16 ? 2 : 4;
+  const size_t nx = (size_t)(rows * cols) * es, ny = (size_t)(rows * cols) * 2,
+               no = (size_t)rows * 4, ng = (size_t)cols * 4;
+  if (overlaps(x, nx, out_bf16, ny) || overlaps(gamma, ng, out_bf16, ny) ||
+      overlaps(beta, ng, out_bf16, ny))
+    return RR_ERR_INVALID;
+  if ((mean && (overlaps(mean, no, out_bf16, ny) || overlaps(mean, no, x, nx))) ||
+      (rstd && (overlaps(rstd, no, out_bf16, ny) || overlaps(rstd, no, x, nx))) ||
+      (mean && rstd && overlaps(mean, no, rstd, no)))
+    return RR_ERR_INVALID;
+  if ((uintptr_t)x % es != 0 || (uintptr_t)gamma % 4 || (uintptr_t)beta % 4 ||
+      (uintptr_t)out_bf16 % 2)
+    return RR_ERR_INVALID;
+  int st = RR_OK;
+  const DevInfo *d = current_device(&st);
+  if (!d) return st;
+  int tier = RR_TIER_BLOCK;
+  st = launch_layernorm(x, rows, cols, in_dtype, eps, gamma, beta, out_bf16, mean, rstd,
+                        as_stream(stream), *d, &tier, opts ? opts->tier : RR_TIER_AUTO,
+                        opts ? opts->cluster_size : 0);
+  if (st == RR_OK) g_last_tier.store(tier);
+  return st;
+}
+
 int rr_cluster_allreduce(const void *vals, int clusters, int cluster_size, int width, int op,
                          int dtype, int iters, int two_slot, int64_t skew_cycles, void *res,
                          int64_t *mismatches, void *stream) {

@@ -9,6 +9,8 @@
 // alignment): the row is streamed from global memory once per pass.
 #include <cstdio>
 
+#include <cuda_bf16.h>
+
 #include "rr.h"
 #include "rr_device.cuh"
 #include "rr_internal.h"
@@ -286,6 +288,137 @@ k_lnstats_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, 
   }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// Layernorm, statistics and rewrite fused ("reduce" page: the rewrite is the
+// map pass after the statistics reduce), register-resident row: the
+// statistics as in k_lnstats_reg, then y = bf16_rn((x - mean) * rstd *
+// gamma + beta) from the registers.  One HBM read of x, one write of y.
+// Requires cols % EPV == 0, x / gamma / beta 16-byte aligned, y aligned to
+// 2 * EPV bytes.  mean, rstd may be null.
+// ---------------------------------------------------------------------------
+template <int THREADS, int NV, class In>
+__global__ void __launch_bounds__(THREADS)
+k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+                const float *__restrict__ gamma, const float *__restrict__ beta,
+                uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
+  constexpr int EPV = In::EPV;
+  __shared__ float red[THREADS / 32 + 1];
+  const int tid = threadIdx.x;
+  const int nvec = cols / EPV;
+  const float inv_n = 1.0f / (float)cols;
+  uint4 raw[NV];
+  auto fetch = [&](int64_t r) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(x + r * (int64_t)cols);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx < nvec) raw[k] = ld_stream_u4(q + idx);
+    }
+  };
+  if ((int64_t)blockIdx.x < rows) fetch(blockIdx.x);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    float v[NV][EPV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx < nvec) {
+        In::unpack(raw[k], v[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
+      }
+    }
+    if (row + gridDim.x < rows) fetch(row + gridDim.x);
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) s += v[k][e];
+    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    float qs = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (k * THREADS + tid < nvec) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float dlt = v[k][e] - mu;
+          qs = fmaf(dlt, dlt, qs);
+        }
+      }
+    }
+    const float var = sum_block_allreduce<THREADS>(qs, red) * inv_n;
+    const float rs = 1.0f / sqrtf(var + eps);
+    uint16_t *yr = y + row * (int64_t)cols;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx < nvec) {
+        float g[EPV], b[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; e += 4) {
+          const float4 gv = __ldg(reinterpret_cast<const float4 *>(gamma + idx * EPV + e));
+          const float4 bv = __ldg(reinterpret_cast<const float4 *>(beta + idx * EPV + e));
+          g[e] = gv.x; g[e + 1] = gv.y; g[e + 2] = gv.z; g[e + 3] = gv.w;
+          b[e] = bv.x; b[e + 1] = bv.y; b[e + 2] = bv.z; b[e + 3] = bv.w;
+        }
+        uint32_t pk[EPV / 2];
+#pragma unroll
+        for (int e = 0; e < EPV; e += 2)
+          pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
+                                  fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
+        if (EPV == 8) {
+          *reinterpret_cast<uint4 *>(yr + idx * EPV) = make_uint4(pk[0], pk[1 % (EPV / 2)],
+                                                                  pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
+        } else {
+          *reinterpret_cast<uint2 *>(yr + idx * EPV) = make_uint2(pk[0], pk[1 % (EPV / 2)]);
+        }
+      }
+    }
+    if (tid == 0) {
+      if (mean) mean[row] = mu;
+      if (rstd) rstd[row] = rs;
+    }
+  }
+}
+
+// Layernorm, generic: any cols, any alignment; statistics in two passes over
+// global memory, then the rewrite in a third.
+template <int THREADS, class In>
+__global__ void __launch_bounds__(THREADS)
+k_layernorm_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
+                const float *__restrict__ gamma, const float *__restrict__ beta,
+                uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
+  __shared__ float red[THREADS / 32 + 1];
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const typename In::S *p = x + row * cols;
+    float s = 0.0f;
+    for (int64_t i = tid; i < cols; i += THREADS) s += In::load1(p + i);
+    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    float qs = 0.0f;
+    for (int64_t i = tid; i < cols; i += THREADS) {
+      const float dlt = In::load1(p + i) - mu;
+      qs = fmaf(dlt, dlt, qs);
+    }
+    const float rs = 1.0f / sqrtf(sum_block_allreduce<THREADS>(qs, red) / (float)cols + eps);
+    uint16_t *yr = y + row * cols;
+    for (int64_t i = tid; i < cols; i += THREADS) {
+      const __nv_bfloat16 h =
+          __float2bfloat16_rn(fmaf((In::load1(p + i) - mu) * rs, __ldg(gamma + i), __ldg(beta + i)));
+      yr[i] = *reinterpret_cast<const uint16_t *>(&h);
+    }
+    if (tid == 0) {
+      if (mean) mean[row] = mu;
+      if (rstd) rstd[row] = rs;
+    }
+  }
+}
+
 template <class K>
 int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d) {
   const int nb = occupancy_blocks((const void *)kernel, threads, 0, d.device);
@@ -318,11 +451,16 @@ inline int pick_nv(int64_t nvec) {
 // Every CTA folds the partials in rank order, so every CTA holds the same
 // M, S (mean, var) bits.
 // ---------------------------------------------------------------------------
-template <int THREADS, class In, bool SOFTMAX>
+enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
+
+// MODE: kModeSoftmax (y fp32), kModeStats (mean, rstd), kModeLayernorm
+// (mean, rstd and the rewrite ybf = bf16((x - mean) * rstd * gamma + beta)).
+template <int THREADS, class In, int MODE>
 __global__ void __launch_bounds__(THREADS)
 k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
                  float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
-                 int64_t stage_cap, int *err) {
+                 const float *__restrict__ gamma, const float *__restrict__ beta,
+                 uint16_t *__restrict__ ybf, int64_t stage_cap, int *err) {
   using S = typename In::S;
   extern __shared__ __align__(128) unsigned char dyn_raw[];
   S *st = reinterpret_cast<S *>(dyn_raw);
@@ -368,7 +506,7 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   }
   auto val = [&](int64_t i) -> float { return staged ? In::cvt(st[i]) : In::load1(ps + i); };
 
-  if (SOFTMAX) {
+  if (MODE == kModeSoftmax) {
     // per-thread online (max, sum) over the slice, then the CTA pair
     float m = -INFINITY, s = 0.0f;
     for (int64_t i = tid; i < n; i += THREADS) ms_combine(m, s, val(i), 1.0f);
@@ -400,21 +538,31 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
     q = block_reduce<SumF32, THREADS>(q, red_s);
     float v2[1] = {q}, tq[1];
     cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, tq);
+    const float rs = 1.0f / sqrtf(tq[0] / (float)cols + eps);
     if (r == 0 && tid == 0) {
-      mean[row] = mu;
-      rstd[row] = 1.0f / sqrtf(tq[0] / (float)cols + eps);
+      if (mean) mean[row] = mu;
+      if (rstd) rstd[row] = rs;
+    }
+    if (MODE == kModeLayernorm) {
+      uint16_t *yr = ybf + row * cols + b0;
+      for (int64_t i = tid; i < n; i += THREADS) {
+        const float o = fmaf((val(i) - mu) * rs, __ldg(gamma + b0 + i), __ldg(beta + b0 + i));
+        const __nv_bfloat16 h = __float2bfloat16_rn(o);
+        yr[i] = *reinterpret_cast<const uint16_t *>(&h);
+      }
     }
   }
   // the second combine dropped its tail sync: retire both slots before exit
   cluster_sync();
 }
 
-template <class In, bool SOFTMAX>
+template <class In, int MODE>
 int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps, float *y,
-                          float *mean, float *rstd, int C, cudaStream_t s, const DevInfo &d) {
+                          float *mean, float *rstd, const float *gamma, const float *beta,
+                          uint16_t *ybf, int C, cudaStream_t s, const DevInfo &d) {
   using S = typename In::S;
   constexpr int T = 512;
-  auto kern = k_rowwise_splitk<T, In, SOFTMAX>;
+  auto kern = k_rowwise_splitk<T, In, MODE>;
   // stage the slice when it fits in shared memory (one slice per CTA)
   const int64_t chunk = ((cols + C - 1) / C + 7) & ~int64_t(7);
   const int64_t slice_max = chunk + 8;
@@ -453,10 +601,10 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
   cfg.numAttrs = 1;
   if (log_enabled())
     std::fprintf(stderr, "rr: %s split-K rows=%lld cols=%lld C=%d stage=%lld smem=%zu\n",
-                 SOFTMAX ? "softmax" : "layernorm", (long long)rows, (long long)cols, C,
-                 (long long)stage_cap, smem);
+                 MODE == kModeSoftmax ? "softmax" : (MODE == kModeStats ? "lnstats" : "layernorm"),
+                 (long long)rows, (long long)cols, C, (long long)stage_cap, smem);
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const S *)xv, rows, cols, eps, y, mean, rstd,
-                                        stage_cap, d.err_word));
+                                        gamma, beta, ybf, stage_cap, d.err_word));
 }
 
 // Split-K cluster size for a two-pass row op: a staged slice fills most of
@@ -493,7 +641,8 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   if (c < 0) return RR_ERR_UNSUPPORTED;
   if (c > 0) {
     *tier_out = RR_TIER_SPLITK | (c << 8);
-    return launch_rowwise_splitk<In, true>(xv, rows, cols, 0.0f, y, nullptr, nullptr, c, s, d);
+    return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
+                                                   nullptr, nullptr, nullptr, c, s, d);
   }
   const uintptr_t ax = (uintptr_t)xv, ay = (uintptr_t)y;
   const int64_t nvec = cols / In::EPV;
@@ -530,7 +679,8 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   if (c < 0) return RR_ERR_UNSUPPORTED;
   if (c > 0) {
     *tier_out = RR_TIER_SPLITK | (c << 8);
-    return launch_rowwise_splitk<In, false>(xv, rows, cols, eps, nullptr, mean, rstd, c, s, d);
+    return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
+                                                 nullptr, nullptr, nullptr, c, s, d);
   }
   const int64_t nvec = cols / In::EPV;
   const bool reg = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) && pick_nv(nvec) > 0;
@@ -555,7 +705,57 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   return cuda_status(cudaGetLastError());
 }
 
+template <class In>
+int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const float *gamma,
+                   const float *beta, uint16_t *y, float *mean, float *rstd, cudaStream_t s,
+                   const DevInfo &d, int *tier_out, int tier, int C) {
+  using S = typename In::S;
+  const S *x = (const S *)xv;
+  const int c = rowwise_pick(rows, cols, tier, C, d);
+  if (c < 0) return RR_ERR_UNSUPPORTED;
+  if (c > 0) {
+    *tier_out = RR_TIER_SPLITK | (c << 8);
+    return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
+                                                     gamma, beta, y, c, s, d);
+  }
+  *tier_out = RR_TIER_BLOCK | (1 << 8);
+  const int64_t nvec = cols / In::EPV;
+  const bool reg = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
+                   ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
+                   ((uintptr_t)y % (2 * In::EPV) == 0) && pick_nv(nvec) > 0;
+  if (reg) {
+#define RR_LNF_REG(NV)                                                         \
+  {                                                                            \
+    auto k = k_layernorm_reg<kRowThreads, NV, In>;                             \
+    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(        \
+        x, rows, (int)cols, eps, gamma, beta, y, mean, rstd);                  \
+  }
+    switch (pick_nv(nvec)) {
+      case 1: RR_LNF_REG(1) break;
+      case 2: RR_LNF_REG(2) break;
+      case 4: RR_LNF_REG(4) break;
+      default: RR_LNF_REG(8) break;
+    }
+#undef RR_LNF_REG
+  } else {
+    auto k = k_layernorm_gen<kRowThreads, In>;
+    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, cols, eps, gamma,
+                                                                        beta, y, mean, rstd);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
+
+int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
+                     const float *gamma, const float *beta, uint16_t *y, float *mean, float *rstd,
+                     cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
+  if (in_dtype == RR_BF16)
+    return layernorm_impl<InBF16>(x, rows, cols, eps, gamma, beta, y, mean, rstd, s, d, tier_out,
+                                  tier, C);
+  return layernorm_impl<InF32>(x, rows, cols, eps, gamma, beta, y, mean, rstd, s, d, tier_out,
+                               tier, C);
+}
 
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
                    cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {

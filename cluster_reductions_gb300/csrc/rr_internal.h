@@ -38,6 +38,12 @@ int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols,
                            cudaStream_t s, const DevInfo &d, int *tier_out,
                            int tier, int C);
 
+// Layernorm (statistics + rewrite, bf16 out); mean / rstd may be null.
+int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
+                     const float *gamma, const float *beta, uint16_t *y, float *mean,
+                     float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier,
+                     int C);
+
 // ---- split-K combine (combine.cu)
 int launch_combine(const float *O, const float *m, const float *l, int P,
                    int64_t rows, int D, float scale_log2e, uint16_t *out,

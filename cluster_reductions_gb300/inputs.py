@@ -60,6 +60,15 @@ def normal_bf16(rows: int, cols: int, seed: int, device="cpu",
     return normal_f32(rows, cols, seed, device, std).to(torch.bfloat16)
 
 
+def layernorm_params(cols: int, seed: int, device="cpu"):
+    """Layernorm affine parameters: gamma = 1 + 0.1 N(0,1), beta = 0.1 N(0,1),
+    fp32 [cols] each."""
+    g = _gen(seed, device)
+    gamma = torch.randn(cols, generator=g, device=device, dtype=torch.float32).mul_(0.1).add_(1.0)
+    beta = torch.randn(cols, generator=g, device=device, dtype=torch.float32).mul_(0.1)
+    return gamma, beta
+
+
 def combine_partials(P: int, rows: int, D: int, seed: int, device="cpu"):
     """Split-K attention partials: per (p, row) l ~ U[1, 64), m ~ 2 * N(0,1);
     O[p, row, :] = N(0,1) * l[p, row].  Returns (O [P,rows,D], m [P,rows],

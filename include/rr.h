@@ -170,6 +170,27 @@ int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols,
                           void *stream, const rr_rowwise_opts *opts);
 
 /*
+ * rr_layernorm -- the layernorm rewrite fused with its statistics ([RW]: the
+ * map pass that follows the statistics reduce):
+ *   out[i,j] = bf16_rn((x[i,j] - mean_i) * rstd_i * gamma[j] + beta[j])
+ * with mean_i, rstd_i as in rr_layernorm_stats.  The row is read from HBM
+ * once when it fits on chip.
+ *   x        device, rows x cols, in_dtype RR_BF16 or RR_F32; cols >= 1.
+ *   gamma, beta  device fp32, cols elements each.
+ *   out_bf16 device, rows x cols bf16 bit patterns; must not overlap x.
+ *   mean, rstd   device fp32 rows elements each, or NULL if not wanted.
+ */
+int rr_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype,
+                 float eps, const float *gamma, const float *beta,
+                 uint16_t *out_bf16, float *mean, float *rstd, void *stream);
+
+/* rr_layernorm with options (block or split-K tier); opts may be NULL. */
+int rr_layernorm_ex(const void *x, int64_t rows, int64_t cols, int in_dtype,
+                    float eps, const float *gamma, const float *beta,
+                    uint16_t *out_bf16, float *mean, float *rstd, void *stream,
+                    const rr_rowwise_opts *opts);
+
+/*
  * rr_cluster_allreduce -- the [CA] primitive, run `iters` times back to back
  * by `clusters` clusters of `cluster_size` CTAs.  For iteration t, cluster
  * c, rank r, the CTA's block-reduced vector is vals[((t*clusters + c)*C

@@ -68,6 +68,39 @@ def assert_bf16_ulp(gpu_bits: np.ndarray, ref_bits: np.ndarray, ulp: int = 1):
                               f"ref={ref_bits[bad][:3]}")
 
 
+def assert_layernorm_close(gpu_bits, ref_f64, ref_bits, x_f64, gamma, beta, mean, rstd,
+                           max_relaxed_frac: float = 1e-3):
+    """Layernorm rewrite parity: each output within 1 bf16 ulp of the
+    oracle's correctly rounded value, or -- where (x - mean) * rstd * gamma
+    cancels against beta -- within one ulp plus the fp32 bound
+        64u (|x - mean| rstd |gamma| + |beta|) + 64u rstd |gamma| sum|x| / N,
+    u = 2^-24: the kernel's mean carries the fp32 summation error of the
+    row (serial per-thread chains plus a tree, well under 64u sum|x| / N),
+    and each of the few roundings after it adds u relative to its operand.
+    At most `max_relaxed_frac` of the outputs may need the second form."""
+    d = np.abs(bf16_ord(gpu_bits) - bf16_ord(ref_bits))
+    strict = d <= 1
+    g = bf16_value(gpu_bits)
+    ref = np.asarray(ref_f64, np.float64)
+    a = np.abs(ref)
+    ex = np.floor(np.log2(np.where(a > 0, a, 2.0 ** -133)))
+    ulp = 2.0 ** (np.maximum(ex, -126) - 7)
+    u = 2.0 ** -24
+    xc = np.asarray(x_f64, np.float64) - np.asarray(mean, np.float64)[:, None]
+    rs = np.asarray(rstd, np.float64)[:, None]
+    gm = np.abs(np.asarray(gamma, np.float64))[None, :]
+    bt = np.abs(np.asarray(beta, np.float64))[None, :]
+    sabs = np.abs(np.asarray(x_f64, np.float64)).sum(axis=1, keepdims=True) / x_f64.shape[1]
+    bound = ulp + 64 * u * (np.abs(xc) * rs * gm + bt) + 64 * u * rs * gm * sabs
+    relaxed = np.abs(g - ref) <= bound
+    bad = np.nonzero(~(strict | relaxed))
+    assert bad[0].size == 0, (f"{bad[0].size} layernorm outputs out of tolerance; first at "
+                              f"{tuple(b[:3] for b in bad)}: gpu={g[bad][:3]} ref={ref[bad][:3]}")
+    n_relaxed = int((~strict).sum())
+    assert n_relaxed <= max(2, max_relaxed_frac * strict.size), (
+        f"{n_relaxed} of {strict.size} outputs needed the cancellation bound")
+
+
 def bf16_value(bits: np.ndarray) -> np.ndarray:
     b = np.asarray(bits, np.uint32) << 16
     return b.view(np.float32).astype(np.float64)

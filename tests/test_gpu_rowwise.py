@@ -177,6 +177,64 @@ def test_splitk_rowwise_long_rows_auto(rr, oracle_mod):
                      what="softmax fp32 unstaged")
 
 
+def check_layernorm(rr, oracle_mod, x, gamma, beta, **kw):
+    from _util import assert_layernorm_close
+    rows = x.shape[0]
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    y = rr.layernorm(x, gamma, beta, 1e-5, mean=mean, rstd=rstd, **kw)
+    xh = to_np(x)
+    y64, y16, rm, rr_ = oracle_mod.layernorm(xh, to_np(gamma), to_np(beta), 1e-5)
+    xf = x.to(torch.float64).cpu().numpy()
+    assert_layernorm_close(to_np(y), y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_)
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="layernorm rstd")
+    return y, mean, rstd
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_layernorm_rewrite_small(rr, oracle_mod, dtype):
+    from cluster_reductions_gb300 import inputs
+    for i, (rows, cols) in enumerate(SHAPES):
+        gamma, beta = inputs.layernorm_params(cols, 700 + i, "cuda")
+        for offset in (0, 1):
+            check_layernorm(rr, oracle_mod, _x(rows, cols, dtype, 710 + i, 1.0, offset), gamma, beta)
+
+
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+def test_layernorm_rewrite_splitk(rr, oracle_mod, C):
+    from cluster_reductions_gb300 import inputs
+    for i, (rows, cols) in enumerate(SPLITK_SHAPES):
+        gamma, beta = inputs.layernorm_params(cols, 800 + i, "cuda")
+        x = _x(rows, cols, torch.bfloat16, 810 + i, 1.0, i % 2)
+        try:
+            check_layernorm(rr, oracle_mod, x, gamma, beta, tier="splitk", cluster_size=C)
+        except rr.RRError as e:
+            if C == 16 and e.status == 2:
+                pytest.skip("cluster of 16 not schedulable")
+            raise
+        assert rr.last_tier() == ("splitk", C)
+
+
+def test_layernorm_rewrite_workload_and_stats_agree(rr, oracle_mod):
+    # 16384 x 8192 bf16 with gamma = 1 + 0.1 N, beta = 0.1 N: sampled rows
+    # against the oracle; the fused kernel's mean / rstd are the statistics
+    # kernel's, bit for bit
+    from cluster_reductions_gb300 import inputs
+    from _util import assert_layernorm_close
+    x = inputs.normal_bf16(16384, 8192, inputs.seed_for(3, 2), "cuda")
+    gamma, beta = inputs.layernorm_params(8192, inputs.seed_for(3, 3), "cuda")
+    mean, rstd = torch.empty(16384, device="cuda"), torch.empty(16384, device="cuda")
+    y = rr.layernorm(x, gamma, beta, 1e-5, mean=mean, rstd=rstd)
+    m2, r2 = rr.layernorm_stats(x, 1e-5)
+    assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
+    assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
+    idx = torch.arange(0, 16384, 509, device="cuda")
+    xs = x[idx]
+    y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(gamma), to_np(beta), 1e-5)
+    assert_layernorm_close(to_np(y[idx]), y64, y16, xs.to(torch.float64).cpu().numpy(),
+                           to_np(gamma), to_np(beta), rm, rr_)
+
+
 def test_argument_errors(rr):
     with pytest.raises(rr.RRError):
         rr.softmax(torch.zeros((3, 0), device="cuda"))
