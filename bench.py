@@ -501,6 +501,20 @@ def bench_ours(args):
                                                   out=outs[0], mode=mode), nbytes)
                 except rr.RRError as e:
                     combine_v[f"{name}_{mode}"] = {"unsupported": str(e)}
+        # multi-cluster split-K on two very long rows (2 x 128M fp32, 1 GiB)
+        # against one cluster of 16 per row
+        x2 = torch.randn((2, 1 << 27), device=dev)
+        o2 = torch.empty(2, device=dev)
+        ws2 = torch.empty(2 * 1024, dtype=torch.int32, device=dev)
+        nb2 = 2 * (1 << 27) * 4 + 8
+        try:
+            splitk_c["2x128M_one_cluster_per_row"] = timed(
+                lambda: rr.reduce(x2, "sum", tier="splitk", cluster_size=16, out=o2), nb2)
+            splitk_c["2x128M_multi_cluster"] = timed(
+                lambda: rr.reduce_splitk_multi(x2, "sum", out=o2, workspace=ws2), nb2)
+        except rr.RRError as e:
+            splitk_c["2x128M"] = {"unsupported": str(e)}
+        del x2
         # split-K tier of the two-pass row ops (a few very long rows)
         from cluster_reductions_gb300 import inputs as _inp
         xs = _inp.normal_bf16(16, 1 << 20, 777, dev, 3.0)

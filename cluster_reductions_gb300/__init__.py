@@ -94,6 +94,33 @@ def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tie
     return _to_host(o, x)
 
 
+def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
+                        clusters_per_row: int = 0, out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_reduce_splitk_multi: the split-K reduction with several clusters
+    per row (for very few, very long rows).  The workspace (rows * G
+    elements) is allocated here when not given."""
+    x = _as_2d(x)
+    xd = _to_device(x)
+    rows, cols = xd.shape
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_F32, RR_I32):
+        raise TypeError(f"reduce: dtype {xd.dtype} not supported (float32, int32)")
+    o = out if (out is not None and out.is_cuda) else torch.empty(rows, dtype=xd.dtype,
+                                                                  device=xd.device)
+    g = clusters_per_row if clusters_per_row > 0 else 1024
+    ws = workspace if workspace is not None else torch.empty(max(1, rows * g), dtype=torch.int32,
+                                                             device=xd.device)
+    check(load().rr_reduce_splitk_multi(_ptr(xd), rows, cols, _op(op), dt, _ptr(o),
+                                        int(cluster_size), int(clusters_per_row), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream()),
+          "rr_reduce_splitk_multi")
+    if out is not None and not out.is_cuda:
+        out.copy_(o)
+        return out
+    return _to_host(o, x)
+
+
 def _rowwise_opts(tier, cluster_size):
     if tier is None and not cluster_size:
         return None

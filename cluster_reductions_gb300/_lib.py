@@ -37,6 +37,8 @@ SIGNATURES = {
     "rr_reduce": (_int, [_vp, _i64, _i64, _int, _int, _vp, _vp]),
     "rr_reduce_ex": (_int, [_vp, _i64, _i64, _int, _int, _vp, _vp,
                             ctypes.POINTER(rr_reduce_opts)]),
+    "rr_reduce_splitk_multi": (_int, [_vp, _i64, _i64, _int, _int, _vp, _int, _int, _vp,
+                                      ctypes.c_size_t, _vp]),
     "rr_softmax": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
     "rr_layernorm_stats": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp]),
     "rr_softmax_ex": (_int, [_vp, _i64, _i64, _int, _vp, _vp, ctypes.POINTER(rr_rowwise_opts)]),

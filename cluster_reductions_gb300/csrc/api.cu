@@ -251,6 +251,43 @@ int rr_reduce_ex(const void *x, int64_t rows, int64_t cols, int op, int dtype, v
   return st;
 }
 
+int rr_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op, int dtype, void *out,
+                           int cluster_size, int clusters_per_row, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  if (rows < 0 || cols < 0) return RR_ERR_INVALID;
+  if (op < RR_OP_SUM || op > RR_OP_MIN) return RR_ERR_INVALID;
+  if (dtype != RR_F32 && dtype != RR_I32) return RR_ERR_INVALID;
+  if (!(cluster_size == 0 || cluster_size == 1 || cluster_size == 2 || cluster_size == 4 ||
+        cluster_size == 8 || cluster_size == 16))
+    return RR_ERR_INVALID;
+  if (clusters_per_row < 0 || clusters_per_row > 1024) return RR_ERR_INVALID;
+  if (rows == 0) return RR_OK;
+  if (!out || !workspace || (cols > 0 && !x)) return RR_ERR_INVALID;
+  if (mul_overflows(rows, cols, INT64_MAX / 4)) return RR_ERR_INVALID;
+  if (overlaps(x, (size_t)(rows * cols * 4), out, (size_t)rows * 4)) return RR_ERR_INVALID;
+  int st = RR_OK;
+  const DevInfo *d = current_device(&st);
+  if (!d) return st;
+  const int maxc = max_cluster_cached(op, dtype, *d);
+  int C = cluster_size == 0 ? (maxc < 16 ? maxc : 16) : cluster_size;
+  if (C < 1) C = 1;
+  if (C > 1 && (!d->cluster_launch || maxc < C)) return RR_ERR_UNSUPPORTED;
+  int G = clusters_per_row;
+  if (G == 0) {  // enough clusters that every SM holds a CTA
+    const int64_t need = (d->sm_count + rows * C - 1) / (rows * C);
+    G = (int)(need < 1 ? 1 : (need > 1024 ? 1024 : need));
+  }
+  if (rows * (int64_t)G * C > INT_MAX) return RR_ERR_INVALID;
+  if (workspace_bytes < (size_t)rows * G * 4) return RR_ERR_INVALID;
+  if (overlaps(workspace, (size_t)rows * G * 4, x, (size_t)(rows * cols * 4)) ||
+      overlaps(workspace, (size_t)rows * G * 4, out, (size_t)rows * 4))
+    return RR_ERR_INVALID;
+  st = launch_reduce_splitk_multi(x, rows, cols, op, dtype, out, C, G, workspace,
+                                  as_stream(stream));
+  if (st == RR_OK) g_last_tier.store((C << 8) | RR_TIER_SPLITK);
+  return st;
+}
+
 int rr_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype, void *out,
               void *stream) {
   return rr_reduce_ex(x, rows, cols, op, dtype, out, stream, nullptr);

@@ -311,6 +311,54 @@ k_splitk(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
 }
 
 // ---------------------------------------------------------------------------
+// Multi-cluster split-K: G clusters of C CTAs per row, for rows too few to
+// cover the GPU with one cluster each.  The row is cut into G*C slices (as
+// the split-K tier cuts it into C); cluster g of the row folds slices
+// g*C .. g*C + C - 1, combines its CTAs with cluster_allreduce and rank 0
+// stores the cluster's partial in partial[row * G + g].  A second kernel
+// folds the G partials of each row in order g = 0..G-1.  Every step has a
+// fixed order, so the result is the same on every run.
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int UNROLL>
+__global__ void __launch_bounds__(THREADS)
+k_splitk_multi(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols, int G,
+               typename Op::T *__restrict__ partial) {
+  using T = typename Op::T;
+  __shared__ T red[THREADS / 32];
+  __shared__ T slot[2];
+  const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
+  const int64_t cid = cluster_id_x();
+  const int64_t row = cid / G, g = cid - row * G;
+  const T *p = x + row * cols;
+  const int64_t S = (int64_t)G * C;
+  const int64_t chunk = ((cols + S - 1) / S + 3) & ~int64_t(3);
+  const int64_t mis = (int64_t)(((uint32_t)(uintptr_t)p & 15u) / sizeof(T));
+  auto bound = [&](int64_t k) -> int64_t {
+    if (k == 0) return 0;
+    if (k >= S) return cols;
+    const int64_t b = k * chunk - mis;
+    return b < 0 ? 0 : (b > cols ? cols : b);
+  };
+  const int64_t k0 = g * C + r;
+  T a = fold_range<Op, THREADS, UNROLL>(p, bound(k0), bound(k0 + 1));
+  a = block_reduce<Op, THREADS>(a, red);
+  const T v[1] = {a};
+  T res[1];
+  cluster_allreduce<Op, 1>(slot, v, C, /*tail_sync=*/true, res);
+  if (r == 0 && threadIdx.x == 0) partial[row * G + g] = res[0];
+}
+
+template <class Op>
+__global__ void k_fold_partials(const typename Op::T *__restrict__ partial, int64_t rows, int G,
+                                typename Op::T *__restrict__ out) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= rows) return;
+  typename Op::T acc = partial[row * G];
+  for (int g = 1; g < G; ++g) acc = Op::f(acc, partial[row * G + g]);
+  out[row] = Op::finalize(acc);
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 template <class K>
@@ -468,7 +516,49 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
   }
 }
 
+template <class Op>
+int launch_splitk_multi(const void *x, int64_t rows, int64_t cols, void *out, int C, int G,
+                        void *ws, cudaStream_t s) {
+  using T = typename Op::T;
+  auto kern = k_splitk_multi<Op, kSplitThreads, kSplitUnroll>;
+  if (C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * G * C), 1, 1);
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: reduce split-K multi rows=%lld cols=%lld C=%d G=%d\n",
+                 (long long)rows, (long long)cols, C, G);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, (const T *)x, rows, cols, G, (T *)ws);
+  if (e != cudaSuccess) return cuda_status(e);
+  k_fold_partials<Op><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>((const T *)ws, rows, G,
+                                                                     (T *)out);
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
+
+int launch_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op, int dtype,
+                               void *out, int C, int G, void *ws, cudaStream_t s) {
+  if (dtype == RR_F32) {
+    if (op == RR_OP_SUM) return launch_splitk_multi<SumF32>(x, rows, cols, out, C, G, ws, s);
+    if (op == RR_OP_MAX) return launch_splitk_multi<MaxF32>(x, rows, cols, out, C, G, ws, s);
+    return launch_splitk_multi<MinF32>(x, rows, cols, out, C, G, ws, s);
+  }
+  if (op == RR_OP_SUM) return launch_splitk_multi<SumI32>(x, rows, cols, out, C, G, ws, s);
+  if (op == RR_OP_MAX) return launch_splitk_multi<MaxI32>(x, rows, cols, out, C, G, ws, s);
+  return launch_splitk_multi<MinI32>(x, rows, cols, out, C, G, ws, s);
+}
 
 int splitk_max_cluster(int op, int dtype, int want, const DevInfo &d) {
   (void)d;

@@ -45,7 +45,6 @@ struct InBF16 {
   static __device__ __forceinline__ float load1(const S *p) {
     return __uint_as_float(((uint32_t)__ldg(p)) << 16);
   }
-  static __device__ __forceinline__ float cvt(S v) { return __uint_as_float(((uint32_t)v) << 16); }
 };
 struct InF32 {
   using S = float;
@@ -55,7 +54,6 @@ struct InF32 {
     o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
   }
   static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
-  static __device__ __forceinline__ float cvt(S v) { return v; }
 };
 
 // ---------------------------------------------------------------------------
@@ -439,19 +437,34 @@ inline int pick_nv(int64_t nvec) {
 // "cluster_allreduce" page, two-slot mode).  A cluster of C CTAs per row;
 // CTA r owns slice r of the row (a multiple of 8 elements, shifted like the
 // reduce tier's so that every slice but the first starts 16-byte aligned).
-// The slice is staged once into shared memory (one 1-D bulk copy when it is
-// 16-byte granular, plain loads otherwise) when it fits, else it is re-read.
-// Each row needs two cluster combines, done back to back on two slots with
-// no tail sync in between and one terminal cluster sync:
-//   softmax:   CTA (max, sum) pair -> combine max -> M;
-//              rescale the CTA sum to M -> combine sum -> S;
-//              y = e^(x - M) / S over the slice.
-//   layernorm: CTA sum -> combine sum -> mean;
-//              CTA sum of (x - mean)^2 -> combine sum -> var; rstd.
+// The first pass reads the slice from HBM; a second read of the same bytes
+// is served by L2 (this tier only runs for a few long rows).  Each row takes
+// two cluster combines, back to back on two slots with no tail sync between
+// them and one terminal cluster sync:
+//   softmax:   one pass of per-thread online (max, sum) over the slice, the
+//              CTA pair; combine the maxima -> M; rescale the CTA sum to M;
+//              combine the sums -> S; then y = e^(x - M) / S over the slice.
+//   layernorm: CTA sum -> combine -> mean; CTA sum of (x - mean)^2 ->
+//              combine -> var; rstd (and the rewrite).
 // Every CTA folds the partials in rank order, so every CTA holds the same
-// M, S (mean, var) bits.
+// M, S (mean, var) bits.  The passes read 8-element vectors where the slice
+// is 16-byte aligned, element by element otherwise.
 // ---------------------------------------------------------------------------
 enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
+
+// 8 consecutive elements of global memory as floats (16-byte aligned p).
+template <class In>
+__device__ __forceinline__ void load8(const typename In::S *p, float (&o)[8]) {
+  if constexpr (In::EPV == 8) {
+    In::unpack(ld_stream_u4(p), o);
+  } else {
+    const uint4 w0 = ld_stream_u4(p), w1 = ld_stream_u4(p + 4);
+    o[0] = __uint_as_float(w0.x); o[1] = __uint_as_float(w0.y);
+    o[2] = __uint_as_float(w0.z); o[3] = __uint_as_float(w0.w);
+    o[4] = __uint_as_float(w1.x); o[5] = __uint_as_float(w1.y);
+    o[6] = __uint_as_float(w1.z); o[7] = __uint_as_float(w1.w);
+  }
+}
 
 // MODE: kModeSoftmax (y fp32), kModeStats (mean, rstd), kModeLayernorm
 // (mean, rstd and the rewrite ybf = bf16((x - mean) * rstd * gamma + beta)).
@@ -460,13 +473,10 @@ __global__ void __launch_bounds__(THREADS)
 k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
                  float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
                  const float *__restrict__ gamma, const float *__restrict__ beta,
-                 uint16_t *__restrict__ ybf, int64_t stage_cap, int *err) {
+                 uint16_t *__restrict__ ybf) {
   using S = typename In::S;
-  extern __shared__ __align__(128) unsigned char dyn_raw[];
-  S *st = reinterpret_cast<S *>(dyn_raw);
   __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
   __shared__ float slot[2][2];
-  __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
   const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
   const int64_t row = cluster_id_x();
@@ -482,62 +492,83 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   const int64_t b0 = bound(r), b1 = bound(r + 1);
   const int64_t n = b1 > b0 ? b1 - b0 : 0;
   const S *ps = p + b0;
-  const bool staged = n > 0 && n <= stage_cap;
-
-  // ---- stage the slice on chip
-  if (staged) {
-    const bool bulk = ((uintptr_t)ps % 16 == 0) && ((n * (int64_t)sizeof(S)) % 16 == 0);
-    if (bulk) {
-      if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-      }
-      __syncthreads();
-      if (tid == 0) {
-        const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
-        mbar_arrive_expect_tx(&bar, bytes);
-        bulk_g2s(st, ps, bytes, &bar);
-      }
-      if (!mbar_wait_bounded(&bar, 0, kWaitBudget)) set_error(err, kErrTimeout);
-    } else {
-      for (int64_t i = tid; i < n; i += THREADS) st[i] = ps[i];
-      __syncthreads();
-    }
-  }
-  auto val = [&](int64_t i) -> float { return staged ? In::cvt(st[i]) : In::load1(ps + i); };
+  const int64_t nv = ((uintptr_t)ps % 16 == 0) ? (n >> 3) : 0;  // vectors; then a scalar tail
 
   if (MODE == kModeSoftmax) {
-    // per-thread online (max, sum) over the slice, then the CTA pair
     float m = -INFINITY, s = 0.0f;
-    for (int64_t i = tid; i < n; i += THREADS) ms_combine(m, s, val(i), 1.0f);
-    ms_block_allreduce<THREADS>(m, s, red_m, red_s);
-    // combine 1 (slot 0, no tail sync): the row max
+    for (int64_t v = tid; v < nv; v += THREADS) {
+      float e[8];
+      load8<In>(ps + v * 8, e);
+      float cm = e[0];
+#pragma unroll
+      for (int j = 1; j < 8; ++j) cm = fmaxf(cm, e[j]);
+      if (cm > m) {
+        s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kLog2e);
+        m = cm;
+      }
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += ex2_approx(fmaf(e[j], kLog2e, -mb));
+      }
+    }
+    for (int64_t i = nv * 8 + tid; i < n; i += THREADS) ms_combine(m, s, In::load1(ps + i), 1.0f);
+    ms_block_allreduce<THREADS>(m, s, red_m, red_s);  // the CTA pair, in every thread
     float v1[1] = {m}, M[1];
-    cluster_allreduce<MaxF32, 1>(slot[0], v1, C, /*tail_sync=*/false, M);
-    // combine 2 (slot 1, no tail sync): the CTA sums rescaled to that max
+    cluster_allreduce<MaxF32, 1>(slot[0], v1, C, /*tail_sync=*/false, M);  // combine 1
     float v2[1] = {(m == -INFINITY) ? 0.0f : s * ex2_approx((m - M[0]) * kLog2e)}, Ssum[1];
-    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, Ssum);
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, Ssum);  // combine 2
     const float inv = 1.0f / Ssum[0];
     const float mb = M[0] * kLog2e;
     float *yr = y + row * cols + b0;
-    for (int64_t i = tid; i < n; i += THREADS)
-      yr[i] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(val(i), kLog2e, -mb)) * inv;
+    const bool vy = ((uintptr_t)yr % 16 == 0);
+    for (int64_t v = tid; v < nv; v += THREADS) {
+      float e[8];
+      load8<In>(ps + v * 8, e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        e[j] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(e[j], kLog2e, -mb)) * inv;
+      if (vy) {
+        st_stream_v4(yr + v * 8, e[0], e[1], e[2], e[3]);
+        st_stream_v4(yr + v * 8 + 4, e[4], e[5], e[6], e[7]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) yr[v * 8 + j] = e[j];
+      }
+    }
+    for (int64_t i = nv * 8 + tid; i < n; i += THREADS)
+      yr[i] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(In::load1(ps + i), kLog2e, -mb)) * inv;
   } else {
     float acc = 0.0f;
-    for (int64_t i = tid; i < n; i += THREADS) acc += val(i);
+    for (int64_t v = tid; v < nv; v += THREADS) {
+      float e[8];
+      load8<In>(ps + v * 8, e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += e[j];
+    }
+    for (int64_t i = nv * 8 + tid; i < n; i += THREADS) acc += In::load1(ps + i);
     acc = block_reduce<SumF32, THREADS>(acc, red_s);
     float v1[1] = {acc}, tot[1];
-    cluster_allreduce<SumF32, 1>(slot[0], v1, C, /*tail_sync=*/false, tot);
+    cluster_allreduce<SumF32, 1>(slot[0], v1, C, /*tail_sync=*/false, tot);  // combine 1
     const float mu = tot[0] / (float)cols;
     float q = 0.0f;
-    for (int64_t i = tid; i < n; i += THREADS) {
-      const float d = val(i) - mu;
+    for (int64_t v = tid; v < nv; v += THREADS) {
+      float e[8];
+      load8<In>(ps + v * 8, e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = e[j] - mu;
+        q = fmaf(d, d, q);
+      }
+    }
+    for (int64_t i = nv * 8 + tid; i < n; i += THREADS) {
+      const float d = In::load1(ps + i) - mu;
       q = fmaf(d, d, q);
     }
     __syncthreads();  // red_s is reused
     q = block_reduce<SumF32, THREADS>(q, red_s);
     float v2[1] = {q}, tq[1];
-    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, tq);
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, tq);  // combine 2
     const float rs = 1.0f / sqrtf(tq[0] / (float)cols + eps);
     if (r == 0 && tid == 0) {
       if (mean) mean[row] = mu;
@@ -545,9 +576,35 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
     }
     if (MODE == kModeLayernorm) {
       uint16_t *yr = ybf + row * cols + b0;
-      for (int64_t i = tid; i < n; i += THREADS) {
-        const float o = fmaf((val(i) - mu) * rs, __ldg(gamma + b0 + i), __ldg(beta + b0 + i));
-        const __nv_bfloat16 h = __float2bfloat16_rn(o);
+      const bool vy = ((uintptr_t)yr % 16 == 0) && ((uintptr_t)(gamma + b0) % 16 == 0) &&
+                      ((uintptr_t)(beta + b0) % 16 == 0);
+      for (int64_t v = tid; v < nv; v += THREADS) {
+        float e[8];
+        load8<In>(ps + v * 8, e);
+        if (vy) {
+          const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + b0 + v * 8));
+          const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + b0 + v * 8 + 4));
+          const float4 c0 = __ldg(reinterpret_cast<const float4 *>(beta + b0 + v * 8));
+          const float4 c1 = __ldg(reinterpret_cast<const float4 *>(beta + b0 + v * 8 + 4));
+          uint4 o;
+          o.x = bf16x2_bits(fmaf((e[0] - mu) * rs, g0.x, c0.x), fmaf((e[1] - mu) * rs, g0.y, c0.y));
+          o.y = bf16x2_bits(fmaf((e[2] - mu) * rs, g0.z, c0.z), fmaf((e[3] - mu) * rs, g0.w, c0.w));
+          o.z = bf16x2_bits(fmaf((e[4] - mu) * rs, g1.x, c1.x), fmaf((e[5] - mu) * rs, g1.y, c1.y));
+          o.w = bf16x2_bits(fmaf((e[6] - mu) * rs, g1.z, c1.z), fmaf((e[7] - mu) * rs, g1.w, c1.w));
+          *reinterpret_cast<uint4 *>(yr + v * 8) = o;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int64_t i = v * 8 + j;
+            const __nv_bfloat16 h = __float2bfloat16_rn(
+                fmaf((e[j] - mu) * rs, __ldg(gamma + b0 + i), __ldg(beta + b0 + i)));
+            yr[i] = *reinterpret_cast<const uint16_t *>(&h);
+          }
+        }
+      }
+      for (int64_t i = nv * 8 + tid; i < n; i += THREADS) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(
+            fmaf((In::load1(ps + i) - mu) * rs, __ldg(gamma + b0 + i), __ldg(beta + b0 + i)));
         yr[i] = *reinterpret_cast<const uint16_t *>(&h);
       }
     }
@@ -563,34 +620,16 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
   using S = typename In::S;
   constexpr int T = 512;
   auto kern = k_rowwise_splitk<T, In, MODE>;
-  // stage the slice when it fits in shared memory (one slice per CTA)
-  const int64_t chunk = ((cols + C - 1) / C + 7) & ~int64_t(7);
-  const int64_t slice_max = chunk + 8;
-  const int64_t cap_bytes = (int64_t)d.max_smem_optin - 4096;
-  int64_t stage_cap = 0;
-  size_t smem = 0;
-  if (slice_max * (int64_t)sizeof(S) <= cap_bytes) {
-    stage_cap = slice_max;
-    smem = (size_t)(slice_max * (int64_t)sizeof(S) + 15) & ~(size_t)15;
-  }
-  cudaError_t e;
   if (C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return cuda_status(e);
-  if (C > 1 && occupancy_clusters((const void *)kern, T, smem, C, d.device) < 1) {
-    // not schedulable with this much shared memory: stream the slice twice
-    stage_cap = 0;
-    smem = 0;
-    if (occupancy_clusters((const void *)kern, T, 0, C, d.device) < 1) return RR_ERR_UNSUPPORTED;
-  }
+  if (C > 1 && occupancy_clusters((const void *)kern, T, 0, C, d.device) < 1)
+    return RR_ERR_UNSUPPORTED;
   if (rows * C > 0x7fffffffLL) return RR_ERR_INVALID;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
   cfg.blockDim = dim3(T, 1, 1);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -600,21 +639,20 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (log_enabled())
-    std::fprintf(stderr, "rr: %s split-K rows=%lld cols=%lld C=%d stage=%lld smem=%zu\n",
+    std::fprintf(stderr, "rr: %s split-K rows=%lld cols=%lld C=%d\n",
                  MODE == kModeSoftmax ? "softmax" : (MODE == kModeStats ? "lnstats" : "layernorm"),
-                 (long long)rows, (long long)cols, C, (long long)stage_cap, smem);
+                 (long long)rows, (long long)cols, C);
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const S *)xv, rows, cols, eps, y, mean, rstd,
-                                        gamma, beta, ybf, stage_cap, d.err_word));
+                                        gamma, beta, ybf));
 }
 
-// Split-K cluster size for a two-pass row op: a staged slice fills most of
-// an SM's shared memory, so one CTA per SM: the largest power of two (2..16)
-// with rows * C <= SMs; 0 when the tier does not apply (then the block tier
-// runs).
+// Split-K cluster size for a two-pass row op: the smallest power of two >= 2
+// that puts a CTA on every SM, at most 16; 0 when the tier does not apply
+// (then the block tier runs).
 inline int rowwise_splitk_cluster(int64_t rows, int64_t cols, const DevInfo &d) {
-  if (!d.cluster_launch || rows < 1 || 2 * rows > d.sm_count || cols < 16384) return 0;
+  if (!d.cluster_launch || rows < 1 || rows >= d.sm_count || cols < 16384) return 0;
   int c = 2;
-  while (c < 16 && (int64_t)(2 * c) * rows <= d.sm_count) c *= 2;
+  while (c < 16 && (int64_t)c * rows < d.sm_count) c *= 2;
   return c;
 }
 

@@ -27,6 +27,10 @@ int launch_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype,
                   void *out, cudaStream_t s, int tier, int C, int ewt,
                   void *rank_out, const DevInfo &d);
 
+// Multi-cluster split-K (G clusters of C CTAs per row, partials in ws).
+int launch_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op, int dtype,
+                               void *out, int C, int G, void *ws, cudaStream_t s);
+
 // ---- softmax / layernorm statistics (rowwise.cu)
 // tier: RR_TIER_AUTO, RR_TIER_BLOCK or RR_TIER_SPLITK; C: split-K cluster
 // size (0 = automatic).  *tier_out receives (C << 8) | tier.

@@ -117,6 +117,28 @@ int rr_reduce_ex(const void *x, int64_t rows, int64_t cols, int op, int dtype,
                  void *out, void *stream, const rr_reduce_opts *opts);
 
 /*
+ * rr_reduce_splitk_multi -- the split-K tier with several clusters per row,
+ * for rows too few to cover the GPU with one cluster each ([RW] split-K
+ * tier; [CA] within each cluster).  The row is cut into G * C slices; the G
+ * clusters of C CTAs of a row each fold C consecutive slices and combine
+ * them through distributed shared memory; the cluster results go to
+ * `workspace` (rows * G elements of the output type) and a second kernel
+ * folds each row's G partials in order.  Deterministic like every tier.
+ *   cluster_size      0 = largest the device co-schedules (<= 16), else
+ *                     1, 2, 4, 8 or 16.
+ *   clusters_per_row  G; 0 = enough that every SM gets a CTA
+ *                     (ceil(SMs / (rows * C))), at most 1024.
+ *   workspace         device, at least rows * G * 4 bytes (G as resolved;
+ *                     rows * 1024 * 4 always suffices), caller-owned, not
+ *                     overlapping x or out; its contents are scratch.
+ * Same arguments and results as rr_reduce otherwise.
+ */
+int rr_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op,
+                           int dtype, void *out, int cluster_size,
+                           int clusters_per_row, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * rr_softmax -- out[i,:] = exp(x[i,:] - m_i) / s_i with m_i = max_j x[i,j],
  * s_i = sum_j exp(x[i,j] - m_i) ([RW]: pass 1 reduces the (max, sum)
  * monoid, pass 2 is a stateless map over the row).  The row is read from
@@ -145,14 +167,14 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  *   tier          RR_TIER_AUTO, RR_TIER_BLOCK (a CTA per row, the row on
  *                 chip) or RR_TIER_SPLITK (a cluster of C CTAs per row).
  *   cluster_size  split-K: 0 = automatic, else 1, 2, 4, 8 or 16.
- * Split-K: CTA r stages slice r of the row in its shared memory when it fits
- * (one 1-D bulk copy), and the row takes two cluster combines ([CA]) on two
- * slots without a tail sync between them: softmax combines the CTA maxima,
- * then the CTA sums rescaled to the row max; layernorm combines the sums,
- * then the squared deviations about the mean.  Every CTA folds in rank
- * order, so every CTA holds the same row statistics.  AUTO picks split-K
- * when 2 * rows <= SMs and cols >= 16384, with C the largest power of two
- * (2..16) such that rows * C <= SMs.
+ * Split-K: CTA r owns slice r of the row, and the row takes two cluster
+ * combines ([CA]) on two slots without a tail sync between them: softmax
+ * combines the CTA maxima, then the CTA sums rescaled to the row max (one
+ * read of the slice for both); layernorm combines the sums, then the
+ * squared deviations about the mean.  Every CTA folds in rank order, so
+ * every CTA holds the same row statistics.  AUTO picks split-K when
+ * rows < SMs and cols >= 16384, with C the smallest power of two >= 2 such
+ * that rows * C >= SMs, at most 16.
  */
 typedef struct {
     int tier;

@@ -188,6 +188,47 @@ def test_splitk_bit_identical_100_runs(rr):
         assert (outs.view(torch.int32) == first.view(torch.int32)).all()
 
 
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int32], ids=["f32", "i32"])
+def test_splitk_multi_small(rr, oracle_mod, op, dtype):
+    for i, (rows, cols) in enumerate([(1, 1), (2, 100), (3, 4099), (1, 70000), (2, 33333)]):
+        for C, G in ((1, 1), (2, 3), (4, 0), (16, 7), (0, 0)):
+            x = gen(rows, cols, dtype, 900 + i, i % 3)
+            try:
+                got = to_np(rr.reduce_splitk_multi(x, op, cluster_size=C, clusters_per_row=G))
+            except rr.RRError as e:
+                if C == 16 and e.status == 2:
+                    continue
+                raise
+            xh = to_np(x)
+            ref = oracle_mod.reduce_rows(xh, op)
+            if op == "sum" and dtype == torch.float32:
+                assert_sum_close(got, ref, xh)
+            else:
+                assert_bits_equal(got, ref.astype(xh.dtype) if dtype == torch.int32 else ref)
+
+
+def test_splitk_multi_long_rows(rr, oracle_mod):
+    # two rows of 64M fp32: one 16-CTA cluster per row would use 32 SMs; the
+    # automatic G spreads each row over enough clusters to cover the GPU
+    from cluster_reductions_gb300 import inputs
+    x = inputs.normal_f32(2, 1 << 26, inputs.seed_for(2, 5), "cuda")
+    xh = to_np(x)
+    for op in ("sum", "max"):
+        got = rr.reduce_splitk_multi(x, op)
+        ref = oracle_mod.reduce_rows(xh, op)
+        if op == "sum":
+            assert_sum_close(to_np(got), ref, xh)
+        else:
+            assert_bits_equal(to_np(got), ref)
+        for _ in range(10):   # the same bits every run
+            assert torch.equal(rr.reduce_splitk_multi(x, op).view(torch.int32), got.view(torch.int32))
+    # one cluster per row gives the single-cluster split-K tier's bits
+    a = rr.reduce_splitk_multi(x, "sum", cluster_size=8, clusters_per_row=1)
+    b = rr.reduce(x, "sum", tier="splitk", cluster_size=8)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_argument_errors(rr):
     x = torch.zeros((4, 8), device="cuda")
     with pytest.raises(rr.RRError) as e:
