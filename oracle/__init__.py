@@ -61,6 +61,8 @@ def _load():
         lib.oracle_layernorm.argtypes = [vp, i32, i64, i64, ctypes.c_double, vp, vp,
                                          vp, vp, vp, vp]
         lib.oracle_layernorm.restype = None
+        lib.oracle_reduce_axis.argtypes = [vp, i64, i64, i64, i32, i32, vp]
+        lib.oracle_reduce_axis.restype = None
         lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         for f in (lib.oracle_reduce_f32, lib.oracle_reduce_i32,
@@ -99,6 +101,26 @@ def reduce_rows(x: np.ndarray, op) -> np.ndarray:
         lib.oracle_reduce_i32(_ptr(x), rows, cols, _op(op), _ptr(out))
     else:
         raise TypeError(f"oracle reduce: unsupported dtype {x.dtype}")
+    return out
+
+
+def reduce_axis(x: np.ndarray, op) -> np.ndarray:
+    """Reduction over the middle axis of a 3-D [outer, axis, inner] array
+    ("reduce" page: the reduce axis is ctx.axis, the other coordinates are
+    pinned), folding in axis order.  float32 -> float64 [outer, inner] (sum
+    in fp64, max/min exact); int32 -> int32 (sum wraps)."""
+    x = np.ascontiguousarray(x)
+    assert x.ndim == 3
+    outer, axis, inner = x.shape
+    if x.dtype == np.float32:
+        out = np.empty((outer, inner), np.float64)
+        dt = 0
+    elif x.dtype == np.int32:
+        out = np.empty((outer, inner), np.int32)
+        dt = 1
+    else:
+        raise TypeError(f"oracle reduce_axis: unsupported dtype {x.dtype}")
+    _load().oracle_reduce_axis(_ptr(x), outer, axis, inner, _op(op), dt, _ptr(out))
     return out
 
 

@@ -150,6 +150,46 @@ void oracle_reduce_i32(const int32_t *x, int64_t rows, int64_t cols, int op,
     }
 }
 
+/*
+ * Reduction over a non-last axis ("reduce" page: row_coords pins every
+ * dimension but ctx.axis, the reduce axis).  x is [outer][axis][inner],
+ * dense; out[o][i] folds x[o][0][i], x[o][1][i], ... in axis order, with the
+ * same element types and rules as oracle_reduce_f32 / oracle_reduce_i32
+ * (out is double for fp32 input, int32 for int32 input).  dtype: 0 = fp32,
+ * 1 = int32.
+ */
+void oracle_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner,
+                        int op, int dtype, void *out)
+{
+    for (int64_t o = 0; o < outer; ++o) {
+        for (int64_t i = 0; i < inner; ++i) {
+            if (dtype == 0) {
+                const float *xf = (const float *)x;
+                double s = 0.0;
+                float m = (op == ORC_MAX) ? -INFINITY : INFINITY;
+                for (int64_t a = 0; a < axis; ++a) {
+                    float v = xf[(o * axis + a) * inner + i];
+                    if (op == ORC_SUM) s += (double)v;
+                    else if (op == ORC_MAX) m = orc_fmax(m, v);
+                    else m = orc_fmin(m, v);
+                }
+                ((double *)out)[o * inner + i] = (op == ORC_SUM) ? s : (double)m;
+            } else {
+                const int32_t *xi = (const int32_t *)x;
+                uint32_t s = 0u;
+                int32_t m = (op == ORC_MAX) ? INT32_MIN : INT32_MAX;
+                for (int64_t a = 0; a < axis; ++a) {
+                    int32_t v = xi[(o * axis + a) * inner + i];
+                    if (op == ORC_SUM) s += (uint32_t)v;
+                    else if (op == ORC_MAX) { if (v > m) m = v; }
+                    else { if (v < m) m = v; }
+                }
+                ((int32_t *)out)[o * inner + i] = (op == ORC_SUM) ? (int32_t)s : m;
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* cluster fold ("cluster_allreduce" page: every CTA folds the peers'  */
 /* block-reduced vectors in rank order; cluster_size 1 is a broadcast) */

@@ -122,6 +122,31 @@ def test_int32_sum_wraps_like_modular_arithmetic(oracle_mod):
                                   xb.astype(np.int64).sum(axis=1))
 
 
+def test_reduce_axis_matches_numpy_and_closed_forms(oracle_mod):
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((3, 50, 7)).astype(np.float32)
+    np.testing.assert_allclose(oracle_mod.reduce_axis(x, "sum"),
+                               x.astype(np.float64).sum(axis=1), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(oracle_mod.reduce_axis(x, "max"), x.max(axis=1))
+    np.testing.assert_array_equal(oracle_mod.reduce_axis(x, "min"), x.min(axis=1))
+    # sum over the axis of arange along the axis: axis * (axis - 1) / 2 in every column
+    a = np.broadcast_to(np.arange(64, dtype=np.int32)[None, :, None], (2, 64, 5)).copy()
+    np.testing.assert_array_equal(oracle_mod.reduce_axis(a, "sum"), np.full((2, 5), 64 * 63 // 2))
+    # the reduce runs over the middle index only: a value planted at (o, a, i)
+    # shows up in out[o, i] and nowhere else
+    z = np.zeros((4, 9, 6), np.float32)
+    z[2, 5, 3] = 7.0
+    got = oracle_mod.reduce_axis(z, "sum")
+    assert got[2, 3] == 7.0 and got.sum() == 7.0
+    # inner == 1 is the row reduction
+    r = rng.standard_normal((5, 33, 1)).astype(np.float32)
+    np.testing.assert_array_equal(oracle_mod.reduce_axis(r, "max")[:, 0],
+                                  oracle_mod.reduce_rows(r[:, :, 0], "max"))
+    ri = rng.integers(-2**31, 2**31, (2, 40, 3), dtype=np.int64).astype(np.int32)
+    wrap = (ri.astype(np.int64).sum(axis=1) + 2**31) % 2**32 - 2**31
+    np.testing.assert_array_equal(oracle_mod.reduce_axis(ri, "sum"), wrap)
+
+
 # ---------------------------------------------------------------- cluster fold
 
 def _golden_fold_cases():
