@@ -23,6 +23,7 @@ workload (the method has no other reference implementation to run).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -41,6 +42,10 @@ WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx
             "sum/max/min; tiled 1Mx8 f32 sum/max/min; split-K 16x16M f32 sum/max; softmax "
             "32768x4096 bf16->f32; layernorm stats 16384x8192 bf16; split-K combine "
             "P=2,4,8 x 131072x128")
+# Reductions over a non-last axis timed beside the step ([outer, axis, inner],
+# fp32, 256 MiB each): a column reduce, a middle axis, a narrow inner axis and
+# a single long, narrow tile that needs the split workspace.
+AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 22, 16)]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -397,7 +402,7 @@ def bench_ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
-    rr.load()
+    lib = rr.load()
     specs = op_specs()
     data = []
     for name, tier, spec in specs:
@@ -406,6 +411,7 @@ def bench_ours(args):
         data.append((name, tier, spec, ins, outs))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    stream_ptr = ctypes.c_void_p(stream.cuda_stream)
 
     def step():
         for name, tier, spec, ins, outs in data:
@@ -464,7 +470,7 @@ def bench_ours(args):
                 "traffic": traffic, "algorithmic_bytes": dbytes,
                 "traffic_source": tr["profile"] if traffic is not None else None}
 
-    splitk_c, combine_v, callreduce_us, rowwise_sk, e2e = {}, {}, {}, {}, None
+    splitk_c, combine_v, callreduce_us, rowwise_sk, axis_r, e2e = {}, {}, {}, {}, {}, None
     if not args.no_extras:
         def timed(fn, nbytes, reps=20):
             for _ in range(3):
@@ -537,6 +543,33 @@ def bench_ours(args):
         rowwise_sk["layernorm_rewrite_16384x8192_bf16"] = timed(
             lambda: rr.layernorm(xl, gl, bl, 1e-5, out=yl), 16384 * 8192 * 4 + 8192 * 8)
         del xl, yl
+        # reduction over a non-last axis (automatic plan), 256 MiB inputs, two
+        # rotating buffers; called straight through the C ABI so that host
+        # overhead does not starve the ~40 us launches
+        for shape in AXIS_WORKLOADS:
+            outer, axis_n, inner = shape
+            key = "x".join(map(str, shape))
+            xa = [_inp.normal_f32(outer * axis_n, inner, 790 + i, dev) for i in range(2)]
+            oa = torch.empty((outer, inner), device=dev)
+            need = ctypes.c_size_t(0)
+            rr.check(lib.rr_reduce_axis_workspace_size(outer, axis_n, inner, 16,
+                                                        ctypes.byref(need)), "workspace size")
+            wsa = torch.empty(max(1, need.value // 4), dtype=torch.int32, device=dev)
+            opts = rr._lib.rr_axis_opts(0, 0, 0, 0, 0, wsa.data_ptr(), wsa.numel() * 4)
+            nb = outer * axis_n * inner * 4 + outer * inner * 4
+            for opname, opc in (("sum", 0), ("max", 1)):
+                calls = [(t.data_ptr(), outer, axis_n, inner, opc, 0, oa.data_ptr(),
+                          stream_ptr, ctypes.byref(opts)) for t in xa]
+                k = [0]
+
+                def one():
+                    k[0] ^= 1
+                    rr.check(lib.rr_reduce_axis_ex(*calls[k[0]]), "rr_reduce_axis_ex")
+                axis_r[f"{key}_{opname}_f32"] = timed(one, nb)
+            t, c = rr.last_tier()
+            axis_r[f"{key}_plan"] = {"tier": t, "cluster_size": c,
+                                     "workspace_bytes": need.value}
+            del xa
         # the cluster all-reduce primitive alone: one cluster, 4096 back-to-back
         # combines of one fp32 per CTA, with the tail sync and with two slots
         for C in (2, 4, 8, 16):
@@ -568,6 +601,7 @@ def bench_ours(args):
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
         "tiers": tiers, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
         "cluster_allreduce_latency": callreduce_us, "rowwise_splitk": rowwise_sk,
+        "axis_reduce": axis_r,
         "roofline": roofline,
         "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
     }

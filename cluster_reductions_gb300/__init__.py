@@ -121,6 +121,59 @@ def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
     return _to_host(o, x)
 
 
+def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.Tensor] = None,
+                tier=None, cluster_size: int = 0, emit_tile_width: int = 0, tile_rows: int = 0,
+                splits: int = 0, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """rr_reduce_axis_ex: reduce a contiguous fp32 or int32 tensor over
+    dimension `dim` (viewed as [outer, axis, inner]).  Returns the tensor's
+    shape without `dim`, same dtype.  The workspace the automatic plan asks
+    for (rr_reduce_axis_workspace_size; shapes with too few output tiles to
+    cover the GPU) is allocated here when not given."""
+    if not x.is_contiguous():
+        raise ValueError("reduce_axis: x must be contiguous")
+    if x.dim() == 0:
+        raise ValueError("reduce_axis: x must have at least one dimension")
+    dim = dim % x.dim()
+    shape = tuple(x.shape)
+    outer = 1
+    for n in shape[:dim]:
+        outer *= n
+    inner = 1
+    for n in shape[dim + 1:]:
+        inner *= n
+    axis = shape[dim]
+    xd = _to_device(x)
+    dt = _DT.get(xd.dtype)
+    if dt not in (RR_F32, RR_I32):
+        raise TypeError(f"reduce_axis: dtype {xd.dtype} not supported (float32, int32)")
+    oshape = shape[:dim] + shape[dim + 1:]
+    o = out if (out is not None and out.is_cuda) else torch.empty(oshape, dtype=xd.dtype,
+                                                                  device=xd.device)
+    lib = load()
+    ws = workspace
+    if ws is None and inner > 1 and (tier is None or splits > 1):
+        addr = xd.data_ptr()
+        align = 16 if addr % 16 == 0 else (8 if addr % 8 == 0 else 4)
+        nbytes = ctypes.c_size_t(0)
+        check(lib.rr_reduce_axis_workspace_size(outer, axis, inner, align, ctypes.byref(nbytes)),
+              "rr_reduce_axis_workspace_size")
+        need = nbytes.value
+        if splits > 1:
+            need = max(need, splits * outer * inner * 4)
+        if need:
+            ws = torch.empty((need + 3) // 4, dtype=torch.int32, device=xd.device)
+    opts = _lib.rr_axis_opts(_TIERS[tier] if not isinstance(tier, int) else tier,
+                             int(cluster_size), int(emit_tile_width), int(tile_rows), int(splits),
+                             _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size())
+    st = lib.rr_reduce_axis_ex(_ptr(xd), outer, axis, inner, _op(op), dt, _ptr(o), _stream(),
+                               ctypes.byref(opts))
+    check(st, "rr_reduce_axis")
+    if out is not None and not out.is_cuda:
+        out.copy_(o)
+        return out
+    return _to_host(o, x)
+
+
 def _rowwise_opts(tier, cluster_size):
     if tier is None and not cluster_size:
         return None
@@ -299,6 +352,18 @@ def plan_reduce(rows: int, cols: int, sm_count: int, max_cluster: int) -> Tuple[
     check(load().rr_plan_reduce(int(rows), int(cols), int(sm_count), int(max_cluster),
                                 ctypes.byref(t), ctypes.byref(c)), "rr_plan_reduce")
     return TIER_NAMES[t.value], c.value
+
+
+def plan_reduce_axis(outer: int, axis: int, inner: int, sm_count: int, max_cluster: int,
+                     x_align: int = 16, with_workspace: bool = True) -> dict:
+    """rr_plan_reduce_axis (host only): the launch rr_reduce_axis_ex picks."""
+    p = _lib.rr_axis_plan()
+    check(load().rr_plan_reduce_axis(int(outer), int(axis), int(inner), int(sm_count),
+                                     int(max_cluster), int(x_align), 1 if with_workspace else 0,
+                                     ctypes.byref(p)), "rr_plan_reduce_axis")
+    return {"tier": TIER_NAMES[p.tier], "cluster_size": p.cluster_size,
+            "emit_tile_width": p.emit_tile_width, "tile_rows": p.tile_rows,
+            "splits": p.splits, "workspace_bytes": p.workspace_bytes}
 
 
 def test_wait_timeout(budget_iters: int = 64) -> None:

@@ -31,6 +31,19 @@ class rr_rowwise_opts(ctypes.Structure):
     _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int)]
 
 
+class rr_axis_opts(ctypes.Structure):
+    _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int),
+                ("emit_tile_width", ctypes.c_int), ("tile_rows", ctypes.c_int),
+                ("splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class rr_axis_plan(ctypes.Structure):
+    _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int),
+                ("emit_tile_width", ctypes.c_int), ("tile_rows", ctypes.c_int),
+                ("splits", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
 # name -> (restype, argtypes), mirroring include/rr.h
 _i64, _int, _vp, _f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
 SIGNATURES = {
@@ -39,6 +52,13 @@ SIGNATURES = {
                             ctypes.POINTER(rr_reduce_opts)]),
     "rr_reduce_splitk_multi": (_int, [_vp, _i64, _i64, _int, _int, _vp, _int, _int, _vp,
                                       ctypes.c_size_t, _vp]),
+    "rr_reduce_axis": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp]),
+    "rr_reduce_axis_ex": (_int, [_vp, _i64, _i64, _i64, _int, _int, _vp, _vp,
+                                 ctypes.POINTER(rr_axis_opts)]),
+    "rr_plan_reduce_axis": (_int, [_i64, _i64, _i64, _int, _int, _int, _int,
+                                   ctypes.POINTER(rr_axis_plan)]),
+    "rr_reduce_axis_workspace_size": (_int, [_i64, _i64, _i64, _int,
+                                             ctypes.POINTER(ctypes.c_size_t)]),
     "rr_softmax": (_int, [_vp, _i64, _i64, _int, _vp, _vp]),
     "rr_layernorm_stats": (_int, [_vp, _i64, _i64, _int, _f32, _vp, _vp, _vp]),
     "rr_softmax_ex": (_int, [_vp, _i64, _i64, _int, _vp, _vp, ctypes.POINTER(rr_rowwise_opts)]),

@@ -293,6 +293,237 @@ int rr_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype, void
   return rr_reduce_ex(x, rows, cols, op, dtype, out, stream, nullptr);
 }
 
+// ---------------------------------------------------------------------------
+// Reduction over a non-last axis.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+// Tiles of the warp / block / split-K tiers: (o, L*V adjacent rows).
+int64_t axis_units(int64_t outer, int64_t inner, int V, int lg_L) {
+  const int64_t TW = ((int64_t)1 << lg_L) * V;
+  return outer * ((inner + TW - 1) / TW);
+}
+
+// The automatic plan for inner > 1.  Targets (S = SM count):
+//  - tiled when there are at least 2048 * S independent row groups: every
+//    thread of a full GPU owns rows and no combine is needed;
+//  - warp when the full-width tiles number at least 32 * S;
+//  - block when they number at least 2 * S, after narrowing the tile (down
+//    to 64-byte row segments) to make more of them;
+//  - split-K otherwise: the smallest power-of-two cluster giving 2 * S CTAs
+//    (at most 16 and what the device co-schedules); if even that falls
+//    short and a workspace may be used, clusters of at most 8 CTAs (16-CTA
+//    clusters pack less densely onto the SMs) and G of them per tile,
+//    enough for 3 * S CTAs, each folding at least 256 axis positions,
+//    G <= 1024.
+AxisPlan plan_axis(int64_t outer, int64_t axis, int64_t inner, int S, int max_cluster,
+                   int x_align, bool with_ws) {
+  AxisPlan p;
+  p.V = (x_align % 16 == 0 && inner % 4 == 0) ? 4 : 1;
+  const int E = p.V == 4 ? 4 : ((x_align % 8 == 0 && inner % 2 == 0) ? 2 : 1);
+  if (outer * (inner / E) >= (int64_t)S * 2048) {
+    p.tier = RR_TIER_TILED;
+    p.E = E;
+    return p;
+  }
+  int lg = 0;
+  while (lg < 5 && ((int64_t)p.V << lg) < inner) ++lg;
+  p.lg_L = lg;
+  int64_t units = axis_units(outer, inner, p.V, lg);
+  if (units >= (int64_t)S * 32) {
+    p.tier = RR_TIER_WARP;
+    return p;
+  }
+  const int lg_min = p.V == 4 ? 2 : 4;  // 64-byte segments
+  while (p.lg_L > lg_min && units < (int64_t)S * 2) {
+    --p.lg_L;
+    units = axis_units(outer, inner, p.V, p.lg_L);
+  }
+  p.tier = RR_TIER_BLOCK;
+  if (units >= (int64_t)S * 2) return p;
+  if (max_cluster >= 2) {
+    const int cap = max_cluster < 16 ? max_cluster : 16;
+    p.tier = RR_TIER_SPLITK;
+    p.C = 2;
+    while (p.C < cap && units * p.C < (int64_t)S * 2) p.C *= 2;
+    if (units * p.C >= (int64_t)S * 2) return p;
+  }
+  if (!with_ws) return p;
+  if (p.C > 8) p.C = 8;
+  int64_t G = ((int64_t)S * 3 + units * p.C - 1) / (units * p.C);
+  const int64_t gmax = axis / ((int64_t)p.C * 256);
+  if (G > gmax) G = gmax;
+  if (G > 1024) G = 1024;
+  p.G = G < 1 ? 1 : (int)G;
+  return p;
+}
+
+void plan_to_c(const AxisPlan &p, int64_t outer, int64_t inner, rr_axis_plan *c) {
+  c->tier = p.tier;
+  c->cluster_size = p.tier == RR_TIER_SPLITK ? p.C : 1;
+  c->emit_tile_width = p.tier == RR_TIER_TILED ? p.E : 0;
+  c->tile_rows = p.tier == RR_TIER_TILED ? 0 : (p.V << p.lg_L);
+  c->splits = p.G;
+  c->workspace_bytes = p.G > 1 ? (size_t)p.G * (size_t)(outer * inner) * 4 : 0;
+}
+
+std::mutex g_axis_mu;
+int g_axis_maxc[rr::kMaxDevices];
+bool g_axis_maxc_known[rr::kMaxDevices];
+
+int axis_max_cluster_cached(const rr::DevInfo &d) {
+  std::lock_guard<std::mutex> lock(g_axis_mu);
+  if (!g_axis_maxc_known[d.device]) {
+    g_axis_maxc[d.device] = rr::axis_max_cluster(16, d);
+    g_axis_maxc_known[d.device] = true;
+  }
+  return g_axis_maxc[d.device];
+}
+
+bool axis_sizes_ok(int64_t outer, int64_t axis, int64_t inner) {
+  return outer >= 0 && axis >= 0 && inner >= 0 && !mul_overflows(outer, axis, INT64_MAX / 4) &&
+         !mul_overflows(outer * axis, inner, INT64_MAX / 4) &&
+         !mul_overflows(outer, inner, INT64_MAX / 4096);
+}
+}  // namespace
+
+extern "C" {
+
+int rr_plan_reduce_axis(int64_t outer, int64_t axis, int64_t inner, int sm_count,
+                        int max_cluster, int x_align, int with_workspace, rr_axis_plan *plan) {
+  if (!axis_sizes_ok(outer, axis, inner) || sm_count < 1 || !plan ||
+      !(x_align == 4 || x_align == 8 || x_align == 16))
+    return RR_ERR_INVALID;
+  if (inner == 1) {
+    std::memset(plan, 0, sizeof(*plan));
+    plan->splits = 1;
+    return rr_plan_reduce(outer, axis, sm_count, max_cluster, &plan->tier, &plan->cluster_size);
+  }
+  plan_to_c(plan_axis(outer, axis, inner, sm_count, max_cluster, x_align, with_workspace != 0),
+            outer, inner, plan);
+  return RR_OK;
+}
+
+int rr_reduce_axis_workspace_size(int64_t outer, int64_t axis, int64_t inner, int x_align,
+                                  size_t *bytes_out) {
+  if (!bytes_out || !axis_sizes_ok(outer, axis, inner) ||
+      !(x_align == 4 || x_align == 8 || x_align == 16))
+    return RR_ERR_INVALID;
+  *bytes_out = 0;
+  if (inner <= 1 || outer == 0) return RR_OK;
+  int st = RR_OK;
+  const DevInfo *d = current_device(&st);
+  if (!d) return st;
+  rr_axis_plan c;
+  plan_to_c(plan_axis(outer, axis, inner, d->sm_count, axis_max_cluster_cached(*d), x_align, true),
+            outer, inner, &c);
+  *bytes_out = c.workspace_bytes;
+  return RR_OK;
+}
+
+int rr_reduce_axis_ex(const void *x, int64_t outer, int64_t axis, int64_t inner, int op,
+                      int dtype, void *out, void *stream, const rr_axis_opts *opts) {
+  if (!axis_sizes_ok(outer, axis, inner)) return RR_ERR_INVALID;
+  if (op < RR_OP_SUM || op > RR_OP_MIN) return RR_ERR_INVALID;
+  if (dtype != RR_F32 && dtype != RR_I32) return RR_ERR_INVALID;
+  rr_axis_opts o;
+  std::memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  if (o.tier < RR_TIER_AUTO || o.tier > RR_TIER_SPLITK) return RR_ERR_INVALID;
+  if (!(o.cluster_size == 0 || o.cluster_size == 1 || o.cluster_size == 2 ||
+        o.cluster_size == 4 || o.cluster_size == 8 || o.cluster_size == 16))
+    return RR_ERR_INVALID;
+  if (!(o.emit_tile_width == 0 || o.emit_tile_width == 1 || o.emit_tile_width == 2 ||
+        o.emit_tile_width == 4))
+    return RR_ERR_INVALID;
+  if (o.tile_rows < 0 || o.tile_rows > 128 || (o.tile_rows & (o.tile_rows - 1)) != 0)
+    return RR_ERR_INVALID;
+  if (o.splits < 0 || o.splits > 65536) return RR_ERR_INVALID;
+  if (inner == 1) {
+    if (o.tile_rows != 0 || o.splits > 1) return RR_ERR_INVALID;
+    rr_reduce_opts ro;
+    std::memset(&ro, 0, sizeof(ro));
+    ro.tier = o.tier;
+    ro.cluster_size = o.cluster_size;
+    ro.emit_tile_width = o.emit_tile_width;
+    return rr_reduce_ex(x, outer, axis, op, dtype, out, stream, &ro);
+  }
+  if (outer == 0 || inner == 0) return RR_OK;
+  const int64_t nx = outer * axis * inner, nout = outer * inner;
+  if (!out || (nx > 0 && !x)) return RR_ERR_INVALID;
+  if (overlaps(x, (size_t)nx * 4, out, (size_t)nout * 4)) return RR_ERR_INVALID;
+  if (((uintptr_t)x & 3u) != 0) return RR_ERR_INVALID;
+  const bool have_ws = o.workspace != nullptr && o.workspace_bytes > 0;
+  if (have_ws && (overlaps(o.workspace, o.workspace_bytes, x, (size_t)nx * 4) ||
+                  overlaps(o.workspace, o.workspace_bytes, out, (size_t)nout * 4)))
+    return RR_ERR_INVALID;
+  int st = RR_OK;
+  const DevInfo *d = current_device(&st);
+  if (!d) return st;
+  const int x_align = ((uintptr_t)x & 15u) == 0 ? 16 : (((uintptr_t)x & 7u) == 0 ? 8 : 4);
+  const int maxc = d->cluster_launch ? axis_max_cluster_cached(*d) : 1;
+  AxisPlan p = plan_axis(outer, axis, inner, d->sm_count, maxc, x_align, have_ws);
+  if (o.tier != RR_TIER_AUTO && o.tier != p.tier) {
+    // a forced tier: its own defaults, from the same rules
+    AxisPlan f;
+    f.tier = o.tier;
+    f.V = p.V;
+    int lg = 0;
+    while (lg < 5 && ((int64_t)f.V << lg) < inner) ++lg;
+    f.lg_L = lg;
+    if (o.tier == RR_TIER_TILED) {
+      f.E = f.V == 4 ? 4 : ((x_align >= 8 && inner % 2 == 0) ? 2 : 1);
+    } else if (o.tier == RR_TIER_SPLITK) {
+      const int64_t units = axis_units(outer, inner, f.V, f.lg_L);
+      const int cap = maxc < 16 ? maxc : 16;
+      f.C = cap < 2 ? 1 : 2;
+      while (f.C < cap && units * f.C < (int64_t)d->sm_count * 2) f.C *= 2;
+    }
+    p = f;
+  }
+  if (p.tier == RR_TIER_TILED) {
+    if (o.emit_tile_width) p.E = o.emit_tile_width;
+    if ((p.E == 4 && !(x_align == 16 && inner % 4 == 0)) ||
+        (p.E == 2 && !(x_align >= 8 && inner % 2 == 0)))
+      return RR_ERR_INVALID;
+    p.C = 1;
+    p.G = 1;
+  } else {
+    if (o.tile_rows) {
+      if (o.tile_rows % p.V != 0 || o.tile_rows / p.V > 32) return RR_ERR_INVALID;
+      int lg = 0;
+      while ((p.V << lg) < o.tile_rows) ++lg;
+      p.lg_L = lg;
+    }
+    if (p.tier == RR_TIER_SPLITK) {
+      if (o.cluster_size) p.C = o.cluster_size;
+      if (p.C > 1 && (!d->cluster_launch || maxc < p.C)) return RR_ERR_UNSUPPORTED;
+    } else {
+      p.C = 1;
+    }
+    if (p.tier == RR_TIER_WARP) p.G = 1;
+    if (o.splits) {
+      if (p.tier == RR_TIER_WARP && o.splits > 1) return RR_ERR_INVALID;
+      p.G = o.splits;
+    }
+    if (p.G > 1) {
+      if (!have_ws || o.workspace_bytes / 4 / (size_t)p.G < (size_t)nout) return RR_ERR_INVALID;
+      if (((uintptr_t)o.workspace & 3u) != 0) return RR_ERR_INVALID;
+      if (axis_units(outer, inner, p.V, p.lg_L) * p.G > ((int64_t)1 << 40)) return RR_ERR_INVALID;
+    }
+  }
+  st = launch_reduce_axis(x, outer, axis, inner, op, dtype, out, p, o.workspace,
+                          as_stream(stream), *d);
+  if (st == RR_OK) g_last_tier.store((p.C << 8) | p.tier);
+  return st;
+}
+
+int rr_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner, int op, int dtype,
+                   void *out, void *stream) {
+  return rr_reduce_axis_ex(x, outer, axis, inner, op, dtype, out, stream, nullptr);
+}
+
 static bool rowwise_opts_ok(const rr_rowwise_opts *o) {
   if (!o) return true;
   if (!(o->tier == RR_TIER_AUTO || o->tier == RR_TIER_BLOCK || o->tier == RR_TIER_SPLITK))

@@ -31,6 +31,26 @@ int launch_reduce(const void *x, int64_t rows, int64_t cols, int op, int dtype,
 int launch_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op, int dtype,
                                void *out, int C, int G, void *ws, cudaStream_t s);
 
+// ---- reduction over a non-last axis (axis.cu)
+// Largest cluster size in {16, 8, 4, 2} <= want the split-K axis kernel can
+// co-schedule, else 1.
+int axis_max_cluster(int want, const DevInfo &d);
+// One resolved launch of rr_reduce_axis for inner > 1.
+struct AxisPlan {
+  int tier = 0;  // RR_TIER_TILED, RR_TIER_WARP, RR_TIER_BLOCK or RR_TIER_SPLITK
+  int C = 1;     // split-K cluster size
+  int E = 1;     // tiled: rows per thread (1, 2 or 4)
+  int V = 1;     // warp / block / split-K: 4 (16-byte loads; inner % 4 == 0
+                 // and x 16-byte aligned) or 1
+  int lg_L = 0;  // warp / block / split-K: log2 of lanes per axis position
+                 // (tile = (1 << lg_L) * V adjacent rows)
+  int G = 1;     // block / split-K: independent CTAs / clusters per tile; G > 1
+                 // writes G partials per output to the workspace, then folds
+};
+int launch_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner, int op,
+                       int dtype, void *out, const AxisPlan &plan, void *workspace,
+                       cudaStream_t s, const DevInfo &d);
+
 // ---- softmax / layernorm statistics (rowwise.cu)
 // tier: RR_TIER_AUTO, RR_TIER_BLOCK or RR_TIER_SPLITK; C: split-K cluster
 // size (0 = automatic).  *tier_out receives (C << 8) | tier.

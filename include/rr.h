@@ -33,6 +33,7 @@
 #ifndef RR_H_
 #define RR_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -137,6 +138,95 @@ int rr_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op,
                            int dtype, void *out, int cluster_size,
                            int clusters_per_row, void *workspace,
                            size_t workspace_bytes, void *stream);
+
+/*
+ * rr_reduce_axis -- reduction over a non-last axis ([RW] Args: row_coords
+ * pins every dimension but ctx.axis, the reduce axis).  x is viewed as a
+ * dense row-major [outer][axis][inner] array and
+ *   out[o * inner + i] = x[o,0,i] (+) x[o,1,i] (+) ... (+) x[o,axis-1,i].
+ *   x      device, outer * axis * inner elements of dtype RR_F32 or RR_I32,
+ *          4-byte aligned (16-byte alignment with inner % 4 == 0 enables
+ *          128-bit loads).
+ *   out    device, outer * inner elements of the same dtype; must not
+ *          overlap x.
+ * Same element rules as rr_reduce (fp32 sum accumulated in fp32 in a fixed
+ * order, int32 sum wraps, max / min exact with the same signed-zero and NaN
+ * rules); axis == 0 writes the identity.  inner == 1 is the last-axis
+ * reduction and runs rr_reduce's tiers on (rows = outer, cols = axis).
+ * For inner > 1 the tiers are laid over the strided rows x[o,:,i]:
+ *   RR_TIER_TILED  a thread owns emit_tile_width adjacent rows (1 = the
+ *                  serial tier; 2 needs inner even and x 8-byte aligned; 4
+ *                  needs inner % 4 == 0 and x 16-byte aligned) and walks the
+ *                  axis in order;
+ *   RR_TIER_WARP   a warp owns a tile of tile_rows adjacent rows, its lanes
+ *                  split the axis and combine with shuffles;
+ *   RR_TIER_BLOCK  a CTA owns a tile, its warps split the axis and combine
+ *                  in shared memory;
+ *   RR_TIER_SPLITK a cluster of cluster_size CTAs owns a tile, each CTA
+ *                  folds one chunk of the axis, and each row is folded over
+ *                  the CTAs in rank order through distributed shared memory.
+ * Block and split-K may also cut each tile's axis into `splits` (G) parts
+ * handled by independent CTAs / clusters; their G partial results go to a
+ * caller-owned workspace of G * outer * inner * 4 bytes and a second kernel
+ * folds them in order g = 0 .. G-1.  rr_reduce_axis itself never splits
+ * (it has no workspace); rr_reduce_axis_ex splits when given a workspace,
+ * automatically when the shape has too few tiles to cover the GPU.
+ * The automatic choice is rr_plan_reduce_axis's.
+ * Errors: RR_ERR_INVALID (null pointer with work to do, negative sizes, bad
+ * op / dtype / options, overlap, a forced tile width, tile size or split
+ * count the shape, alignment or workspace does not allow),
+ * RR_ERR_UNSUPPORTED (forced cluster size the device cannot co-schedule),
+ * RR_ERR_CUDA.
+ */
+typedef struct {
+    int tier;            /* RR_TIER_AUTO or a forced tier */
+    int cluster_size;    /* split-K: 0 = automatic, else 1, 2, 4, 8 or 16 */
+    int emit_tile_width; /* tiled: 0 = automatic, else 1, 2 or 4 */
+    int tile_rows;       /* warp / block / split-K: 0 = automatic, else a
+                            power of two from V to 32 * V, where V = 4 when
+                            inner % 4 == 0 and x is 16-byte aligned (128-bit
+                            loads), else 1 */
+    int splits;          /* block / split-K: 0 = automatic (1 without a
+                            workspace), else G >= 1 */
+    void *workspace;     /* device scratch for G > 1, caller-owned, not
+                            overlapping x or out; contents are scratch */
+    size_t workspace_bytes;
+} rr_axis_opts;
+
+int rr_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner,
+                   int op, int dtype, void *out, void *stream);
+int rr_reduce_axis_ex(const void *x, int64_t outer, int64_t axis,
+                      int64_t inner, int op, int dtype, void *out,
+                      void *stream, const rr_axis_opts *opts);
+
+/* A resolved rr_reduce_axis launch (see rr_plan_reduce_axis). */
+typedef struct {
+    int tier;               /* RR_TIER_TILED / WARP / BLOCK / SPLITK */
+    int cluster_size;       /* split-K CTAs per cluster, else 1 */
+    int emit_tile_width;    /* tiled: rows per thread, else 0 */
+    int tile_rows;          /* warp / block / split-K: rows per tile, else 0 */
+    int splits;             /* G, clusters (or CTAs) per tile */
+    size_t workspace_bytes; /* G * outer * inner * 4 when G > 1, else 0 */
+} rr_axis_plan;
+
+/*
+ * rr_plan_reduce_axis -- the host-only tier choice of rr_reduce_axis_ex for
+ * a device with `sm_count` SMs whose largest co-schedulable cluster is
+ * `max_cluster` CTAs, x aligned to `x_align` bytes (4, 8 or 16), with
+ * (with_workspace != 0) or without a workspace.  inner == 1 reports the
+ * last-axis plan of rr_plan_reduce.  Touches no GPU.
+ */
+int rr_plan_reduce_axis(int64_t outer, int64_t axis, int64_t inner,
+                        int sm_count, int max_cluster, int x_align,
+                        int with_workspace, rr_axis_plan *plan);
+
+/*
+ * rr_reduce_axis_workspace_size -- bytes of workspace the automatic plan of
+ * rr_reduce_axis_ex wants on the current device for this shape and x
+ * alignment (0: it does not split).  Queries device properties only.
+ */
+int rr_reduce_axis_workspace_size(int64_t outer, int64_t axis, int64_t inner,
+                                  int x_align, size_t *bytes_out);
 
 /*
  * rr_softmax -- out[i,:] = exp(x[i,:] - m_i) / s_i with m_i = max_j x[i,j],

@@ -70,6 +70,24 @@ def test_arguments_rejected_on_the_host(lib):
                                                      ctypes.byref(n)) == INVALID
     assert n.value == -1
     assert lib.rr_test_wait_timeout(-1, null) == INVALID
+    # reduction over a non-last axis
+    from cluster_reductions_gb300._lib import rr_axis_opts
+    assert lib.rr_reduce_axis(null, -1, 4, 4, 0, 0, null, null) == INVALID
+    assert lib.rr_reduce_axis(null, 2, 4, -4, 0, 0, null, null) == INVALID
+    assert lib.rr_reduce_axis(null, 2, 4, 4, 3, 0, null, null) == INVALID    # bad op
+    assert lib.rr_reduce_axis(null, 2, 4, 4, 0, 2, null, null) == INVALID    # bf16
+    assert lib.rr_reduce_axis(null, 0, 4, 4, 0, 0, null, null) == 0          # empty: no-op
+    assert lib.rr_reduce_axis(null, 2, 4, 0, 0, 0, null, null) == 0
+    assert lib.rr_reduce_axis(null, 2, 4, 4, 0, 0, null, null) == INVALID    # null pointers
+    assert lib.rr_reduce_axis(p, 1, 2, 4, 0, 0, p + 16, null) == INVALID     # out overlaps x
+    assert lib.rr_reduce_axis(p + 2, 1, 2, 4, 0, 0, p + 128, null) == INVALID  # x not 4-aligned
+    assert lib.rr_reduce_axis(p, 1 << 40, 1 << 40, 4, 0, 0, p + 128, null) == INVALID
+    bad = rr_axis_opts(2, 0, 3)                                            # tile width 3
+    assert lib.rr_reduce_axis_ex(p, 1, 2, 4, 0, 0, p + 64, null, ctypes.byref(bad)) == INVALID
+    bad = rr_axis_opts(4, 5, 0)                                            # cluster size 5
+    assert lib.rr_reduce_axis_ex(p, 1, 2, 4, 0, 0, p + 64, null, ctypes.byref(bad)) == INVALID
+    bad = rr_axis_opts(9, 0, 0)                                            # no such tier
+    assert lib.rr_reduce_axis_ex(p, 1, 2, 4, 0, 0, p + 64, null, ctypes.byref(bad)) == INVALID
 
 
 def test_status_strings(lib):
@@ -99,6 +117,48 @@ def test_status_strings(lib):
 def test_tier_dispatch(lib, rows, cols, sms, maxc, expect):
     import cluster_reductions_gb300 as rr
     assert rr.plan_reduce(rows, cols, sms, maxc) == expect
+
+
+@pytest.mark.parametrize("shape,align,ws,expect", [
+    # (tier, cluster_size, emit_tile_width, tile_rows, splits)
+    ((262144, 16, 16), 16, True, ("tiled", 1, 4, 0, 1)),       # many short lines: no combine
+    ((262144, 16, 16), 8, True, ("tiled", 1, 2, 0, 1)),        # 8-byte aligned: pairs
+    ((32768, 256, 8), 16, True, ("warp", 1, 0, 8, 1)),
+    ((32768, 256, 8), 4, True, ("warp", 1, 0, 8, 1)),          # unaligned: scalar lanes
+    ((256, 1024, 256), 16, True, ("block", 1, 0, 128, 1)),
+    ((1, 8192, 8192), 16, True, ("block", 1, 0, 16, 1)),       # tiles narrowed to 64 bytes
+    ((16, 4096, 1024), 16, True, ("block", 1, 0, 32, 1)),
+    ((1, 65536, 1024), 16, True, ("splitk", 8, 0, 16, 1)),
+    ((64, 65536, 64), 16, True, ("splitk", 2, 0, 16, 1)),
+    ((1, 1 << 22, 16), 16, True, ("splitk", 8, 0, 16, 57)),    # one tile: G clusters
+    ((1, 1 << 22, 16), 16, False, ("splitk", 16, 0, 16, 1)),   # no workspace: one cluster
+    ((1, 1 << 22, 16), 16, True, ("splitk", 8, 0, 16, 57)),
+    ((2, 4096, 3), 4, True, ("splitk", 8, 0, 4, 2)),
+])
+def test_axis_dispatch(lib, shape, align, ws, expect):
+    import cluster_reductions_gb300 as rr
+    p = rr.plan_reduce_axis(*shape, 152, 16, x_align=align, with_workspace=ws)
+    got = (p["tier"], p["cluster_size"], p["emit_tile_width"], p["tile_rows"], p["splits"])
+    assert got == expect
+    outer, _, inner = shape
+    assert p["workspace_bytes"] == (p["splits"] * outer * inner * 4 if p["splits"] > 1 else 0)
+
+
+def test_axis_dispatch_last_axis_and_limits(lib):
+    import cluster_reductions_gb300 as rr
+    # inner == 1 is the row reduction's plan
+    p = rr.plan_reduce_axis(1 << 20, 32, 1, 152, 16)
+    assert (p["tier"], p["cluster_size"]) == rr.plan_reduce(1 << 20, 32, 152, 16)
+    p = rr.plan_reduce_axis(16, 1 << 24, 1, 152, 16)
+    assert (p["tier"], p["cluster_size"]) == ("splitk", 16)
+    # no clusters on the device: block, with the split workspace when one tile
+    p = rr.plan_reduce_axis(1, 1 << 22, 16, 152, 1)
+    assert (p["tier"], p["cluster_size"], p["splits"]) == ("block", 1, 456)
+    # G never exceeds 1024 and every split folds at least 256 positions
+    p = rr.plan_reduce_axis(1, 1 << 14, 4, 4096, 8)
+    assert p["splits"] == (1 << 14) // (8 * 256)
+    with pytest.raises(RuntimeError, match="invalid"):
+        rr.plan_reduce_axis(1, 2, 3, 152, 16, x_align=2)
 
 
 def _rank_main(rank, world, port, q):
