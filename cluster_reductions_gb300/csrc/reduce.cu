@@ -131,22 +131,19 @@ k_warp_vec(const typename Op::T *__restrict__ x, int64_t rows,
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const V *q = reinterpret_cast<const V *>(x);
   for (int64_t r0 = warp * (RPW * U); r0 < rows; r0 += nwarps * (RPW * U)) {
+    // Unconditional loads (a row past the end re-reads the last row, a valid
+    // address; its value is dropped below), so all U go out back to back.
     V v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t row = r0 + u * RPW + seg;
-      if (row < rows) {
-        v[u] = ld_stream(q + row * LPR + sub);
-      } else {
-        const T e = Op::id();
-        v[u].x = e; v[u].y = e; v[u].z = e; v[u].w = e;
-      }
+      v[u] = ld_stream(q + (row < rows ? row : rows - 1) * LPR + sub);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      T a = fold4<Op>(Op::id(), v[u]);
-      a = warp_allreduce<Op, LPR>(a);
       const int64_t row = r0 + u * RPW + seg;
+      T a = row < rows ? fold4<Op>(Op::id(), v[u]) : Op::id();
+      a = warp_allreduce<Op, LPR>(a);
       if (sub == 0 && row < rows) out[row] = Op::finalize(a);
     }
   }
@@ -200,34 +197,23 @@ k_tiled_vec(const typename Op::T *__restrict__ x, int64_t rows,
       const int64_t g = g0 + (int64_t)u * nth;
 #pragma unroll
       for (int e = 0; e < EWT; ++e) {
+        // unconditional loads: a row past the end re-reads the last row (a
+        // valid address) and is dropped below, so all loads go out back to back
         const int64_t row = g * EWT + e;
-        const bool ok = (g < groups) && (row < rows);
+        const int64_t rl = row < rows ? row : rows - 1;
         if (V8) {
 #pragma unroll
           for (int k = 0; k < NV; k += 2) {
-            if (ok) {
-              uint32_t r8[8];
-              ld_stream_v8(q + row * NV + k, r8);
-              v[u][e][k].x = from_bits<T>(r8[0]); v[u][e][k].y = from_bits<T>(r8[1]);
-              v[u][e][k].z = from_bits<T>(r8[2]); v[u][e][k].w = from_bits<T>(r8[3]);
-              v[u][e][k + 1].x = from_bits<T>(r8[4]); v[u][e][k + 1].y = from_bits<T>(r8[5]);
-              v[u][e][k + 1].z = from_bits<T>(r8[6]); v[u][e][k + 1].w = from_bits<T>(r8[7]);
-            } else {
-              const T i0 = Op::id();
-              v[u][e][k].x = i0; v[u][e][k].y = i0; v[u][e][k].z = i0; v[u][e][k].w = i0;
-              v[u][e][k + 1] = v[u][e][k];
-            }
+            uint32_t r8[8];
+            ld_stream_v8(q + rl * NV + k, r8);
+            v[u][e][k].x = from_bits<T>(r8[0]); v[u][e][k].y = from_bits<T>(r8[1]);
+            v[u][e][k].z = from_bits<T>(r8[2]); v[u][e][k].w = from_bits<T>(r8[3]);
+            v[u][e][k + 1].x = from_bits<T>(r8[4]); v[u][e][k + 1].y = from_bits<T>(r8[5]);
+            v[u][e][k + 1].z = from_bits<T>(r8[6]); v[u][e][k + 1].w = from_bits<T>(r8[7]);
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < NV; ++k) {
-            if (ok) {
-              v[u][e][k] = ld_stream(q + row * NV + k);
-            } else {
-              const T i0 = Op::id();
-              v[u][e][k].x = i0; v[u][e][k].y = i0; v[u][e][k].z = i0; v[u][e][k].w = i0;
-            }
-          }
+          for (int k = 0; k < NV; ++k) v[u][e][k] = ld_stream(q + rl * NV + k);
         }
       }
     }

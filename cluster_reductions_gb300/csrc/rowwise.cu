@@ -466,6 +466,55 @@ __device__ __forceinline__ void load8(const typename In::S *p, float (&o)[8]) {
   }
 }
 
+// Folds the 8-element vectors v = tid, tid + THREADS, ... < nv of ps, in that
+// order: st = f(st, v, e).  U vectors per thread are loaded back to back
+// before the first is used (raw words first, unpacked after), so U * 16 bytes
+// (bf16) or U * 32 bytes (fp32) per thread are in flight; the order of the
+// calls, and so every fold done in f, is the same as a one-at-a-time loop.
+// The state is passed by value so that it stays in registers.
+#ifndef RR_ROWSK_UNROLL
+#define RR_ROWSK_UNROLL 4
+#endif
+template <class In, int NW>
+__device__ __forceinline__ void unpack8(const uint4 (&w)[NW], float (&o)[8]) {
+  if constexpr (NW == 1) {
+    In::unpack(w[0], o);
+  } else {
+    o[0] = __uint_as_float(w[0].x); o[1] = __uint_as_float(w[0].y);
+    o[2] = __uint_as_float(w[0].z); o[3] = __uint_as_float(w[0].w);
+    o[4] = __uint_as_float(w[1].x); o[5] = __uint_as_float(w[1].y);
+    o[6] = __uint_as_float(w[1].z); o[7] = __uint_as_float(w[1].w);
+  }
+}
+template <int THREADS, int U, class In, class St, class F>
+__device__ __forceinline__ St fold_vectors(const typename In::S *ps, int64_t nv, St st, F f) {
+  constexpr int NW = In::EPV == 8 ? 1 : 2;  // 16-byte words per vector
+  int64_t v = threadIdx.x;
+  for (; v + (int64_t)(U - 1) * THREADS < nv; v += (int64_t)U * THREADS) {
+    uint4 w[U][NW];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NW; ++k)
+        w[u][k] = ld_stream_u4(ps + (v + (int64_t)u * THREADS) * 8 + 4 * k);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float e[8];
+      unpack8<In, NW>(w[u], e);
+      st = f(st, v + (int64_t)u * THREADS, e);
+    }
+  }
+  for (; v < nv; v += THREADS) {
+    uint4 w[NW];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) w[k] = ld_stream_u4(ps + v * 8 + 4 * k);
+    float e[8];
+    unpack8<In, NW>(w, e);
+    st = f(st, v, e);
+  }
+  return st;
+}
+
 // MODE: kModeSoftmax (y fp32), kModeStats (mean, rstd), kModeLayernorm
 // (mean, rstd and the rewrite ybf = bf16((x - mean) * rstd * gamma + beta)).
 template <int THREADS, class In, int MODE>
@@ -495,23 +544,23 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   const int64_t nv = ((uintptr_t)ps % 16 == 0) ? (n >> 3) : 0;  // vectors; then a scalar tail
 
   if (MODE == kModeSoftmax) {
-    float m = -INFINITY, s = 0.0f;
-    for (int64_t v = tid; v < nv; v += THREADS) {
-      float e[8];
-      load8<In>(ps + v * 8, e);
-      float cm = e[0];
+    const float2 ms = fold_vectors<THREADS, RR_ROWSK_UNROLL, In>(
+        ps, nv, make_float2(-INFINITY, 0.0f), [](float2 st, int64_t, const float (&e)[8]) {
+          float cm = e[0];
 #pragma unroll
-      for (int j = 1; j < 8; ++j) cm = fmaxf(cm, e[j]);
-      if (cm > m) {
-        s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - cm) * kLog2e);
-        m = cm;
-      }
-      if (m != -INFINITY) {
-        const float mb = m * kLog2e;
+          for (int j = 1; j < 8; ++j) cm = fmaxf(cm, e[j]);
+          if (cm > st.x) {
+            st.y = (st.x == -INFINITY) ? 0.0f : st.y * ex2_approx((st.x - cm) * kLog2e);
+            st.x = cm;
+          }
+          if (st.x != -INFINITY) {
+            const float mb = st.x * kLog2e;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s += ex2_approx(fmaf(e[j], kLog2e, -mb));
-      }
-    }
+            for (int j = 0; j < 8; ++j) st.y += ex2_approx(fmaf(e[j], kLog2e, -mb));
+          }
+          return st;
+        });
+    float m = ms.x, s = ms.y;
     for (int64_t i = nv * 8 + tid; i < n; i += THREADS) ms_combine(m, s, In::load1(ps + i), 1.0f);
     ms_block_allreduce<THREADS>(m, s, red_m, red_s);  // the CTA pair, in every thread
     float v1[1] = {m}, M[1];
@@ -522,45 +571,45 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
     const float mb = M[0] * kLog2e;
     float *yr = y + row * cols + b0;
     const bool vy = ((uintptr_t)yr % 16 == 0);
-    for (int64_t v = tid; v < nv; v += THREADS) {
-      float e[8];
-      load8<In>(ps + v * 8, e);
+    const float Mx = M[0];
+    fold_vectors<THREADS, RR_ROWSK_UNROLL, In>(
+        ps, nv, 0, [=](int st, int64_t v, const float (&x8)[8]) {
+          float e[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        e[j] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(e[j], kLog2e, -mb)) * inv;
-      if (vy) {
-        st_stream_v4(yr + v * 8, e[0], e[1], e[2], e[3]);
-        st_stream_v4(yr + v * 8 + 4, e[4], e[5], e[6], e[7]);
-      } else {
+          for (int j = 0; j < 8; ++j)
+            e[j] = (Mx == -INFINITY) ? 0.0f : ex2_approx(fmaf(x8[j], kLog2e, -mb)) * inv;
+          if (vy) {
+            st_stream_v4(yr + v * 8, e[0], e[1], e[2], e[3]);
+            st_stream_v4(yr + v * 8 + 4, e[4], e[5], e[6], e[7]);
+          } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) yr[v * 8 + j] = e[j];
-      }
-    }
+            for (int j = 0; j < 8; ++j) yr[v * 8 + j] = e[j];
+          }
+          return st;
+        });
     for (int64_t i = nv * 8 + tid; i < n; i += THREADS)
       yr[i] = (M[0] == -INFINITY) ? 0.0f : ex2_approx(fmaf(In::load1(ps + i), kLog2e, -mb)) * inv;
   } else {
-    float acc = 0.0f;
-    for (int64_t v = tid; v < nv; v += THREADS) {
-      float e[8];
-      load8<In>(ps + v * 8, e);
+    float acc = fold_vectors<THREADS, RR_ROWSK_UNROLL, In>(
+        ps, nv, 0.0f, [](float a, int64_t, const float (&e)[8]) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc += e[j];
-    }
+          for (int j = 0; j < 8; ++j) a += e[j];
+          return a;
+        });
     for (int64_t i = nv * 8 + tid; i < n; i += THREADS) acc += In::load1(ps + i);
     acc = block_reduce<SumF32, THREADS>(acc, red_s);
     float v1[1] = {acc}, tot[1];
     cluster_allreduce<SumF32, 1>(slot[0], v1, C, /*tail_sync=*/false, tot);  // combine 1
     const float mu = tot[0] / (float)cols;
-    float q = 0.0f;
-    for (int64_t v = tid; v < nv; v += THREADS) {
-      float e[8];
-      load8<In>(ps + v * 8, e);
+    float q = fold_vectors<THREADS, RR_ROWSK_UNROLL, In>(
+        ps, nv, 0.0f, [=](float a, int64_t, const float (&e)[8]) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float d = e[j] - mu;
-        q = fmaf(d, d, q);
-      }
-    }
+          for (int j = 0; j < 8; ++j) {
+            const float d = e[j] - mu;
+            a = fmaf(d, d, a);
+          }
+          return a;
+        });
     for (int64_t i = nv * 8 + tid; i < n; i += THREADS) {
       const float d = In::load1(ps + i) - mu;
       q = fmaf(d, d, q);
@@ -578,9 +627,8 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
       uint16_t *yr = ybf + row * cols + b0;
       const bool vy = ((uintptr_t)yr % 16 == 0) && ((uintptr_t)(gamma + b0) % 16 == 0) &&
                       ((uintptr_t)(beta + b0) % 16 == 0);
-      for (int64_t v = tid; v < nv; v += THREADS) {
-        float e[8];
-        load8<In>(ps + v * 8, e);
+      fold_vectors<THREADS, RR_ROWSK_UNROLL, In>(
+          ps, nv, 0, [=](int st, int64_t v, const float (&e)[8]) {
         if (vy) {
           const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gamma + b0 + v * 8));
           const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gamma + b0 + v * 8 + 4));
@@ -601,7 +649,8 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
             yr[i] = *reinterpret_cast<const uint16_t *>(&h);
           }
         }
-      }
+        return st;
+      });
       for (int64_t i = nv * 8 + tid; i < n; i += THREADS) {
         const __nv_bfloat16 h = __float2bfloat16_rn(
             fmaf((In::load1(ps + i) - mu) * rs, __ldg(gamma + b0 + i), __ldg(beta + b0 + i)));
