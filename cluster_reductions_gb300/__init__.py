@@ -369,3 +369,9 @@ def plan_reduce_axis(outer: int, axis: int, inner: int, sm_count: int, max_clust
 def test_wait_timeout(budget_iters: int = 64) -> None:
     """rr_test_wait_timeout: enqueue the bounded-wait probe (see rr.h)."""
     check(load().rr_test_wait_timeout(int(budget_iters), _stream()), "rr_test_wait_timeout")
+
+
+def test_inject_error(count: int = 1) -> None:
+    """rr_test_inject_error: the next `count` calls fail with RR_ERR_CUDA
+    after validating their arguments (see rr.h)."""
+    check(load().rr_test_inject_error(int(count)), "rr_test_inject_error")

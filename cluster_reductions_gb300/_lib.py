@@ -83,6 +83,7 @@ SIGNATURES = {
     "rr_plan_reduce": (_int, [_i64, _i64, _int, _int, ctypes.POINTER(_int),
                               ctypes.POINTER(_int)]),
     "rr_test_wait_timeout": (_int, [_i64, _vp]),
+    "rr_test_inject_error": (_int, [_int]),
 }
 
 _lib = None

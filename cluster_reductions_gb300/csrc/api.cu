@@ -75,7 +75,18 @@ int occupancy_blocks(const void *func, int threads, size_t smem, int device) {
   return nb;
 }
 
+int cluster_cap() {
+  static const int cap = [] {
+    const char *v = std::getenv("RR_MAX_CLUSTER");
+    if (!v || !*v) return 16;
+    const int c = std::atoi(v);
+    return c < 1 ? 1 : (c > 16 ? 16 : c);
+  }();
+  return cap;
+}
+
 int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, int device) {
+  if (cluster > cluster_cap()) return 0;
   const OccKey key{func, threads, cluster, device, smem};
   {
     std::lock_guard<std::mutex> lock(g_occ_mu);
@@ -111,7 +122,18 @@ bool log_enabled() {
   return on;
 }
 
+namespace {
+std::atomic<int> g_inject_errors{0};
+}  // namespace
+
 const DevInfo *current_device(int *status) {
+  // failure injection for tests: fail before touching the device
+  for (int n = g_inject_errors.load(); n > 0; n = g_inject_errors.load()) {
+    if (g_inject_errors.compare_exchange_weak(n, n - 1)) {
+      *status = RR_ERR_CUDA;
+      return nullptr;
+    }
+  }
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -177,6 +199,12 @@ const char *rr_status_string(int status) {
 }
 
 int rr_last_tier(void) { return g_last_tier.load(); }
+
+int rr_test_inject_error(int count) {
+  if (count < 0) return RR_ERR_INVALID;
+  g_inject_errors.store(count);
+  return RR_OK;
+}
 
 int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster, int *tier_out,
                    int *cluster_out) {

@@ -100,7 +100,7 @@ __global__ void k_wait_probe(int64_t budget, int *err) {
 
 template <class Op, int W>
 int launch_ca_w(const void *vals, int clusters, int C, int iters, int two_slot, int64_t skew,
-                void *res, int64_t *mism, cudaStream_t s) {
+                void *res, int64_t *mism, cudaStream_t s, int device) {
   using T = typename Op::T;
   auto kern = k_cluster_allreduce<Op, W>;
   if (C > 8) {
@@ -118,30 +118,22 @@ int launch_ca_w(const void *vals, int clusters, int C, int iters, int two_slot, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (C > 1) {
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return RR_ERR_UNSUPPORTED;
-    }
-    // Every cluster of the launch must be resident at once only in the
-    // sense that each one completes on its own; clusters do not wait on
-    // one another, so n >= 1 suffices.
-    if (n < 1) return RR_ERR_UNSUPPORTED;
-  }
+  // Clusters do not wait on one another, so one co-resident cluster
+  // (n >= 1) suffices.
+  if (C > 1 && occupancy_clusters((const void *)kern, kCaThreads, 0, C, device) < 1)
+    return RR_ERR_UNSUPPORTED;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const T *)vals, (T *)res, iters, two_slot,
                                         skew, (unsigned long long *)mism));
 }
 
 template <class Op>
 int launch_ca(const void *vals, int clusters, int C, int W, int iters, int two_slot,
-              int64_t skew, void *res, int64_t *mism, cudaStream_t s) {
+              int64_t skew, void *res, int64_t *mism, cudaStream_t s, int dev) {
   switch (W) {
-    case 1: return launch_ca_w<Op, 1>(vals, clusters, C, iters, two_slot, skew, res, mism, s);
-    case 2: return launch_ca_w<Op, 2>(vals, clusters, C, iters, two_slot, skew, res, mism, s);
-    case 4: return launch_ca_w<Op, 4>(vals, clusters, C, iters, two_slot, skew, res, mism, s);
-    case 8: return launch_ca_w<Op, 8>(vals, clusters, C, iters, two_slot, skew, res, mism, s);
+    case 1: return launch_ca_w<Op, 1>(vals, clusters, C, iters, two_slot, skew, res, mism, s, dev);
+    case 2: return launch_ca_w<Op, 2>(vals, clusters, C, iters, two_slot, skew, res, mism, s, dev);
+    case 4: return launch_ca_w<Op, 4>(vals, clusters, C, iters, two_slot, skew, res, mism, s, dev);
+    case 8: return launch_ca_w<Op, 8>(vals, clusters, C, iters, two_slot, skew, res, mism, s, dev);
     default: return RR_ERR_INVALID;
   }
 }
@@ -151,15 +143,14 @@ int launch_ca(const void *vals, int clusters, int C, int W, int iters, int two_s
 int launch_cluster_allreduce(const void *vals, int clusters, int C, int width, int op, int dtype,
                              int iters, int two_slot, int64_t skew_cycles, void *res,
                              int64_t *mismatches, cudaStream_t s, const DevInfo &d) {
-  (void)d;
   if (dtype == RR_F32) {
-    if (op == RR_OP_SUM) return launch_ca<SumF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
-    if (op == RR_OP_MAX) return launch_ca<MaxF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
-    return launch_ca<MinF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
+    if (op == RR_OP_SUM) return launch_ca<SumF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
+    if (op == RR_OP_MAX) return launch_ca<MaxF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
+    return launch_ca<MinF32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
   }
-  if (op == RR_OP_SUM) return launch_ca<SumI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
-  if (op == RR_OP_MAX) return launch_ca<MaxI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
-  return launch_ca<MinI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s);
+  if (op == RR_OP_SUM) return launch_ca<SumI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
+  if (op == RR_OP_MAX) return launch_ca<MaxI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
+  return launch_ca<MinI32>(vals, clusters, C, width, iters, two_slot, skew_cycles, res, mismatches, s, d.device);
 }
 
 int launch_fill_selftest_values(void *vals, int64_t n, int dtype, uint64_t seed, cudaStream_t s) {

@@ -733,13 +733,11 @@ int launch_generic(const float *O, const float *m, const float *l, int P, int64_
   if (tiles * P > 0x7fffffffLL) return RR_ERR_INVALID;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_cfg((int)tiles, P, smem, s, attr, kCombThreads);
-  if (P > 1) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_combine_generic, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      return RR_ERR_UNSUPPORTED;
-    }
-    if (n < 1) return RR_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (P > 1 && (cudaGetDevice(&dev) != cudaSuccess ||
+                occupancy_clusters((const void *)k_combine_generic, kCombThreads, smem, P, dev) < 1)) {
+    cudaGetLastError();
+    return RR_ERR_UNSUPPORTED;
   }
   if (log_enabled())
     std::fprintf(stderr, "rr: combine generic P=%d D=%d TR=%d clusters=%lld smem=%zu\n", P, D, TR,

@@ -394,19 +394,7 @@ int max_cluster_for(int want, const DevInfo &d) {
       continue;
     }
     if (C == 1) return 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)C, 1, 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) return C;
-    cudaGetLastError();
+    if (occupancy_clusters((const void *)kern, kSplitThreads, 0, C, d.device) > 0) return C;
   }
   return 0;
 }

@@ -699,9 +699,10 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
 // that puts a CTA on every SM, at most 16; 0 when the tier does not apply
 // (then the block tier runs).
 inline int rowwise_splitk_cluster(int64_t rows, int64_t cols, const DevInfo &d) {
-  if (!d.cluster_launch || rows < 1 || rows >= d.sm_count || cols < 16384) return 0;
+  const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
+  if (!d.cluster_launch || cap < 2 || rows < 1 || rows >= d.sm_count || cols < 16384) return 0;
   int c = 2;
-  while (c < 16 && (int64_t)c * rows < d.sm_count) c *= 2;
+  while (2 * c <= cap && (int64_t)c * rows < d.sm_count) c *= 2;
   return c;
 }
 

@@ -92,8 +92,16 @@ int cuda_status(cudaError_t e);
 int occupancy_blocks(const void *func, int threads, size_t smem, int device);
 
 // Largest number of co-resident clusters of `cluster` CTAs of `func`
-// (cudaOccupancyMaxActiveClusters), cached; 0 if none can run.
+// (cudaOccupancyMaxActiveClusters), cached; 0 if none can run or if
+// `cluster` exceeds cluster_cap().  Every cluster launch of the library is
+// checked through here.
 int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, int device);
+
+// Largest cluster size the library launches: the environment variable
+// RR_MAX_CLUSTER (1..16) read once, else 16.  Lets a process that shares
+// the GPU keep clusters small; the automatic plans stay within it and a
+// forced larger size returns RR_ERR_UNSUPPORTED.
+int cluster_cap();
 
 // True when the environment variable RR_LOG is set to a non-zero value:
 // launchers then print their tier and launch configuration to stderr.

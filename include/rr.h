@@ -29,6 +29,10 @@
  *   - Results are deterministic: the same inputs, shapes, pointer
  *     alignments and options give the same bits on every run (no float
  *     atomics, no occupancy-dependent partitioning of a row).
+ *   - Cluster sizes: the library launches clusters of at most 16 CTAs and
+ *     at most RR_MAX_CLUSTER (environment variable, 1..16, read once) when
+ *     that is set; automatic plans stay within it, and a forced larger
+ *     cluster size returns RR_ERR_UNSUPPORTED.
  */
 #ifndef RR_H_
 #define RR_H_
@@ -452,6 +456,15 @@ int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster,
  * reports RR_ERR_TIMEOUT and the context stays usable.
  */
 int rr_test_wait_timeout(int64_t budget_iters, void *stream);
+
+/*
+ * rr_test_inject_error -- failure-injection hook: the next `count` calls
+ * that would enqueue work validate their arguments and then return
+ * RR_ERR_CUDA, as if the CUDA runtime had refused them, without touching
+ * the device; later calls run normally.  count 0 clears a pending count.
+ * Returns RR_ERR_INVALID for count < 0.
+ */
+int rr_test_inject_error(int count);
 
 #ifdef __cplusplus
 }
