@@ -682,36 +682,33 @@ def bench_ours(args):
 
 
 def bench_e2e(args, rr, data, dev, stream, world):
-    """Same step through the public API from pinned host buffers: every
-    step copies each operation's inputs host -> device and its results
-    device -> host inside the timed region."""
+    """The same step through the public API with pinned host buffers: every
+    call takes its inputs from host memory and writes its results to host
+    memory, so each step's host -> device copies of the inputs and device ->
+    host copies of the results (staged by the binding) are inside the timed
+    region.  The 17 calls alternate between two CUDA streams, so one call's
+    results travel back while the next call's inputs travel in."""
     import torch
-    host_in, h2d, d2h = [], 0, 0
+    host_in, host_out, h2d, d2h = [], [], 0, 0
     for name, tier, spec, ins, outs in data:
         hi = []
         for t in ins:
             if t.dim() == 0:
-                hi.append(t)
+                hi.append(t.cpu())
                 continue
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
             hi.append(h)
             h2d += t.numel() * t.element_size()
-        for o in outs:
-            d2h += o.numel() * o.element_size()
         host_in.append(hi)
-    host_out = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-                for (_, _, _, _, outs) in data]
-    dev_in = [[t for t in ins] for (_, _, _, ins, _) in data]
+        host_out.append([torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs])
+        d2h += sum(o.numel() * o.element_size() for o in outs)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
 
     def step():
         for i, (name, tier, spec, ins, outs) in enumerate(data):
-            for h, d in zip(host_in[i], dev_in[i]):
-                if h.dim():
-                    d.copy_(h, non_blocking=True)
-            run_op(rr, spec, dev_in[i], outs)
-            for h, o in zip(host_out[i], outs):
-                h.copy_(o, non_blocking=True)
+            with torch.cuda.stream(streams[i % 2]):
+                run_op(rr, spec, host_in[i], host_out[i])
 
     steps = max(3, min(args.steps, args.e2e_steps))
     step()
@@ -719,8 +716,12 @@ def bench_e2e(args, rr, data, dev, stream, world):
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    for s_ in streams:
+        s_.wait_event(a)
     for _ in range(steps):
         step()
+    for s_ in streams:
+        stream.wait_stream(s_)
     b.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -728,7 +729,8 @@ def bench_e2e(args, rr, data, dev, stream, world):
     step_bytes = sum(sum(algorithmic_bytes(spec)) for _, _, spec, _, _ in data)
     return {"value": round(job_gbs(step_bytes, steps, world, ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(ms / steps, 3)}
+            "ms_per_step": round(ms / steps, 3),
+            "path": "public Python API with pinned host tensors in and out, two streams"}
 
 
 # --------------------------------------------------------------------- reference arm

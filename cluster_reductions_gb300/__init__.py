@@ -66,6 +66,35 @@ def _to_host(y: torch.Tensor, like: torch.Tensor) -> torch.Tensor:
     return h
 
 
+def _out_buf(out: Optional[torch.Tensor], shape, dtype, device) -> torch.Tensor:
+    """Device buffer a kernel writes: `out` itself when it is a CUDA tensor,
+    else a fresh device tensor (copied into a CPU `out` by _deliver).  A given
+    `out` must have exactly the result's shape and dtype and be contiguous:
+    the kernels write every element of it and nothing else."""
+    shape = tuple(shape)
+    if out is not None:
+        if tuple(out.shape) != shape or out.dtype != dtype or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous {dtype} tensor of shape {shape}, "
+                             f"got {out.dtype} {tuple(out.shape)}")
+        if out.is_cuda:
+            if out.device != device:
+                raise ValueError(f"out is on {out.device}, the input on {device}")
+            return out
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def _deliver(y: torch.Tensor, out: Optional[torch.Tensor], like: torch.Tensor) -> torch.Tensor:
+    """The result where the caller asked for it.  A CPU `out` receives a
+    copy, asynchronous when it is pinned (like torch's non_blocking copies:
+    valid once the current stream has passed this point); with no `out`, a
+    CPU input gets a CPU result the same way."""
+    if out is not None:
+        if not out.is_cuda:
+            out.copy_(y, non_blocking=out.is_pinned())
+        return out
+    return _to_host(y, like)
+
+
 def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tier=None,
            cluster_size: int = 0, emit_tile_width: int = 0,
            rank_out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -77,8 +106,7 @@ def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tie
     dt = _DT.get(xd.dtype)
     if dt not in (RR_F32, RR_I32):
         raise TypeError(f"reduce: dtype {xd.dtype} not supported (float32, int32)")
-    o = out if (out is not None and out.is_cuda) else torch.empty(rows, dtype=xd.dtype,
-                                                                  device=xd.device)
+    o = _out_buf(out, (rows,), xd.dtype, xd.device)
     lib = load()
     if tier is None and cluster_size == 0 and emit_tile_width == 0 and rank_out is None:
         st = lib.rr_reduce(_ptr(xd), rows, cols, _op(op), dt, _ptr(o), _stream())
@@ -88,10 +116,7 @@ def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tie
         st = lib.rr_reduce_ex(_ptr(xd), rows, cols, _op(op), dt, _ptr(o), _stream(),
                               ctypes.byref(opts))
     check(st, "rr_reduce")
-    if out is not None and not out.is_cuda:
-        out.copy_(o)
-        return out
-    return _to_host(o, x)
+    return _deliver(o, out, x)
 
 
 def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
@@ -106,8 +131,7 @@ def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
     dt = _DT.get(xd.dtype)
     if dt not in (RR_F32, RR_I32):
         raise TypeError(f"reduce: dtype {xd.dtype} not supported (float32, int32)")
-    o = out if (out is not None and out.is_cuda) else torch.empty(rows, dtype=xd.dtype,
-                                                                  device=xd.device)
+    o = _out_buf(out, (rows,), xd.dtype, xd.device)
     g = clusters_per_row if clusters_per_row > 0 else 1024
     ws = workspace if workspace is not None else torch.empty(max(1, rows * g), dtype=torch.int32,
                                                              device=xd.device)
@@ -115,10 +139,7 @@ def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
                                         int(cluster_size), int(clusters_per_row), _ptr(ws),
                                         ws.numel() * ws.element_size(), _stream()),
           "rr_reduce_splitk_multi")
-    if out is not None and not out.is_cuda:
-        out.copy_(o)
-        return out
-    return _to_host(o, x)
+    return _deliver(o, out, x)
 
 
 def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.Tensor] = None,
@@ -147,8 +168,7 @@ def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.
     if dt not in (RR_F32, RR_I32):
         raise TypeError(f"reduce_axis: dtype {xd.dtype} not supported (float32, int32)")
     oshape = shape[:dim] + shape[dim + 1:]
-    o = out if (out is not None and out.is_cuda) else torch.empty(oshape, dtype=xd.dtype,
-                                                                  device=xd.device)
+    o = _out_buf(out, oshape, xd.dtype, xd.device)
     lib = load()
     ws = workspace
     if ws is None and inner > 1 and (tier is None or splits > 1):
@@ -168,10 +188,7 @@ def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.
     st = lib.rr_reduce_axis_ex(_ptr(xd), outer, axis, inner, _op(op), dt, _ptr(o), _stream(),
                                ctypes.byref(opts))
     check(st, "rr_reduce_axis")
-    if out is not None and not out.is_cuda:
-        out.copy_(o)
-        return out
-    return _to_host(o, x)
+    return _deliver(o, out, x)
 
 
 def _rowwise_opts(tier, cluster_size):
@@ -191,15 +208,14 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
     dt = _DT.get(xd.dtype)
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"softmax: dtype {xd.dtype} not supported (bfloat16, float32)")
-    o = out if out is not None else torch.empty((rows, cols), dtype=torch.float32,
-                                                device=xd.device)
+    o = _out_buf(out, (rows, cols), torch.float32, xd.device)
     opts = _rowwise_opts(tier, cluster_size)
     if opts is None:
         st = load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream())
     else:
         st = load().rr_softmax_ex(_ptr(xd), rows, cols, dt, _ptr(o), _stream(), opts)
     check(st, "rr_softmax")
-    return _to_host(o, x)
+    return _deliver(o, out, x)
 
 
 def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
@@ -214,8 +230,8 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
     dt = _DT.get(xd.dtype)
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"layernorm_stats: dtype {xd.dtype} not supported")
-    mu = mean if mean is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
-    rs = rstd if rstd is not None else torch.empty(rows, dtype=torch.float32, device=xd.device)
+    mu = _out_buf(mean, (rows,), torch.float32, xd.device)
+    rs = _out_buf(rstd, (rows,), torch.float32, xd.device)
     opts = _rowwise_opts(tier, cluster_size)
     if opts is None:
         st = load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
@@ -224,7 +240,7 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
         st = load().rr_layernorm_stats_ex(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu),
                                           _ptr(rs), _stream(), opts)
     check(st, "rr_layernorm_stats")
-    return _to_host(mu, x), _to_host(rs, x)
+    return _deliver(mu, mean, x), _deliver(rs, rstd, x)
 
 
 def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
@@ -245,14 +261,19 @@ def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: flo
     if gamma.numel() != cols or beta.numel() != cols:
         raise ValueError("gamma and beta must have cols elements")
     gd, bd = _to_device(gamma.contiguous()), _to_device(beta.contiguous())
-    o = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16,
-                                                device=xd.device)
+    o = _out_buf(out, (rows, cols), torch.bfloat16, xd.device)
+    mu = None if mean is None else _out_buf(mean, (rows,), torch.float32, xd.device)
+    rs = None if rstd is None else _out_buf(rstd, (rows,), torch.float32, xd.device)
     opts = _rowwise_opts(tier, cluster_size)
-    args = (_ptr(xd), rows, cols, dt, float(eps), _ptr(gd), _ptr(bd), _ptr(o), _ptr(mean),
-            _ptr(rstd), _stream())
+    args = (_ptr(xd), rows, cols, dt, float(eps), _ptr(gd), _ptr(bd), _ptr(o), _ptr(mu),
+            _ptr(rs), _stream())
     st = load().rr_layernorm(*args) if opts is None else load().rr_layernorm_ex(*args, opts)
     check(st, "rr_layernorm")
-    return _to_host(o, x)
+    if mu is not None:
+        _deliver(mu, mean, x)
+    if rs is not None:
+        _deliver(rs, rstd, x)
+    return _deliver(o, out, x)
 
 
 def cluster_allreduce(vals: torch.Tensor, op="sum", *, two_slot: bool = False,
@@ -323,8 +344,7 @@ def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise TypeError("O, m, l must be contiguous float32")
     Od, md, ld = _to_device(O), _to_device(m), _to_device(l)
-    o = out if out is not None else torch.empty((rows, D), dtype=torch.bfloat16,
-                                                device=Od.device)
+    o = _out_buf(out, (rows, D), torch.bfloat16, Od.device)
     if mode is None:
         st = load().rr_splitk_combine(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
                                       float(scale_log2e), _ptr(o), _stream())
@@ -333,7 +353,7 @@ def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2
                                          float(scale_log2e), _ptr(o), _stream(),
                                          COMBINE_MODES[mode])
     check(st, "rr_splitk_combine")
-    return _to_host(o, O)
+    return _deliver(o, out, O)
 
 
 def device_status() -> int:
