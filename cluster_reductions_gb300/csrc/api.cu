@@ -114,6 +114,14 @@ int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, 
   return n;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *v = std::getenv("RR_PDL");
+    return !(v && std::strcmp(v, "0") == 0);
+  }();
+  return on;
+}
+
 bool log_enabled() {
   static const bool on = [] {
     const char *v = std::getenv("RR_LOG");

@@ -77,6 +77,7 @@ template <class Op, int E>
 __global__ void __launch_bounds__(kAxisThreads)
 k_axis_tiled(const typename Op::T *__restrict__ x, int64_t outer, int64_t axis,
              int64_t inner, typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   const int64_t gpo = inner / E;
   const int64_t groups = outer * gpo;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kAxisThreads, WPU == 1 ? 1 : RR_AXIS_MIN_BLOCK
 k_axis_coop(const typename Op::T *__restrict__ x, int64_t outer, int64_t axis,
             int64_t inner, int lg_L, int G, typename Op::T *__restrict__ out,
             typename Op::T *__restrict__ ws) {
+  pdl_begin();
   using T = typename Op::T;
   __shared__ T part[WPU][32 * V];
   __shared__ T slot[2][32 * V];
@@ -258,6 +260,7 @@ template <class Op>
 __global__ void __launch_bounds__(kAxisThreads)
 k_axis_fold(const typename Op::T *__restrict__ ws, int64_t n, int G,
             typename Op::T *__restrict__ out) {
+  pdl_begin();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   typename Op::T acc = ws[i];
@@ -284,11 +287,11 @@ int launch_axis_tiled(const void *xv, int64_t outer, int64_t axis, int64_t inner
     std::fprintf(stderr, "[rr] axis tiled E=%d outer=%lld axis=%lld inner=%lld grid=%lld\n", E,
                  (long long)outer, (long long)axis, (long long)inner, (long long)grid);
   if (E == 4)
-    k_axis_tiled<Op, 4><<<(unsigned)grid, kAxisThreads, 0, s>>>(x, outer, axis, inner, out);
+    launch_kernel(k_axis_tiled<Op, 4>, dim3((unsigned)grid), dim3(kAxisThreads), 0, s, 0, x, outer, axis, inner, out);
   else if (E == 2)
-    k_axis_tiled<Op, 2><<<(unsigned)grid, kAxisThreads, 0, s>>>(x, outer, axis, inner, out);
+    launch_kernel(k_axis_tiled<Op, 2>, dim3((unsigned)grid), dim3(kAxisThreads), 0, s, 0, x, outer, axis, inner, out);
   else
-    k_axis_tiled<Op, 1><<<(unsigned)grid, kAxisThreads, 0, s>>>(x, outer, axis, inner, out);
+    launch_kernel(k_axis_tiled<Op, 1>, dim3((unsigned)grid), dim3(kAxisThreads), 0, s, 0, x, outer, axis, inner, out);
   return cuda_status(cudaGetLastError());
 }
 
@@ -313,7 +316,7 @@ int launch_axis_coop(const void *xv, int64_t outer, int64_t axis, int64_t inner,
     if (log_enabled())
       std::fprintf(stderr, "[rr] axis warp V=%d L=%d units=%lld grid=%lld\n", V, 1 << lg_L,
                    (long long)units, (long long)grid);
-    kern<<<(unsigned)grid, kAxisThreads, 0, s>>>(x, outer, axis, inner, lg_L, 1, out, nullptr);
+    launch_kernel(kern, dim3((unsigned)grid), dim3(kAxisThreads), 0, s, 0, x, outer, axis, inner, lg_L, 1, out, nullptr);
     return cuda_status(cudaGetLastError());
   }
   auto kern = k_axis_coop<Op, V, kAxisWarps>;
@@ -325,7 +328,7 @@ int launch_axis_coop(const void *xv, int64_t outer, int64_t axis, int64_t inner,
     if (log_enabled())
       std::fprintf(stderr, "[rr] axis block V=%d L=%d G=%d units=%lld grid=%lld\n", V,
                    1 << lg_L, G, (long long)units, (long long)grid);
-    kern<<<(unsigned)grid, kAxisThreads, 0, s>>>(x, outer, axis, inner, lg_L, G, out, ws);
+    launch_kernel(kern, dim3((unsigned)grid), dim3(kAxisThreads), 0, s, 0, x, outer, axis, inner, lg_L, G, out, ws);
     e = cudaGetLastError();
   } else {
     if (C > 8) {
@@ -338,22 +341,12 @@ int launch_axis_coop(const void *xv, int64_t outer, int64_t axis, int64_t inner,
     if (log_enabled())
       std::fprintf(stderr, "[rr] axis split-K V=%d L=%d C=%d G=%d units=%lld clusters=%lld\n",
                    V, 1 << lg_L, C, G, (long long)units, (long long)clusters);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
-    cfg.blockDim = dim3(kAxisThreads, 1, 1);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, x, outer, axis, inner, lg_L, G, out, ws);
+    e = launch_kernel(kern, dim3((unsigned)(clusters * C)), dim3(kAxisThreads), 0, s, C, x, outer,
+                      axis, inner, lg_L, G, out, ws);
   }
   if (e != cudaSuccess || G == 1) return cuda_status(e);
   const int64_t n = outer * inner;
-  k_axis_fold<Op><<<(unsigned)((n + kAxisThreads - 1) / kAxisThreads), kAxisThreads, 0, s>>>(
+  launch_kernel(k_axis_fold<Op>, dim3((unsigned)((n + kAxisThreads - 1) / kAxisThreads)), dim3(kAxisThreads), 0, s, 0, 
       ws, n, G, out);
   return cuda_status(cudaGetLastError());
 }

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kCaThreads)
 k_cluster_allreduce(const typename Op::T *__restrict__ vals, typename Op::T *__restrict__ res,
                     int iters, int two_slot, int64_t skew,
                     unsigned long long *__restrict__ mismatches) {
+  pdl_begin();
   using T = typename Op::T;
   __shared__ T slot[2][2 * W];
   const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
@@ -69,6 +70,7 @@ k_cluster_allreduce(const typename Op::T *__restrict__ vals, typename Op::T *__r
 // Seeded per-rank values: fp32 with widely spread magnitudes (so the fold
 // order shows in the bits), or full-range int32 (so sums wrap).
 __global__ void k_fill(void *vals, int64_t n, int dtype, uint64_t seed) {
+  pdl_begin();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const uint64_t u = splitmix64(seed ^ splitmix64((uint64_t)i));
@@ -86,6 +88,7 @@ __global__ void k_fill(void *vals, int64_t n, int dtype, uint64_t seed) {
 // its phase never completes; the bounded wait gives up and records
 // kErrTimeout.  Nothing is in flight, so the kernel then returns normally.
 __global__ void k_wait_probe(int64_t budget, int *err) {
+  pdl_begin();
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 2);
@@ -107,23 +110,13 @@ int launch_ca_w(const void *vals, int clusters, int C, int iters, int two_slot, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
-  cfg.blockDim = dim3(kCaThreads, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   // Clusters do not wait on one another, so one co-resident cluster
   // (n >= 1) suffices.
   if (C > 1 && occupancy_clusters((const void *)kern, kCaThreads, 0, C, device) < 1)
     return RR_ERR_UNSUPPORTED;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const T *)vals, (T *)res, iters, two_slot,
-                                        skew, (unsigned long long *)mism));
+  return cuda_status(launch_kernel(kern, dim3((unsigned)(clusters * C)), dim3(kCaThreads), 0, s, C,
+                                   (const T *)vals, (T *)res, iters, two_slot, skew,
+                                   (unsigned long long *)mism));
 }
 
 template <class Op>
@@ -157,12 +150,12 @@ int launch_fill_selftest_values(void *vals, int64_t n, int dtype, uint64_t seed,
   if (n <= 0) return RR_OK;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  k_fill<<<(unsigned)blocks, 256, 0, s>>>(vals, n, dtype, seed);
+  launch_kernel(k_fill, dim3((unsigned)blocks), dim3(256), 0, s, 0, vals, n, dtype, seed);
   return cuda_status(cudaGetLastError());
 }
 
 int launch_wait_timeout_probe(int64_t budget, cudaStream_t s, const DevInfo &d) {
-  k_wait_probe<<<1, 32, 0, s>>>(budget, d.err_word);
+  launch_kernel(k_wait_probe, dim3(1), dim3(32), 0, s, 0, budget, d.err_word);
   return cuda_status(cudaGetLastError());
 }
 

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kPipeThreads)
 k_combine_pipe(const float *__restrict__ O, const float *__restrict__ m,
                const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
                uint16_t *__restrict__ out, int ml_bulk, int *err) {
+  pdl_begin();
   extern __shared__ __align__(128) float dyn[];
   __shared__ __align__(8) uint64_t full[kStages], pub[kStages], cons[kStages];
   __shared__ int dead;
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kPipeThreads)
 k_combine_push(const float *__restrict__ O, const float *__restrict__ m,
                const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
                uint16_t *__restrict__ out, int ml_bulk, int *err) {
+  pdl_begin();
   extern __shared__ __align__(128) float dyn[];
   __shared__ __align__(8) uint64_t full[kStages], rfull[kStages], cons[kStages];
   __shared__ int dead;
@@ -426,6 +428,7 @@ __global__ void __launch_bounds__(kPipeThreads)
 k_combine_direct(const float *__restrict__ O, const float *__restrict__ m,
                  const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
                  uint16_t *__restrict__ out, int *err) {
+  pdl_begin();
   extern __shared__ __align__(128) float dyn[];
   __shared__ __align__(8) uint64_t full[S], freed[S];
   __shared__ int dead;
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(kCombThreads)
 k_combine_generic(const float *__restrict__ O, const float *__restrict__ m,
                   const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
                   uint16_t *__restrict__ out) {
+  pdl_begin();
   extern __shared__ __align__(128) float dyn[];
   const int tid = threadIdx.x;
   const uint32_t P = cluster_nctarank(), p = cluster_ctarank();
@@ -596,22 +600,6 @@ int tile_rows(int64_t rows, int D) {
   return TR;
 }
 
-cudaLaunchConfig_t cluster_cfg(int grid_clusters, int P, size_t smem, cudaStream_t s,
-                               cudaLaunchAttribute *attr, int threads) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(grid_clusters * P), 1, 1);
-  cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = P;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
 template <class K>
 int prepare(K kern, int P, size_t smem) {
   cudaError_t e;
@@ -637,7 +625,6 @@ int launch_pipe(const float *O, const float *m, const float *l, int64_t rows, in
   int st = prepare(kern, P, smem);
   if (st != RR_OK) return st;
   const int64_t ntiles = (rows + TR - 1) / TR;
-  cudaLaunchAttribute attr[1];
   int clusters = 1;
   {
     const int n = occupancy_clusters((const void *)kern, kPipeThreads, smem, P, d.device);
@@ -650,9 +637,8 @@ int launch_pipe(const float *O, const float *m, const float *l, int64_t rows, in
   if (log_enabled())
     std::fprintf(stderr, "rr: combine pipe P=%d D=%d TR=%d stages=%d clusters=%d smem=%zu ml_bulk=%d\n",
                  P, D, TR, kStages, clusters, smem, ml_bulk);
-  cudaLaunchConfig_t cfg = cluster_cfg(clusters, P, smem, s, attr, kPipeThreads);
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, O, m, l, rows, D, TR, scale_log2e, out,
-                                        ml_bulk, d.err_word));
+  return cuda_status(launch_kernel(kern, dim3((unsigned)(clusters * P)), dim3(kPipeThreads), smem, s, P,
+                                   O, m, l, rows, D, TR, scale_log2e, out, ml_bulk, d.err_word));
 }
 
 template <int P>
@@ -671,7 +657,6 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
   int st = prepare(kern, P, smem);
   if (st != RR_OK) return st;
   const int64_t ntiles = (rows + TR - 1) / TR;
-  cudaLaunchAttribute attr[1];
   int clusters = 1;
   {
     const int n = occupancy_clusters((const void *)kern, kPipeThreads, smem, P, d.device);
@@ -683,9 +668,8 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
   if (log_enabled())
     std::fprintf(stderr, "rr: combine push P=%d D=%d TR=%d stages=%d clusters=%d smem=%zu ml_bulk=%d\n",
                  P, D, TR, kStages, clusters, smem, ml_bulk);
-  cudaLaunchConfig_t cfg = cluster_cfg(clusters, P, smem, s, attr, kPipeThreads);
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, O, m, l, rows, D, TR, scale_log2e, out,
-                                        ml_bulk, d.err_word));
+  return cuda_status(launch_kernel(kern, dim3((unsigned)(clusters * P)), dim3(kPipeThreads), smem, s, P,
+                                   O, m, l, rows, D, TR, scale_log2e, out, ml_bulk, d.err_word));
 }
 
 // Direct variant geometry per P, from a sweep on GB300 (131072 x 128 rows):
@@ -718,7 +702,7 @@ int launch_direct(const float *O, const float *m, const float *l, int64_t rows, 
   if (log_enabled())
     std::fprintf(stderr, "rr: combine direct P=%d D=%d TR=%d stages=%d ctas=%lld smem=%zu\n", P, D,
                  TR, S, (long long)grid, smem);
-  kern<<<(unsigned)grid, kPipeThreads, smem, s>>>(O, m, l, rows, D, TR, scale_log2e, out,
+  launch_kernel(kern, dim3((unsigned)grid), dim3(kPipeThreads), smem, s, 0, O, m, l, rows, D, TR, scale_log2e, out,
                                                   d.err_word);
   return cuda_status(cudaGetLastError());
 }
@@ -731,8 +715,6 @@ int launch_generic(const float *O, const float *m, const float *l, int P, int64_
   if (st != RR_OK) return st;
   const int64_t tiles = (rows + TR - 1) / TR;
   if (tiles * P > 0x7fffffffLL) return RR_ERR_INVALID;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_cfg((int)tiles, P, smem, s, attr, kCombThreads);
   int dev = 0;
   if (P > 1 && (cudaGetDevice(&dev) != cudaSuccess ||
                 occupancy_clusters((const void *)k_combine_generic, kCombThreads, smem, P, dev) < 1)) {
@@ -742,8 +724,8 @@ int launch_generic(const float *O, const float *m, const float *l, int P, int64_
   if (log_enabled())
     std::fprintf(stderr, "rr: combine generic P=%d D=%d TR=%d clusters=%lld smem=%zu\n", P, D, TR,
                  (long long)tiles, smem);
-  return cuda_status(cudaLaunchKernelEx(&cfg, k_combine_generic, O, m, l, rows, D, TR,
-                                        scale_log2e, out));
+  return cuda_status(launch_kernel(k_combine_generic, dim3((unsigned)(tiles * P)), dim3(kCombThreads),
+                                   smem, s, P, O, m, l, rows, D, TR, scale_log2e, out));
 }
 
 }  // namespace

@@ -102,6 +102,7 @@ template <class Op, int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS)
 k_block(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
         typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   __shared__ T red[THREADS / 32];
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -123,6 +124,7 @@ template <class Op, int LPR, int U>
 __global__ void __launch_bounds__(kWarpBlock)
 k_warp_vec(const typename Op::T *__restrict__ x, int64_t rows,
            typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   using V = typename Vec4<T>::type;
   constexpr int RPW = 32 / LPR;
@@ -155,6 +157,7 @@ template <class Op, int U>
 __global__ void __launch_bounds__(kWarpBlock)
 k_warp_scalar(const typename Op::T *__restrict__ x, int64_t rows, int cols,
               typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -184,6 +187,7 @@ template <class Op, int NV, int EWT, bool V8, int U>
 __global__ void __launch_bounds__(kTiledBlock)
 k_tiled_vec(const typename Op::T *__restrict__ x, int64_t rows,
             typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   using V = typename Vec4<T>::type;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -238,6 +242,7 @@ template <class Op, int EWT>
 __global__ void __launch_bounds__(kTiledBlock)
 k_tiled_scalar(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
                typename Op::T *__restrict__ out) {
+  pdl_begin();
   using T = typename Op::T;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nth = (int64_t)gridDim.x * blockDim.x;
@@ -270,6 +275,7 @@ template <class Op, int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS)
 k_splitk(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
          typename Op::T *__restrict__ out, typename Op::T *__restrict__ rank_out) {
+  pdl_begin();
   using T = typename Op::T;
   __shared__ T red[THREADS / 32];
   __shared__ T slot[2];
@@ -309,6 +315,7 @@ template <class Op, int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS)
 k_splitk_multi(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols, int G,
                typename Op::T *__restrict__ partial) {
+  pdl_begin();
   using T = typename Op::T;
   __shared__ T red[THREADS / 32];
   __shared__ T slot[2];
@@ -337,6 +344,7 @@ k_splitk_multi(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
 template <class Op>
 __global__ void k_fold_partials(const typename Op::T *__restrict__ partial, int64_t rows, int G,
                                 typename Op::T *__restrict__ out) {
+  pdl_begin();
   const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= rows) return;
   typename Op::T acc = partial[row * G];
@@ -368,20 +376,8 @@ int launch_splitk_kernel(const void *x, int64_t rows, int64_t cols, void *out,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
-  cfg.blockDim = dim3(kSplitThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const T *)x, rows, cols, (T *)out,
-                                        (T *)rank_out));
+  return cuda_status(launch_kernel(kern, dim3((unsigned)(rows * C)), dim3(kSplitThreads), 0, s, C,
+                                   (const T *)x, rows, cols, (T *)out, (T *)rank_out));
 }
 
 template <class Op>
@@ -410,7 +406,7 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
     case RR_TIER_BLOCK: {
       auto k = k_block<Op, kBlockThreads, kBlockUnroll>;
       const int g = grid_for(k, kBlockThreads, rows, d);
-      k<<<g, kBlockThreads, 0, s>>>(x, rows, cols, out);
+      launch_kernel(k, dim3(g), dim3(kBlockThreads), 0, s, 0, x, rows, cols, out);
       return cuda_status(cudaGetLastError());
     }
     case RR_TIER_WARP: {
@@ -424,7 +420,7 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
   {                                                                            \
     auto k = k_warp_vec<Op, L, kWarpUnroll>;                                   \
     const int g = grid_for(k, kWarpBlock, blocks, d);                          \
-    k<<<g, kWarpBlock, 0, s>>>(x, rows, out);                                  \
+    launch_kernel(k, dim3(g), dim3(kWarpBlock), 0, s, 0, x, rows, out);                                  \
     break;                                                                     \
   }
         switch (lpr) {
@@ -438,7 +434,7 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
         auto k = k_warp_scalar<Op, kWarpUnroll>;
         const int64_t rows_per_block = (int64_t)(kWarpBlock / 32) * kWarpUnroll;
         const int g = grid_for(k, kWarpBlock, (rows + rows_per_block - 1) / rows_per_block, d);
-        k<<<g, kWarpBlock, 0, s>>>(x, rows, (int)cols, out);
+        launch_kernel(k, dim3(g), dim3(kWarpBlock), 0, s, 0, x, rows, (int)cols, out);
       }
       return cuda_status(cudaGetLastError());
     }
@@ -454,7 +450,7 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
   {                                                                            \
     auto k = k_tiled_vec<Op, NV, E, V8, tiled_unroll(NV, E)>;                  \
     const int g = grid_for(k, kTiledBlock, blocks, d);                         \
-    k<<<g, kTiledBlock, 0, s>>>(x, rows, out);                                 \
+    launch_kernel(k, dim3(g), dim3(kTiledBlock), 0, s, 0, x, rows, out);                                 \
   }
 #define RR_TILED_E(NV, V8)                                                     \
   {                                                                            \
@@ -472,13 +468,13 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
         const int64_t blocks = (groups + kTiledBlock - 1) / kTiledBlock;
         if (e == 1) {
           auto k = k_tiled_scalar<Op, 1>;
-          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+          launch_kernel(k, dim3(grid_for(k, kTiledBlock, blocks, d)), dim3(kTiledBlock), 0, s, 0, x, rows, cols, out);
         } else if (e == 2) {
           auto k = k_tiled_scalar<Op, 2>;
-          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+          launch_kernel(k, dim3(grid_for(k, kTiledBlock, blocks, d)), dim3(kTiledBlock), 0, s, 0, x, rows, cols, out);
         } else {
           auto k = k_tiled_scalar<Op, 4>;
-          k<<<grid_for(k, kTiledBlock, blocks, d), kTiledBlock, 0, s>>>(x, rows, cols, out);
+          launch_kernel(k, dim3(grid_for(k, kTiledBlock, blocks, d)), dim3(kTiledBlock), 0, s, 0, x, rows, cols, out);
         }
       }
       return cuda_status(cudaGetLastError());
@@ -499,23 +495,13 @@ int launch_splitk_multi(const void *x, int64_t rows, int64_t cols, void *out, in
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * G * C), 1, 1);
-  cfg.blockDim = dim3(kSplitThreads, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (log_enabled())
     std::fprintf(stderr, "rr: reduce split-K multi rows=%lld cols=%lld C=%d G=%d\n",
                  (long long)rows, (long long)cols, C, G);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, (const T *)x, rows, cols, G, (T *)ws);
+  cudaError_t e = launch_kernel(kern, dim3((unsigned)(rows * G * C)), dim3(kSplitThreads), 0, s, C,
+                                (const T *)x, rows, cols, G, (T *)ws);
   if (e != cudaSuccess) return cuda_status(e);
-  k_fold_partials<Op><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>((const T *)ws, rows, G,
+  launch_kernel(k_fold_partials<Op>, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s, 0, (const T *)ws, rows, G,
                                                                      (T *)out);
   return cuda_status(cudaGetLastError());
 }

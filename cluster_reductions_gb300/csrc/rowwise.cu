@@ -117,6 +117,7 @@ template <int THREADS, int NV, class In>
 __global__ void __launch_bounds__(THREADS)
 k_softmax_reg(const typename In::S *__restrict__ x, int64_t rows, int cols,
               float *__restrict__ y) {
+  pdl_begin();
   constexpr int EPV = In::EPV;
   __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
   const int tid = threadIdx.x;
@@ -180,6 +181,7 @@ template <int THREADS, class In>
 __global__ void __launch_bounds__(THREADS)
 k_softmax_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols,
               float *__restrict__ y) {
+  pdl_begin();
   __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -207,6 +209,7 @@ template <int THREADS, int NV, class In>
 __global__ void __launch_bounds__(THREADS)
 k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
               float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
   constexpr int EPV = In::EPV;
   __shared__ float red[THREADS / 32 + 1];
   const int tid = threadIdx.x;
@@ -266,6 +269,7 @@ template <int THREADS, class In>
 __global__ void __launch_bounds__(THREADS)
 k_lnstats_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
               float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
   __shared__ float red[THREADS / 32 + 1];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -304,6 +308,7 @@ __global__ void __launch_bounds__(THREADS)
 k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
                 const float *__restrict__ gamma, const float *__restrict__ beta,
                 uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
   constexpr int EPV = In::EPV;
   __shared__ float red[THREADS / 32 + 1];
   const int tid = threadIdx.x;
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(THREADS)
 k_layernorm_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
                 const float *__restrict__ gamma, const float *__restrict__ beta,
                 uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
   __shared__ float red[THREADS / 32 + 1];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -523,6 +529,7 @@ k_rowwise_splitk(const typename In::S *__restrict__ x, int64_t rows, int64_t col
                  float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
                  const float *__restrict__ gamma, const float *__restrict__ beta,
                  uint16_t *__restrict__ ybf) {
+  pdl_begin();
   using S = typename In::S;
   __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
   __shared__ float slot[2][2];
@@ -676,23 +683,13 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
   if (C > 1 && occupancy_clusters((const void *)kern, T, 0, C, d.device) < 1)
     return RR_ERR_UNSUPPORTED;
   if (rows * C > 0x7fffffffLL) return RR_ERR_INVALID;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * C), 1, 1);
-  cfg.blockDim = dim3(T, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (log_enabled())
     std::fprintf(stderr, "rr: %s split-K rows=%lld cols=%lld C=%d\n",
                  MODE == kModeSoftmax ? "softmax" : (MODE == kModeStats ? "lnstats" : "layernorm"),
                  (long long)rows, (long long)cols, C);
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, (const S *)xv, rows, cols, eps, y, mean, rstd,
-                                        gamma, beta, ybf));
+  return cuda_status(launch_kernel(kern, dim3((unsigned)(rows * C)), dim3(T), 0, s, C,
+                                   (const S *)xv, rows, cols, eps, y, mean, rstd, gamma, beta,
+                                   ybf));
 }
 
 // Split-K cluster size for a two-pass row op: the smallest power of two >= 2
@@ -741,7 +738,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
 #define RR_SM_REG(NV)                                                          \
   {                                                                            \
     auto k = k_softmax_reg<kRowThreads, NV, In>;                               \
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, (int)cols, y); \
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, (int)cols, y); \
   }
     switch (pick_nv(nvec)) {
       case 1: RR_SM_REG(1) break;
@@ -753,7 +750,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   } else {
     *tier_out = RR_TIER_BLOCK | (1 << 8);
     auto k = k_softmax_gen<kRowThreads, In>;
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, cols, y);
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, cols, y);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -777,7 +774,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
 #define RR_LN_REG(NV)                                                          \
   {                                                                            \
     auto k = k_lnstats_reg<kRowThreads, NV, In>;                               \
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, (int)cols, eps, mean, rstd); \
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, (int)cols, eps, mean, rstd); \
   }
     switch (pick_nv(nvec)) {
       case 1: RR_LN_REG(1) break;
@@ -788,7 +785,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
 #undef RR_LN_REG
   } else {
     auto k = k_lnstats_gen<kRowThreads, In>;
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, cols, eps, mean, rstd);
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, cols, eps, mean, rstd);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -815,7 +812,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
 #define RR_LNF_REG(NV)                                                         \
   {                                                                            \
     auto k = k_layernorm_reg<kRowThreads, NV, In>;                             \
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(        \
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0,         \
         x, rows, (int)cols, eps, gamma, beta, y, mean, rstd);                  \
   }
     switch (pick_nv(nvec)) {
@@ -827,7 +824,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
 #undef RR_LNF_REG
   } else {
     auto k = k_layernorm_gen<kRowThreads, In>;
-    k<<<persistent_grid(k, kRowThreads, rows, d), kRowThreads, 0, s>>>(x, rows, cols, eps, gamma,
+    launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, cols, eps, gamma,
                                                                         beta, y, mean, rstd);
   }
   return cuda_status(cudaGetLastError());

@@ -182,6 +182,19 @@ __device__ __forceinline__ typename Op::T block_reduce(typename Op::T v,
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  First statement of every kernel: wait until
+// the previous grid in the stream has completed and its memory operations are
+// visible (griddepcontrol.wait), then let the next grid be scheduled as this
+// one's CTAs retire (griddepcontrol.launch_dependents).  The next grid runs
+// its own wait before it touches memory, so stream order holds; without the
+// launch attribute both instructions do nothing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Thread-block cluster primitives (PTX).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {

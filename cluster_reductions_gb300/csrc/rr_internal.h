@@ -103,6 +103,46 @@ int occupancy_clusters(const void *func, int threads, size_t smem, int cluster, 
 // forced larger size returns RR_ERR_UNSUPPORTED.
 int cluster_cap();
 
+// Programmatic dependent launch: unless the environment variable RR_PDL is
+// "0", every launch carries the programmatic-stream-serialization attribute,
+// so the next kernel in a stream is scheduled while this one drains.  Every
+// kernel starts with pdl_begin() (rr_device.cuh), which waits for the
+// previous grid to complete and its memory to be visible before touching
+// global memory, so stream order is kept.
+bool pdl_enabled();
+
+// Launches `kern` on `s` with the programmatic-dependent-launch attribute
+// (pdl_enabled()).  cluster == 0: a plain launch; cluster >= 1: a cluster
+// launch with 1-D clusters of `cluster` CTAs -- a kernel that uses cluster
+// instructions (distributed shared memory, bulk copies to shared::cluster,
+// cluster barriers) must be launched this way even when the size is 1.
+template <class... KArgs, class... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, int cluster, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cluster >= 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // True when the environment variable RR_LOG is set to a non-zero value:
 // launchers then print their tier and launch configuration to stderr.
 bool log_enabled();
