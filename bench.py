@@ -57,18 +57,18 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1084725248, "src_sha": "a33fcd57c83270da",
-                       "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 575941632, "src_sha": "a33fcd57c83270da",
-                   "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 562900992, "src_sha": "a33fcd57c83270da",
-                     "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271407360, "src_sha": "a33fcd57c83270da",
-                      "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271453696, "src_sha": "a33fcd57c83270da",
-                       "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 137698048, "src_sha": "a33fcd57c83270da",
-                     "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "splitk_sum_f32": {"bytes": 1086637056, "src_sha": "d561edecfa3fdb91",
+                      "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 577272832, "src_sha": "d561edecfa3fdb91",
+                  "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+    "softmax_bf16": {"bytes": 563722240, "src_sha": "d561edecfa3fdb91",
+                    "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271636480, "src_sha": "d561edecfa3fdb91",
+                     "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271495680, "src_sha": "d561edecfa3fdb91",
+                      "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 138011136, "src_sha": "d561edecfa3fdb91",
+                    "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
