@@ -57,17 +57,17 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1086637056, "src_sha": "d561edecfa3fdb91",
+    "splitk_sum_f32": {"bytes": 1085805568, "src_sha": "29017bc1ec288863",
                       "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 577272832, "src_sha": "d561edecfa3fdb91",
+    "combine_p8": {"bytes": 574952448, "src_sha": "29017bc1ec288863",
                   "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 563722240, "src_sha": "d561edecfa3fdb91",
+    "softmax_bf16": {"bytes": 563512320, "src_sha": "29017bc1ec288863",
                     "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271636480, "src_sha": "d561edecfa3fdb91",
+    "block_sum_f32": {"bytes": 271382784, "src_sha": "29017bc1ec288863",
                      "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271495680, "src_sha": "d561edecfa3fdb91",
+    "layernorm_bf16": {"bytes": 271763712, "src_sha": "29017bc1ec288863",
                       "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 138011136, "src_sha": "d561edecfa3fdb91",
+    "warp_sum_f32": {"bytes": 137933312, "src_sha": "29017bc1ec288863",
                     "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
@@ -833,7 +833,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",

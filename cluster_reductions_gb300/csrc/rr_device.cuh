@@ -184,15 +184,14 @@ __device__ __forceinline__ typename Op::T block_reduce(typename Op::T v,
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  First statement of every kernel: wait until
 // the previous grid in the stream has completed and its memory operations are
-// visible (griddepcontrol.wait), then let the next grid be scheduled as this
-// one's CTAs retire (griddepcontrol.launch_dependents).  The next grid runs
-// its own wait before it touches memory, so stream order holds; without the
-// launch attribute both instructions do nothing.
+// visible (griddepcontrol.wait).  The launch attribute lets this grid be set
+// up while the previous one drains; the dependency on the previous grid is
+// released as its blocks exit (no explicit launch_dependents: releasing it at
+// a kernel's start let the next grid's CTAs take SM slots from persistent
+// cluster kernels and slowed them).  Without the attribute the wait does
+// nothing.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void pdl_begin() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+__device__ __forceinline__ void pdl_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Thread-block cluster primitives (PTX).

@@ -105,7 +105,7 @@ int cluster_cap();
 
 // Programmatic dependent launch: unless the environment variable RR_PDL is
 // "0", every launch carries the programmatic-stream-serialization attribute,
-// so the next kernel in a stream is scheduled while this one drains.  Every
+// so a kernel is set up while the previous one in the stream drains.  Every
 // kernel starts with pdl_begin() (rr_device.cuh), which waits for the
 // previous grid to complete and its memory to be visible before touching
 // global memory, so stream order is kept.
