@@ -52,23 +52,24 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per full-size launch from ncu captures (dram__bytes_read.sum +
 # dram__bytes_write.sum of one launch of `bench.py --case <op>`, scaled by
 # the units the full workload has over the captured case), keyed by
-# operation name, valid only while the kernel sources hash to `src_sha`.
+# operation name, valid only while the kernel's sources (`src`: its
+# translation unit and the device header) hash to `src_sha`.
 # The captures and their commands are summarised in profiles/.  Softmax's
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1085805568, "src_sha": "29017bc1ec288863",
-                      "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 574952448, "src_sha": "29017bc1ec288863",
-                  "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 563512320, "src_sha": "29017bc1ec288863",
-                    "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271382784, "src_sha": "29017bc1ec288863",
-                     "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271763712, "src_sha": "29017bc1ec288863",
-                      "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 137933312, "src_sha": "29017bc1ec288863",
-                    "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "splitk_sum_f32": {"bytes": 1085805568, "src": ["reduce.cu", "rr_device.cuh"],
+                      "src_sha": "ff130b7d5dec070b", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 574952448, "src": ["combine.cu", "rr_device.cuh"],
+                  "src_sha": "4940fce09d72f11f", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+    "softmax_bf16": {"bytes": 563512320, "src": ["rowwise.cu", "rr_device.cuh"],
+                    "src_sha": "bb50ab4b17fa3a86", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271382784, "src": ["reduce.cu", "rr_device.cuh"],
+                     "src_sha": "ff130b7d5dec070b", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271763712, "src": ["rowwise.cu", "rr_device.cuh"],
+                      "src_sha": "bb50ab4b17fa3a86", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137933312, "src": ["reduce.cu", "rr_device.cuh"],
+                    "src_sha": "ff130b7d5dec070b", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
@@ -226,10 +227,13 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_src_sha() -> str:
+def kernel_src_sha(files=None) -> str:
+    """Hash of kernel sources under cluster_reductions_gb300/csrc: the named
+    files (a kernel's translation unit and the device header it includes),
+    else every file."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "cluster_reductions_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files if files else os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -479,9 +483,8 @@ def bench_ours(args):
     dname, _, dspec, _, _ = data[dom]
     dbytes = sum(algorithmic_bytes(dspec))
     achieved = dbytes / (dom_ms / 1e3) / 1e9
-    sha = kernel_src_sha()
     tr = NCU_TRAFFIC.get(dname)
-    traffic = tr["bytes"] if (tr and tr.get("src_sha") == sha) else None
+    traffic = tr["bytes"] if (tr and tr.get("src_sha") == kernel_src_sha(tr.get("src"))) else None
     roofline = {"bound": "hbm", "kernel": dname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": f"{peak_kind} copy bandwidth (read+write)",

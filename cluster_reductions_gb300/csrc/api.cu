@@ -676,6 +676,8 @@ int rr_cluster_allreduce(const void *vals, int clusters, int cluster_size, int w
   if ((int64_t)clusters * cluster_size > INT_MAX) return RR_ERR_INVALID;
   if (iters == 0) return RR_OK;
   if (!vals || !res) return RR_ERR_INVALID;
+  if (mul_overflows((int64_t)iters, (int64_t)clusters * cluster_size * width, INT64_MAX / 4))
+    return RR_ERR_INVALID;
   const size_t n = (size_t)iters * clusters * cluster_size * width * 4;
   if (overlaps(vals, n, res, n)) return RR_ERR_INVALID;
   int st = RR_OK;
@@ -757,7 +759,6 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P, 
   int st = RR_OK;
   const DevInfo *d = current_device(&st);
   if (!d) return st;
-  if (P > 1 && !d->cluster_launch) return RR_ERR_UNSUPPORTED;
   return launch_combine(O, m, l, P, rows, D, scale_log2e, out_bf16, as_stream(stream), *d, mode);
 }
 

@@ -750,6 +750,8 @@ int launch_combine(const float *O, const float *m, const float *l, int P, int64_
       default: return launch_direct<16>(O, m, l, rows, D, scale_log2e, out, s, d);
     }
   }
+  // the remaining variants exchange through a cluster of P CTAs
+  if (P > 1 && !d.cluster_launch) return RR_ERR_UNSUPPORTED;
   if (mode == RR_COMBINE_PUSH) {
     if (!push_ok) return RR_ERR_UNSUPPORTED;
     switch (P) {

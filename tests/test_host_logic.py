@@ -64,6 +64,9 @@ def test_arguments_rejected_on_the_host(lib):
     assert lib.rr_splitk_combine(p, p, p, 2, 4, 0, ctypes.c_float(1.0), p, null) == INVALID
     assert lib.rr_splitk_combine(p, p, p, 2, 4, 8, ctypes.c_float(float("inf")), p, null) == INVALID
     assert lib.rr_cluster_allreduce(p, 1, 2, 3, 0, 0, 4, 0, 0, p, null, null) == INVALID
+    # iters * clusters * cluster_size * width elements would not fit a size_t
+    assert lib.rr_cluster_allreduce(p, 1 << 30, 16, 8, 0, 0, 1 << 30, 0, 0, p + 4096, null,
+                                    null) == INVALID
     n = ctypes.c_int64(-1)
     assert lib.rr_cluster_allreduce_selftest(2, 1, 0, 0, 0, 0, 1, null, ctypes.byref(n)) == INVALID
     assert lib.rr_cluster_allreduce_selftest_noalloc(16, 8, 0, 0, 1025, 1, 1, null,
