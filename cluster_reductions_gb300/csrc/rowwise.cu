@@ -93,16 +93,24 @@ __device__ __forceinline__ void ms_block_allreduce(float &m, float &s, float *re
   s = red_s[NW];
 }
 
-// Block sum; every thread receives the result.
+// Block sum returned to every thread with one barrier: an xor butterfly in
+// each warp (every lane ends with the same bits), the warp sums to `red`, one
+// barrier, then every thread folds red[0..NW-1] in warp order.  Consecutive
+// calls must alternate between two `red` buffers: a thread may still be
+// reading one call's sums while a faster thread writes the next call's, and
+// the barrier of the call in between keeps the third call off the first
+// buffer.  (The (max, sum) pair above keeps its two barriers: folding NW
+// pairs in every thread costs more exp2 than the barrier saves.)
 template <int THREADS>
 __device__ __forceinline__ float sum_block_allreduce(float v, float *red) {
   constexpr int NW = THREADS / 32;
-  v = block_reduce<SumF32, THREADS>(v, red);
-  if (threadIdx.x == 0) red[NW] = v;
+  v = warp_allreduce<SumF32, 32>(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  v = red[NW];
-  __syncthreads();
-  return v;
+  float t = red[0];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) t += red[i];
+  return t;
 }
 
 // ---------------------------------------------------------------------------
@@ -211,7 +219,7 @@ k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, floa
               float *__restrict__ mean, float *__restrict__ rstd) {
   pdl_begin();
   constexpr int EPV = In::EPV;
-  __shared__ float red[THREADS / 32 + 1];
+  __shared__ float red[2][THREADS / 32];
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
   const float inv_n = 1.0f / (float)cols;
@@ -243,7 +251,7 @@ k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, floa
     for (int k = 0; k < NV; ++k)
 #pragma unroll
       for (int e = 0; e < EPV; ++e) s += v[k][e];
-    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    const float mu = sum_block_allreduce<THREADS>(s, red[0]) / (float)cols;
     float qs = 0.0f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
@@ -255,7 +263,7 @@ k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, floa
         }
       }
     }
-    const float var = sum_block_allreduce<THREADS>(qs, red) * inv_n;
+    const float var = sum_block_allreduce<THREADS>(qs, red[1]) * inv_n;
     if (tid == 0) {
       mean[row] = mu;
       rstd[row] = 1.0f / sqrtf(var + eps);
@@ -270,19 +278,19 @@ __global__ void __launch_bounds__(THREADS)
 k_lnstats_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, float eps,
               float *__restrict__ mean, float *__restrict__ rstd) {
   pdl_begin();
-  __shared__ float red[THREADS / 32 + 1];
+  __shared__ float red[2][THREADS / 32];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const typename In::S *p = x + row * cols;
     float s = 0.0f;
     for (int64_t i = tid; i < cols; i += THREADS) s += In::load1(p + i);
-    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    const float mu = sum_block_allreduce<THREADS>(s, red[0]) / (float)cols;
     float qs = 0.0f;
     for (int64_t i = tid; i < cols; i += THREADS) {
       const float dlt = In::load1(p + i) - mu;
       qs = fmaf(dlt, dlt, qs);
     }
-    const float var = sum_block_allreduce<THREADS>(qs, red) / (float)cols;
+    const float var = sum_block_allreduce<THREADS>(qs, red[1]) / (float)cols;
     if (tid == 0) {
       mean[row] = mu;
       rstd[row] = 1.0f / sqrtf(var + eps);
@@ -310,7 +318,7 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
                 uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
   pdl_begin();
   constexpr int EPV = In::EPV;
-  __shared__ float red[THREADS / 32 + 1];
+  __shared__ float red[2][THREADS / 32];
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
   const float inv_n = 1.0f / (float)cols;
@@ -342,7 +350,7 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
     for (int k = 0; k < NV; ++k)
 #pragma unroll
       for (int e = 0; e < EPV; ++e) s += v[k][e];
-    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    const float mu = sum_block_allreduce<THREADS>(s, red[0]) / (float)cols;
     float qs = 0.0f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
@@ -354,7 +362,7 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
         }
       }
     }
-    const float var = sum_block_allreduce<THREADS>(qs, red) * inv_n;
+    const float var = sum_block_allreduce<THREADS>(qs, red[1]) * inv_n;
     const float rs = 1.0f / sqrtf(var + eps);
     uint16_t *yr = y + row * (int64_t)cols;
 #pragma unroll
@@ -397,19 +405,19 @@ k_layernorm_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols
                 const float *__restrict__ gamma, const float *__restrict__ beta,
                 uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
   pdl_begin();
-  __shared__ float red[THREADS / 32 + 1];
+  __shared__ float red[2][THREADS / 32];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const typename In::S *p = x + row * cols;
     float s = 0.0f;
     for (int64_t i = tid; i < cols; i += THREADS) s += In::load1(p + i);
-    const float mu = sum_block_allreduce<THREADS>(s, red) / (float)cols;
+    const float mu = sum_block_allreduce<THREADS>(s, red[0]) / (float)cols;
     float qs = 0.0f;
     for (int64_t i = tid; i < cols; i += THREADS) {
       const float dlt = In::load1(p + i) - mu;
       qs = fmaf(dlt, dlt, qs);
     }
-    const float rs = 1.0f / sqrtf(sum_block_allreduce<THREADS>(qs, red) / (float)cols + eps);
+    const float rs = 1.0f / sqrtf(sum_block_allreduce<THREADS>(qs, red[1]) / (float)cols + eps);
     uint16_t *yr = y + row * cols;
     for (int64_t i = tid; i < cols; i += THREADS) {
       const __nv_bfloat16 h =
