@@ -289,19 +289,21 @@ __device__ __forceinline__ void cluster_allreduce(typename Op::T *slot,
     }
     cluster_sync();
     if (threadIdx.x == 0) {
+      // all C loads of an element go out before the first is folded (C <= 16),
+      // so the gather costs about one distributed-shared-memory round trip
       const uint32_t base = smem_u32(slot);
-      T acc[W];
 #pragma unroll
-      for (int j = 0; j < W; ++j)
-        acc[j] = from_bits<T>(ld_dsmem_u32(map_peer(base + 4u * j, 0)));
-      for (uint32_t r = 1; r < C; ++r) {
-        const uint32_t peer = map_peer(base, r);
+      for (int j = 0; j < W; ++j) {
+        uint32_t raw[16];
 #pragma unroll
-        for (int j = 0; j < W; ++j)
-          acc[j] = Op::f(acc[j], from_bits<T>(ld_dsmem_u32(peer + 4u * j)));
+        for (int r = 0; r < 16; ++r)
+          if ((uint32_t)r < C) raw[r] = ld_dsmem_u32(map_peer(base + 4u * j, (uint32_t)r));
+        T acc = from_bits<T>(raw[0]);
+#pragma unroll
+        for (int r = 1; r < 16; ++r)
+          if ((uint32_t)r < C) acc = Op::f(acc, from_bits<T>(raw[r]));
+        slot[W + j] = acc;
       }
-#pragma unroll
-      for (int j = 0; j < W; ++j) slot[W + j] = acc[j];
     }
   } else {
     if (threadIdx.x == 0) {
