@@ -675,9 +675,15 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
 // Direct variant geometry per P, from a sweep on GB300 (131072 x 128 rows):
 // one slot of 16 KiB per CTA (overlap comes from the other CTAs on the SM)
 // up to P = 8, two slots of 32 KiB for P = 16.
+#ifndef RR_DIRECT_SLOTS
+#define RR_DIRECT_SLOTS 1
+#endif
+#ifndef RR_DIRECT_BYTES
+#define RR_DIRECT_BYTES 16384
+#endif
 template <int P> struct DirectGeom {
-  static constexpr int S = (P <= 8) ? 1 : 2;
-  static constexpr int bytes = (P <= 8) ? 16384 : 32768;
+  static constexpr int S = (P <= 8) ? RR_DIRECT_SLOTS : 2;
+  static constexpr int bytes = (P <= 8) ? RR_DIRECT_BYTES : 32768;
 };
 
 template <int P>
