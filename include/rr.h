@@ -29,6 +29,10 @@
  *   - Results are deterministic: the same inputs, shapes, pointer
  *     alignments and options give the same bits on every run (no float
  *     atomics, no occupancy-dependent partitioning of a row).
+ *   - Launches carry the programmatic-dependent-launch attribute (the
+ *     environment variable RR_PDL=0 turns it off): a kernel is set up
+ *     while the previous one in the stream drains, and waits for it to
+ *     complete before touching memory, so stream order is kept.
  *   - Cluster sizes: the library launches clusters of at most 16 CTAs and
  *     at most RR_MAX_CLUSTER (environment variable, 1..16, read once) when
  *     that is set; automatic plans stay within it, and a forced larger
