@@ -492,6 +492,7 @@ def bench_ours(args):
                 "traffic_source": tr["profile"] if traffic is not None else None}
 
     splitk_c, combine_v, callreduce_us, rowwise_sk, axis_r, e2e = {}, {}, {}, {}, {}, None
+    tiers_b2b = {}
     step_graph = None
     if not args.no_extras:
         def timed(fn, nbytes, reps=20):
@@ -540,6 +541,26 @@ def bench_ours(args):
             del gstep
         except Exception as e:  # graph capture unavailable: report, do not fail
             step_graph = {"unavailable": str(e)[:200]}
+        # every operation of the step alone, back to back: 10 launches in one
+        # CUDA graph rotating over copies of its inputs (enough copies that
+        # the set exceeds L2), so the figure is the kernel's own streaming
+        # rate without the launch gaps and event records of the per-operation
+        # pass above
+        tiers_b2b = {}
+        L2_BYTES = 128 << 20
+        for name, tier, spec, ins, outs in data:
+            bi, bo = algorithmic_bytes(spec)
+            ncopy = max(1, min(8, -(-2 * L2_BYTES // bi)))
+            sets = [(ins, outs)] + [([t.clone() for t in ins], [o.clone() for o in outs])
+                                    for _ in range(ncopy - 1)]
+            kk = [0]
+
+            def one():
+                kk[0] = (kk[0] + 1) % len(sets)
+                run_op(rr, spec, sets[kk[0]][0], sets[kk[0]][1])
+            tiers_b2b[name] = timed(one, bi + bo, reps=max(10, 2 * len(sets)))
+            tiers_b2b[name]["input_copies"] = len(sets)
+            del sets
         # split-K tier at every cluster size (same input, outside the step)
         x_sk = next(ins[0] for name, _, _, ins, _ in data if name == "splitk_sum_f32")
         out_sk = torch.empty(16, dtype=torch.float32, device=dev)
@@ -669,7 +690,7 @@ def bench_ours(args):
                    "l2": "inputs larger than L2: every operation reads its own buffer once "
                          "per step; a step moves %.2f GB" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
-        "tiers": tiers, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
+        "tiers": tiers, "tiers_back_to_back": tiers_b2b, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
         "cluster_allreduce_latency": callreduce_us, "rowwise_splitk": rowwise_sk,
         "axis_reduce": axis_r, "step_graph": step_graph,
         "roofline": roofline,
