@@ -25,6 +25,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_noalloc_mu;
+// Held for a whole self-test: every call uses the same scratch, so calls
+// from several host threads run one after another (each is blocking anyway).
+std::mutex g_noalloc_run_mu;
 void *g_noalloc_ptr[kMaxDev];  // device address of g_noalloc_scratch, per device
 
 // Device address of the scratch array on the current device.  The symbol
@@ -77,6 +80,7 @@ extern "C" int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width
   }
   if (cluster_size > 1 && !d.cluster_launch) return RR_ERR_UNSUPPORTED;
 
+  std::lock_guard<std::mutex> run(g_noalloc_run_mu);
   unsigned char *base = nullptr;
   int st = scratch_address(dev, &base);
   if (st != RR_OK) return st;

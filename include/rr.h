@@ -366,8 +366,9 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op,
  *   The first call on a device looks up the array's device address (once
  *   per device, with that device current); make that first call before any
  *   stream capture.  Each call resets the counter it needs; the array keeps
- *   the last call's other contents.  All calls share the one array, so calls
- *   that overlap on the GPU (other streams, other host threads) race.
+ *   the last call's other contents.  All calls share the one array: calls
+ *   from several host threads of a process run one after another (each holds
+ *   a process-wide lock for its whole, blocking, duration).
  * Returns RR_OK, RR_ERR_MISMATCH, RR_ERR_INVALID, RR_ERR_UNSUPPORTED or
  * RR_ERR_CUDA.
  */

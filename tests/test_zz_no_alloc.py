@@ -53,3 +53,32 @@ def test_noalloc_rejects_more_than_its_scratch(lib):
     if st == 2:
         pytest.skip("cluster of 16 not schedulable")
     assert (st, n) == (0, 0)                 # exactly at the limit is accepted
+
+
+def test_noalloc_from_two_host_threads(lib):
+    """Calls from several host threads share the one scratch array; the
+    library runs them one after another, so every call still checks out."""
+    import threading
+    import torch
+    import cluster_reductions_gb300 as rr
+    results, errors = [], []
+
+    def worker(C, width, seed):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for i in range(20):
+                    results.append(rr.cluster_allreduce_selftest_noalloc(
+                        C, width=width, op="sum", iters=256, seed=seed + i))
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    ts = [threading.Thread(target=worker, args=(4, 8, 100)),
+          threading.Thread(target=worker, args=(8, 4, 900))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    assert results == [0] * 40
