@@ -10,6 +10,7 @@ stream, which is what an end-to-end call from host buffers costs.
 from __future__ import annotations
 
 import ctypes
+import functools
 from typing import Optional, Tuple
 
 import torch
@@ -66,6 +67,24 @@ def _to_host(y: torch.Tensor, like: torch.Tensor) -> torch.Tensor:
     return h
 
 
+def _on_input_device(fn):
+    """Run a binding call with the first argument's GPU as the current device
+    (the library launches on the current device and stream)."""
+    @functools.wraps(fn)
+    def call(x, *args, **kwargs):
+        if isinstance(x, torch.Tensor) and x.is_cuda and x.device.index != torch.cuda.current_device():
+            with torch.cuda.device(x.device):
+                return fn(x, *args, **kwargs)
+        return fn(x, *args, **kwargs)
+    return call
+
+
+def _same_device(device, *ts):
+    for t in ts:
+        if t is not None and t.is_cuda and t.device != device:
+            raise ValueError(f"tensor on {t.device}, the input on {device}")
+
+
 def _out_buf(out: Optional[torch.Tensor], shape, dtype, device) -> torch.Tensor:
     """Device buffer a kernel writes: `out` itself when it is a CUDA tensor,
     else a fresh device tensor (copied into a CPU `out` by _deliver).  A given
@@ -95,6 +114,7 @@ def _deliver(y: torch.Tensor, out: Optional[torch.Tensor], like: torch.Tensor) -
     return _to_host(y, like)
 
 
+@_on_input_device
 def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tier=None,
            cluster_size: int = 0, emit_tile_width: int = 0,
            rank_out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -119,6 +139,7 @@ def reduce(x: torch.Tensor, op="sum", *, out: Optional[torch.Tensor] = None, tie
     return _deliver(o, out, x)
 
 
+@_on_input_device
 def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
                         clusters_per_row: int = 0, out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -142,6 +163,7 @@ def reduce_splitk_multi(x: torch.Tensor, op="sum", *, cluster_size: int = 0,
     return _deliver(o, out, x)
 
 
+@_on_input_device
 def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.Tensor] = None,
                 tier=None, cluster_size: int = 0, emit_tile_width: int = 0, tile_rows: int = 0,
                 splits: int = 0, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -198,6 +220,7 @@ def _rowwise_opts(tier, cluster_size):
                                              int(cluster_size)))
 
 
+@_on_input_device
 def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
             cluster_size: int = 0) -> torch.Tensor:
     """rr_softmax / rr_softmax_ex: row softmax of a bf16 or fp32 [rows, cols]
@@ -218,6 +241,7 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
     return _deliver(o, out, x)
 
 
+@_on_input_device
 def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
                     mean: Optional[torch.Tensor] = None,
                     rstd: Optional[torch.Tensor] = None, tier=None,
@@ -243,6 +267,7 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
     return _deliver(mu, mean, x), _deliver(rs, rstd, x)
 
 
+@_on_input_device
 def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
               out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
               rstd: Optional[torch.Tensor] = None, tier=None,
@@ -260,6 +285,7 @@ def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: flo
         raise TypeError("gamma and beta must be float32")
     if gamma.numel() != cols or beta.numel() != cols:
         raise ValueError("gamma and beta must have cols elements")
+    _same_device(xd.device, gamma, beta)
     gd, bd = _to_device(gamma.contiguous()), _to_device(beta.contiguous())
     o = _out_buf(out, (rows, cols), torch.bfloat16, xd.device)
     mu = None if mean is None else _out_buf(mean, (rows,), torch.float32, xd.device)
@@ -276,6 +302,7 @@ def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: flo
     return _deliver(o, out, x)
 
 
+@_on_input_device
 def cluster_allreduce(vals: torch.Tensor, op="sum", *, two_slot: bool = False,
                       skew_cycles: int = 0, res: Optional[torch.Tensor] = None,
                       mismatches: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -330,6 +357,7 @@ def cluster_allreduce_selftest_noalloc(cluster_size: int, width: int = 1, op="su
 COMBINE_MODES = {None: 0, "auto": 0, "pull": 1, "push": 2, "generic": 3, "direct": 4}
 
 
+@_on_input_device
 def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2e: float, *,
                    out: Optional[torch.Tensor] = None, mode=None) -> torch.Tensor:
     """rr_splitk_combine / rr_splitk_combine_ex: O [P, rows, D], m and l
@@ -343,7 +371,9 @@ def splitk_combine(O: torch.Tensor, m: torch.Tensor, l: torch.Tensor, scale_log2
     for t in (O, m, l):
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise TypeError("O, m, l must be contiguous float32")
-    Od, md, ld = _to_device(O), _to_device(m), _to_device(l)
+    Od = _to_device(O)
+    _same_device(Od.device, m, l)
+    md, ld = _to_device(m), _to_device(l)
     o = _out_buf(out, (rows, D), torch.bfloat16, Od.device)
     if mode is None:
         st = load().rr_splitk_combine(_ptr(Od), _ptr(md), _ptr(ld), P, rows, D,
