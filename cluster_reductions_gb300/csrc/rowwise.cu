@@ -466,20 +466,6 @@ inline int pick_nv(int64_t nvec) {
 // ---------------------------------------------------------------------------
 enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
 
-// 8 consecutive elements of global memory as floats (16-byte aligned p).
-template <class In>
-__device__ __forceinline__ void load8(const typename In::S *p, float (&o)[8]) {
-  if constexpr (In::EPV == 8) {
-    In::unpack(ld_stream_u4(p), o);
-  } else {
-    const uint4 w0 = ld_stream_u4(p), w1 = ld_stream_u4(p + 4);
-    o[0] = __uint_as_float(w0.x); o[1] = __uint_as_float(w0.y);
-    o[2] = __uint_as_float(w0.z); o[3] = __uint_as_float(w0.w);
-    o[4] = __uint_as_float(w1.x); o[5] = __uint_as_float(w1.y);
-    o[6] = __uint_as_float(w1.z); o[7] = __uint_as_float(w1.w);
-  }
-}
-
 // Folds the 8-element vectors v = tid, tid + THREADS, ... < nv of ps, in that
 // order: st = f(st, v, e).  U vectors per thread are loaded back to back
 // before the first is used (raw words first, unpacked after), so U * 16 bytes
