@@ -58,17 +58,17 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1087051776, "src": ["reduce.cu", "rr_device.cuh"],
+    "splitk_sum_f32": {"bytes": 1084762112, "src": ["reduce.cu", "rr_device.cuh"],
                       "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 577334272, "src": ["combine.cu", "rr_device.cuh"],
+    "combine_p8": {"bytes": 576032768, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "e41b009ab53904ca", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 562970624, "src": ["rowwise.cu", "rr_device.cuh"],
-                    "src_sha": "50c52594d73ae7bb", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271417344, "src": ["reduce.cu", "rr_device.cuh"],
+    "softmax_bf16": {"bytes": 563821568, "src": ["rowwise.cu", "rr_device.cuh"],
+                    "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271528448, "src": ["reduce.cu", "rr_device.cuh"],
                      "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271553792, "src": ["rowwise.cu", "rr_device.cuh"],
-                      "src_sha": "50c52594d73ae7bb", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 137869824, "src": ["reduce.cu", "rr_device.cuh"],
+    "layernorm_bf16": {"bytes": 271666176, "src": ["rowwise.cu", "rr_device.cuh"],
+                      "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 138524416, "src": ["reduce.cu", "rr_device.cuh"],
                     "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
