@@ -184,7 +184,13 @@ k_warp_scalar(const typename Op::T *__restrict__ x, int64_t rows, int cols,
 // loads, so a warp instruction covers 32 * 32 contiguous bytes.
 // ---------------------------------------------------------------------------
 template <class Op, int NV, int EWT, bool V8, int U>
-__global__ void __launch_bounds__(kTiledBlock)
+// Narrow rows (NV * EWT <= 2): held to 32 registers, 8 CTAs per SM, so the
+// persistent grid covers the usual row counts in one pass of loads per
+// thread (the max / min forms otherwise took 40 and a second pass).
+#ifndef RR_TILED_MIN_BLOCKS
+#define RR_TILED_MIN_BLOCKS 8
+#endif
+__global__ void __launch_bounds__(kTiledBlock, (NV * EWT <= 2) ? RR_TILED_MIN_BLOCKS : 1)
 k_tiled_vec(const typename Op::T *__restrict__ x, int64_t rows,
             typename Op::T *__restrict__ out) {
   pdl_begin();
