@@ -46,6 +46,8 @@ WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx
 # fp32, 256 MiB each): a column reduce, a middle axis, a narrow inner axis and
 # a single long, narrow tile that needs the split workspace.
 AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 22, 16)]
+# Row reductions of medium width timed beside the step (fp32, 256 MiB each).
+MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -492,6 +494,7 @@ def bench_ours(args):
                 "traffic_source": tr["profile"] if traffic is not None else None}
 
     splitk_c, combine_v, callreduce_us, rowwise_sk, axis_r, e2e = {}, {}, {}, {}, {}, None
+    medium_r = {}
     tiers_b2b = {}
     step_graph = None
     if not args.no_extras:
@@ -631,6 +634,19 @@ def bench_ours(args):
         rowwise_sk["layernorm_rewrite_16384x8192_bf16"] = timed(
             lambda: rr.layernorm(xl, gl, bl, 1e-5, out=yl), 16384 * 8192 * 4 + 8192 * 8)
         del xl, yl
+        # rows of medium width (33 to 4095 elements, many rows): the warp tier
+        # with a warp segment per row, automatic plan, two 256 MiB inputs
+        for mr, mc in MEDIUM_ROWS:
+            xm = [_inp.normal_f32(mr, mc, 810 + i, dev) for i in range(2)]
+            om = torch.empty(mr, device=dev)
+            km = [0]
+
+            def one_m():
+                km[0] ^= 1
+                rr.reduce(xm[km[0]], "sum", out=om)
+            medium_r[f"{mr}x{mc}_sum_f32"] = timed(one_m, mr * mc * 4 + mr * 4)
+            medium_r[f"{mr}x{mc}_sum_f32"]["tier"] = "%s C=%d" % rr.last_tier()
+            del xm
         # reduction over a non-last axis (automatic plan), 256 MiB inputs, two
         # rotating buffers; called straight through the C ABI so that host
         # overhead does not starve the ~40 us launches
@@ -692,7 +708,7 @@ def bench_ours(args):
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
         "tiers": tiers, "tiers_back_to_back": tiers_b2b, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
         "cluster_allreduce_latency": callreduce_us, "rowwise_splitk": rowwise_sk,
-        "axis_reduce": axis_r, "step_graph": step_graph,
+        "axis_reduce": axis_r, "medium_rows": medium_r, "step_graph": step_graph,
         "roofline": roofline,
         "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
     }

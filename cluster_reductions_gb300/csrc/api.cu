@@ -222,6 +222,10 @@ int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster, in
     tier = RR_TIER_TILED;
   } else if (cols <= 32) {
     tier = RR_TIER_WARP;
+  } else if (cols < 4096 && rows >= sm_count) {
+    // warp segments per row: rows too short for a CTA each, enough of them
+    // to fill the GPU
+    tier = RR_TIER_WARP;
   } else if (rows >= 1 && rows < sm_count && cols >= 4096 && max_cluster >= 2) {
     // the smallest power of two that puts at least one CTA on every SM,
     // capped by 16 and by what the device can co-schedule
@@ -251,7 +255,6 @@ int rr_reduce_ex(const void *x, int64_t rows, int64_t cols, int op, int dtype, v
   if (!(o.emit_tile_width == 0 || o.emit_tile_width == 1 || o.emit_tile_width == 2 ||
         o.emit_tile_width == 4))
     return RR_ERR_INVALID;
-  if (o.tier == RR_TIER_WARP && cols > 32) return RR_ERR_INVALID;
   if (rows == 0) return RR_OK;
   if (!out || (cols > 0 && !x)) return RR_ERR_INVALID;
   if (mul_overflows(rows, cols, INT64_MAX / 4)) return RR_ERR_INVALID;

@@ -7,6 +7,7 @@
 // Every tier folds each row in a fixed order that depends only on the shape,
 // the tier's compile-time geometry and the row's address alignment, so the
 // same call gives the same bits on every run.
+#include <climits>
 #include <cstdio>
 
 #include "rr.h"
@@ -174,6 +175,65 @@ k_warp_scalar(const typename Op::T *__restrict__ x, int64_t rows, int cols,
       const T a = warp_allreduce<Op, 32>(v[u]);
       if (lane == 0 && r0 + u < rows) out[r0 + u] = Op::finalize(a);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warp tier for rows longer than a warp ("reduce" page, warp tier, read for
+// rows wider than 32: the lanes of a warp segment stride the row).  A
+// segment of LPR lanes owns a row; lane `sub` folds units sub, sub + LPR, ...
+// of it (VEC: 16-byte vectors, else single elements), KV per pass: the KV
+// loads go out first and are folded last-loaded first, so the first fold
+// needs the last load and all KV are in flight together (a unit past the
+// row's end re-reads the row's last unit and is not folded); passes repeat
+// until the row is covered; then an xor butterfly over the segment.  32 / LPR rows per warp,
+// grid-stride over warps; no shared memory and no barrier, so rows of 33 to
+// a few thousand elements need no 256-thread CTA each.
+// ---------------------------------------------------------------------------
+template <class Op, bool VEC, int LPR, int KV>
+__global__ void __launch_bounds__(kWarpBlock)
+k_warp_seg(const typename Op::T *__restrict__ x, int64_t rows, int64_t cols,
+           typename Op::T *__restrict__ out) {
+  pdl_begin();
+  using T = typename Op::T;
+  using V = typename Vec4<T>::type;
+  constexpr int RPW = 32 / LPR;
+  const int lane = threadIdx.x & 31, seg = lane / LPR, sub = lane % LPR;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t n = VEC ? cols / 4 : cols;  // units per row
+  for (int64_t r0 = warp * RPW; r0 < rows; r0 += nwarps * RPW) {
+    const int64_t row = r0 + seg;
+    // a segment past the last row re-reads the last row and writes nothing
+    const int64_t rr = row < rows ? row : rows - 1;
+    T acc = Op::id();
+    for (int64_t k0 = sub; k0 < n; k0 += (int64_t)KV * LPR) {
+      if constexpr (VEC) {
+        const V *q = reinterpret_cast<const V *>(x) + rr * n;
+        V v[KV];
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+          const int64_t k = k0 + (int64_t)j * LPR;
+          v[j] = ld_stream(q + (k < n ? k : n - 1));
+        }
+#pragma unroll
+        for (int j = KV - 1; j >= 0; --j)
+          if (k0 + (int64_t)j * LPR < n) acc = fold4<Op>(acc, v[j]);
+      } else {
+        const T *q = x + rr * n;
+        T v[KV];
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+          const int64_t k = k0 + (int64_t)j * LPR;
+          v[j] = __ldg(q + (k < n ? k : n - 1));
+        }
+#pragma unroll
+        for (int j = KV - 1; j >= 0; --j)
+          if (k0 + (int64_t)j * LPR < n) acc = Op::f(acc, v[j]);
+      }
+    }
+    acc = warp_allreduce<Op, LPR>(acc);
+    if (sub == 0 && row < rows) out[row] = Op::finalize(acc);
   }
 }
 
@@ -416,6 +476,49 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
       return cuda_status(cudaGetLastError());
     }
     case RR_TIER_WARP: {
+      if (cols > 32) {
+        // a segment of LPR lanes per row, 8 units per lane and pass, at least
+        // 32 bytes per segment and pass (2 vector lanes, 8 scalar lanes), at
+        // most 32: enough lanes to cover the row in one pass (long rows then
+        // read 32 lanes' worth of contiguous bytes per instruction), halved
+        // while more than 30% of the slots would fall past the row's end
+        const bool vec = (cols % 4 == 0) && (a % 16 == 0);
+        const int64_t n = vec ? cols / 4 : cols;
+        const int lmin = vec ? 2 : 8;
+        auto fill = [n](int l) {
+          const int64_t per = (int64_t)l * 8;
+          return (double)n / (double)((n + per - 1) / per * per);
+        };
+        int lpr = lmin;
+        while (lpr < 32 && (int64_t)lpr * 8 < n) lpr *= 2;
+        while (lpr > lmin && fill(lpr) < 0.7 && fill(lpr / 2) > fill(lpr)) lpr /= 2;
+        const int64_t rows_per_block = (int64_t)(kWarpBlock / 32) * (32 / lpr);
+        const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+#define RR_WARP_SEG(VEC, L)                                                    \
+  {                                                                            \
+    auto k = k_warp_seg<Op, VEC, L, 8>;                                        \
+    const int g = grid_for(k, kWarpBlock, blocks, d);                          \
+    launch_kernel(k, dim3(g), dim3(kWarpBlock), 0, s, 0, x, rows, cols, out);  \
+    break;                                                                     \
+  }
+        if (vec) {
+          switch (lpr) {
+            case 2: RR_WARP_SEG(true, 2)
+            case 4: RR_WARP_SEG(true, 4)
+            case 8: RR_WARP_SEG(true, 8)
+            case 16: RR_WARP_SEG(true, 16)
+            default: RR_WARP_SEG(true, 32)
+          }
+        } else {
+          switch (lpr) {
+            case 8: RR_WARP_SEG(false, 8)
+            case 16: RR_WARP_SEG(false, 16)
+            default: RR_WARP_SEG(false, 32)
+          }
+        }
+#undef RR_WARP_SEG
+        return cuda_status(cudaGetLastError());
+      }
       const bool vec = (cols % 4 == 0) && cols >= 4 && (a % 16 == 0) &&
                        (cols == 4 || cols == 8 || cols == 16 || cols == 32);
       if (vec) {

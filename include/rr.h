@@ -66,7 +66,9 @@ typedef enum { RR_F32 = 0, RR_I32 = 1, RR_BF16 = 2 } rr_dtype;
 /* Reduction tiers of [RW] "tier semantics". */
 typedef enum {
     RR_TIER_AUTO = 0,
-    RR_TIER_WARP = 1,    /* axis <= 32: a warp (or a warp segment) per row */
+    RR_TIER_WARP = 1,    /* a warp segment per row: lane i takes element i
+                            for rows of up to 32, and lanes stride longer
+                            rows */
     RR_TIER_TILED = 2,   /* a thread owns emit_tile_width adjacent rows; no
                             cross-thread combine ([RW] tiled and serial tiers:
                             emit_tile_width 1 is the serial tier) */
@@ -109,10 +111,11 @@ typedef struct {
  * exact, with max(+0,-0) = +0, min(+0,-0) = -0 and NaN propagating as the
  * quiet NaN 0x7fc00000.  cols == 0 writes the identity (0, -inf / INT_MIN,
  * +inf / INT_MAX).  The tier is picked from rows, cols and the SM count:
- * cols <= 16 tiled; cols <= 32 warp; rows < SMs and cols >= 4096 split-K
- * with C the smallest power of two >= 2 such that rows * C >= SMs, capped
- * at 16 and at the largest cluster the device can co-schedule; otherwise
- * block.
+ * cols <= 16 tiled; cols <= 32 warp; cols < 4096 and rows >= SMs warp (a
+ * warp segment per row, lanes striding it); rows < SMs and cols >= 4096
+ * split-K with C the smallest power of two >= 2 such that rows * C >= SMs,
+ * capped at 16 and at the largest cluster the device can co-schedule;
+ * otherwise block.
  * Errors: RR_ERR_INVALID (null pointer with rows > 0, negative sizes, bad
  * op / dtype, overlap), RR_ERR_UNSUPPORTED, RR_ERR_CUDA.
  */

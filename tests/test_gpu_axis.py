@@ -60,8 +60,8 @@ TIER_CASES = [("tiled", 0, 1, 0, 0), ("tiled", 0, 2, 0, 0), ("tiled", 0, 4, 0, 0
 
 def allowed(shape, offset, tier, ewt, tile_rows, splits):
     inner = shape[2]
-    if inner == 1:        # the last-axis reduction: no tiles or splits; warp needs axis <= 32
-        return not (tier == "warp" and shape[1] > 32) and not tile_rows and splits <= 1
+    if inner == 1:        # the last-axis reduction: no tiles or splits
+        return not tile_rows and splits <= 1
     V = 4 if (inner % 4 == 0 and offset % 4 == 0) else 1
     if tile_rows and (tile_rows % V or tile_rows // V > 32):
         return False

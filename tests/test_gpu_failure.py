@@ -44,7 +44,7 @@ def test_injected_error_then_recovery(rr, oracle_mod):
     # not consume the injected failure
     rr.test_inject_error(1)
     with pytest.raises(rr.RRError, match="invalid"):
-        rr.reduce(x, "max", tier="warp")                    # warp tier, 4096 cols
+        rr.reduce(x, "max", tier="tiled", emit_tile_width=3)  # no such tile width
     with pytest.raises(rr.RRError, match="CUDA runtime error"):
         rr.reduce(x, "sum")
     assert rr.device_status() == 0

@@ -55,8 +55,6 @@ SHAPES = [(1, 1), (3, 3), (5, 4), (7, 5), (9, 8), (4, 13), (6, 16), (5, 17), (33
 @pytest.mark.parametrize("dtype", [torch.float32, torch.int32], ids=["f32", "i32"])
 def test_forced_tiers_small(rr, oracle_mod, tier, op, dtype):
     for i, (rows, cols) in enumerate(SHAPES):
-        if tier == "warp" and cols > 32:
-            continue
         for offset in (0, 1, 3):
             x = gen(rows, cols, dtype, 100 + i, offset)
             kw = {"tier": tier}
@@ -235,8 +233,30 @@ def test_argument_errors(rr):
         rr.reduce(x, "sum", tier="warp", out=None, emit_tile_width=3)
     assert e.value.status == 1
     with pytest.raises(rr.RRError):
-        rr.reduce(torch.zeros((4, 64), device="cuda"), "sum", tier="warp")
+        rr.reduce(torch.zeros((4, 64), device="cuda"), "sum", tier="splitk", cluster_size=3)
     with pytest.raises(rr.RRError):
         rr.reduce(x, "sum", out=x.view(-1)[:4])   # out overlaps x
     with pytest.raises(TypeError):
         rr.reduce(torch.zeros((4, 8), device="cuda", dtype=torch.float64), "sum")
+
+
+@pytest.mark.parametrize("rows,cols,offset", [(1 << 20, 64, 0), (65536, 1024, 0), (262144, 256, 1),
+                                              (671088, 100, 0), (2033601, 33, 0)])
+def test_medium_width_rows(rr, oracle_mod, rows, cols, offset):
+    """Rows of 33 to 4095 elements and at least an SM's count of them take the
+    warp tier (a warp segment per row): all ops against the oracle on every
+    row of a sampled set, vector and scalar paths."""
+    x = gen(rows, cols, torch.float32, 300 + cols, offset)
+    idx = np.r_[np.arange(0, rows, max(1, rows // 4096)), rows - 1]
+    xs = to_np(x[torch.from_numpy(idx).cuda()])
+    for op in ("sum", "max", "min"):
+        got = to_np(rr.reduce(x, op))
+        assert rr.last_tier() == ("warp", 1)
+        ref = oracle_mod.reduce_rows(xs, op)
+        if op == "sum":
+            assert_sum_close(got[idx], ref, xs)
+        else:
+            assert_bits_equal(got[idx], ref)
+    xi = gen(rows, cols, torch.int32, 400 + cols, offset)
+    got = to_np(rr.reduce(xi, "sum"))
+    assert_bits_equal(got[idx], oracle_mod.reduce_rows(to_np(xi[torch.from_numpy(idx).cuda()]), "sum"))

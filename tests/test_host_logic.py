@@ -53,8 +53,8 @@ def test_arguments_rejected_on_the_host(lib):
     p = ctypes.addressof(buf)
     assert lib.rr_reduce(p, 4, 8, 0, 0, p + 16, null) == INVALID       # out overlaps x
     from cluster_reductions_gb300._lib import rr_reduce_opts
-    bad = rr_reduce_opts(1, 0, 0, 0, None)                             # warp tier, 64 cols
-    assert lib.rr_reduce_ex(p, 1, 64, 0, 0, p, null, ctypes.byref(bad)) == INVALID
+    bad = rr_reduce_opts(1, 0, 0, 5, None)                             # tile width 5
+    assert lib.rr_reduce_ex(p, 1, 64, 0, 0, p + 256, null, ctypes.byref(bad)) == INVALID
     bad = rr_reduce_opts(4, 3, 0, 0, None)                             # cluster size 3
     assert lib.rr_reduce_ex(p, 1, 8, 0, 0, p + 64, null, ctypes.byref(bad)) == INVALID
     assert lib.rr_softmax(p, 2, 0, 2, p, null) == INVALID              # cols == 0
@@ -107,6 +107,12 @@ def test_status_strings(lib):
     (1 << 20, 17, 152, 16, ("warp", 1)),
     (1 << 20, 32, 152, 16, ("warp", 1)),
     (8192, 8192, 152, 16, ("block", 1)),
+    (1 << 20, 33, 152, 16, ("warp", 1)),       # medium rows: warp segments
+    (1 << 20, 64, 152, 16, ("warp", 1)),
+    (65536, 1024, 152, 16, ("warp", 1)),
+    (152, 4095, 152, 16, ("warp", 1)),
+    (16384, 4096, 152, 16, ("block", 1)),
+    (151, 1000, 152, 16, ("block", 1)),        # too few rows for warps
     (16, 1 << 24, 152, 16, ("splitk", 16)),
     (16, 1 << 24, 152, 8, ("splitk", 8)),
     (64, 4096, 152, 16, ("splitk", 4)),
