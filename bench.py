@@ -48,6 +48,9 @@ WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx
 AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 22, 16)]
 # Row reductions of medium width timed beside the step (fp32, 256 MiB each).
 MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
+# Softmax / layernorm rows of medium width timed beside the step (bf16,
+# 256 MiB each): the warp tier of the two-pass row operations.
+MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048)]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -64,11 +67,11 @@ NCU_TRAFFIC = {
                       "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
     "combine_p8": {"bytes": 576032768, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "e41b009ab53904ca", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 563821568, "src": ["rowwise.cu", "rr_device.cuh"],
+    "softmax_bf16": {"bytes": 563821568, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
                     "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
     "block_sum_f32": {"bytes": 271528448, "src": ["reduce.cu", "rr_device.cuh"],
                      "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271666176, "src": ["rowwise.cu", "rr_device.cuh"],
+    "layernorm_bf16": {"bytes": 271666176, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
                       "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
     "warp_sum_f32": {"bytes": 138524416, "src": ["reduce.cu", "rr_device.cuh"],
                     "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
@@ -647,6 +650,29 @@ def bench_ours(args):
             medium_r[f"{mr}x{mc}_sum_f32"] = timed(one_m, mr * mc * 4 + mr * 4)
             medium_r[f"{mr}x{mc}_sum_f32"]["tier"] = "%s C=%d" % rr.last_tier()
             del xm
+        for mr, mc in MEDIUM_ROWOPS:
+            xm = [_inp.normal_bf16(mr, mc, 820 + i, dev, 3.0) for i in range(2)]
+            ym = torch.empty((mr, mc), device=dev)
+            yb = torch.empty((mr, mc), dtype=torch.bfloat16, device=dev)
+            mu, rs = torch.empty(mr, device=dev), torch.empty(mr, device=dev)
+            gm, bm = _inp.layernorm_params(mc, 822, dev)
+            km = [0]
+            ops = {
+                "softmax": (lambda x: rr.softmax(x, out=ym), mr * mc * 6),
+                "lnstats": (lambda x: rr.layernorm_stats(x, 1e-5, mean=mu, rstd=rs),
+                            mr * mc * 2 + mr * 8),
+                "layernorm": (lambda x: rr.layernorm(x, gm, bm, 1e-5, out=yb),
+                              mr * mc * 4 + mc * 8),
+            }
+            for name, (fn, nb) in ops.items():
+                def one_r(fn=fn):
+                    km[0] ^= 1
+                    fn(xm[km[0]])
+                key = f"{mr}x{mc}_{name}_bf16"
+                medium_r[key] = timed(one_r, nb)
+                t, c = rr.last_tier()
+                medium_r[key]["tier"] = f"{t} {'L' if t == 'warp' else 'C'}={c}"
+            del xm, ym, yb
         # reduction over a non-last axis (automatic plan), 256 MiB inputs, two
         # rotating buffers; called straight through the C ABI so that host
         # overhead does not starve the ~40 us launches
@@ -825,6 +851,11 @@ PROFILE_CASES = {
     "axis_32768x256x8": ({"shape": (32768, 256, 8)}, "axis", 1.0),
     "axis_1x8192x8192": ({"shape": (1, 8192, 8192)}, "axis", 1.0),
     "axis_1x4194304x16": ({"shape": (1, 1 << 22, 16)}, "axis", 1.0),
+    # rows of medium width (the warp-segment kernels), automatic plan
+    "medium_sum_1048576x64_f32": ({"shape": (1 << 20, 64), "op": "sum"}, "medium", 1.0),
+    "medium_softmax_131072x1024_bf16": ({"shape": (131072, 1024), "op": "softmax"}, "medium", 1.0),
+    "medium_layernorm_131072x1024_bf16": ({"shape": (131072, 1024), "op": "layernorm"},
+                                          "medium", 1.0),
 }
 
 
@@ -846,6 +877,31 @@ def run_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"case": args.case, "launches": args.steps,
                           "algorithmic_bytes": (outer * axis_n * inner + outer * inner) * 4,
+                          "plan": rr.last_tier(), "scale_to_full": scale,
+                          "status": rr.device_status()}), flush=True)
+        return
+    if mode == "medium":
+        from cluster_reductions_gb300 import inputs
+        r, c = over["shape"]
+        op = over["op"]
+        if op == "sum":
+            x = inputs.normal_f32(r, c, inputs.seed_for(5, 1), "cuda")
+            o = torch.empty(r, device="cuda")
+            fn, nb = (lambda: rr.reduce(x, "sum", out=o)), r * c * 4 + r * 4
+        elif op == "softmax":
+            x = inputs.normal_bf16(r, c, inputs.seed_for(5, 2), "cuda", 3.0)
+            y = torch.empty((r, c), device="cuda")
+            fn, nb = (lambda: rr.softmax(x, out=y)), r * c * 6
+        else:
+            x = inputs.normal_bf16(r, c, inputs.seed_for(5, 3), "cuda")
+            g, b = inputs.layernorm_params(c, inputs.seed_for(5, 4), "cuda")
+            yb = torch.empty((r, c), dtype=torch.bfloat16, device="cuda")
+            fn, nb = (lambda: rr.layernorm(x, g, b, 1e-5, out=yb)), r * c * 4 + c * 8
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            fn()
+        torch.cuda.synchronize()
+        print(json.dumps({"case": args.case, "launches": args.steps, "algorithmic_bytes": nb,
                           "plan": rr.last_tier(), "scale_to_full": scale,
                           "status": rr.device_status()}), flush=True)
         return

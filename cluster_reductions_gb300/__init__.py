@@ -213,18 +213,19 @@ def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.
     return _deliver(o, out, x)
 
 
-def _rowwise_opts(tier, cluster_size):
-    if tier is None and not cluster_size:
+def _rowwise_opts(tier, cluster_size, lanes_per_row=0):
+    if tier is None and not cluster_size and not lanes_per_row:
         return None
     return ctypes.byref(_lib.rr_rowwise_opts(_TIERS[tier] if not isinstance(tier, int) else tier,
-                                             int(cluster_size)))
+                                             int(cluster_size), int(lanes_per_row)))
 
 
 @_on_input_device
 def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
-            cluster_size: int = 0) -> torch.Tensor:
+            cluster_size: int = 0, lanes_per_row: int = 0) -> torch.Tensor:
     """rr_softmax / rr_softmax_ex: row softmax of a bf16 or fp32 [rows, cols]
-    tensor, fp32 out.  tier: None/"auto", "block" or "splitk"."""
+    tensor, fp32 out.  tier: None/"auto", "warp", "block" or "splitk";
+    cluster_size for split-K, lanes_per_row for the warp tier."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -232,7 +233,7 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"softmax: dtype {xd.dtype} not supported (bfloat16, float32)")
     o = _out_buf(out, (rows, cols), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
     if opts is None:
         st = load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream())
     else:
@@ -245,9 +246,11 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
 def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
                     mean: Optional[torch.Tensor] = None,
                     rstd: Optional[torch.Tensor] = None, tier=None,
-                    cluster_size: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+                    cluster_size: int = 0,
+                    lanes_per_row: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """rr_layernorm_stats / rr_layernorm_stats_ex: per-row mean and
-    1/sqrt(var + eps), fp32.  tier: None/"auto", "block" or "splitk"."""
+    1/sqrt(var + eps), fp32.  tier: None/"auto", "warp", "block" or
+    "splitk"."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -256,7 +259,7 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
         raise TypeError(f"layernorm_stats: dtype {xd.dtype} not supported")
     mu = _out_buf(mean, (rows,), torch.float32, xd.device)
     rs = _out_buf(rstd, (rows,), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
     if opts is None:
         st = load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
                                        _stream())
@@ -271,7 +274,7 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
 def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
               out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
               rstd: Optional[torch.Tensor] = None, tier=None,
-              cluster_size: int = 0) -> torch.Tensor:
+              cluster_size: int = 0, lanes_per_row: int = 0) -> torch.Tensor:
     """rr_layernorm / rr_layernorm_ex: bf16 (x - mean) * rstd * gamma + beta per
     row of a bf16 or fp32 [rows, cols] tensor; gamma, beta fp32 [cols].
     mean / rstd (fp32 [rows]) are filled when given."""
@@ -290,7 +293,7 @@ def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: flo
     o = _out_buf(out, (rows, cols), torch.bfloat16, xd.device)
     mu = None if mean is None else _out_buf(mean, (rows,), torch.float32, xd.device)
     rs = None if rstd is None else _out_buf(rstd, (rows,), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
     args = (_ptr(xd), rows, cols, dt, float(eps), _ptr(gd), _ptr(bd), _ptr(o), _ptr(mu),
             _ptr(rs), _stream())
     st = load().rr_layernorm(*args) if opts is None else load().rr_layernorm_ex(*args, opts)

@@ -28,7 +28,8 @@ class rr_reduce_opts(ctypes.Structure):
 
 
 class rr_rowwise_opts(ctypes.Structure):
-    _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int)]
+    _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int),
+                ("lanes_per_row", ctypes.c_int)]
 
 
 class rr_axis_opts(ctypes.Structure):

@@ -565,10 +565,20 @@ int rr_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner, in
 
 static bool rowwise_opts_ok(const rr_rowwise_opts *o) {
   if (!o) return true;
-  if (!(o->tier == RR_TIER_AUTO || o->tier == RR_TIER_BLOCK || o->tier == RR_TIER_SPLITK))
+  if (!(o->tier == RR_TIER_AUTO || o->tier == RR_TIER_WARP || o->tier == RR_TIER_BLOCK ||
+        o->tier == RR_TIER_SPLITK))
     return false;
+  const int l = o->lanes_per_row;
+  if (!(l == 0 || l == 1 || l == 2 || l == 4 || l == 8 || l == 16 || l == 32)) return false;
   return o->cluster_size == 0 || o->cluster_size == 1 || o->cluster_size == 2 ||
          o->cluster_size == 4 || o->cluster_size == 8 || o->cluster_size == 16;
+}
+
+// The width a forced row-op tier takes: lanes per row for the warp tier, the
+// cluster size otherwise.
+static int rowwise_width(const rr_rowwise_opts *o) {
+  if (!o) return 0;
+  return o->tier == RR_TIER_WARP ? o->lanes_per_row : o->cluster_size;
 }
 
 int rr_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
@@ -592,7 +602,7 @@ int rr_softmax_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, float
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
   st = launch_softmax(x, rows, cols, in_dtype, out, as_stream(stream), *d, &tier,
-                      opts ? opts->tier : RR_TIER_AUTO, opts ? opts->cluster_size : 0);
+                      opts ? opts->tier : RR_TIER_AUTO, rowwise_width(opts));
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
@@ -622,7 +632,7 @@ int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols, int in_dtyp
   int tier = RR_TIER_BLOCK;
   st = launch_layernorm_stats(x, rows, cols, in_dtype, eps, mean, rstd, as_stream(stream), *d,
                               &tier, opts ? opts->tier : RR_TIER_AUTO,
-                              opts ? opts->cluster_size : 0);
+                              rowwise_width(opts));
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
@@ -663,7 +673,7 @@ int rr_layernorm_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, flo
   int tier = RR_TIER_BLOCK;
   st = launch_layernorm(x, rows, cols, in_dtype, eps, gamma, beta, out_bf16, mean, rstd,
                         as_stream(stream), *d, &tier, opts ? opts->tier : RR_TIER_AUTO,
-                        opts ? opts->cluster_size : 0);
+                        rowwise_width(opts));
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }

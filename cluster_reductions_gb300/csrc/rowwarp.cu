@@ -1,0 +1,278 @@
+// rowwarp.cu -- warp tier of the two-pass row operations of the "reduce" page
+// (algorithm/gpu/rowwise, tier semantics: a warp per row for rows too short
+// to keep a CTA busy): softmax, layernorm statistics and the layernorm
+// rewrite for rows of up to 256 16-byte vectors (2048 bf16 / 1024 fp32
+// elements) when there are many of them.
+//
+// A segment of L lanes of a warp owns a row (32 / L rows per warp at a
+// time; L = 1 is a thread per row) and holds it in registers: lane `sub` of
+// the segment holds vectors k * L + sub, k < NV, so each load instruction of
+// the segment covers L * 16 contiguous bytes.  Both reductions of a row are xor butterflies inside the
+// segment -- no shared memory and no barrier -- and the next row's raw
+// vectors are loaded before the current row is reduced and written, so a
+// lane keeps up to 2 * NV 16-byte loads in flight.  Vector indices past the
+// row end are clamped to the row's last vector (loaded, then left out of
+// every fold); a segment past the last row re-reads the last row and writes
+// nothing.  So every load is unconditional and every lane takes part in
+// every shuffle.
+#include <cstdio>
+
+#include "rr.h"
+#include "rr_device.cuh"
+#include "rr_internal.h"
+#include "rowwise.cuh"
+
+namespace rr {
+namespace {
+
+constexpr int kWarpRowMaxThreads = 256;
+
+// MODE kModeSoftmax: y (fp32) = e^(x - M) / S with (M, S) the row's (max,
+// sum) pair; kModeStats: mean, rstd; kModeLayernorm: ybf (bf16) =
+// (x - mean) * rstd * gamma + beta, mean / rstd optional.  The arithmetic
+// per element is that of the block tier's register form; only the order in
+// which the per-lane partials are combined differs (a butterfly over the L
+// lanes instead of warp trees and a block fold).
+template <class In, int MODE, int L, int NV>
+__global__ void __launch_bounds__(kWarpRowMaxThreads)
+k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+               float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
+               const float *__restrict__ gamma, const float *__restrict__ beta,
+               uint16_t *__restrict__ ybf) {
+  pdl_begin();
+  constexpr int EPV = In::EPV, RPW = 32 / L;
+  const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
+  const int nvec = cols / EPV;
+  uint4 raw[NV];
+  auto fetch = [&](int64_t r) {
+    const int64_t rc = r < rows ? r : rows - 1;
+    const uint4 *q = reinterpret_cast<const uint4 *>(x + rc * (int64_t)cols);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * L + sub;
+      raw[k] = ld_stream_u4(q + (idx < nvec ? idx : nvec - 1));
+    }
+  };
+  int64_t r0 = warp * RPW;
+  if (r0 < rows) fetch(r0 + seg);
+  for (; r0 < rows; r0 += stride) {  // warp-uniform trip count
+    const int64_t row = r0 + seg;
+    float v[NV][EPV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) In::unpack(raw[k], v[k]);
+    if (r0 + stride < rows) fetch(r0 + stride + seg);
+    if constexpr (MODE == kModeSoftmax) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (k * L + sub < nvec) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) m = fmaxf(m, v[k][e]);
+        }
+      float s = 0.0f;
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          float sk = 0.0f;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float p = ex2_approx(fmaf(v[k][e], kLog2e, -mb));
+            v[k][e] = p;
+            sk += p;
+          }
+          if (k * L + sub < nvec) s += sk;
+        }
+      } else {
+        // every element the lane holds is -inf: e^(x - M) = 0, not -inf * 0
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
+      }
+      float M = m, S = s;
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1)
+        ms_combine(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
+      const float f = (m == -INFINITY) ? 0.0f : ex2_approx((m - M) * kLog2e) * (1.0f / S);
+      if (row < rows) {
+        float *yr = y + row * (int64_t)cols;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          const int idx = k * L + sub;
+          if (idx < nvec) {
+            if constexpr (EPV == 8) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = v[k][e % EPV] * f;
+              st_stream_v8(yr + (int64_t)idx * EPV, o);
+            } else {
+              st_stream_v4(yr + (int64_t)idx * EPV, v[k][0] * f, v[k][1 % EPV] * f,
+                           v[k][2 % EPV] * f, v[k][3 % EPV] * f);
+            }
+          }
+        }
+      }
+    } else {
+      float s = 0.0f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (k * L + sub < nvec) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) s += v[k][e];
+        }
+      const float mu = warp_allreduce<SumF32, L>(s) / (float)cols;
+      float qs = 0.0f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (k * L + sub < nvec) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float dlt = v[k][e] - mu;
+            qs = fmaf(dlt, dlt, qs);
+          }
+        }
+      const float var = warp_allreduce<SumF32, L>(qs) * (1.0f / (float)cols);
+      const float rs = 1.0f / sqrtf(var + eps);
+      if (row < rows) {
+        if constexpr (MODE == kModeLayernorm) {
+          uint16_t *yr = ybf + row * (int64_t)cols;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            const int idx = k * L + sub;
+            if (idx < nvec) {
+              float g[EPV], b[EPV];
+#pragma unroll
+              for (int e = 0; e < EPV; e += 4) {
+                const float4 gv = __ldg(reinterpret_cast<const float4 *>(gamma + idx * EPV + e));
+                const float4 bv = __ldg(reinterpret_cast<const float4 *>(beta + idx * EPV + e));
+                g[e] = gv.x; g[e + 1] = gv.y; g[e + 2] = gv.z; g[e + 3] = gv.w;
+                b[e] = bv.x; b[e + 1] = bv.y; b[e + 2] = bv.z; b[e + 3] = bv.w;
+              }
+              uint32_t pk[EPV / 2];
+#pragma unroll
+              for (int e = 0; e < EPV; e += 2)
+                pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
+                                        fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
+              if constexpr (EPV == 8) {
+                *reinterpret_cast<uint4 *>(yr + idx * EPV) =
+                    make_uint4(pk[0], pk[1 % (EPV / 2)], pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
+              } else {
+                *reinterpret_cast<uint2 *>(yr + idx * EPV) = make_uint2(pk[0], pk[1 % (EPV / 2)]);
+              }
+            }
+          }
+        }
+        if (sub == 0) {
+          if (mean) mean[row] = mu;
+          if (rstd) rstd[row] = rs;
+        }
+      }
+    }
+  }
+}
+
+// CTAs of up to 8 warps, persistent over the rows.  With fewer rows than
+// 8 warps per SM take, the CTAs shrink (down to one warp) so that the warps
+// spread over every SM instead of filling a few.
+template <class In, int MODE, int L, int NV>
+int launch_one(const void *x, int64_t rows, int64_t cols, float eps, float *y, float *mean,
+               float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
+               cudaStream_t s, const DevInfo &d) {
+  auto k = k_rowwise_warp<In, MODE, L, NV>;
+  constexpr int RPW = 32 / L;
+  const int64_t warps = (rows + RPW - 1) / RPW;
+  int wpb = kWarpRowMaxThreads / 32;
+  if (warps < (int64_t)wpb * d.sm_count) {
+    const int64_t w = warps / d.sm_count;
+    wpb = w < 1 ? 1 : (int)w;
+  }
+  const int threads = wpb * 32;
+  const int nb = occupancy_blocks((const void *)k, threads, 0, d.device);
+  const int64_t need = (warps + wpb - 1) / wpb;
+  const int64_t cap = (int64_t)(nb > 0 ? nb : 1) * d.sm_count;
+  const int grid = (int)(need < cap ? need : cap);
+  return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), 0, s, 0,
+                                   (const typename In::S *)x, rows, (int)cols, eps, y, mean,
+                                   rstd, gamma, beta, ybf));
+}
+
+template <class In, int MODE, int L>
+int launch_nv(int nv, const void *x, int64_t rows, int64_t cols, float eps, float *y,
+              float *mean, float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
+              cudaStream_t s, const DevInfo &d) {
+  switch (nv) {
+    case 1: return launch_one<In, MODE, L, 1>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 2: return launch_one<In, MODE, L, 2>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 4: return launch_one<In, MODE, L, 4>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_one<In, MODE, L, 8>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
+}
+
+template <class In, int MODE>
+int launch_mode(int L, int nv, const void *x, int64_t rows, int64_t cols, float eps, float *y,
+                float *mean, float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
+                cudaStream_t s, const DevInfo &d) {
+  switch (L) {
+    case 1: return launch_nv<In, MODE, 1>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 2: return launch_nv<In, MODE, 2>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 4: return launch_nv<In, MODE, 4>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 8: return launch_nv<In, MODE, 8>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 16: return launch_nv<In, MODE, 16>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_nv<In, MODE, 32>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
+}
+
+}  // namespace
+
+int rowwise_warp_lanes(int64_t nvec, int lanes) {
+  if (nvec < 1 || nvec > (int64_t)32 * kRowWarpMaxNV) return 0;
+  if (lanes != 0) {
+    if (!(lanes == 1 || lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16 || lanes == 32))
+      return 0;
+    return (int64_t)lanes * kRowWarpMaxNV >= nvec ? lanes : 0;
+  }
+  // rows of up to 8 vectors: about 2 vectors per lane; longer rows: about
+  // kRowWarpTargetNV per lane, up to 32 lanes
+  const int per = nvec <= 8 ? 2 : kRowWarpTargetNV;
+  int L = 1;
+  while (L < 32 && (int64_t)L * per < nvec) L *= 2;
+  return L;
+}
+
+int rowwise_warp_nv(int64_t nvec, int lanes) {
+  const int64_t per = (nvec + lanes - 1) / lanes;
+  int nv = 1;
+  while (nv < per) nv *= 2;
+  return nv;
+}
+
+int launch_rowwise_warp(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                        float eps, float *y, float *mean, float *rstd, const float *gamma,
+                        const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                        const DevInfo &d) {
+  const int epv = in_dtype == RR_BF16 ? 8 : 4;
+  const int64_t nvec = cols / epv;
+  const int nv = rowwise_warp_nv(nvec, lanes);
+  if (nv > kRowWarpMaxNV || cols > 0x7fffffffLL) return RR_ERR_INVALID;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: %s warp rows=%lld cols=%lld L=%d NV=%d\n",
+                 mode == kModeSoftmax ? "softmax" : (mode == kModeStats ? "lnstats" : "layernorm"),
+                 (long long)rows, (long long)cols, lanes, nv);
+  if (in_dtype == RR_BF16) {
+    switch (mode) {
+      case kModeSoftmax: return launch_mode<InBF16, kModeSoftmax>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      case kModeStats: return launch_mode<InBF16, kModeStats>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      default: return launch_mode<InBF16, kModeLayernorm>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    }
+  }
+  switch (mode) {
+    case kModeSoftmax: return launch_mode<InF32, kModeSoftmax>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case kModeStats: return launch_mode<InF32, kModeStats>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_mode<InF32, kModeLayernorm>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
+}
+
+}  // namespace rr

@@ -14,6 +14,7 @@
 #include "rr.h"
 #include "rr_device.cuh"
 #include "rr_internal.h"
+#include "rowwise.cuh"
 
 namespace rr {
 namespace {
@@ -22,52 +23,6 @@ namespace {
 #define RR_ROW_THREADS 256
 #endif
 constexpr int kRowThreads = RR_ROW_THREADS;
-constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Input element types: bf16 (held as its raw 16 bits) or fp32.
-struct InBF16 {
-  using S = unsigned short;
-  static constexpr int EPV = 8;  // elements per 16-byte vector
-  static __device__ __forceinline__ void unpack(const uint4 &w, float (&o)[8]) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o[2 * i] = __uint_as_float(u[i] << 16);
-      o[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-    }
-  }
-  static __device__ __forceinline__ float load1(const S *p) {
-    return __uint_as_float(((uint32_t)__ldg(p)) << 16);
-  }
-};
-struct InF32 {
-  using S = float;
-  static constexpr int EPV = 4;
-  static __device__ __forceinline__ void unpack(const uint4 &w, float (&o)[4]) {
-    o[0] = __uint_as_float(w.x); o[1] = __uint_as_float(w.y);
-    o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
-  }
-  static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
-};
-
-// ---------------------------------------------------------------------------
-// The online-softmax (max, sum) monoid: (m1, s1) + (m2, s2) =
-// (M, s1 * e^(m1 - M) + s2 * e^(m2 - M)), M = max(m1, m2), identity
-// (-inf, 0).  A side whose max is -inf contributes 0 (no -inf - -inf NaN).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2) {
-  const float M = fmaxf(m, m2);
-  const float a = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - M) * kLog2e);
-  const float b = (m2 == -INFINITY) ? 0.0f : s2 * ex2_approx((m2 - M) * kLog2e);
-  m = M;
-  s = a + b;
-}
 
 // Block reduce of the (max, sum) pair; every thread receives the result.
 template <int THREADS>
@@ -159,6 +114,13 @@ k_softmax_reg(const typename In::S *__restrict__ x, int64_t rows, int cols,
           v[k][e] = p;
           s += p;
         }
+    } else {
+      // every element this thread holds is -inf: e^(x - M) = 0 (and not
+      // -inf * 0 = NaN in the write below)
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
     }
     float M = m, S = s;
     ms_block_allreduce<THREADS>(M, S, red_m, red_s);
@@ -296,11 +258,6 @@ k_lnstats_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, 
       rstd[row] = 1.0f / sqrtf(var + eps);
     }
   }
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // ---------------------------------------------------------------------------
@@ -464,8 +421,6 @@ inline int pick_nv(int64_t nvec) {
 // M, S (mean, var) bits.  The passes read 8-element vectors where the slice
 // is 16-byte aligned, element by element otherwise.
 // ---------------------------------------------------------------------------
-enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
-
 // Folds the 8-element vectors v = tid, tid + THREADS, ... < nv of ps, in that
 // order: st = f(st, v, e).  U vectors per thread are loaded back to back
 // before the first is used (raw words first, unpacked after), so U * 16 bytes
@@ -697,18 +652,41 @@ inline int rowwise_splitk_cluster(int64_t rows, int64_t cols, const DevInfo &d) 
   return c;
 }
 
-// Tier of a two-pass row op: forced (tier, C) or automatic.  Returns the
-// cluster size for the split-K tier, 0 for the block tier, -1 if a forced
-// split-K cluster size cannot run.
-inline int rowwise_pick(int64_t rows, int64_t cols, int tier, int C, const DevInfo &d) {
-  if (tier == RR_TIER_BLOCK) return 0;
+// Rows per SM from which the automatic choice takes the warp tier for rows
+// that fit it; below that a CTA per row finishes sooner.  The layernorm
+// rewrite, whose lanes also load gamma and beta for every vector they
+// write, needs more rows to come out ahead.
+constexpr int kRowWarpMinRowsPerSM = 4;
+constexpr int kRowWarpMinRowsPerSMRewrite = 8;
+
+// Tier of a two-pass row op: forced (tier, C) or automatic.  `vec`: the row
+// can be read as nvec 16-byte vectors and the outputs are aligned for the
+// register forms (the warp tier needs it).  c is the split-K cluster size or
+// the warp tier's lanes per row; tier < 0 when a forced choice cannot run.
+struct RowPick {
+  int tier;
+  int c;
+};
+inline RowPick rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, int tier, int C,
+                            const DevInfo &d, int warp_min_rows_per_sm = kRowWarpMinRowsPerSM) {
+  if (tier == RR_TIER_BLOCK) return {RR_TIER_BLOCK, 1};
+  if (tier == RR_TIER_WARP) {
+    const int L = vec ? rowwise_warp_lanes(nvec, C) : 0;
+    return L ? RowPick{RR_TIER_WARP, L} : RowPick{-1, 0};
+  }
   if (tier == RR_TIER_SPLITK) {
     if (C == 0) C = rowwise_splitk_cluster(rows, cols, d);
     if (C == 0) C = 2;
-    if (C > 1 && !d.cluster_launch) return -1;
-    return C;
+    if (C > 1 && !d.cluster_launch) return {-1, 0};
+    return {RR_TIER_SPLITK, C};
   }
-  return rowwise_splitk_cluster(rows, cols, d);
+  const int c = rowwise_splitk_cluster(rows, cols, d);
+  if (c > 0) return {RR_TIER_SPLITK, c};
+  if (vec && rows >= (int64_t)warp_min_rows_per_sm * d.sm_count) {
+    const int L = rowwise_warp_lanes(nvec, 0);
+    if (L) return {RR_TIER_WARP, L};
+  }
+  return {RR_TIER_BLOCK, 1};
 }
 
 template <class In>
@@ -716,19 +694,21 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
                  const DevInfo &d, int *tier_out, int tier, int C) {
   using S = typename In::S;
   const S *x = (const S *)xv;
-  const int c = rowwise_pick(rows, cols, tier, C, d);
-  if (c < 0) return RR_ERR_UNSUPPORTED;
-  if (c > 0) {
-    *tier_out = RR_TIER_SPLITK | (c << 8);
-    return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
-                                                   nullptr, nullptr, nullptr, c, s, d);
-  }
   const uintptr_t ax = (uintptr_t)xv, ay = (uintptr_t)y;
   const int64_t nvec = cols / In::EPV;
-  const bool reg = (cols % In::EPV == 0) && ax % 16 == 0 &&
-                   (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0) && pick_nv(nvec) > 0;
+  const bool vec = (cols % In::EPV == 0) && ax % 16 == 0 &&
+                   (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
+  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
+  *tier_out = pk.tier | (pk.c << 8);
+  if (pk.tier == RR_TIER_SPLITK)
+    return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
+                                                   nullptr, nullptr, nullptr, pk.c, s, d);
+  if (pk.tier == RR_TIER_WARP)
+    return launch_rowwise_warp(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+                               0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.c, s, d);
+  const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
-    *tier_out = RR_TIER_BLOCK | (1 << 8);
 #define RR_SM_REG(NV)                                                          \
   {                                                                            \
     auto k = k_softmax_reg<kRowThreads, NV, In>;                               \
@@ -742,7 +722,6 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
     }
 #undef RR_SM_REG
   } else {
-    *tier_out = RR_TIER_BLOCK | (1 << 8);
     auto k = k_softmax_gen<kRowThreads, In>;
     launch_kernel(k, dim3(persistent_grid(k, kRowThreads, rows, d)), dim3(kRowThreads), 0, s, 0, x, rows, cols, y);
   }
@@ -754,16 +733,18 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
                  float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
   using S = typename In::S;
   const S *x = (const S *)xv;
-  const int c = rowwise_pick(rows, cols, tier, C, d);
-  if (c < 0) return RR_ERR_UNSUPPORTED;
-  if (c > 0) {
-    *tier_out = RR_TIER_SPLITK | (c << 8);
-    return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
-                                                 nullptr, nullptr, nullptr, c, s, d);
-  }
   const int64_t nvec = cols / In::EPV;
-  const bool reg = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) && pick_nv(nvec) > 0;
-  *tier_out = RR_TIER_BLOCK | (1 << 8);
+  const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
+  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
+  *tier_out = pk.tier | (pk.c << 8);
+  if (pk.tier == RR_TIER_SPLITK)
+    return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
+                                                 nullptr, nullptr, nullptr, pk.c, s, d);
+  if (pk.tier == RR_TIER_WARP)
+    return launch_rowwise_warp(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+                               nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.c, s, d);
+  const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
 #define RR_LN_REG(NV)                                                          \
   {                                                                            \
@@ -790,18 +771,20 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
                    const DevInfo &d, int *tier_out, int tier, int C) {
   using S = typename In::S;
   const S *x = (const S *)xv;
-  const int c = rowwise_pick(rows, cols, tier, C, d);
-  if (c < 0) return RR_ERR_UNSUPPORTED;
-  if (c > 0) {
-    *tier_out = RR_TIER_SPLITK | (c << 8);
-    return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
-                                                     gamma, beta, y, c, s, d);
-  }
-  *tier_out = RR_TIER_BLOCK | (1 << 8);
   const int64_t nvec = cols / In::EPV;
-  const bool reg = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
+  const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
-                   ((uintptr_t)y % (2 * In::EPV) == 0) && pick_nv(nvec) > 0;
+                   ((uintptr_t)y % (2 * In::EPV) == 0);
+  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, kRowWarpMinRowsPerSMRewrite);
+  if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
+  *tier_out = pk.tier | (pk.c << 8);
+  if (pk.tier == RR_TIER_SPLITK)
+    return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
+                                                     gamma, beta, y, pk.c, s, d);
+  if (pk.tier == RR_TIER_WARP)
+    return launch_rowwise_warp(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+                               eps, nullptr, mean, rstd, gamma, beta, y, pk.c, s, d);
+  const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
 #define RR_LNF_REG(NV)                                                         \
   {                                                                            \

@@ -52,8 +52,9 @@ int launch_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner
                        cudaStream_t s, const DevInfo &d);
 
 // ---- softmax / layernorm statistics (rowwise.cu)
-// tier: RR_TIER_AUTO, RR_TIER_BLOCK or RR_TIER_SPLITK; C: split-K cluster
-// size (0 = automatic).  *tier_out receives (C << 8) | tier.
+// tier: RR_TIER_AUTO, RR_TIER_WARP, RR_TIER_BLOCK or RR_TIER_SPLITK; C:
+// split-K cluster size, or the warp tier's lanes per row (0 = automatic).
+// *tier_out receives (C << 8) | tier (C = lanes per row for the warp tier).
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype,
                    float *out, cudaStream_t s, const DevInfo &d, int *tier_out,
                    int tier, int C);
@@ -67,6 +68,26 @@ int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, fl
                      const float *gamma, const float *beta, uint16_t *y, float *mean,
                      float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier,
                      int C);
+
+// ---- warp tier of the row operations (rowwarp.cu)
+// A segment of L lanes per row holding NV 16-byte vectors per lane, NV a
+// power of two up to kRowWarpMaxNV.
+constexpr int kRowWarpMaxNV = 8;
+constexpr int kRowWarpTargetNV = 4;  // automatic L: about this many vectors per lane
+// Lanes per row for a row of nvec 16-byte vectors: `lanes` (1..32, a power
+// of two) if it can hold the row, else 0; lanes == 0 picks one.  0 when the
+// row does not fit the tier.
+int rowwise_warp_lanes(int64_t nvec, int lanes);
+// Vectors per lane for nvec vectors over `lanes` lanes (a power of two).
+int rowwise_warp_nv(int64_t nvec, int lanes);
+// mode 0 softmax (y), 1 statistics (mean, rstd), 2 layernorm (ybf; mean /
+// rstd optional).  The caller has checked the alignment: cols a multiple
+// of the 16-byte vector, x 16-byte aligned, y as the block tier's register
+// form needs it, gamma / beta 16-byte aligned.
+int launch_rowwise_warp(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                        float eps, float *y, float *mean, float *rstd, const float *gamma,
+                        const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                        const DevInfo &d);
 
 // ---- split-K combine (combine.cu)
 int launch_combine(const float *O, const float *m, const float *l, int P,

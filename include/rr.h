@@ -263,11 +263,26 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
                        float eps, float *mean, float *rstd, void *stream);
 
 /*
- * Options of rr_softmax_ex / rr_layernorm_stats_ex ([RW] tier semantics for
- * the two-pass row operations).  Zero-initialise and set what you need.
- *   tier          RR_TIER_AUTO, RR_TIER_BLOCK (a CTA per row, the row on
- *                 chip) or RR_TIER_SPLITK (a cluster of C CTAs per row).
+ * Options of rr_softmax_ex / rr_layernorm_stats_ex / rr_layernorm_ex ([RW]
+ * tier semantics for the two-pass row operations).  Zero-initialise and set
+ * what you need.
+ *   tier          RR_TIER_AUTO, RR_TIER_WARP (a segment of lanes_per_row
+ *                 lanes of a warp per row, the row in its registers),
+ *                 RR_TIER_BLOCK (a CTA per row, the row on chip) or
+ *                 RR_TIER_SPLITK (a cluster of C CTAs per row).
  *   cluster_size  split-K: 0 = automatic, else 1, 2, 4, 8 or 16.
+ *   lanes_per_row warp tier: 0 = automatic, else 1, 2, 4, 8, 16 or 32.
+ * Warp tier: lane j of a row's segment holds the row's 16-byte vectors j,
+ * j + L, j + 2L, ... (at most 8 per lane, so rows of up to 256 vectors:
+ * 2048 bf16 or 1024 fp32 elements); both reductions of a row are shuffles
+ * inside the segment.  It needs cols a multiple of 8 (bf16) or 4 (fp32), x
+ * 16-byte aligned, the softmax output 32-byte (bf16 input) or 16-byte
+ * (fp32) aligned, and for the layernorm gamma / beta 16-byte and the output
+ * 16-byte (bf16 input) or 8-byte (fp32) aligned; a forced warp tier
+ * returns RR_ERR_UNSUPPORTED when these do not hold or the row does not fit
+ * lanes_per_row lanes.  AUTO picks it for rows that fit when there are at
+ * least 4 rows per SM (8 for rr_layernorm), with about 4 vectors per lane
+ * (2 for rows of up to 8 vectors, a lane per row for up to 2).
  * Split-K: CTA r owns slice r of the row, and the row takes two cluster
  * combines ([CA]) on two slots without a tail sync between them: softmax
  * combines the CTA maxima, then the CTA sums rescaled to the row max (one
@@ -280,6 +295,7 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
 typedef struct {
     int tier;
     int cluster_size;
+    int lanes_per_row;
 } rr_rowwise_opts;
 
 /* rr_softmax with options; opts may be NULL.  RR_ERR_UNSUPPORTED if a
@@ -307,7 +323,7 @@ int rr_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype,
                  float eps, const float *gamma, const float *beta,
                  uint16_t *out_bf16, float *mean, float *rstd, void *stream);
 
-/* rr_layernorm with options (block or split-K tier); opts may be NULL. */
+/* rr_layernorm with options (warp, block or split-K tier); opts may be NULL. */
 int rr_layernorm_ex(const void *x, int64_t rows, int64_t cols, int in_dtype,
                     float eps, const float *gamma, const float *beta,
                     uint16_t *out_bf16, float *mean, float *rstd, void *stream,

@@ -242,3 +242,144 @@ def test_argument_errors(rr):
         rr.layernorm_stats(torch.zeros((3, 0), device="cuda"))
     with pytest.raises(rr.RRError):
         rr.layernorm_stats(torch.zeros((3, 4), device="cuda"), eps=-1.0)
+
+
+# ---------------------------------------------------------------------------
+# Warp tier: a segment of L lanes per row, up to 8 16-byte vectors per lane.
+# Widths cover one vector, fewer vectors than lanes (idle lanes), ragged
+# multiples of L and the largest row a segment holds; row counts cover a
+# partial segment group, a partial CTA and, for one width per L, more rows
+# than the persistent grid takes in one pass (the prefetch path).
+# ---------------------------------------------------------------------------
+def _warp_widths(L, epv):
+    nv = sorted({1, max(1, L - 1), L, L + 1, 3 * L - 1, 8 * L - 1, 8 * L})
+    return [n * epv for n in nv if n <= 8 * L]
+
+
+def _warp_rows(L, cols, elt):
+    # one more pass than a full grid needs at 2 CTAs per SM (the fewest any
+    # variant gets), capped at 64 MiB of input
+    many = min(152 * 2 * 8 * (32 // L) * 2 + 37, (64 << 20) // (cols * elt))
+    return [1, 7, 300, many]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("L", [1, 2, 4, 8, 16, 32])
+def test_softmax_warp_forced(rr, oracle_mod, dtype, L):
+    epv = 8 if dtype == torch.bfloat16 else 4
+    elt = 2 if dtype == torch.bfloat16 else 4
+    for i, cols in enumerate(_warp_widths(L, epv)):
+        for rows in (_warp_rows(L, cols, elt) if i == len(_warp_widths(L, epv)) - 2 else [7, 300]):
+            x = _x(rows, cols, dtype, 1000 + 10 * L + i, 3.0)
+            y = to_np(rr.softmax(x, tier="warp", lanes_per_row=L))
+            assert rr.last_tier() == ("warp", L)
+            idx = np.r_[0:min(rows, 64), max(rows - 64, 0):rows]
+            ref = oracle_mod.softmax(to_np(x[torch.from_numpy(idx).cuda()]))
+            assert_rel_close(y[idx], ref, 1e-5, floor=1e-30, what=f"softmax warp L={L} {rows}x{cols}")
+            np.testing.assert_allclose(y.astype(np.float64).sum(axis=1), 1.0, rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("L", [1, 2, 4, 8, 16, 32])
+def test_layernorm_warp_forced(rr, oracle_mod, dtype, L):
+    from cluster_reductions_gb300 import inputs
+    from _util import assert_layernorm_close
+    epv = 8 if dtype == torch.bfloat16 else 4
+    elt = 2 if dtype == torch.bfloat16 else 4
+    widths = _warp_widths(L, epv)
+    for i, cols in enumerate(widths):
+        gamma, beta = inputs.layernorm_params(cols, 1100 + i, "cuda")
+        for rows in (_warp_rows(L, cols, elt) if i == len(widths) - 1 else [7, 300]):
+            x = _x(rows, cols, dtype, 1200 + 10 * L + i, 1.0)
+            mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+            y = rr.layernorm(x, gamma, beta, 1e-5, mean=mean, rstd=rstd, tier="warp",
+                             lanes_per_row=L)
+            assert rr.last_tier() == ("warp", L)
+            m2, r2 = rr.layernorm_stats(x, 1e-5, tier="warp", lanes_per_row=L)
+            assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
+            assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
+            idx = np.r_[0:min(rows, 48), max(rows - 48, 0):rows]
+            xs = x[torch.from_numpy(idx).cuda()]
+            y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(gamma), to_np(beta), 1e-5)
+            xf = xs.to(torch.float64).cpu().numpy()
+            assert_layernorm_close(to_np(y)[idx], y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_)
+            bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+            assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
+            assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd warp L={L} {rows}x{cols}")
+
+
+def test_warp_rowwise_special_rows(rr, oracle_mod):
+    # constant rows, alternating +-a, and -inf over whole lanes of a segment
+    x = torch.full((5, 512), 3.25, dtype=torch.bfloat16, device="cuda")
+    y = to_np(rr.softmax(x, tier="warp"))
+    np.testing.assert_allclose(y, 1.0 / 512, rtol=1e-6)
+    mean, rstd = rr.layernorm_stats(x, 1e-5, tier="warp")
+    assert (to_np(mean) == 3.25).all()
+    np.testing.assert_allclose(to_np(rstd), 1.0 / np.sqrt(1e-5), rtol=1e-5)
+    a = 1.75
+    x = torch.tensor([a, -a] * 256, dtype=torch.bfloat16, device="cuda").view(1, -1).repeat(3, 1)
+    mean, rstd = rr.layernorm_stats(x, 1e-5, tier="warp", lanes_per_row=8)
+    assert (np.abs(to_np(mean)) <= 1e-6).all()
+    assert (np.abs(to_np(rstd) - 1.0 / np.sqrt(a * a + 1e-5)) <= 1e-5 / a).all()
+    for L in (4, 8, 32):                      # L = 4 holds the 32 vectors at 8 per lane
+        x = _x(9, 256, torch.bfloat16, 1300 + L, 3.0)
+        x[:, :128] = float("-inf")
+        x[3, :] = float("-inf")
+        x[4, 255] = float("-inf")
+        y = to_np(rr.softmax(x, tier="warp", lanes_per_row=L))
+        ref = oracle_mod.softmax(to_np(x))
+        live = [r for r in range(9) if r != 3]
+        assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what=f"softmax -inf L={L}")
+        assert (y[:, :128] == 0).all()
+        # an all -inf row is 0/0: the oracle's fp64 exp(-inf - -inf) is NaN, the
+        # kernels write 0 (the combine's convention for a row with no mass)
+        assert np.isnan(ref[3]).all() and (y[3] == 0).all()
+
+
+def test_warp_rowwise_auto_and_unsupported(rr, oracle_mod):
+    # AUTO takes the warp tier for many short aligned rows, with about 4
+    # vectors per lane (2 for rows of up to 8 vectors); misaligned or
+    # over-long rows cannot be forced onto it
+    x = _x(4096, 512, torch.bfloat16, 1400, 3.0)
+    rr.softmax(x)
+    assert rr.last_tier() == ("warp", 16)
+    rr.layernorm_stats(x[:, :64].contiguous())
+    assert rr.last_tier() == ("warp", 4)
+    rr.layernorm_stats(x[:, :16].contiguous())
+    assert rr.last_tier() == ("warp", 1)
+    xf = _x(4096, 1024, torch.float32, 1401, 1.0)
+    rr.layernorm_stats(xf)
+    assert rr.last_tier() == ("warp", 32)
+    check_lnstats(rr, oracle_mod, xf[:200].contiguous())
+    rr.softmax(x[:8])
+    assert rr.last_tier() == ("block", 1)
+    for bad in (_x(8, 512, torch.bfloat16, 1402, 1.0, 1),      # x not 16-byte aligned
+                _x(8, 100, torch.bfloat16, 1403, 1.0),         # cols not a vector multiple
+                _x(8, 4096, torch.bfloat16, 1404, 1.0)):       # 512 vectors > 8 per lane
+        with pytest.raises(rr.RRError) as e:
+            rr.softmax(bad, tier="warp")
+        assert e.value.status == 2
+    with pytest.raises(rr.RRError) as e:
+        rr.softmax(_x(8, 1024, torch.bfloat16, 1405, 1.0), tier="warp", lanes_per_row=8)
+    assert e.value.status == 2                                  # 128 vectors > 8 x 8
+    for bad_l in (3, 64):
+        with pytest.raises(rr.RRError) as e:
+            rr.softmax(x, tier="warp", lanes_per_row=bad_l)
+        assert e.value.status == 1
+
+
+@pytest.mark.parametrize("tier", ["block", "splitk"])
+def test_softmax_neg_inf_spans(rr, oracle_mod, tier):
+    # -inf over whole threads' (or CTAs') share of a row: those elements are
+    # exactly 0, the rest match the oracle; an all -inf row (0/0, NaN in the
+    # oracle) is written as 0
+    for cols in (4096, 20000, 65536):
+        x = _x(4, cols, torch.bfloat16, 1500 + cols % 97, 3.0)
+        x[:, : cols // 2] = float("-inf")
+        x[2, :] = float("-inf")
+        y = to_np(rr.softmax(x, tier=tier))
+        ref = oracle_mod.softmax(to_np(x))
+        live = [0, 1, 3]
+        assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what=f"softmax -inf {tier} {cols}")
+        assert (y[:, : cols // 2] == 0).all()
+        assert np.isnan(ref[2]).all() and (y[2] == 0).all()
