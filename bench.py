@@ -63,18 +63,18 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1084762112, "src": ["reduce.cu", "rr_device.cuh"],
-                      "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 576032768, "src": ["combine.cu", "rr_device.cuh"],
+    "splitk_sum_f32": {"bytes": 1085681664, "src": ["reduce.cu", "rr_device.cuh"],
+                      "src_sha": "7187092cae58b53b", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 577034240, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "e41b009ab53904ca", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 563821568, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271528448, "src": ["reduce.cu", "rr_device.cuh"],
-                     "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271666176, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "5bbefd24407cdb80", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 138524416, "src": ["reduce.cu", "rr_device.cuh"],
-                    "src_sha": "d0af3e4375ae1127", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "softmax_bf16": {"bytes": 560532480, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "3ec31e6ec6a17222", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271550976, "src": ["reduce.cu", "rr_device.cuh"],
+                     "src_sha": "7187092cae58b53b", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271616256, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "3ec31e6ec6a17222", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137868544, "src": ["reduce.cu", "rr_device.cuh"],
+                    "src_sha": "7187092cae58b53b", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
