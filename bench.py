@@ -27,6 +27,7 @@ import ctypes
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -396,11 +397,37 @@ def cpu_baseline(target_s: float):
         passes += 1
         dt = time.perf_counter() - t0
     b = sample_bytes(data)
+    # one pass on a single thread beside it
+    t1 = time.perf_counter()
+    run_oracle_step(data, 1)
+    dt1 = time.perf_counter() - t1
     return {"value": round(b * passes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": f"every operation of the step on {scale:.2e} of its rows "
                       f"({b / 1e6:.1f} MB algorithmic per pass), {passes} passes, fp64 C oracle, "
-                      f"{threads} host threads, {dt:.2f} s"}
+                      f"{threads} host threads, {dt:.2f} s",
+            "single_thread_value": round(b / dt1 / 1e9, 4),
+            "single_thread_sample": f"one pass of the same sample on one thread, {dt1:.2f} s",
+            "cpu_model": host_cpu_model()}
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it, else /proc/cpuinfo's."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
 
 
 # --------------------------------------------------------------------- our arm

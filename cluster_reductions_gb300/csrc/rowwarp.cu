@@ -45,6 +45,7 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
   const int nvec = cols / EPV;
+  const bool gb32 = MODE == kModeLayernorm && aligned32(gamma, beta);
   uint4 raw[NV];
   auto fetch = [&](int64_t r) {
     const int64_t rc = r < rows ? r : rows - 1;
@@ -144,13 +145,7 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
             const int idx = k * L + sub;
             if (idx < nvec) {
               float g[EPV], b[EPV];
-#pragma unroll
-              for (int e = 0; e < EPV; e += 4) {
-                const float4 gv = __ldg(reinterpret_cast<const float4 *>(gamma + idx * EPV + e));
-                const float4 bv = __ldg(reinterpret_cast<const float4 *>(beta + idx * EPV + e));
-                g[e] = gv.x; g[e + 1] = gv.y; g[e + 2] = gv.z; g[e + 3] = gv.w;
-                b[e] = bv.x; b[e + 1] = bv.y; b[e + 2] = bv.z; b[e + 3] = bv.w;
-              }
+              load_gamma_beta<EPV>(gamma, beta, (int64_t)idx * EPV, gb32, g, b);
               uint32_t pk[EPV / 2];
 #pragma unroll
               for (int e = 0; e < EPV; e += 2)
@@ -227,7 +222,7 @@ int launch_mode(int L, int nv, const void *x, int64_t rows, int64_t cols, float 
 
 }  // namespace
 
-int rowwise_warp_lanes(int64_t nvec, int lanes) {
+int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite) {
   if (nvec < 1 || nvec > (int64_t)32 * kRowWarpMaxNV) return 0;
   if (lanes != 0) {
     if (!(lanes == 1 || lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16 || lanes == 32))
@@ -235,8 +230,10 @@ int rowwise_warp_lanes(int64_t nvec, int lanes) {
     return (int64_t)lanes * kRowWarpMaxNV >= nvec ? lanes : 0;
   }
   // rows of up to 8 vectors: about 2 vectors per lane; longer rows: about
-  // kRowWarpTargetNV per lane, up to 32 lanes
-  const int per = nvec <= 8 ? 2 : kRowWarpTargetNV;
+  // kRowWarpTargetNV per lane, up to 32 lanes.  The layernorm rewrite, which
+  // also holds gamma and beta for its vectors, takes 2 per lane throughout:
+  // at 4 it needs ~120 registers and half the resident warps.
+  const int per = (nvec <= 8 || rewrite) ? 2 : kRowWarpTargetNV;
   int L = 1;
   while (L < 32 && (int64_t)L * per < nvec) L *= 2;
   return L;

@@ -278,6 +278,7 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
   __shared__ float red[2][THREADS / 32];
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
+  const bool gb32 = aligned32(gamma, beta);
   const float inv_n = 1.0f / (float)cols;
   uint4 raw[NV];
   auto fetch = [&](int64_t r) {
@@ -327,13 +328,7 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
       const int idx = k * THREADS + tid;
       if (idx < nvec) {
         float g[EPV], b[EPV];
-#pragma unroll
-        for (int e = 0; e < EPV; e += 4) {
-          const float4 gv = __ldg(reinterpret_cast<const float4 *>(gamma + idx * EPV + e));
-          const float4 bv = __ldg(reinterpret_cast<const float4 *>(beta + idx * EPV + e));
-          g[e] = gv.x; g[e + 1] = gv.y; g[e + 2] = gv.z; g[e + 3] = gv.w;
-          b[e] = bv.x; b[e + 1] = bv.y; b[e + 2] = bv.z; b[e + 3] = bv.w;
-        }
+        load_gamma_beta<EPV>(gamma, beta, (int64_t)idx * EPV, gb32, g, b);
         uint32_t pk[EPV / 2];
 #pragma unroll
         for (int e = 0; e < EPV; e += 2)
@@ -668,10 +663,11 @@ struct RowPick {
   int c;
 };
 inline RowPick rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, int tier, int C,
-                            const DevInfo &d, int warp_min_rows_per_sm = kRowWarpMinRowsPerSM) {
+                            const DevInfo &d, bool rewrite = false) {
+  const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
   if (tier == RR_TIER_BLOCK) return {RR_TIER_BLOCK, 1};
   if (tier == RR_TIER_WARP) {
-    const int L = vec ? rowwise_warp_lanes(nvec, C) : 0;
+    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : 0;
     return L ? RowPick{RR_TIER_WARP, L} : RowPick{-1, 0};
   }
   if (tier == RR_TIER_SPLITK) {
@@ -683,7 +679,7 @@ inline RowPick rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, 
   const int c = rowwise_splitk_cluster(rows, cols, d);
   if (c > 0) return {RR_TIER_SPLITK, c};
   if (vec && rows >= (int64_t)warp_min_rows_per_sm * d.sm_count) {
-    const int L = rowwise_warp_lanes(nvec, 0);
+    const int L = rowwise_warp_lanes(nvec, 0, rewrite);
     if (L) return {RR_TIER_WARP, L};
   }
   return {RR_TIER_BLOCK, 1};
@@ -775,7 +771,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
                    ((uintptr_t)y % (2 * In::EPV) == 0);
-  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, kRowWarpMinRowsPerSMRewrite);
+  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, /*rewrite=*/true);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.c << 8);
   if (pk.tier == RR_TIER_SPLITK)

@@ -67,5 +67,43 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 
 enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
 
+// gamma[off .. off+N) and beta[off .. off+N) of the layernorm rewrite
+// (N = 4 or 8, 16-byte aligned), through the read-only path and kept in L1:
+// every row reads the same values.  With both 32-byte aligned (`a32`) an
+// 8-value group is one 256-bit load per array.  Lanes of a warp hold
+// adjacent groups, so a warp's load spans 32 groups either way; two 128-bit
+// loads per array each cover every other 16 bytes of that span and cost the
+// L1 as many wavefronts as one 256-bit load, which halves the rewrite's L1
+// traffic (the L1, not DRAM, bounded it).
+template <int N>
+__device__ __forceinline__ void load_gamma_beta(const float *__restrict__ gamma,
+                                                const float *__restrict__ beta, int64_t off,
+                                                bool a32, float (&g)[N], float (&b)[N]) {
+  if constexpr (N == 8) {
+    if (a32) {
+      asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=f"(g[0]), "=f"(g[1]), "=f"(g[2]), "=f"(g[3]), "=f"(g[4]), "=f"(g[5]), "=f"(g[6]),
+            "=f"(g[7])
+          : "l"(gamma + off));
+      asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3]), "=f"(b[4]), "=f"(b[5]), "=f"(b[6]),
+            "=f"(b[7])
+          : "l"(beta + off));
+      return;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < N; e += 4) {
+    const float4 gv = __ldg(reinterpret_cast<const float4 *>(gamma + off + e));
+    const float4 bv = __ldg(reinterpret_cast<const float4 *>(beta + off + e));
+    g[e] = gv.x; g[e + 1] = gv.y; g[e + 2] = gv.z; g[e + 3] = gv.w;
+    b[e] = bv.x; b[e + 1] = bv.y; b[e + 2] = bv.z; b[e + 3] = bv.w;
+  }
+}
+
+__device__ __forceinline__ bool aligned32(const float *a, const float *b) {
+  return (((uintptr_t)a | (uintptr_t)b) & 31) == 0;
+}
+
 }  // namespace
 }  // namespace rr

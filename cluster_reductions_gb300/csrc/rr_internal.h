@@ -75,9 +75,9 @@ int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, fl
 constexpr int kRowWarpMaxNV = 8;
 constexpr int kRowWarpTargetNV = 4;  // automatic L: about this many vectors per lane
 // Lanes per row for a row of nvec 16-byte vectors: `lanes` (1..32, a power
-// of two) if it can hold the row, else 0; lanes == 0 picks one.  0 when the
-// row does not fit the tier.
-int rowwise_warp_lanes(int64_t nvec, int lanes);
+// of two) if it can hold the row, else 0; lanes == 0 picks one (for the
+// layernorm rewrite when `rewrite`).  0 when the row does not fit the tier.
+int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite);
 // Vectors per lane for nvec vectors over `lanes` lanes (a power of two).
 int rowwise_warp_nv(int64_t nvec, int lanes);
 // mode 0 softmax (y), 1 statistics (mean, rstd), 2 layernorm (ybf; mean /

@@ -282,7 +282,8 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * returns RR_ERR_UNSUPPORTED when these do not hold or the row does not fit
  * lanes_per_row lanes.  AUTO picks it for rows that fit when there are at
  * least 4 rows per SM (8 for rr_layernorm), with about 4 vectors per lane
- * (2 for rows of up to 8 vectors, a lane per row for up to 2).
+ * (2 for rows of up to 8 vectors and for rr_layernorm; a lane per row for
+ * rows of up to 2).
  * Split-K: CTA r owns slice r of the row, and the row takes two cluster
  * combines ([CA]) on two slots without a tail sync between them: softmax
  * combines the CTA maxima, then the CTA sums rescaled to the row max (one

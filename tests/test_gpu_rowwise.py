@@ -347,6 +347,12 @@ def test_warp_rowwise_auto_and_unsupported(rr, oracle_mod):
     assert rr.last_tier() == ("warp", 4)
     rr.layernorm_stats(x[:, :16].contiguous())
     assert rr.last_tier() == ("warp", 1)
+    from cluster_reductions_gb300 import inputs
+    g, b = inputs.layernorm_params(512, 1406, "cuda")
+    rr.layernorm(x, g, b, 1e-5)                                 # the rewrite: ~2 vectors per lane
+    assert rr.last_tier() == ("warp", 32)
+    rr.layernorm(x[:1000], g, b, 1e-5)                          # < 8 rows per SM
+    assert rr.last_tier() == ("block", 1)
     xf = _x(4096, 1024, torch.float32, 1401, 1.0)
     rr.layernorm_stats(xf)
     assert rr.last_tier() == ("warp", 32)
