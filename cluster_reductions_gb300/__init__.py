@@ -407,6 +407,23 @@ def plan_reduce(rows: int, cols: int, sm_count: int, max_cluster: int) -> Tuple[
     return TIER_NAMES[t.value], c.value
 
 
+_ROW_OPS = {"softmax": 0, "lnstats": 1, "layernorm_stats": 1, "layernorm": 2}
+
+
+def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: int,
+                 dtype=torch.bfloat16, aligned: bool = True) -> Tuple[str, int]:
+    """rr_plan_rowwise (host only): the tier and width (lanes per row, cluster
+    size or 1) that softmax / layernorm_stats / layernorm pick."""
+    dt = _DT.get(dtype)
+    if dt not in (RR_BF16, RR_F32):
+        raise TypeError(f"plan_rowwise: dtype {dtype} not supported")
+    t, w = ctypes.c_int(), ctypes.c_int()
+    check(load().rr_plan_rowwise(int(rows), int(cols), dt, _ROW_OPS[row_op], 1 if aligned else 0,
+                                 int(sm_count), int(max_cluster), ctypes.byref(t),
+                                 ctypes.byref(w)), "rr_plan_rowwise")
+    return TIER_NAMES[t.value], w.value
+
+
 def plan_reduce_axis(outer: int, axis: int, inner: int, sm_count: int, max_cluster: int,
                      x_align: int = 16, with_workspace: bool = True) -> dict:
     """rr_plan_reduce_axis (host only): the launch rr_reduce_axis_ex picks."""

@@ -636,53 +636,13 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
                                    ybf));
 }
 
-// Split-K cluster size for a two-pass row op: the smallest power of two >= 2
-// that puts a CTA on every SM, at most 16; 0 when the tier does not apply
-// (then the block tier runs).
-inline int rowwise_splitk_cluster(int64_t rows, int64_t cols, const DevInfo &d) {
-  const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
-  if (!d.cluster_launch || cap < 2 || rows < 1 || rows >= d.sm_count || cols < 16384) return 0;
-  int c = 2;
-  while (2 * c <= cap && (int64_t)c * rows < d.sm_count) c *= 2;
-  return c;
-}
-
-// Rows per SM from which the automatic choice takes the warp tier for rows
-// that fit it; below that a CTA per row finishes sooner.  The layernorm
-// rewrite, whose lanes also load gamma and beta for every vector they
-// write, needs more rows to come out ahead.
-constexpr int kRowWarpMinRowsPerSM = 4;
-constexpr int kRowWarpMinRowsPerSMRewrite = 8;
-
-// Tier of a two-pass row op: forced (tier, C) or automatic.  `vec`: the row
-// can be read as nvec 16-byte vectors and the outputs are aligned for the
-// register forms (the warp tier needs it).  c is the split-K cluster size or
-// the warp tier's lanes per row; tier < 0 when a forced choice cannot run.
-struct RowPick {
-  int tier;
-  int c;
-};
-inline RowPick rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, int tier, int C,
+// Tier of a two-pass row op on a device (its SM count, and its largest
+// cluster: RR_MAX_CLUSTER caps it, no cluster launch makes it 1).
+inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, int tier, int C,
                             const DevInfo &d, bool rewrite = false) {
-  const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
-  if (tier == RR_TIER_BLOCK) return {RR_TIER_BLOCK, 1};
-  if (tier == RR_TIER_WARP) {
-    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : 0;
-    return L ? RowPick{RR_TIER_WARP, L} : RowPick{-1, 0};
-  }
-  if (tier == RR_TIER_SPLITK) {
-    if (C == 0) C = rowwise_splitk_cluster(rows, cols, d);
-    if (C == 0) C = 2;
-    if (C > 1 && !d.cluster_launch) return {-1, 0};
-    return {RR_TIER_SPLITK, C};
-  }
-  const int c = rowwise_splitk_cluster(rows, cols, d);
-  if (c > 0) return {RR_TIER_SPLITK, c};
-  if (vec && rows >= (int64_t)warp_min_rows_per_sm * d.sm_count) {
-    const int L = rowwise_warp_lanes(nvec, 0, rewrite);
-    if (L) return {RR_TIER_WARP, L};
-  }
-  return {RR_TIER_BLOCK, 1};
+  const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
+  return plan_rowwise(rows, cols, vec, nvec, rewrite, tier, C, d.sm_count,
+                      d.cluster_launch ? cap : 1);
 }
 
 template <class In>
@@ -694,15 +654,15 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ax % 16 == 0 &&
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
-  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.c << 8);
+  *tier_out = pk.tier | (pk.width << 8);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
-                                                   nullptr, nullptr, nullptr, pk.c, s, d);
+                                                   nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
     return launch_rowwise_warp(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
-                               0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.c, s, d);
+                               0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
 #define RR_SM_REG(NV)                                                          \
@@ -731,15 +691,15 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
-  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.c << 8);
+  *tier_out = pk.tier | (pk.width << 8);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
-                                                 nullptr, nullptr, nullptr, pk.c, s, d);
+                                                 nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
     return launch_rowwise_warp(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
-                               nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.c, s, d);
+                               nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
 #define RR_LN_REG(NV)                                                          \
@@ -771,15 +731,15 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
                    ((uintptr_t)y % (2 * In::EPV) == 0);
-  const RowPick pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, /*rewrite=*/true);
+  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, /*rewrite=*/true);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.c << 8);
+  *tier_out = pk.tier | (pk.width << 8);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
-                                                     gamma, beta, y, pk.c, s, d);
+                                                     gamma, beta, y, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
     return launch_rowwise_warp(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
-                               eps, nullptr, mean, rstd, gamma, beta, y, pk.c, s, d);
+                               eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
 #define RR_LNF_REG(NV)                                                         \
@@ -804,6 +764,39 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
 }
 
 }  // namespace
+
+// Split-K cluster size for a two-pass row op: the smallest power of two >= 2
+// that puts a CTA on every SM, at most max_cluster (<= 16); 0 when the tier
+// does not apply (a few long rows only).
+static int rowwise_splitk_cluster(int64_t rows, int64_t cols, int sm_count, int max_cluster) {
+  if (max_cluster < 2 || rows < 1 || rows >= sm_count || cols < 16384) return 0;
+  int c = 2;
+  while (2 * c <= max_cluster && (int64_t)c * rows < sm_count) c *= 2;
+  return c;
+}
+
+RowPlan plan_rowwise(int64_t rows, int64_t cols, bool vec, int64_t nvec, bool rewrite, int tier,
+                     int C, int sm_count, int max_cluster) {
+  const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
+  if (tier == RR_TIER_BLOCK) return {RR_TIER_BLOCK, 1};
+  if (tier == RR_TIER_WARP) {
+    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : 0;
+    return L ? RowPlan{RR_TIER_WARP, L} : RowPlan{-1, 0};
+  }
+  if (tier == RR_TIER_SPLITK) {
+    if (C == 0) C = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
+    if (C == 0) C = 2;
+    if (C > 1 && C > max_cluster) return {-1, 0};
+    return {RR_TIER_SPLITK, C};
+  }
+  const int c = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
+  if (c > 0) return {RR_TIER_SPLITK, c};
+  if (vec && rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
+    const int L = rowwise_warp_lanes(nvec, 0, rewrite);
+    if (L) return {RR_TIER_WARP, L};
+  }
+  return {RR_TIER_BLOCK, 1};
+}
 
 int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                      const float *gamma, const float *beta, uint16_t *y, float *mean, float *rstd,

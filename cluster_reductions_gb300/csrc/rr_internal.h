@@ -69,6 +69,27 @@ int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, fl
                      float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier,
                      int C);
 
+// ---- tier choice of the row operations (rowwise.cu, host only)
+// Rows per SM from which the automatic choice takes the warp tier for rows
+// that fit it; below that a CTA per row finishes sooner.  The layernorm
+// rewrite, whose lanes also load gamma and beta for every vector they
+// write, needs more rows to come out ahead.
+constexpr int kRowWarpMinRowsPerSM = 4;
+constexpr int kRowWarpMinRowsPerSMRewrite = 8;
+// tier RR_TIER_WARP (width = lanes per row), RR_TIER_SPLITK (width =
+// cluster size) or RR_TIER_BLOCK (width 1); tier < 0 when a forced choice
+// cannot run.
+struct RowPlan {
+  int tier;
+  int width;
+};
+// Forced (tier, C) or automatic choice for rows x cols; `vec`: the row is
+// nvec aligned 16-byte vectors and the outputs meet the register forms'
+// alignment; `rewrite`: the layernorm rewrite (else softmax / statistics).
+// A forced split-K cluster larger than max_cluster cannot run.
+RowPlan plan_rowwise(int64_t rows, int64_t cols, bool vec, int64_t nvec, bool rewrite, int tier,
+                     int C, int sm_count, int max_cluster);
+
 // ---- warp tier of the row operations (rowwarp.cu)
 // A segment of L lanes per row holding NV 16-byte vectors per lane, NV a
 // power of two up to kRowWarpMaxNV.

@@ -473,6 +473,24 @@ const char *rr_status_string(int status);
 int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster,
                    int *tier_out, int *cluster_out);
 
+/* The two-pass row operations, for rr_plan_rowwise. */
+typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr_row_op;
+
+/*
+ * rr_plan_rowwise -- the host-only tier choice of rr_softmax (row_op
+ * RR_ROW_SOFTMAX), rr_layernorm_stats (RR_ROW_LNSTATS) or rr_layernorm
+ * (RR_ROW_LAYERNORM) with automatic options ([RW] tier semantics), for a
+ * device with `sm_count` SMs whose largest co-schedulable cluster is
+ * `max_cluster` CTAs.  `aligned` != 0 says every operand meets the warp
+ * tier's alignment (rr_rowwise_opts); cols must also be a multiple of the
+ * 16-byte vector.  Writes the tier and its width: lanes per row (warp),
+ * cluster size (split-K) or 1 (block).  Touches no GPU.  RR_ERR_INVALID on
+ * negative sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
+ */
+int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,
+                    int aligned, int sm_count, int max_cluster, int *tier_out,
+                    int *width_out);
+
 /*
  * rr_test_wait_timeout -- failure-detection hook: launches one CTA that
  * waits on a shared-memory mbarrier that nothing completes, with a budget

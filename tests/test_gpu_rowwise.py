@@ -389,3 +389,19 @@ def test_softmax_neg_inf_spans(rr, oracle_mod, tier):
         assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what=f"softmax -inf {tier} {cols}")
         assert (y[:, : cols // 2] == 0).all()
         assert np.isnan(ref[2]).all() and (y[2] == 0).all()
+
+
+def test_rowwise_launch_matches_host_plan(rr):
+    # the tier a call takes on this device is the one rr_plan_rowwise reports
+    from cluster_reductions_gb300 import inputs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows, cols, dt in [(4 * sms, 256, torch.bfloat16), (4 * sms - 1, 256, torch.bfloat16),
+                           (8 * sms, 1024, torch.float32), (3000, 2048, torch.bfloat16),
+                           (2000, 4096, torch.bfloat16), (40000, 16, torch.bfloat16)]:
+        x = _x(rows, cols, dt, 1600 + cols, 1.0)
+        g, b = inputs.layernorm_params(cols, 1601, "cuda")
+        for op, call in (("softmax", lambda: rr.softmax(x)),
+                         ("lnstats", lambda: rr.layernorm_stats(x)),
+                         ("layernorm", lambda: rr.layernorm(x, g, b))):
+            call()
+            assert rr.last_tier() == rr.plan_rowwise(rows, cols, op, sms, 16, dtype=dt), (rows, cols, op)

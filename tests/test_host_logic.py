@@ -128,6 +128,56 @@ def test_tier_dispatch(lib, rows, cols, sms, maxc, expect):
     assert rr.plan_reduce(rows, cols, sms, maxc) == expect
 
 
+@pytest.mark.parametrize("rows,cols,op,dtype,aligned,maxc,expect", [
+    # split-K for a few long rows, the smallest C that covers the SMs
+    (16, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16)),
+    (16, 1 << 20, "layernorm", "bf16", True, 8, ("splitk", 8)),
+    (151, 16384, "lnstats", "bf16", True, 16, ("splitk", 2)),
+    (16, 1 << 20, "softmax", "bf16", True, 1, ("block", 1)),      # no clusters
+    (151, 16376, "softmax", "bf16", True, 16, ("block", 1)),      # below 16384 columns
+    # a CTA per row once rows fill the SMs and do not fit a warp segment
+    (32768, 4096, "softmax", "bf16", True, 16, ("block", 1)),
+    (16384, 8192, "layernorm", "bf16", True, 16, ("block", 1)),
+    (65536, 2048, "softmax", "f32", True, 16, ("block", 1)),      # 512 vectors > 256
+    # warp segments: about 4 vectors per lane, 2 for short rows and the rewrite
+    (65536, 2048, "softmax", "bf16", True, 16, ("warp", 32)),
+    (65536, 1024, "lnstats", "f32", True, 16, ("warp", 32)),
+    (1 << 20, 128, "softmax", "bf16", True, 16, ("warp", 4)),
+    (1 << 20, 128, "layernorm", "bf16", True, 16, ("warp", 8)),
+    (1 << 20, 64, "lnstats", "bf16", True, 16, ("warp", 4)),
+    (1 << 20, 16, "lnstats", "bf16", True, 16, ("warp", 1)),
+    (1 << 20, 4, "softmax", "f32", True, 16, ("warp", 1)),
+    # enough rows: 4 per SM, 8 for the rewrite
+    (607, 256, "softmax", "bf16", True, 16, ("block", 1)),
+    (608, 256, "softmax", "bf16", True, 16, ("warp", 8)),
+    (1215, 256, "layernorm", "bf16", True, 16, ("block", 1)),
+    (1216, 256, "layernorm", "bf16", True, 16, ("warp", 16)),
+    # alignment: operands or a width that is not a vector multiple
+    (1 << 20, 128, "softmax", "bf16", False, 16, ("block", 1)),
+    (1 << 20, 100, "softmax", "bf16", True, 16, ("block", 1)),
+    (1 << 20, 6, "lnstats", "f32", True, 16, ("block", 1)),
+])
+def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
+    import torch
+    import cluster_reductions_gb300 as rr
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    assert rr.plan_rowwise(rows, cols, op, 152, maxc, dtype=dt, aligned=aligned) == expect
+
+
+def test_rowwise_plan_rejects_bad_arguments(lib):
+    t, w = ctypes.c_int(), ctypes.c_int()
+    bt, bw = ctypes.byref(t), ctypes.byref(w)
+    RR_BF16, RR_I32 = 2, 1
+    assert lib.rr_plan_rowwise(-1, 8, RR_BF16, 0, 1, 152, 16, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, -8, RR_BF16, 0, 1, 152, 16, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_I32, 0, 1, 152, 16, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 3, 1, 152, 16, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 0, 16, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 0, bt, bw) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 16, None, bw) == 1
+    assert lib.rr_plan_rowwise(0, 8, RR_BF16, 0, 1, 152, 16, bt, bw) == 0
+
+
 @pytest.mark.parametrize("shape,align,ws,expect", [
     # (tier, cluster_size, emit_tile_width, tile_rows, splits)
     ((262144, 16, 16), 16, True, ("tiled", 1, 4, 0, 1)),       # many short lines: no combine
