@@ -106,3 +106,24 @@ def test_combine_past_2_31(rr, oracle_mod):
     mh, lh = np.ascontiguousarray(to_np(m[:, tail])), np.ascontiguousarray(to_np(l[:, tail]))
     ref64, ref = oracle_mod.splitk_combine(Oh, mh, lh, s)
     assert_combine_close(to_np(out[tail]), ref64, ref, Oh, mh, lh, s)
+
+
+def test_rowwise_warp_past_2_31(rr, oracle_mod):
+    # the warp tier of the row ops: 2,098,152 rows of 1024 bf16 (2.1 G elements)
+    rows, cols = (BIG >> 10) + 1000, 1024
+    xb = _f32(rows, cols, 9007).to(torch.bfloat16)
+    tail = [0, rows - 2, rows - 1]
+    xh = to_np(xb[tail])
+    y = rr.softmax(xb)
+    assert rr.last_tier()[0] == "warp"
+    assert_rel_close(to_np(y[tail]), oracle_mod.softmax(xh), 1e-5, floor=1e-30, what="softmax warp")
+    del y
+    from cluster_reductions_gb300 import inputs
+    g, b = inputs.layernorm_params(cols, 9008, "cuda")
+    rstd = torch.empty(rows, device="cuda")
+    yb = rr.layernorm(xb, g, b, 1e-5, rstd=rstd)
+    assert rr.last_tier()[0] == "warp"
+    y64, y16, m64, r64 = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
+    xf = xb[tail].to(torch.float64).cpu().numpy()
+    assert_layernorm_close(to_np(yb[tail]), y64, y16, xf, to_np(g), to_np(b), m64, r64)
+    assert_rel_close(to_np(rstd[tail]), r64, 1e-5, what="layernorm rstd warp")
