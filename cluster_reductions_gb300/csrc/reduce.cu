@@ -37,6 +37,16 @@ namespace {
 #define RR_GRID_CAP 1
 #endif
 constexpr int kBlockThreads = RR_BLOCK_THREADS, kBlockUnroll = RR_BLOCK_UNROLL;
+// Block tier on long rows: a CTA per row keeps threads x unroll 16-byte
+// loads in flight, and with few rows per SM 256 x 8 is too little to cover
+// HBM latency (152 rows of 441505 fp32: 2941 GB/s).  Rows of at least
+// RR_BLOCK_LONG_COLS elements take 16 loads per thread (such a row spans two
+// or more passes of them, so the predicated remainder stays small; shorter
+// rows keep 8, which leaves room for more CTAs per SM).
+#ifndef RR_BLOCK_LONG_COLS
+#define RR_BLOCK_LONG_COLS 32768
+#endif
+constexpr int kBlockLongUnroll = 16;
 constexpr int kSplitThreads = 512, kSplitUnroll = 8;
 constexpr int kWarpBlock = 256, kWarpUnroll = RR_WARP_UNROLL;
 constexpr int kTiledBlock = 256;
@@ -470,6 +480,12 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
   const uintptr_t a = (uintptr_t)xv;
   switch (tier) {
     case RR_TIER_BLOCK: {
+      if (cols >= RR_BLOCK_LONG_COLS) {
+        auto k = k_block<Op, kBlockThreads, kBlockLongUnroll>;
+        const int g = grid_for(k, kBlockThreads, rows, d);
+        launch_kernel(k, dim3(g), dim3(kBlockThreads), 0, s, 0, x, rows, cols, out);
+        return cuda_status(cudaGetLastError());
+      }
       auto k = k_block<Op, kBlockThreads, kBlockUnroll>;
       const int g = grid_for(k, kBlockThreads, rows, d);
       launch_kernel(k, dim3(g), dim3(kBlockThreads), 0, s, 0, x, rows, cols, out);

@@ -70,6 +70,18 @@ def test_forced_tiers_small(rr, oracle_mod, tier, op, dtype):
 
 
 @pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int32], ids=["f32", "i32"])
+def test_block_long_rows(rr, oracle_mod, op, dtype):
+    # rows of >= 32768 elements take the block kernel with 16 loads per
+    # thread: exactly one and two passes of them, ragged tails, misaligned
+    # bases, and a few-rows-per-SM count
+    for i, (rows, cols) in enumerate([(3, 32768), (2, 32769), (4, 65536 + 4 * 256 + 3),
+                                      (5, 100003), (160, 40000)]):
+        for offset in (0, 1, 3):
+            check(rr, oracle_mod, gen(rows, cols, dtype, 150 + i, offset), op, tier="block")
+
+
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
 def test_auto_tier_and_empty(rr, oracle_mod, op):
     for rows, cols in [(0, 5), (4, 0), (1, 0)]:
         x = torch.zeros((rows, cols), device="cuda")
