@@ -52,6 +52,11 @@ MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
 # Softmax / layernorm rows of medium width timed beside the step (bf16,
 # 256 MiB each): the warp tier of the two-pass row operations.
 MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048)]
+# Long rows timed beside the step (256 MiB each): softmax / layernorm rows
+# staged in shared memory (a CTA per row; clusters of 8 for 256K-element
+# rows), and a few long fp32 rows per SM for the block reduce.
+LONG_ROWOPS = [(4096, 32768), (608, 262144)]
+LONG_REDUCE = [(200, 335544)]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -524,7 +529,7 @@ def bench_ours(args):
                 "traffic_source": tr["profile"] if traffic is not None else None}
 
     splitk_c, combine_v, callreduce_us, rowwise_sk, axis_r, e2e = {}, {}, {}, {}, {}, None
-    medium_r = {}
+    medium_r, long_r = {}, {}
     tiers_b2b = {}
     step_graph = None
     if not args.no_extras:
@@ -700,6 +705,40 @@ def bench_ours(args):
                 t, c = rr.last_tier()
                 medium_r[key]["tier"] = f"{t} {'L' if t == 'warp' else 'C'}={c}"
             del xm, ym, yb
+        for mr, mc in LONG_ROWOPS:
+            xm = [_inp.normal_bf16(mr, mc, 830 + i, dev, 3.0) for i in range(2)]
+            ym = torch.empty((mr, mc), device=dev)
+            yb = torch.empty((mr, mc), dtype=torch.bfloat16, device=dev)
+            mu, rs = torch.empty(mr, device=dev), torch.empty(mr, device=dev)
+            gm, bm = _inp.layernorm_params(mc, 832, dev)
+            km = [0]
+            ops = {
+                "softmax": (lambda x: rr.softmax(x, out=ym), mr * mc * 6),
+                "lnstats": (lambda x: rr.layernorm_stats(x, 1e-5, mean=mu, rstd=rs),
+                            mr * mc * 2 + mr * 8),
+                "layernorm": (lambda x: rr.layernorm(x, gm, bm, 1e-5, out=yb),
+                              mr * mc * 4 + mc * 8),
+            }
+            for name, (fn, nb) in ops.items():
+                def one_l(fn=fn):
+                    km[0] ^= 1
+                    fn(xm[km[0]])
+                key = f"{mr}x{mc}_{name}_bf16"
+                long_r[key] = timed(one_l, nb)
+                t, c = rr.last_tier()
+                long_r[key]["tier"] = f"{t} C={c}" + (" staged" if rr.last_staged() else "")
+            del xm, ym, yb
+        for mr, mc in LONG_REDUCE:
+            xm = [_inp.normal_f32(mr, mc, 840 + i, dev) for i in range(2)]
+            om = torch.empty(mr, device=dev)
+            km = [0]
+
+            def one_lr():
+                km[0] ^= 1
+                rr.reduce(xm[km[0]], "sum", out=om)
+            long_r[f"{mr}x{mc}_sum_f32"] = timed(one_lr, mr * mc * 4 + mr * 4)
+            long_r[f"{mr}x{mc}_sum_f32"]["tier"] = "%s C=%d" % rr.last_tier()
+            del xm
         # reduction over a non-last axis (automatic plan), 256 MiB inputs, two
         # rotating buffers; called straight through the C ABI so that host
         # overhead does not starve the ~40 us launches
@@ -761,7 +800,8 @@ def bench_ours(args):
                    "parallelism": f"replicas x{world}", "step_bytes": step_bytes},
         "tiers": tiers, "tiers_back_to_back": tiers_b2b, "splitk_by_cluster": splitk_c, "combine_variants": combine_v,
         "cluster_allreduce_latency": callreduce_us, "rowwise_splitk": rowwise_sk,
-        "axis_reduce": axis_r, "medium_rows": medium_r, "step_graph": step_graph,
+        "axis_reduce": axis_r, "medium_rows": medium_r, "long_rows": long_r,
+        "step_graph": step_graph,
         "roofline": roofline,
         "clocks": clk.summary(), "gpu_launches": nops * args.steps, "e2e": e2e,
     }

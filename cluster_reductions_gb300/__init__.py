@@ -395,8 +395,14 @@ def device_status() -> int:
 
 
 def last_tier() -> Tuple[str, int]:
+    """(tier, width) of the last reduce / softmax / layernorm call."""
     v = int(load().rr_last_tier())
-    return TIER_NAMES.get(v & 0xff, "?"), v >> 8
+    return TIER_NAMES.get(v & 0xff, "?"), (v >> 8) & 0xff
+
+
+def last_staged() -> bool:
+    """Whether the last row operation staged its rows in shared memory."""
+    return bool((int(load().rr_last_tier()) >> 16) & 1)
 
 
 def plan_reduce(rows: int, cols: int, sm_count: int, max_cluster: int) -> Tuple[str, int]:
@@ -411,16 +417,19 @@ _ROW_OPS = {"softmax": 0, "lnstats": 1, "layernorm_stats": 1, "layernorm": 2}
 
 
 def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: int,
-                 dtype=torch.bfloat16, aligned: bool = True) -> Tuple[str, int]:
+                 dtype=torch.bfloat16, aligned: bool = True, staged: bool = False):
     """rr_plan_rowwise (host only): the tier and width (lanes per row, cluster
-    size or 1) that softmax / layernorm_stats / layernorm pick."""
+    size or 1) that softmax / layernorm_stats / layernorm pick; with
+    staged=True also whether the rows are staged in shared memory."""
     dt = _DT.get(dtype)
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"plan_rowwise: dtype {dtype} not supported")
-    t, w = ctypes.c_int(), ctypes.c_int()
+    t, w, st = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(load().rr_plan_rowwise(int(rows), int(cols), dt, _ROW_OPS[row_op], 1 if aligned else 0,
                                  int(sm_count), int(max_cluster), ctypes.byref(t),
-                                 ctypes.byref(w)), "rr_plan_rowwise")
+                                 ctypes.byref(w), ctypes.byref(st)), "rr_plan_rowwise")
+    if staged:
+        return TIER_NAMES[t.value], w.value, bool(st.value)
     return TIER_NAMES[t.value], w.value
 
 

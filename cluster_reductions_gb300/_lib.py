@@ -82,7 +82,7 @@ SIGNATURES = {
     "rr_last_tier": (_int, []),
     "rr_status_string": (ctypes.c_char_p, [_int]),
     "rr_plan_rowwise": (_int, [_i64, _i64, _int, _int, _int, _int, _int, ctypes.POINTER(_int),
-                               ctypes.POINTER(_int)]),
+                               ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "rr_plan_reduce": (_int, [_i64, _i64, _int, _int, ctypes.POINTER(_int),
                               ctypes.POINTER(_int)]),
     "rr_test_wait_timeout": (_int, [_i64, _vp]),

@@ -241,17 +241,19 @@ int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster, in
 }
 
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int aligned,
-                    int sm_count, int max_cluster, int *tier_out, int *width_out) {
+                    int sm_count, int max_cluster, int *tier_out, int *width_out,
+                    int *staged_out) {
   if (rows < 0 || cols < 0 || sm_count < 1 || max_cluster < 1 || !tier_out || !width_out)
     return RR_ERR_INVALID;
   if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
   if (row_op < RR_ROW_SOFTMAX || row_op > RR_ROW_LAYERNORM) return RR_ERR_INVALID;
   const int epv = in_dtype == RR_BF16 ? 8 : 4;
   const bool vec = aligned && cols % epv == 0;
-  const RowPlan p = plan_rowwise(rows, cols, vec, cols / epv, row_op == RR_ROW_LAYERNORM,
-                                 RR_TIER_AUTO, 0, sm_count, max_cluster < 16 ? max_cluster : 16);
+  const RowPlan p = plan_rowwise(rows, cols, in_dtype, vec, row_op, RR_TIER_AUTO, 0, sm_count,
+                                 max_cluster < 16 ? max_cluster : 16);
   *tier_out = p.tier;
   *width_out = p.width;
+  if (staged_out) *staged_out = p.staged ? 1 : 0;
   return RR_OK;
 }
 

@@ -638,11 +638,12 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
 
 // Tier of a two-pass row op on a device (its SM count, and its largest
 // cluster: RR_MAX_CLUSTER caps it, no cluster launch makes it 1).
-inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int64_t nvec, int tier, int C,
-                            const DevInfo &d, bool rewrite = false) {
+template <class In>
+inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int tier, int C,
+                            const DevInfo &d, int mode) {
   const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
-  return plan_rowwise(rows, cols, vec, nvec, rewrite, tier, C, d.sm_count,
-                      d.cluster_launch ? cap : 1);
+  return plan_rowwise(rows, cols, In::EPV == 8 ? RR_BF16 : RR_F32, vec, mode, tier, C,
+                      d.sm_count, d.cluster_launch ? cap : 1);
 }
 
 template <class In>
@@ -654,9 +655,12 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ax % 16 == 0 &&
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
-  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8);
+  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.staged)
+    return launch_rowwise_staged(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+                                 0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
                                                    nullptr, nullptr, nullptr, pk.width, s, d);
@@ -691,9 +695,12 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
-  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8);
+  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.staged)
+    return launch_rowwise_staged(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+                                 nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                  nullptr, nullptr, nullptr, pk.width, s, d);
@@ -731,9 +738,12 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
                    ((uintptr_t)y % (2 * In::EPV) == 0);
-  const RowPlan pk = rowwise_pick(rows, cols, vec, nvec, tier, C, d, /*rewrite=*/true);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8);
+  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.staged)
+    return launch_rowwise_staged(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+                                 eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                      gamma, beta, y, pk.width, s, d);
@@ -775,27 +785,67 @@ static int rowwise_splitk_cluster(int64_t rows, int64_t cols, int sm_count, int 
   return c;
 }
 
-RowPlan plan_rowwise(int64_t rows, int64_t cols, bool vec, int64_t nvec, bool rewrite, int tier,
+// Staged rows: the automatic choice stages softmax rows of more than 1024
+// 16-byte vectors and the layernorm's beyond the register form (2048; the
+// register form measured better there for them, worse for softmax, whose
+// 8-vector register rows at 256 threads hold 64 floats and its exponentials
+// per thread); forced split-K stages its slices when RR_ROW_STAGED_SPLITK
+// and they fit.
+constexpr int64_t kRowStagedMinVec[3] = {1024, kRowRegMaxVec, kRowRegMaxVec};
+#ifndef RR_ROW_STAGED_SPLITK
+#define RR_ROW_STAGED_SPLITK 0
+#endif
+
+RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
                      int C, int sm_count, int max_cluster) {
+  const bool rewrite = mode == kModeLayernorm;
+  const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
+  const int64_t nvec = vec ? cols * elt / 16 : 0;
   const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
-  if (tier == RR_TIER_BLOCK) return {RR_TIER_BLOCK, 1};
+  if (tier == RR_TIER_BLOCK) {
+    const bool st = vec && nvec > kRowStagedMinVec[mode] &&
+                    rowwise_staged_chunk(cols, 1) * elt <= kStageMaxBytes;
+    return {RR_TIER_BLOCK, 1, st};
+  }
   if (tier == RR_TIER_WARP) {
     const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : 0;
-    return L ? RowPlan{RR_TIER_WARP, L} : RowPlan{-1, 0};
+    return L ? RowPlan{RR_TIER_WARP, L, false} : RowPlan{-1, 0, false};
   }
   if (tier == RR_TIER_SPLITK) {
     if (C == 0) C = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
     if (C == 0) C = 2;
-    if (C > 1 && C > max_cluster) return {-1, 0};
-    return {RR_TIER_SPLITK, C};
+    if (C > 1 && C > max_cluster) return {-1, 0, false};
+    const bool st = RR_ROW_STAGED_SPLITK && vec &&
+                    rowwise_staged_chunk(cols, C) * elt <= kStageMaxBytes;
+    return {RR_TIER_SPLITK, C, st};
   }
   const int c = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
-  if (c > 0) return {RR_TIER_SPLITK, c};
+  if (c > 0) {
+    const bool st = RR_ROW_STAGED_SPLITK && vec &&
+                    rowwise_staged_chunk(cols, c) * elt <= kStageMaxBytes;
+    return {RR_TIER_SPLITK, c, st};
+  }
   if (vec && rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
     const int L = rowwise_warp_lanes(nvec, 0, rewrite);
-    if (L) return {RR_TIER_WARP, L};
+    if (L) return {RR_TIER_WARP, L, false};
   }
-  return {RR_TIER_BLOCK, 1};
+  if (vec && nvec > kRowStagedMinVec[mode]) {
+    const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster);
+    if (sc == 1) return {RR_TIER_BLOCK, 1, true};
+    // the statistics only read the row: past clusters of 4 the split-K pass
+    // over global memory (its second read served by L2) came out ahead
+    if (sc > 1 && !(mode == kModeStats && sc > 4)) return {RR_TIER_SPLITK, sc, true};
+  }
+  // long rows that cannot be staged (not vector-aligned, or more than 16
+  // slices): split-K over global memory, slices of at most 128 KiB, rather
+  // than the block tier's scalar two-pass form
+  const int64_t row_bytes = cols * elt;
+  if (row_bytes > 16 * kRowStagedMinVec[mode] && max_cluster >= 2) {
+    int c2 = 2;
+    while (c2 < max_cluster && c2 < 16 && row_bytes / c2 > 128 * 1024) c2 *= 2;
+    return {RR_TIER_SPLITK, c2, false};
+  }
+  return {RR_TIER_BLOCK, 1, false};
 }
 
 int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,

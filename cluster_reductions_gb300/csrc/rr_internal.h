@@ -78,17 +78,40 @@ constexpr int kRowWarpMinRowsPerSM = 4;
 constexpr int kRowWarpMinRowsPerSMRewrite = 8;
 // tier RR_TIER_WARP (width = lanes per row), RR_TIER_SPLITK (width =
 // cluster size) or RR_TIER_BLOCK (width 1); tier < 0 when a forced choice
-// cannot run.
+// cannot run.  `staged`: the block / split-K tier with the row's slices
+// staged in shared memory (rowstaged.cu).
 struct RowPlan {
   int tier;
   int width;
+  bool staged;
 };
-// Forced (tier, C) or automatic choice for rows x cols; `vec`: the row is
-// nvec aligned 16-byte vectors and the outputs meet the register forms'
-// alignment; `rewrite`: the layernorm rewrite (else softmax / statistics).
-// A forced split-K cluster larger than max_cluster cannot run.
-RowPlan plan_rowwise(int64_t rows, int64_t cols, bool vec, int64_t nvec, bool rewrite, int tier,
+// Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
+// cols is a multiple of the 16-byte vector and every operand meets the
+// register forms' alignment; `mode`: 0 softmax, 1 layernorm statistics, 2
+// layernorm rewrite.  A forced split-K cluster larger than max_cluster
+// cannot run.
+RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
                      int C, int sm_count, int max_cluster);
+// Vectors per row up to which the block tier holds the row in registers
+// (256 threads x 8 vectors).
+constexpr int64_t kRowRegMaxVec = 2048;
+
+// ---- staged row operations (rowstaged.cu)
+// Largest slice a CTA stages in shared memory: two such CTAs fit on an SM.
+#ifndef RR_STAGE_MAX_KB
+#define RR_STAGE_MAX_KB 96
+#endif
+constexpr int64_t kStageMaxBytes = RR_STAGE_MAX_KB * 1024;
+// Elements per CTA slice for a cluster of C (a multiple of 8); -1 if C < 1.
+int64_t rowwise_staged_chunk(int64_t cols, int C);
+// Smallest cluster size (a power of two up to min(16, max_cluster)) whose
+// slices fit kStageMaxBytes; 0 if none does.
+int rowwise_staged_cluster(int64_t cols, int in_dtype, int max_cluster);
+// mode as launch_rowwise_warp; the rows must be 16-byte aligned vectors.
+int launch_rowwise_staged(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                          float eps, float *y, float *mean, float *rstd, const float *gamma,
+                          const float *beta, uint16_t *ybf, int C, cudaStream_t s,
+                          const DevInfo &d);
 
 // ---- warp tier of the row operations (rowwarp.cu)
 // A segment of L lanes per row holding NV 16-byte vectors per lane, NV a

@@ -292,6 +292,16 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * every CTA holds the same row statistics.  AUTO picks split-K when
  * rows < SMs and cols >= 16384, with C the smallest power of two >= 2 such
  * that rows * C >= SMs, at most 16.
+ * Staged rows: with rows >= SMs, aligned rows beyond the register form
+ * (softmax: more than 1024 16-byte vectors, i.e. 8192 bf16 / 4096 fp32
+ * elements; layernorm: more than 2048) are copied into shared memory with
+ * bulk copies and read from there by every pass, one HBM read per element:
+ * a CTA per row while a row fits 96 KiB, else the smallest cluster (<= 16)
+ * whose slices do, each CTA staging its slice (reported as the split-K tier
+ * of that cluster size); the statistics stage only up to clusters of 4.
+ * Long rows that are not staged take split-K over global memory with
+ * slices of at most 128 KiB.  A forced block tier stages when it applies; a
+ * forced split-K tier reads from global memory.
  */
 typedef struct {
     int tier;
@@ -457,8 +467,10 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
  * last call.  RR_ERR_CUDA if the synchronisation itself failed. */
 int rr_device_status(void *stream);
 
-/* Tier and cluster size of the last reduce / softmax / layernorm call made
- * by this process: (cluster_size << 8) | tier. */
+/* Tier and width of the last reduce / softmax / layernorm call made by this
+ * process: (staged << 16) | (width << 8) | tier, width the cluster size (the
+ * warp tier of the row operations: lanes per row), staged 1 when a row
+ * operation staged its rows in shared memory. */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -484,12 +496,14 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * `max_cluster` CTAs.  `aligned` != 0 says every operand meets the warp
  * tier's alignment (rr_rowwise_opts); cols must also be a multiple of the
  * 16-byte vector.  Writes the tier and its width: lanes per row (warp),
- * cluster size (split-K) or 1 (block).  Touches no GPU.  RR_ERR_INVALID on
- * negative sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
+ * cluster size (split-K) or 1 (block); *staged_out (if not NULL) 1 when the
+ * block / split-K tier stages the rows in shared memory.  Touches no GPU.
+ * RR_ERR_INVALID on negative sizes, sm_count or max_cluster < 1, a bad dtype
+ * or row_op.
  */
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,
                     int aligned, int sm_count, int max_cluster, int *tier_out,
-                    int *width_out);
+                    int *width_out, int *staged_out);
 
 /*
  * rr_test_wait_timeout -- failure-detection hook: launches one CTA that

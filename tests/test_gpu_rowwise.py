@@ -405,3 +405,93 @@ def test_rowwise_launch_matches_host_plan(rr):
                          ("layernorm", lambda: rr.layernorm(x, g, b))):
             call()
             assert rr.last_tier() == rr.plan_rowwise(rows, cols, op, sms, 16, dtype=dt), (rows, cols, op)
+
+
+# ---------------------------------------------------------------------------
+# Staged rows: the row (or each CTA's slice of it) copied into shared memory,
+# persistent clusters with two stage buffers.  Row counts above the
+# persistent grid make clusters take several rows (both buffers, the
+# prefetch); widths give a CTA per row, clusters of 2 and 4, ragged last
+# slices and, for fp32, 4-element tails.
+# ---------------------------------------------------------------------------
+def _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=None, **kw):
+    from cluster_reductions_gb300 import inputs
+    from _util import assert_layernorm_close
+    rows, cols = x.shape
+    xs = x[torch.from_numpy(idx).cuda()]
+    xh = to_np(xs)
+    y = to_np(rr.softmax(x, **kw))
+    got = (rr.last_tier(), rr.last_staged())
+    if expect_tier is not None:
+        assert got == expect_tier, (rows, cols, got)
+    ref = oracle_mod.softmax(xh)
+    assert_rel_close(y[idx], ref, 1e-5, floor=1e-30, what=f"softmax {rows}x{cols} {got}")
+    np.testing.assert_allclose(y[idx].astype(np.float64).sum(axis=1), 1.0, rtol=0, atol=1e-5)
+    del y
+    g, b = inputs.layernorm_params(cols, 1700 + cols % 13, "cuda")
+    mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    yb = rr.layernorm(x, g, b, 1e-5, mean=mean, rstd=rstd, **kw)
+    m2, r2 = rr.layernorm_stats(x, 1e-5, **kw)
+    assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
+    assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
+    y64, y16, rm, rr_ = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
+    xf = xs.to(torch.float64).cpu().numpy()
+    assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_)
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+    assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
+    assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_staged_rows_block(rr, oracle_mod, dtype):
+    # a forced block tier on rows beyond the register form stages each row
+    widths = [16392, 20000, 32768, 49152] if dtype == torch.bfloat16 else [8196, 10004, 24576]
+    for i, cols in enumerate(widths):
+        x = _x(7, cols, dtype, 1800 + i, 2.0)
+        _check_all_row_ops(rr, oracle_mod, x, np.arange(7), (("block", 1), True), tier="block")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_staged_rows_auto(rr, oracle_mod, dtype):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    elt = 2 if dtype == torch.bfloat16 else 4
+    cases = ([(3 * sms + 5, 20000), (sms + 9, 65544), (sms + 3, 100008)] if elt == 2 else
+             [(3 * sms + 5, 10004), (sms + 9, 40004), (sms + 3, 50000)])
+    for i, (rows, cols) in enumerate(cases):
+        x = _x(rows, cols, dtype, 1900 + i, 2.0)
+        plan = rr.plan_rowwise(rows, cols, "softmax", sms, 16, dtype=dtype, staged=True)
+        assert plan[2], plan
+        idx = np.r_[0:6, rows // 2:rows // 2 + 3, rows - 6:rows]
+        _check_all_row_ops(rr, oracle_mod, x, idx, ((plan[0], plan[1]), True))
+
+
+def test_staged_rows_special(rr, oracle_mod):
+    # constant rows, and -inf over whole slices of a clustered row
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, cols = sms + 1, 65544
+    x = torch.full((rows, cols), 1.5, dtype=torch.bfloat16, device="cuda")
+    y = rr.softmax(x)
+    assert rr.last_staged() and rr.last_tier()[0] == "splitk"
+    np.testing.assert_allclose(to_np(y[:4]), 1.0 / cols, rtol=2e-6)
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    assert (to_np(mean) == 1.5).all()
+    x = _x(rows, cols, torch.bfloat16, 1950, 3.0)
+    x[:, : cols // 2 + 100] = float("-inf")
+    x[1, :] = float("-inf")
+    y = to_np(rr.softmax(x)[:4])
+    assert rr.last_staged()
+    ref = oracle_mod.softmax(to_np(x[:4]))
+    live = [0, 2, 3]
+    assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what="staged softmax -inf")
+    assert (y[:, : cols // 2 + 100] == 0).all()
+    assert np.isnan(ref[1]).all() and (y[1] == 0).all()
+
+
+def test_long_rows_split_fallback(rr, oracle_mod):
+    # long rows that cannot be staged take split-K over global memory
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for rows, cols, off in [(sms + 2, 1 << 20, 0), (sms + 5, 32767, 0), (sms + 5, 32768, 1)]:
+        x = _x(rows, cols, torch.bfloat16, 2000 + cols % 11, 2.0, off)
+        idx = np.r_[0:3, rows - 3:rows]
+        _check_all_row_ops(rr, oracle_mod, x, idx)
+        assert rr.last_tier()[0] == "splitk" and not rr.last_staged()

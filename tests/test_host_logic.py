@@ -164,18 +164,46 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     assert rr.plan_rowwise(rows, cols, op, 152, maxc, dtype=dt, aligned=aligned) == expect
 
 
+@pytest.mark.parametrize("rows,cols,op,dtype,aligned,maxc,expect", [
+    # staged in shared memory: softmax beyond 1024 vectors, layernorm beyond 2048
+    (4096, 32768, "softmax", "bf16", True, 16, ("block", 1, True)),
+    (8192, 16384, "softmax", "bf16", True, 16, ("block", 1, True)),
+    (8192, 16384, "lnstats", "bf16", True, 16, ("block", 1, False)),     # register form
+    (16384, 8192, "softmax", "bf16", True, 16, ("block", 1, False)),
+    (4096, 16384, "layernorm", "f32", True, 16, ("block", 1, True)),     # 64 KiB rows
+    (2048, 65536, "lnstats", "bf16", True, 16, ("splitk", 2, True)),     # 2 slices of 64 KiB
+    (304, 524288, "layernorm", "bf16", True, 16, ("splitk", 16, True)),
+    (608, 262144, "softmax", "bf16", True, 16, ("splitk", 8, True)),
+    (608, 262144, "lnstats", "bf16", True, 16, ("splitk", 4, False)),    # statistics: C <= 4 staged
+    (1216, 131072, "lnstats", "bf16", True, 16, ("splitk", 4, True)),
+    # not stageable: split-K over global memory
+    (304, 524288, "layernorm", "bf16", True, 8, ("splitk", 8, False)),   # slices > 96 KiB
+    (152, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16, False)),
+    (4096, 32767, "softmax", "bf16", True, 16, ("splitk", 2, False)),    # not a vector multiple
+    (4096, 32768, "softmax", "bf16", False, 16, ("splitk", 2, False)),   # misaligned operands
+    (4096, 32768, "softmax", "bf16", True, 1, ("block", 1, True)),       # no clusters: C = 1 fits
+    (4096, 40000, "softmax", "f32", True, 1, ("block", 1, False)),       # no clusters, too long
+])
+def test_rowwise_staged_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
+    import torch
+    import cluster_reductions_gb300 as rr
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    assert rr.plan_rowwise(rows, cols, op, 152, maxc, dtype=dt, aligned=aligned,
+                           staged=True) == expect
+
+
 def test_rowwise_plan_rejects_bad_arguments(lib):
     t, w = ctypes.c_int(), ctypes.c_int()
     bt, bw = ctypes.byref(t), ctypes.byref(w)
     RR_BF16, RR_I32 = 2, 1
-    assert lib.rr_plan_rowwise(-1, 8, RR_BF16, 0, 1, 152, 16, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, -8, RR_BF16, 0, 1, 152, 16, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_I32, 0, 1, 152, 16, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 3, 1, 152, 16, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 0, 16, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 0, bt, bw) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 16, None, bw) == 1
-    assert lib.rr_plan_rowwise(0, 8, RR_BF16, 0, 1, 152, 16, bt, bw) == 0
+    assert lib.rr_plan_rowwise(-1, 8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, -8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_I32, 0, 1, 152, 16, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 3, 1, 152, 16, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 0, 16, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 16, None, bw, None) == 1
+    assert lib.rr_plan_rowwise(0, 8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 0
 
 
 @pytest.mark.parametrize("shape,align,ws,expect", [
