@@ -69,18 +69,18 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1085681664, "src": ["reduce.cu", "rr_device.cuh"],
-                      "src_sha": "7187092cae58b53b", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 577034240, "src": ["combine.cu", "rr_device.cuh"],
+    "splitk_sum_f32": {"bytes": 1085626368, "src": ["reduce.cu", "rr_device.cuh"],
+                      "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 575230976, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "e41b009ab53904ca", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 560532480, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "3ec31e6ec6a17222", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271550976, "src": ["reduce.cu", "rr_device.cuh"],
-                     "src_sha": "7187092cae58b53b", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271616256, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "3ec31e6ec6a17222", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 137868544, "src": ["reduce.cu", "rr_device.cuh"],
-                    "src_sha": "7187092cae58b53b", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "softmax_bf16": {"bytes": 560443392, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "362e2593015a6584", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271419648, "src": ["reduce.cu", "rr_device.cuh"],
+                     "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271262464, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "362e2593015a6584", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137985024, "src": ["reduce.cu", "rr_device.cuh"],
+                    "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
@@ -923,6 +923,9 @@ PROFILE_CASES = {
     "medium_softmax_131072x1024_bf16": ({"shape": (131072, 1024), "op": "softmax"}, "medium", 1.0),
     "medium_layernorm_131072x1024_bf16": ({"shape": (131072, 1024), "op": "layernorm"},
                                           "medium", 1.0),
+    # long rows staged in shared memory, automatic plan
+    "long_softmax_4096x32768_bf16": ({"shape": (4096, 32768), "op": "softmax"}, "medium", 1.0),
+    "long_layernorm_2048x65536_bf16": ({"shape": (2048, 65536), "op": "layernorm"}, "medium", 1.0),
 }
 
 
