@@ -423,11 +423,14 @@ k_combine_push(const float *__restrict__ O, const float *__restrict__ m,
 // Slot layout: O_all P*TR*D | m_all P*TRp | l_all P*TRp.
 //   full[s]  (local, 1 arrival + tx)  the slot's copies and loads landed;
 //   free[s]  (local, 1 arrival)       the consumers are done with the slot.
+// Held to 8 CTAs per SM (40 registers at 192 threads): the overlap of this
+// variant comes from the other CTAs on the SM, and the compiler's own
+// choice for P = 8 went to 56 registers and 5 CTAs.
 template <int P, int S>
-__global__ void __launch_bounds__(kPipeThreads)
+__global__ void __launch_bounds__(kPipeThreads, 8)
 k_combine_direct(const float *__restrict__ O, const float *__restrict__ m,
                  const float *__restrict__ l, int64_t rows, int D, int TR, float scale_log2e,
-                 uint16_t *__restrict__ out, int *err) {
+                 uint16_t *__restrict__ out, int ml_bulk, int *err) {
   pdl_begin();
   extern __shared__ __align__(128) float dyn[];
   __shared__ __align__(8) uint64_t full[S], freed[S];
@@ -463,17 +466,29 @@ k_combine_direct(const float *__restrict__ O, const float *__restrict__ m,
           !mbar_wait_or_die(&freed[s], (r - 1) & 1u, kWaitBudget, &dead, false))
         set_error(err, kErrTimeout);
       // arm the byte count and start the big copies first, then fetch the
-      // (m, l) while they fly; the arrival releases the (m, l) stores
+      // (m, l) while they fly (with ml_bulk they ride the copy engine too:
+      // fetched by the lanes, two dependent round trips per tile for P * TR
+      // > 32 sat on the critical path of small tiles); the arrival releases
+      // the (m, l) stores
       if (lane == 0) {
         const uint32_t ob = (uint32_t)nr * (uint32_t)D * 4u;
-        mbar_expect_tx(&full[s], ob * P);
+        const uint32_t mb = ml_bulk ? (uint32_t)nr * 4u : 0u;
+        mbar_expect_tx(&full[s], ob * P + 2u * P * mb);
         for (int q = 0; q < P; ++q)
           bulk_g2s(so + q * TR * D, O + ((int64_t)q * rows + row0) * D, ob, &full[s]);
+        if (ml_bulk) {
+          for (int q = 0; q < P; ++q) {
+            bulk_g2s(mall + q * TRp, m + (int64_t)q * rows + row0, mb, &full[s]);
+            bulk_g2s(lall + q * TRp, l + (int64_t)q * rows + row0, mb, &full[s]);
+          }
+        }
       }
-      for (int j = lane; j < P * nr; j += 32) {
-        const int q = j / nr, i = j - q * nr;
-        mall[q * TRp + i] = __ldg(m + (int64_t)q * rows + row0 + i);
-        lall[q * TRp + i] = __ldg(l + (int64_t)q * rows + row0 + i);
+      if (!ml_bulk) {
+        for (int j = lane; j < P * nr; j += 32) {
+          const int q = j / nr, i = j - q * nr;
+          mall[q * TRp + i] = __ldg(m + (int64_t)q * rows + row0 + i);
+          lall[q * TRp + i] = __ldg(l + (int64_t)q * rows + row0 + i);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
@@ -672,9 +687,11 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
                                    O, m, l, rows, D, TR, scale_log2e, out, ml_bulk, d.err_word));
 }
 
-// Direct variant geometry per P, from a sweep on GB300 (131072 x 128 rows):
-// one slot of 16 KiB per CTA (overlap comes from the other CTAs on the SM)
-// up to P = 8, two slots of 32 KiB for P = 16.
+// Direct variant geometry per P, from a sweep on GB300 (256 MiB of partials,
+// D = 64, 128, 256, with (m, l) by the copy engine): one slot of 16 KiB per
+// CTA for P <= 4 (overlap comes from the other CTAs on the SM), two for
+// P = 8 (its tiles of 2 to 8 rows are short enough for the per-tile
+// handshake to show), two of 32 KiB for P = 16.
 #ifndef RR_DIRECT_SLOTS
 #define RR_DIRECT_SLOTS 1
 #endif
@@ -682,7 +699,7 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
 #define RR_DIRECT_BYTES 16384
 #endif
 template <int P> struct DirectGeom {
-  static constexpr int S = (P <= 8) ? RR_DIRECT_SLOTS : 2;
+  static constexpr int S = (P <= 4) ? RR_DIRECT_SLOTS : 2;
   static constexpr int bytes = (P <= 8) ? RR_DIRECT_BYTES : 32768;
 };
 
@@ -705,11 +722,17 @@ int launch_direct(const float *O, const float *m, const float *l, int64_t rows, 
   const int64_t ntiles = (rows + TR - 1) / TR;
   int64_t grid = (int64_t)nb * d.sm_count;
   if (grid > ntiles) grid = ntiles;
+  // (m, l) by the copy engine when every tile's rows start 16-byte aligned
+#ifndef RR_DIRECT_ML_BULK
+#define RR_DIRECT_ML_BULK 1
+#endif
+  const int ml_bulk = RR_DIRECT_ML_BULK && (rows % 4 == 0) && (TR % 4 == 0) &&
+                      ((uintptr_t)m % 16 == 0) && ((uintptr_t)l % 16 == 0);
   if (log_enabled())
-    std::fprintf(stderr, "rr: combine direct P=%d D=%d TR=%d stages=%d ctas=%lld smem=%zu\n", P, D,
-                 TR, S, (long long)grid, smem);
-  launch_kernel(kern, dim3((unsigned)grid), dim3(kPipeThreads), smem, s, 0, O, m, l, rows, D, TR, scale_log2e, out,
-                                                  d.err_word);
+    std::fprintf(stderr, "rr: combine direct P=%d D=%d TR=%d stages=%d ctas=%lld smem=%zu ml_bulk=%d\n",
+                 P, D, TR, S, (long long)grid, smem, ml_bulk);
+  launch_kernel(kern, dim3((unsigned)grid), dim3(kPipeThreads), smem, s, 0, O, m, l, rows, D, TR,
+                scale_log2e, out, ml_bulk, d.err_word);
   return cuda_status(cudaGetLastError());
 }
 

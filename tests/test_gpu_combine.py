@@ -42,7 +42,9 @@ MODES = [None, "pull", "push", "generic", "direct"]
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("D", [256, 128, 64, 16, 12, 7, 3])
 def test_combine_small(rr, oracle_mod, P, D, mode):
-    for rows in (1, 5, 33, 130, 257):
+    # 132 and 260 rows: multiples of 4, so (m, l) ride the copy engine in the
+    # direct variant, with a short last tile
+    for rows in (1, 5, 33, 130, 132, 257, 260):
         run(rr, oracle_mod, P, rows, D, 400 + P * 7 + D + rows, mode)
 
 
