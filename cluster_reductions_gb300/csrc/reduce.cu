@@ -36,6 +36,10 @@ namespace {
 #ifndef RR_GRID_CAP
 #define RR_GRID_CAP 1
 #endif
+#ifndef RR_TILED_MAX_NV
+#define RR_TILED_MAX_NV 8
+#endif
+
 constexpr int kBlockThreads = RR_BLOCK_THREADS, kBlockUnroll = RR_BLOCK_UNROLL;
 // Block tier on long rows: a CTA per row keeps threads x unroll 16-byte
 // loads in flight, and with few rows per SM 256 x 8 is too little to cover
@@ -566,7 +570,9 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
     case RR_TIER_TILED: {
       const int e = (ewt == 2 || ewt == 4) ? ewt : 1;
       const int64_t groups = (rows + e - 1) / e;
-      const bool vec = cols >= 4 && cols <= 16 && cols % 4 == 0 && (a % 16 == 0);
+      // rows of up to 8 vectors; 5 to 8 only with a row per thread
+      const bool vec = cols >= 4 && cols <= 4 * RR_TILED_MAX_NV && cols % 4 == 0 &&
+                       (a % 16 == 0) && (cols <= 16 || e == 1);
       if (vec) {
         const int nv = (int)(cols / 4);
         const bool v8 = (nv % 2 == 0) && (a % 32 == 0);
@@ -586,7 +592,13 @@ int launch_tier(const void *xv, int64_t rows, int64_t cols, void *outv, cudaStre
         if (nv == 1) RR_TILED_E(1, false)
         else if (nv == 2) { if (v8) RR_TILED_E(2, true) else RR_TILED_E(2, false) }
         else if (nv == 3) RR_TILED_E(3, false)
-        else { if (v8) RR_TILED_E(4, true) else RR_TILED_E(4, false) }
+        else if (nv == 4) { if (v8) RR_TILED_E(4, true) else RR_TILED_E(4, false) }
+#if RR_TILED_MAX_NV > 4
+        else if (nv == 5) RR_TILED_VEC(5, 1, false)
+        else if (nv == 6) { if (v8) RR_TILED_VEC(6, 1, true) else RR_TILED_VEC(6, 1, false) }
+        else if (nv == 7) RR_TILED_VEC(7, 1, false)
+        else { if (v8) RR_TILED_VEC(8, 1, true) else RR_TILED_VEC(8, 1, false) }
+#endif
 #undef RR_TILED_E
 #undef RR_TILED_VEC
       } else {

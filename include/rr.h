@@ -111,7 +111,9 @@ typedef struct {
  * exact, with max(+0,-0) = +0, min(+0,-0) = -0 and NaN propagating as the
  * quiet NaN 0x7fc00000.  cols == 0 writes the identity (0, -inf / INT_MIN,
  * +inf / INT_MAX).  The tier is picked from rows, cols and the SM count:
- * cols <= 16 tiled; cols <= 32 warp; cols < 4096 and rows >= SMs warp (a
+ * cols <= 32 tiled, except 16 and 29..32 warp (a thread per row for the
+ * other widths up to 32; rows of up to 8 16-byte vectors are read as
+ * vectors); cols < 4096 and rows >= SMs warp (a
  * warp segment per row, lanes striding it); rows < SMs and cols >= 4096
  * split-K with C the smallest power of two >= 2 such that rows * C >= SMs,
  * capped at 16 and at the largest cluster the device can co-schedule;

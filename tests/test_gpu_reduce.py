@@ -46,8 +46,8 @@ def gen(rows, cols, dtype, seed, offset=0):
     return base.view(-1)[offset:].view(rows, cols)
 
 
-SHAPES = [(1, 1), (3, 3), (5, 4), (7, 5), (9, 8), (4, 13), (6, 16), (5, 17), (33, 31),
-          (65, 32), (3, 33), (2, 100), (9, 1000), (4, 4099), (3, 8192)]
+SHAPES = [(1, 1), (3, 3), (5, 4), (7, 5), (9, 8), (4, 13), (6, 16), (5, 17), (7, 20), (9, 24),
+          (5, 28), (33, 31), (65, 32), (3, 33), (2, 100), (9, 1000), (4, 4099), (3, 8192)]
 
 
 @pytest.mark.parametrize("tier", TIERS)

@@ -102,9 +102,13 @@ def test_status_strings(lib):
 
 @pytest.mark.parametrize("rows,cols,sms,maxc,expect", [
     (1 << 20, 8, 152, 16, ("tiled", 1)),
-    (1 << 20, 16, 152, 16, ("tiled", 1)),
+    (1 << 20, 12, 152, 16, ("tiled", 1)),
+    (1 << 20, 16, 152, 16, ("warp", 1)),        # 16 and 29-32: the warp tier
     (5, 0, 152, 16, ("tiled", 1)),
-    (1 << 20, 17, 152, 16, ("warp", 1)),
+    (1 << 20, 17, 152, 16, ("tiled", 1)),       # 17-28: a thread per row
+    (1 << 20, 24, 152, 16, ("tiled", 1)),
+    (1 << 20, 28, 152, 16, ("tiled", 1)),
+    (1 << 20, 29, 152, 16, ("warp", 1)),
     (1 << 20, 32, 152, 16, ("warp", 1)),
     (8192, 8192, 152, 16, ("block", 1)),
     (1 << 20, 33, 152, 16, ("warp", 1)),       # medium rows: warp segments
