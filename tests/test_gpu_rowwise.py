@@ -495,3 +495,29 @@ def test_long_rows_split_fallback(rr, oracle_mod):
         idx = np.r_[0:3, rows - 3:rows]
         _check_all_row_ops(rr, oracle_mod, x, idx)
         assert rr.last_tier()[0] == "splitk" and not rr.last_staged()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_register_rows_1025_to_2048_vectors(rr, oracle_mod, dtype):
+    # the block tier's register form past 1024 vectors: 512 threads x 4
+    # vectors for the statistics and the rewrite alike (one vector past a
+    # power of two, and full)
+    from cluster_reductions_gb300 import inputs
+    from _util import assert_layernorm_close
+    epv = 8 if dtype == torch.bfloat16 else 4
+    for i, nvec in enumerate((1025, 1536, 2048)):
+        cols = nvec * epv
+        x = _x(300, cols, dtype, 2100 + i, 1.0)
+        g, b = inputs.layernorm_params(cols, 2110 + i, "cuda")
+        mean, rstd = torch.empty(300, device="cuda"), torch.empty(300, device="cuda")
+        y = rr.layernorm(x, g, b, 1e-5, mean=mean, rstd=rstd, tier="block")
+        assert rr.last_tier() == ("block", 1) and not rr.last_staged()
+        m2, r2 = rr.layernorm_stats(x, 1e-5, tier="block")
+        assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
+        assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
+        idx = np.r_[0:5, 295:300]
+        xs = x[torch.from_numpy(idx).cuda()]
+        y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
+        assert_layernorm_close(to_np(y)[idx], y64, y16, xs.to(torch.float64).cpu().numpy(),
+                               to_np(g), to_np(b), rm, rr_)
+        assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {cols}")
