@@ -687,29 +687,24 @@ int launch_push(const float *O, const float *m, const float *l, int64_t rows, in
                                    O, m, l, rows, D, TR, scale_log2e, out, ml_bulk, d.err_word));
 }
 
-// Direct variant geometry per P, from a sweep on GB300 (256 MiB of partials,
-// D = 64, 128, 256, with (m, l) by the copy engine): one slot of 16 KiB per
-// CTA for P <= 4 (overlap comes from the other CTAs on the SM), two for
-// P = 8 (its tiles of 2 to 8 rows are short enough for the per-tile
-// handshake to show), two of 32 KiB for P = 16.
-#ifndef RR_DIRECT_SLOTS
-#define RR_DIRECT_SLOTS 1
-#endif
+// Direct variant geometry, from sweeps on GB300 (256 MiB of partials, D =
+// 64, 128, 256, and the 131072 x 128 workloads): tiles of 16 KiB for
+// P <= 8, 32 KiB for P = 16.  The (m, l) of a tile go by the copy engine
+// when the producer's lanes would need more than one round trip for them
+// (more than 32 (partition, row) pairs; every tile 16-byte aligned): two
+// dependent round trips sat on the critical path of small tiles (D = 64 ran
+// at 0.66-0.80 of the copy bandwidth for P = 4..16), while for 32 pairs or
+// fewer the copies only add work (P = 8, D = 128: 0.96 against 0.98).  One
+// slot per CTA (the other CTAs on the SM provide the overlap), two for
+// P = 16 and for P = 8 with copied (m, l).
 #ifndef RR_DIRECT_BYTES
 #define RR_DIRECT_BYTES 16384
 #endif
-template <int P> struct DirectGeom {
-  static constexpr int S = (P <= 4) ? RR_DIRECT_SLOTS : 2;
-  static constexpr int bytes = (P <= 8) ? RR_DIRECT_BYTES : 32768;
-};
 
-template <int P>
-int launch_direct(const float *O, const float *m, const float *l, int64_t rows, int D,
-                  float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d) {
-  constexpr int S = DirectGeom<P>::S;
-  int TR = DirectGeom<P>::bytes / (P * D * 4);
-  if (TR < 1) TR = 1;
-  if ((int64_t)TR > rows) TR = (int)rows;
+template <int P, int S>
+int launch_direct_s(const float *O, const float *m, const float *l, int64_t rows, int D, int TR,
+                    int ml_bulk, float scale_log2e, uint16_t *out, cudaStream_t s,
+                    const DevInfo &d) {
   const size_t TRp = ((size_t)TR + 3) & ~(size_t)3;
   const size_t smem = sizeof(float) * ((size_t)S * ((size_t)P * TR * D + 2 * P * TRp) +
                                        (size_t)TR * P + (size_t)TR);
@@ -722,18 +717,31 @@ int launch_direct(const float *O, const float *m, const float *l, int64_t rows, 
   const int64_t ntiles = (rows + TR - 1) / TR;
   int64_t grid = (int64_t)nb * d.sm_count;
   if (grid > ntiles) grid = ntiles;
-  // (m, l) by the copy engine when every tile's rows start 16-byte aligned
-#ifndef RR_DIRECT_ML_BULK
-#define RR_DIRECT_ML_BULK 1
-#endif
-  const int ml_bulk = RR_DIRECT_ML_BULK && (rows % 4 == 0) && (TR % 4 == 0) &&
-                      ((uintptr_t)m % 16 == 0) && ((uintptr_t)l % 16 == 0);
   if (log_enabled())
     std::fprintf(stderr, "rr: combine direct P=%d D=%d TR=%d stages=%d ctas=%lld smem=%zu ml_bulk=%d\n",
                  P, D, TR, S, (long long)grid, smem, ml_bulk);
   launch_kernel(kern, dim3((unsigned)grid), dim3(kPipeThreads), smem, s, 0, O, m, l, rows, D, TR,
                 scale_log2e, out, ml_bulk, d.err_word);
   return cuda_status(cudaGetLastError());
+}
+
+template <int P>
+int launch_direct(const float *O, const float *m, const float *l, int64_t rows, int D,
+                  float scale_log2e, uint16_t *out, cudaStream_t s, const DevInfo &d) {
+  const int bytes = P <= 8 ? RR_DIRECT_BYTES : 32768;
+  int TR = bytes / (P * D * 4);
+  if (TR < 1) TR = 1;
+  if ((int64_t)TR > rows) TR = (int)rows;
+  const int ml_bulk = (P * TR > 32) && (rows % 4 == 0) && (TR % 4 == 0) &&
+                      ((uintptr_t)m % 16 == 0) && ((uintptr_t)l % 16 == 0);
+  if constexpr (P == 16) {
+    return launch_direct_s<P, 2>(O, m, l, rows, D, TR, ml_bulk, scale_log2e, out, s, d);
+  } else if constexpr (P == 8) {
+    if (ml_bulk) return launch_direct_s<P, 2>(O, m, l, rows, D, TR, ml_bulk, scale_log2e, out, s, d);
+    return launch_direct_s<P, 1>(O, m, l, rows, D, TR, ml_bulk, scale_log2e, out, s, d);
+  } else {
+    return launch_direct_s<P, 1>(O, m, l, rows, D, TR, ml_bulk, scale_log2e, out, s, d);
+  }
 }
 
 int launch_generic(const float *O, const float *m, const float *l, int P, int64_t rows, int D,
