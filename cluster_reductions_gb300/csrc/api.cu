@@ -378,6 +378,17 @@ int64_t axis_units(int64_t outer, int64_t inner, int V, int lg_L) {
 AxisPlan plan_axis(int64_t outer, int64_t axis, int64_t inner, int S, int max_cluster,
                    int x_align, bool with_ws) {
   AxisPlan p;
+  // narrow inner widths that are not a multiple of 4: the contiguous slabs
+  // x[o, :, :] read with 16-byte loads, a warp per slab when there are at
+  // least 16 per SM, a CTA per slab from 2 per SM
+  if ((inner == 2 || inner == 3 || inner == 5 || inner == 6 || inner == 7) &&
+      x_align % 16 == 0 && (axis * inner) % 4 == 0 && axis >= 4 &&
+      outer >= (int64_t)S * 2) {
+    p.tier = outer >= (int64_t)S * 16 ? RR_TIER_WARP : RR_TIER_BLOCK;
+    p.V = 1;
+    p.slab = true;
+    return p;
+  }
   p.V = (x_align % 16 == 0 && inner % 4 == 0) ? 4 : 1;
   const int E = p.V == 4 ? 4 : ((x_align % 8 == 0 && inner % 2 == 0) ? 2 : 1);
   if (outer * (inner / E) >= (int64_t)S * 2048) {
@@ -421,7 +432,7 @@ void plan_to_c(const AxisPlan &p, int64_t outer, int64_t inner, rr_axis_plan *c)
   c->tier = p.tier;
   c->cluster_size = p.tier == RR_TIER_SPLITK ? p.C : 1;
   c->emit_tile_width = p.tier == RR_TIER_TILED ? p.E : 0;
-  c->tile_rows = p.tier == RR_TIER_TILED ? 0 : (p.V << p.lg_L);
+  c->tile_rows = p.tier == RR_TIER_TILED ? 0 : (p.slab ? (int)inner : (p.V << p.lg_L));
   c->splits = p.G;
   c->workspace_bytes = p.G > 1 ? (size_t)p.G * (size_t)(outer * inner) * 4 : 0;
 }

@@ -351,11 +351,145 @@ int launch_axis_coop(const void *xv, int64_t outer, int64_t axis, int64_t inner,
   return cuda_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------------------------------
+// Warp tier, slab form, for narrow inner widths that are not a multiple of 4
+// (INNER = 2, 3, 5, 6, 7): WPS warps (1, or a CTA of 8) own the whole slab
+// x[o, :, :], which is contiguous (axis * INNER elements).  Four axis
+// positions are exactly INNER 16-byte vectors, so thread t of the slab's
+// WPS * 32 reads groups t, t + WPS * 32, ... of 4 positions with vector
+// loads (a warp instruction covers 512 contiguous bytes) and folds element
+// e of a group into column e % INNER -- a fixed pattern.  The U groups a
+// thread has in flight fold into U separate accumulator sets (independent
+// dependency chains), joined in order u = 0..U-1 at each chunk end, then the
+// chunks in order; the axis % 4 tail positions go one per thread.  Every
+// column is then combined over the warp with an xor butterfly and, for
+// WPS = 8, over the warps in warp order through shared memory.  Needs x
+// 16-byte aligned and axis * INNER % 4 == 0 (every slab 16-byte aligned).
+// ---------------------------------------------------------------------------
+template <class Op, int INNER, int WPS>
+__global__ void __launch_bounds__(kAxisThreads)
+k_axis_slab(const typename Op::T *__restrict__ x, int64_t outer, int64_t axis,
+            typename Op::T *__restrict__ out) {
+  pdl_begin();
+  using T = typename Op::T;
+  using V = typename Vec4<T>::type;
+  constexpr int U = 4;                              // groups in flight per thread
+  constexpr int TPS = WPS * 32;                     // threads per slab
+  constexpr int64_t kGroupChunk = (int64_t)(kChunk / 4) * (TPS / 32);  // groups per chunk
+  __shared__ T red[WPS][INNER];
+  const int lane = threadIdx.x & 31;
+  const int t = WPS == 1 ? lane : (int)threadIdx.x;  // this thread's index within its slab
+  const int64_t unit = ((int64_t)blockIdx.x * kAxisThreads + threadIdx.x) / TPS;
+  const int64_t nunits = ((int64_t)gridDim.x * kAxisThreads) / TPS;
+  const int64_t ng = axis >> 2;                     // whole groups of 4 positions
+  for (int64_t o = unit; o < outer; o += nunits) {  // uniform over the slab's threads
+    const T *slab = x + o * axis * INNER;
+    const V *q = reinterpret_cast<const V *>(slab);
+    T acc[INNER];
+#pragma unroll
+    for (int c = 0; c < INNER; ++c) acc[c] = Op::id();
+    for (int64_t c0 = 0; c0 < ng; c0 += kGroupChunk) {
+      const int64_t c1 = c0 + kGroupChunk < ng ? c0 + kGroupChunk : ng;
+      T part[U][INNER];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < INNER; ++c) part[u][c] = Op::id();
+      for (int64_t g0 = c0 + t; g0 < c1; g0 += (int64_t)TPS * U) {
+        V v[U][INNER];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t g = g0 + (int64_t)TPS * u;
+          const int64_t gc = g < c1 ? g : c1 - 1;   // clamped: loads stay unconditional
+#pragma unroll
+          for (int k = 0; k < INNER; ++k) v[u][k] = ld_stream(q + gc * INNER + k);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (g0 + (int64_t)TPS * u < c1) {
+#pragma unroll
+            for (int k = 0; k < INNER; ++k) {
+              part[u][(4 * k + 0) % INNER] = Op::f(part[u][(4 * k + 0) % INNER], v[u][k].x);
+              part[u][(4 * k + 1) % INNER] = Op::f(part[u][(4 * k + 1) % INNER], v[u][k].y);
+              part[u][(4 * k + 2) % INNER] = Op::f(part[u][(4 * k + 2) % INNER], v[u][k].z);
+              part[u][(4 * k + 3) % INNER] = Op::f(part[u][(4 * k + 3) % INNER], v[u][k].w);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int c = 0; c < INNER; ++c) acc[c] = Op::f(acc[c], part[u][c]);
+    }
+    const int64_t pos = ng * 4 + t;                 // the axis % 4 tail positions
+    if (pos < axis) {
+#pragma unroll
+      for (int c = 0; c < INNER; ++c) acc[c] = Op::f(acc[c], __ldg(slab + pos * INNER + c));
+    }
+#pragma unroll
+    for (int c = 0; c < INNER; ++c) acc[c] = warp_allreduce<Op, 32>(acc[c]);
+    if constexpr (WPS == 1) {
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < INNER; ++c) out[o * INNER + c] = Op::finalize(acc[c]);
+      }
+    } else {
+      const int w = threadIdx.x >> 5;
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < INNER; ++c) red[w][c] = acc[c];
+      }
+      __syncthreads();
+      if (threadIdx.x < INNER) {
+        T r = red[0][threadIdx.x];
+#pragma unroll
+        for (int ww = 1; ww < WPS; ++ww) r = Op::f(r, red[ww][threadIdx.x]);
+        out[o * INNER + threadIdx.x] = Op::finalize(r);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <class Op, int INNER>
+int launch_axis_slab_n(const void *x, int64_t outer, int64_t axis, void *out, bool cta,
+                       cudaStream_t s, const DevInfo &d) {
+  auto run = [&](auto k, int per_block) {
+    const int nb = occupancy_blocks((const void *)k, kAxisThreads, 0, d.device);
+    const int64_t need = (outer + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)(nb > 0 ? nb : 1) * d.sm_count;
+    const int grid = (int)(need < cap ? need : cap);
+    if (log_enabled())
+      std::fprintf(stderr, "rr: axis slab outer=%lld axis=%lld inner=%d %s ctas=%d\n",
+                   (long long)outer, (long long)axis, INNER, cta ? "cta" : "warp", grid);
+    return cuda_status(launch_kernel(k, dim3(grid), dim3(kAxisThreads), 0, s, 0,
+                                     (const typename Op::T *)x, outer, axis,
+                                     (typename Op::T *)out));
+  };
+  if (cta) return run(k_axis_slab<Op, INNER, kAxisWarps>, 1);
+  return run(k_axis_slab<Op, INNER, 1>, kAxisWarps);
+}
+
+template <class Op>
+int launch_axis_slab(const void *x, int64_t outer, int64_t axis, int64_t inner, void *out,
+                     bool cta, cudaStream_t s, const DevInfo &d) {
+  switch (inner) {
+    case 2: return launch_axis_slab_n<Op, 2>(x, outer, axis, out, cta, s, d);
+    case 3: return launch_axis_slab_n<Op, 3>(x, outer, axis, out, cta, s, d);
+    case 5: return launch_axis_slab_n<Op, 5>(x, outer, axis, out, cta, s, d);
+    case 6: return launch_axis_slab_n<Op, 6>(x, outer, axis, out, cta, s, d);
+    case 7: return launch_axis_slab_n<Op, 7>(x, outer, axis, out, cta, s, d);
+    default: return RR_ERR_INVALID;
+  }
+}
+
 template <class Op>
 int launch_axis_op(const void *x, int64_t outer, int64_t axis, int64_t inner, void *out,
                    const AxisPlan &pl, void *ws, cudaStream_t s, const DevInfo &d) {
   if (pl.tier == RR_TIER_TILED)
     return launch_axis_tiled<Op>(x, outer, axis, inner, out, pl.E, s, d);
+  if (pl.slab) return launch_axis_slab<Op>(x, outer, axis, inner, out, pl.tier == RR_TIER_BLOCK, s, d);
   if (pl.V == 4) return launch_axis_coop<Op, 4>(x, outer, axis, inner, out, pl, ws, s, d);
   return launch_axis_coop<Op, 1>(x, outer, axis, inner, out, pl, ws, s, d);
 }

@@ -46,6 +46,8 @@ struct AxisPlan {
                  // (tile = (1 << lg_L) * V adjacent rows)
   int G = 1;     // block / split-K: independent CTAs / clusters per tile; G > 1
                  // writes G partials per output to the workspace, then folds
+  bool slab = false;  // a warp (warp tier) or a CTA (block tier) per contiguous slab
+                      // x[o, :, :] (inner 2, 3, 5, 6 or 7)
 };
 int launch_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner, int op,
                        int dtype, void *out, const AxisPlan &plan, void *workspace,

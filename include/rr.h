@@ -184,6 +184,12 @@ int rr_reduce_splitk_multi(const void *x, int64_t rows, int64_t cols, int op,
  * folds them in order g = 0 .. G-1.  rr_reduce_axis itself never splits
  * (it has no workspace); rr_reduce_axis_ex splits when given a workspace,
  * automatically when the shape has too few tiles to cover the GPU.
+ * Narrow inner widths that are not a multiple of 4 (2, 3, 5, 6, 7) with a
+ * 16-byte aligned x and axis * inner % 4 == 0 take a slab form of the warp
+ * tier (16 or more slabs x[o, :, :] per SM: a warp per slab) or of the block
+ * tier (2 to 15 per SM: a CTA per slab), reported with tile_rows = inner: the
+ * contiguous slab is read with 16-byte loads, element e of each group of 4
+ * axis positions folded into column e % inner.
  * The automatic choice is rr_plan_reduce_axis's.
  * Errors: RR_ERR_INVALID (null pointer with work to do, negative sizes, bad
  * op / dtype / options, overlap, a forced tile width, tile size or split

@@ -155,3 +155,24 @@ def test_workloads_full_size(rr, oracle_mod, shape, op):
     if op == "sum":
         xi = gen(shape, torch.int32, 7510 + WORKLOADS.index(shape))
         check(rr, oracle_mod, xi, "sum")
+
+
+@pytest.mark.parametrize("inner", [2, 3, 5, 6, 7])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.int32], ids=["f32", "i32"])
+def test_slab_form(rr, oracle_mod, inner, dtype):
+    # narrow inner widths that are not a multiple of 4: the contiguous slabs
+    # x[o, :, :] with 16-byte loads, a warp per slab from 16 slabs per SM, a
+    # CTA per slab from 2; axis lengths give a single group of 4 positions,
+    # a 1-3 position tail and more than one fold chunk
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cases = [(16 * sms + 5, 4, "warp"), (16 * sms + 5, 1020, "warp"), (16 * sms + 5, 1023, "warp"),
+             (2 * sms + 3, 5000, "block"), (2 * sms + 3, 4099, "block"), (2 * sms + 3, 20000, "block")]
+    for outer, axis, tier in cases:
+        if (axis * inner) % 4:
+            continue
+        x = gen((outer, axis, inner), dtype, 3000 + inner * 7 + axis % 97)
+        p = rr.plan_reduce_axis(outer, axis, inner, sms, 16)
+        assert (p["tier"], p["tile_rows"]) == (tier, inner), p
+        for op in (("sum", "max", "min") if dtype == torch.float32 else ("sum", "max")):
+            check(rr, oracle_mod, x, op)
+            assert rr.last_tier()[0] == tier

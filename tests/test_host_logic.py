@@ -225,6 +225,13 @@ def test_rowwise_plan_rejects_bad_arguments(lib):
     ((1, 1 << 22, 16), 16, False, ("splitk", 16, 0, 16, 1)),   # no workspace: one cluster
     ((1, 1 << 22, 16), 16, True, ("splitk", 8, 0, 16, 57)),
     ((2, 4096, 3), 4, True, ("splitk", 8, 0, 4, 2)),
+    ((21845, 1024, 3), 16, True, ("warp", 1, 0, 3, 1)),          # a warp per slab
+    ((13107, 1024, 5), 16, True, ("warp", 1, 0, 5, 1)),
+    ((1216, 1022, 6), 16, True, ("block", 1, 0, 6, 1)),          # 2-15 slabs per SM: a CTA each
+    ((1216, 1021, 6), 16, True, ("block", 1, 0, 8, 1)),          # slabs not 16-byte aligned
+    ((21845, 1024, 3), 8, True, ("warp", 1, 0, 4, 1)),           # x 8-byte aligned: lanes
+    ((2432, 1024, 7), 16, True, ("warp", 1, 0, 7, 1)),
+    ((303, 1024, 3), 16, True, ("splitk", 2, 0, 4, 1)),          # < 2 slabs per SM: tiles
 ])
 def test_axis_dispatch(lib, shape, align, ws, expect):
     import cluster_reductions_gb300 as rr
