@@ -44,9 +44,11 @@ WORKLOAD = ("row reductions: block 8192x8192 f32 sum/max/min + i32 sum; warp 1Mx
             "32768x4096 bf16->f32; layernorm stats 16384x8192 bf16; split-K combine "
             "P=2,4,8 x 131072x128")
 # Reductions over a non-last axis timed beside the step ([outer, axis, inner],
-# fp32, 256 MiB each): a column reduce, a middle axis, a narrow inner axis and
-# a single long, narrow tile that needs the split workspace.
-AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 22, 16)]
+# fp32, 256 MiB each): a column reduce, a middle axis, a narrow inner axis, a
+# single long, narrow tile that needs the split workspace, and three
+# interleaved channels (the slab form).
+AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 22, 16),
+                  (21845, 1024, 3)]
 # Row reductions of medium width timed beside the step (fp32, 256 MiB each).
 MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
 # Softmax / layernorm rows of medium width timed beside the step (bf16,
@@ -918,6 +920,7 @@ PROFILE_CASES = {
     "axis_32768x256x8": ({"shape": (32768, 256, 8)}, "axis", 1.0),
     "axis_1x8192x8192": ({"shape": (1, 8192, 8192)}, "axis", 1.0),
     "axis_1x4194304x16": ({"shape": (1, 1 << 22, 16)}, "axis", 1.0),
+    "axis_21845x1024x3": ({"shape": (21845, 1024, 3)}, "axis", 1.0),
     # rows of medium width (the warp-segment kernels), automatic plan
     "medium_sum_1048576x64_f32": ({"shape": (1 << 20, 64), "op": "sum"}, "medium", 1.0),
     "medium_softmax_131072x1024_bf16": ({"shape": (131072, 1024), "op": "softmax"}, "medium", 1.0),
