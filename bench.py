@@ -71,18 +71,18 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1085626368, "src": ["reduce.cu", "rr_device.cuh"],
-                      "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 575230976, "src": ["combine.cu", "rr_device.cuh"],
-                  "src_sha": "e41b009ab53904ca", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 560443392, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "362e2593015a6584", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271419648, "src": ["reduce.cu", "rr_device.cuh"],
-                     "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271262464, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "362e2593015a6584", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 137985024, "src": ["reduce.cu", "rr_device.cuh"],
-                    "src_sha": "8704b5503d08bf4f", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "splitk_sum_f32": {"bytes": 1087936512, "src": ["reduce.cu", "rr_device.cuh"],
+                      "src_sha": "b514fd872bdfc927", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 567969792, "src": ["combine.cu", "rr_device.cuh"],
+                  "src_sha": "1685f232cca8764e", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+    "softmax_bf16": {"bytes": 559769600, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "ba0339e6f2eef43d", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271251456, "src": ["reduce.cu", "rr_device.cuh"],
+                     "src_sha": "b514fd872bdfc927", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271452160, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "ba0339e6f2eef43d", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137770752, "src": ["reduce.cu", "rr_device.cuh"],
+                    "src_sha": "b514fd872bdfc927", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
