@@ -11,7 +11,10 @@
 //                   one thread, one row);
 //   warp            a warp owns a tile of L*V adjacent rows of one o; lane
 //                   segments of L lanes take 32/L axis positions per step and
-//                   combine with an xor butterfly;
+//                   combine with an xor butterfly (for inner 2, 3, 5, 6 or 7
+//                   the slab form: a warp, or a CTA, owns the whole
+//                   contiguous slab x[o, :, :] and reads it with 16-byte
+//                   loads);
 //   block           a CTA owns a tile; its 8 warps split the axis further and
 //                   combine through shared memory in warp order;
 //   split-K         a cluster of C CTAs owns a tile; each CTA folds one

@@ -25,6 +25,10 @@
 // lanes of one warp, so no all-thread cluster barrier is needed per tile.
 // Generic path: one tile per cluster, plain loads, scalar bands (any P <= 16,
 // any D, bands of unequal width, empty bands when D < P).
+// Two more variants compute the same bits: push (each CTA bulk-copies its
+// peers' row slices into their shared memory) and direct, the default (no
+// exchange at all: a CTA stages the tile rows of all P partitions and folds
+// them locally; same DRAM bytes, no per-tile cluster synchronisation).
 #include <cstdio>
 
 #include <cuda_bf16.h>

@@ -4,9 +4,13 @@
 // and the layernorm statistics (mean, then the variance about the mean, both
 // block reduces over the on-chip row).
 //
-// Fast path: one CTA per row with the whole row held in registers, so the
-// row is read from HBM exactly once.  Generic path (any width, any
-// alignment): the row is streamed from global memory once per pass.
+// This file holds the block tier -- fast path: one CTA per row with the
+// whole row held in registers, so the row is read from HBM exactly once;
+// generic path (any width, any alignment): the row is streamed from global
+// memory once per pass -- and the split-K tier (a cluster of CTAs per row,
+// the slices read from global memory), and the tier choice (plan_rowwise).
+// Many short rows take the warp tier (rowwarp.cu); long rows are staged in
+// shared memory (rowstaged.cu).
 #include <cstdio>
 
 #include <cuda_bf16.h>
