@@ -28,6 +28,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -72,17 +73,17 @@ FALLBACK_HBM_GBS = 6800.0
 # captured launch ended.
 NCU_TRAFFIC = {
     "splitk_sum_f32": {"bytes": 1087936512, "src": ["reduce.cu", "rr_device.cuh"],
-                      "src_sha": "b514fd872bdfc927", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+                      "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
     "combine_p8": {"bytes": 567969792, "src": ["combine.cu", "rr_device.cuh"],
-                  "src_sha": "1685f232cca8764e", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+                  "src_sha": "e448f964a6acd0c9", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
     "softmax_bf16": {"bytes": 559769600, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "ba0339e6f2eef43d", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+                    "src_sha": "fff2240e73e258a1", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
     "block_sum_f32": {"bytes": 271251456, "src": ["reduce.cu", "rr_device.cuh"],
-                     "src_sha": "b514fd872bdfc927", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+                     "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
     "layernorm_bf16": {"bytes": 271452160, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "ba0339e6f2eef43d", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+                      "src_sha": "fff2240e73e258a1", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
     "warp_sum_f32": {"bytes": 137770752, "src": ["reduce.cu", "rr_device.cuh"],
-                    "src_sha": "b514fd872bdfc927", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+                    "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
@@ -242,13 +243,17 @@ def read_peak():
 
 def kernel_src_sha(files=None) -> str:
     """Hash of kernel sources under cluster_reductions_gb300/csrc: the named
-    files (a kernel's translation unit and the device header it includes),
-    else every file."""
+    files (a kernel's translation unit and the device headers it includes),
+    else every file.  Comments and whitespace are left out, so editing a
+    comment does not orphan a traffic figure taken from the same code."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "cluster_reductions_gb300", "csrc")
     for f in sorted(files if files else os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(f.encode() + "".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
