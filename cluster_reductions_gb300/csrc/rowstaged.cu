@@ -244,13 +244,237 @@ k_rowwise_staged(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   if (C > 1) cluster_sync();  // no CTA leaves while a peer may read its slots
 }
 
+// 8 consecutive floats from p, which lies `sh` floats (0..3) past a 16-byte
+// boundary: two or three aligned 16-byte loads and a selection fixed by sh
+// (uniform over the CTA).  The caller checks that the aligned window
+// [p - sh, p - sh + 8 or 12) lies inside the array.
+__device__ __forceinline__ void load8_shifted(const float *p, int sh, float (&o)[8]) {
+  const float4 *q = reinterpret_cast<const float4 *>(p - sh);
+  const float4 a = __ldg(q), b = __ldg(q + 1);
+  if (sh == 0) {
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    return;
+  }
+  const float4 c = __ldg(q + 2);
+  if (sh == 1) {
+    o[0] = a.y; o[1] = a.z; o[2] = a.w; o[3] = b.x; o[4] = b.y; o[5] = b.z; o[6] = b.w; o[7] = c.x;
+  } else if (sh == 2) {
+    o[0] = a.z; o[1] = a.w; o[2] = b.x; o[3] = b.y; o[4] = b.z; o[5] = b.w; o[6] = c.x; o[7] = c.y;
+  } else {
+    o[0] = a.w; o[1] = b.x; o[2] = b.y; o[3] = b.z; o[4] = b.w; o[5] = c.x; o[6] = c.y; o[7] = c.z;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Staged rows that do not start 16-byte aligned (a width that is not a
+// multiple of the 16-byte vector, or a misaligned x): the same passes over
+// a slice copied into shared memory at its address's offset within its
+// 16-byte chunk, so that smem byte k holds global byte floor16(slice) + k.
+// The slice's whole 16-byte chunks come by bulk copies; the elements of its
+// partial first and last chunks by plain loads.  Every pass walks the
+// 8-element vectors of that image, vector v holding slice elements
+// 8v + j - hoff (hoff = the slice's element offset in its first chunk), and
+// leaves the slots outside [0, n) of the first and last vector out of the
+// fold.  Outputs go as vectors where the output row's shifted base is
+// aligned, else element by element; gamma and beta are read element by
+// element (their offset varies with the row).
+// ---------------------------------------------------------------------------
+template <class In, int MODE>
+__global__ void __launch_bounds__(kStageThreads)
+k_rowwise_staged_mis(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, int chunk,
+                     float eps, float *__restrict__ y, float *__restrict__ mean,
+                     float *__restrict__ rstd, const float *__restrict__ gamma,
+                     const float *__restrict__ beta, uint16_t *__restrict__ ybf, int *err) {
+  pdl_begin();
+  using S = typename In::S;
+  constexpr int T = kStageThreads;
+  constexpr int E = (int)sizeof(S);
+  extern __shared__ __align__(128) unsigned char stage[];
+  __shared__ __align__(8) uint64_t full;
+  __shared__ float red[2][T / 32];
+  __shared__ float slot[2][2];
+  __shared__ int dead;
+  const int tid = threadIdx.x;
+  const uint32_t C = cluster_nctarank(), r = cluster_ctarank();
+  const int64_t row = cluster_id_x();
+  const int64_t b0 = (int64_t)r * chunk < cols ? (int64_t)r * chunk : cols;
+  const int64_t b1 = b0 + chunk < cols ? b0 + chunk : cols;
+  const int n = (int)(b1 - b0);
+  const S *ps = x + row * cols + b0;
+  const int hoffB = (int)((uintptr_t)ps & 15u);      // bytes before the slice in its chunk
+  const int hoff = hoffB / E;
+  const unsigned char *base = reinterpret_cast<const unsigned char *>(ps) - hoffB;
+  const int span = hoffB + n * E;                    // bytes of the image
+  const int nch = (span + 15) >> 4;                  // 16-byte chunks
+  const int c_lo = hoffB ? 1 : 0;                    // whole chunks [c_lo, c_hi)
+  const int c_hi = (span & 15) ? nch - 1 : nch;
+  const int head_n = c_lo ? ((16 - hoffB) / E < n ? (16 - hoffB) / E : n) : 0;
+  int tail_0 = n;                                    // elements of a partial last chunk
+  if ((span & 15) && nch - 1 >= c_lo) {
+    const int t0 = (16 * (nch - 1) - hoffB) / E;
+    tail_0 = t0 > head_n ? t0 : head_n;
+  }
+  const int nvt = (hoff + n + 7) >> 3;               // 8-element vectors of the image
+
+  if (tid == 0) {
+    dead = 0;
+    mbar_init(&full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t bytes = c_hi > c_lo ? (uint32_t)(c_hi - c_lo) * 16u : 0u;
+    mbar_arrive_expect_tx(&full, bytes);
+    for (uint32_t off = 0; off < bytes; off += kPiece)
+      bulk_g2s(stage + 16 * c_lo + off, base + 16 * c_lo + off,
+               bytes - off < kPiece ? bytes - off : kPiece, &full);
+  }
+  S *se = reinterpret_cast<S *>(stage);
+  for (int i = tid; i < head_n; i += T) se[hoff + i] = ps[i];
+  for (int i = tail_0 + tid; i < n; i += T) se[hoff + i] = ps[i];
+  if (!mbar_wait_or_die(&full, 0, kWaitBudget, &dead, false)) set_error(err, kErrTimeout);
+  __syncthreads();  // the plain stores of the edge elements
+
+  // fold of vector v: f(e, valid) for each slot; edge vectors mask
+  auto visit = [&](int v, auto f) {
+    float e[8];
+    staged8<In>(stage, v, e);
+    if (v == 0 || v == nvt - 1) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = 8 * v + j - hoff;
+        f(j, e[j], i >= 0 && i < n);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f(j, e[j], true);
+    }
+  };
+
+  if constexpr (MODE == kModeSoftmax) {
+    float m = -INFINITY;
+    for (int v = tid; v < nvt; v += T)
+      visit(v, [&](int, float e, bool ok) { m = ok ? fmaxf(m, e) : m; });
+    m = block_reduce<MaxF32, T>(m, red[0]);
+    float v1[1] = {m}, M[1];
+    cluster_allreduce<MaxF32, 1>(slot[0], v1, C, /*tail_sync=*/false, M);  // combine 1
+    const float Mx = M[0];
+    const float mb = Mx * kLog2e;
+    float s = 0.0f;
+    if (Mx != -INFINITY) {
+      for (int v = tid; v < nvt; v += T)
+        visit(v, [&](int, float e, bool ok) {
+          if (ok) s += ex2_approx(fmaf(e, kLog2e, -mb));
+        });
+    }
+    s = block_reduce<SumF32, T>(s, red[1]);
+    float v2[1] = {s}, Ssum[1];
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, Ssum);  // combine 2
+    const float inv = 1.0f / Ssum[0];
+    float *yv = y + row * cols + b0 - hoff;          // element i of the slice at yv[hoff + i]
+    const bool vy = ((uintptr_t)yv % (In::EPV == 8 ? 32 : 16)) == 0;
+    for (int v = tid; v < nvt; v += T) {
+      float e[8];
+      staged8<In>(stage, v, e);
+      float o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        o[j] = (Mx == -INFINITY) ? 0.0f : ex2_approx(fmaf(e[j], kLog2e, -mb)) * inv;
+      if (vy && v != 0 && v != nvt - 1) {
+        if constexpr (In::EPV == 8) {
+          st_stream_v8(yv + (int64_t)v * 8, o);
+        } else {
+          st_stream_v4(yv + (int64_t)v * 8, o[0], o[1], o[2], o[3]);
+          st_stream_v4(yv + (int64_t)v * 8 + 4, o[4], o[5], o[6], o[7]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = 8 * v + j - hoff;
+          if (i >= 0 && i < n) yv[hoff + i] = o[j];
+        }
+      }
+    }
+  } else {
+    float a = 0.0f;
+    for (int v = tid; v < nvt; v += T)
+      visit(v, [&](int, float e, bool ok) { a += ok ? e : 0.0f; });
+    a = block_reduce<SumF32, T>(a, red[0]);
+    float v1[1] = {a}, tot[1];
+    cluster_allreduce<SumF32, 1>(slot[0], v1, C, /*tail_sync=*/false, tot);  // combine 1
+    const float mu = tot[0] / (float)cols;
+    float q = 0.0f;
+    for (int v = tid; v < nvt; v += T)
+      visit(v, [&](int, float e, bool ok) {
+        const float dl = e - mu;
+        q = ok ? fmaf(dl, dl, q) : q;
+      });
+    q = block_reduce<SumF32, T>(q, red[1]);
+    float v2[1] = {q}, tq[1];
+    cluster_allreduce<SumF32, 1>(slot[1], v2, C, /*tail_sync=*/false, tq);  // combine 2
+    const float rs = 1.0f / sqrtf(tq[0] / (float)cols + eps);
+    if (r == 0 && tid == 0) {
+      if (mean) mean[row] = mu;
+      if (rstd) rstd[row] = rs;
+    }
+    if constexpr (MODE == kModeLayernorm) {
+      uint16_t *yv = ybf + row * cols + b0 - hoff;
+      const float *gv = gamma + b0 - hoff, *bv = beta + b0 - hoff;
+      const bool vy = ((uintptr_t)yv % 16) == 0;
+      const int gsh = (int)(((uintptr_t)gv >> 2) & 3u), bsh = (int)(((uintptr_t)bv >> 2) & 3u);
+      for (int v = tid; v < nvt; v += T) {
+        float e[8];
+        staged8<In>(stage, v, e);
+        const bool edge = v == 0 || v == nvt - 1;
+        float o[8];
+        // gamma / beta as shifted vectors where every slot is in the row and
+        // both aligned windows lie inside [0, cols)
+        const int64_t g0 = b0 - hoff + 8 * (int64_t)v;
+        const bool gin = g0 - gsh >= 0 && g0 - gsh + (gsh ? 12 : 8) <= cols &&
+                         g0 - bsh >= 0 && g0 - bsh + (bsh ? 12 : 8) <= cols;
+        if (!edge && gin) {
+          float g[8], bt[8];
+          load8_shifted(gv + 8 * v, gsh, g);
+          load8_shifted(bv + 8 * v, bsh, bt);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] = fmaf((e[j] - mu) * rs, g[j], bt[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = 8 * v + j - hoff;
+            const bool ok = i >= 0 && i < n;
+            o[j] = ok ? fmaf((e[j] - mu) * rs, __ldg(gv + 8 * v + j), __ldg(bv + 8 * v + j)) : 0.0f;
+          }
+        }
+        if (vy && !edge) {
+          *reinterpret_cast<uint4 *>(yv + (int64_t)v * 8) =
+              make_uint4(bf16x2_bits(o[0], o[1]), bf16x2_bits(o[2], o[3]), bf16x2_bits(o[4], o[5]),
+                         bf16x2_bits(o[6], o[7]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = 8 * v + j - hoff;
+            if (i >= 0 && i < n) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(o[j]);
+              yv[hoff + i] = *reinterpret_cast<const uint16_t *>(&h);
+            }
+          }
+        }
+      }
+    }
+  }
+  if (C > 1) cluster_sync();  // no CTA leaves while a peer may read its slots
+}
+
 template <class In, int MODE>
 int launch_mode(const void *x, int64_t rows, int64_t cols, float eps, float *y, float *mean,
                 float *rstd, const float *gamma, const float *beta, uint16_t *ybf, int C,
-                cudaStream_t s, const DevInfo &d) {
-  auto kern = k_rowwise_staged<In, MODE>;
+                bool aligned, cudaStream_t s, const DevInfo &d) {
+  // every operand aligned for the vector forms: the plain kernel; otherwise
+  // the misaligned one, whose image is up to 8 elements longer than a slice
+  auto kern = aligned ? k_rowwise_staged<In, MODE> : k_rowwise_staged_mis<In, MODE>;
   const int64_t chunk = rowwise_staged_chunk(cols, C);
-  const size_t smem = (size_t)chunk * sizeof(typename In::S);
+  const size_t smem = (size_t)(chunk + (aligned ? 0 : 8)) * sizeof(typename In::S);
   if (chunk < 0 || smem > (size_t)kStageMaxBytes) return RR_ERR_INVALID;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kStageMaxBytes);
@@ -263,9 +487,10 @@ int launch_mode(const void *x, int64_t rows, int64_t cols, float eps, float *y, 
     return RR_ERR_UNSUPPORTED;
   if (rows * C > 0x7fffffffLL) return RR_ERR_INVALID;
   if (log_enabled())
-    std::fprintf(stderr, "rr: %s staged rows=%lld cols=%lld C=%d chunk=%lld smem=%zu\n",
+    std::fprintf(stderr, "rr: %s staged%s rows=%lld cols=%lld C=%d chunk=%lld smem=%zu\n",
                  MODE == kModeSoftmax ? "softmax" : (MODE == kModeStats ? "lnstats" : "layernorm"),
-                 (long long)rows, (long long)cols, C, (long long)chunk, smem);
+                 aligned ? "" : " (misaligned rows)", (long long)rows, (long long)cols, C,
+                 (long long)chunk, smem);
   return cuda_status(launch_kernel(kern, dim3((unsigned)(rows * C)), dim3(kStageThreads), smem, s,
                                    C, (const typename In::S *)x, rows, cols, (int)chunk, eps, y,
                                    mean, rstd, gamma, beta, ybf, d.err_word));
@@ -278,28 +503,28 @@ int64_t rowwise_staged_chunk(int64_t cols, int C) {
   return ((cols + C - 1) / C + 7) & ~int64_t(7);
 }
 
-int rowwise_staged_cluster(int64_t cols, int in_dtype, int max_cluster) {
+int rowwise_staged_cluster(int64_t cols, int in_dtype, int max_cluster, bool aligned) {
   const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
   for (int C = 1; C <= 16 && C <= max_cluster; C *= 2)
-    if (rowwise_staged_chunk(cols, C) * elt <= kStageMaxBytes) return C;
+    if ((rowwise_staged_chunk(cols, C) + (aligned ? 0 : 8)) * elt <= kStageMaxBytes) return C;
   return 0;
 }
 
 int launch_rowwise_staged(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
                           float eps, float *y, float *mean, float *rstd, const float *gamma,
-                          const float *beta, uint16_t *ybf, int C, cudaStream_t s,
+                          const float *beta, uint16_t *ybf, int C, bool aligned, cudaStream_t s,
                           const DevInfo &d) {
   if (in_dtype == RR_BF16) {
     switch (mode) {
-      case kModeSoftmax: return launch_mode<InBF16, kModeSoftmax>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
-      case kModeStats: return launch_mode<InBF16, kModeStats>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
-      default: return launch_mode<InBF16, kModeLayernorm>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
+      case kModeSoftmax: return launch_mode<InBF16, kModeSoftmax>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
+      case kModeStats: return launch_mode<InBF16, kModeStats>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
+      default: return launch_mode<InBF16, kModeLayernorm>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
     }
   }
   switch (mode) {
-    case kModeSoftmax: return launch_mode<InF32, kModeSoftmax>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
-    case kModeStats: return launch_mode<InF32, kModeStats>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
-    default: return launch_mode<InF32, kModeLayernorm>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, s, d);
+    case kModeSoftmax: return launch_mode<InF32, kModeSoftmax>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
+    case kModeStats: return launch_mode<InF32, kModeStats>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
+    default: return launch_mode<InF32, kModeLayernorm>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, C, aligned, s, d);
   }
 }
 

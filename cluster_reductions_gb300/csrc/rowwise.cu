@@ -436,6 +436,9 @@ constexpr int kRowWideThreads = 512;
 #ifndef RR_ROWSK_UNROLL
 #define RR_ROWSK_UNROLL 4
 #endif
+#ifndef RR_ROWSK_THREADS
+#define RR_ROWSK_THREADS 512
+#endif
 template <class In, int NW>
 __device__ __forceinline__ void unpack8(const uint4 (&w)[NW], float (&o)[8]) {
   if constexpr (NW == 1) {
@@ -629,7 +632,7 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
                           float *mean, float *rstd, const float *gamma, const float *beta,
                           uint16_t *ybf, int C, cudaStream_t s, const DevInfo &d) {
   using S = typename In::S;
-  constexpr int T = 512;
+  constexpr int T = RR_ROWSK_THREADS;
   auto kern = k_rowwise_splitk<T, In, MODE>;
   if (C > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -671,7 +674,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
     return launch_rowwise_staged(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
-                                 0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
+                                 0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, vec, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
                                                    nullptr, nullptr, nullptr, pk.width, s, d);
@@ -711,7 +714,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
     return launch_rowwise_staged(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
-                                 nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
+                                 nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, vec, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                  nullptr, nullptr, nullptr, pk.width, s, d);
@@ -754,7 +757,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
     return launch_rowwise_staged(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
-                                 eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
+                                 eps, nullptr, mean, rstd, gamma, beta, y, pk.width, vec, s, d);
   if (pk.tier == RR_TIER_SPLITK)
     return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                      gamma, beta, y, pk.width, s, d);
@@ -803,6 +806,13 @@ static int rowwise_splitk_cluster(int64_t rows, int64_t cols, int sm_count, int 
 // per thread); forced split-K stages its slices when RR_ROW_STAGED_SPLITK
 // and they fit.
 constexpr int64_t kRowStagedMinVec[3] = {1024, kRowRegMaxVec, kRowRegMaxVec};
+// Rows that are not 16-byte aligned have no register form: they are staged
+// beyond these lengths in 16-byte vectors (softmax, statistics, rewrite),
+// shorter ones take the scalar form.  Measured against that form and the
+// split-K fallback: staging wins for softmax from the shortest rows tried
+// (4100 bf16: 5026 against 4315 GB/s; 8193: 6396 against 1620), for the
+// statistics from about 1024 vectors, for the rewrite from about 2048.
+constexpr int64_t kRowStagedMinVecMis[3] = {32, 1024, 2048};
 #ifndef RR_ROW_STAGED_SPLITK
 #define RR_ROW_STAGED_SPLITK 0
 #endif
@@ -812,10 +822,16 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   const bool rewrite = mode == kModeLayernorm;
   const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
   const int64_t nvec = vec ? cols * elt / 16 : 0;
+  const int64_t row_vecs = cols * elt / 16;  // the row's length in 16-byte vectors
+  // staged slices of C CTAs fit shared memory (misaligned rows stage up to
+  // 8 elements more)
+  auto stage_fits = [&](int c) {
+    return (rowwise_staged_chunk(cols, c) + (vec ? 0 : 8)) * elt <= kStageMaxBytes;
+  };
   const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
+  const int64_t staged_min = vec ? kRowStagedMinVec[mode] : kRowStagedMinVecMis[mode];
   if (tier == RR_TIER_BLOCK) {
-    const bool st = vec && nvec > kRowStagedMinVec[mode] &&
-                    rowwise_staged_chunk(cols, 1) * elt <= kStageMaxBytes;
+    const bool st = row_vecs > staged_min && stage_fits(1);
     return {RR_TIER_BLOCK, 1, st};
   }
   if (tier == RR_TIER_WARP) {
@@ -826,22 +842,20 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     if (C == 0) C = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
     if (C == 0) C = 2;
     if (C > 1 && C > max_cluster) return {-1, 0, false};
-    const bool st = RR_ROW_STAGED_SPLITK && vec &&
-                    rowwise_staged_chunk(cols, C) * elt <= kStageMaxBytes;
+    const bool st = RR_ROW_STAGED_SPLITK && stage_fits(C);
     return {RR_TIER_SPLITK, C, st};
   }
   const int c = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
   if (c > 0) {
-    const bool st = RR_ROW_STAGED_SPLITK && vec &&
-                    rowwise_staged_chunk(cols, c) * elt <= kStageMaxBytes;
+    const bool st = RR_ROW_STAGED_SPLITK && stage_fits(c);
     return {RR_TIER_SPLITK, c, st};
   }
   if (vec && rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
     const int L = rowwise_warp_lanes(nvec, 0, rewrite);
     if (L) return {RR_TIER_WARP, L, false};
   }
-  if (vec && nvec > kRowStagedMinVec[mode]) {
-    const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster);
+  if (row_vecs > staged_min) {
+    const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster, vec);
     if (sc == 1) return {RR_TIER_BLOCK, 1, true};
     // the statistics only read the row: past clusters of 4 the split-K pass
     // over global memory (its second read served by L2) came out ahead

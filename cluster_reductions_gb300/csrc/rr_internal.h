@@ -107,12 +107,15 @@ constexpr int64_t kStageMaxBytes = RR_STAGE_MAX_KB * 1024;
 // Elements per CTA slice for a cluster of C (a multiple of 8); -1 if C < 1.
 int64_t rowwise_staged_chunk(int64_t cols, int C);
 // Smallest cluster size (a power of two up to min(16, max_cluster)) whose
-// slices fit kStageMaxBytes; 0 if none does.
-int rowwise_staged_cluster(int64_t cols, int in_dtype, int max_cluster);
-// mode as launch_rowwise_warp; the rows must be 16-byte aligned vectors.
+// slices fit kStageMaxBytes (rows that are not 16-byte aligned stage up to
+// 8 elements more per slice); 0 if none does.
+int rowwise_staged_cluster(int64_t cols, int in_dtype, int max_cluster, bool aligned = true);
+// mode as launch_rowwise_warp.  `aligned`: every operand meets the vector
+// forms' alignment (as for the warp tier); otherwise the misaligned form
+// runs, for any element-aligned x and outputs.
 int launch_rowwise_staged(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
                           float eps, float *y, float *mean, float *rstd, const float *gamma,
-                          const float *beta, uint16_t *ybf, int C, cudaStream_t s,
+                          const float *beta, uint16_t *ybf, int C, bool aligned, cudaStream_t s,
                           const DevInfo &d);
 
 // ---- warp tier of the row operations (rowwarp.cu)

@@ -307,6 +307,10 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * a CTA per row while a row fits 96 KiB, else the smallest cluster (<= 16)
  * whose slices do, each CTA staging its slice (reported as the split-K tier
  * of that cluster size); the statistics stage only up to clusters of 4.
+ * Rows that are not 16-byte aligned (a width that is not a vector multiple,
+ * or a misaligned operand) are staged too, beyond 32 vectors for softmax,
+ * 1024 for the statistics, 2048 for rr_layernorm, with their partial first
+ * and last 16-byte chunks loaded element by element.
  * Long rows that are not staged take split-K over global memory with
  * slices of at most 128 KiB.  A forced block tier stages when it applies; a
  * forced split-K tier reads from global memory.

@@ -488,36 +488,27 @@ def test_staged_rows_special(rr, oracle_mod):
 
 
 def test_long_rows_split_fallback(rr, oracle_mod):
-    # long rows that cannot be staged take split-K over global memory
+    # long rows too long to stage take split-K over global memory
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for rows, cols, off in [(sms + 2, 1 << 20, 0), (sms + 5, 32767, 0), (sms + 5, 32768, 1)]:
-        x = _x(rows, cols, torch.bfloat16, 2000 + cols % 11, 2.0, off)
-        idx = np.r_[0:3, rows - 3:rows]
-        _check_all_row_ops(rr, oracle_mod, x, idx)
-        assert rr.last_tier()[0] == "splitk" and not rr.last_staged()
+    rows, cols = sms + 2, 1 << 20
+    x = _x(rows, cols, torch.bfloat16, 2000, 2.0)
+    _check_all_row_ops(rr, oracle_mod, x, np.r_[0:3, rows - 3:rows])
+    assert rr.last_tier()[0] == "splitk" and not rr.last_staged()
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
-def test_register_rows_1025_to_2048_vectors(rr, oracle_mod, dtype):
-    # the block tier's register form past 1024 vectors: 512 threads x 4
-    # vectors for the statistics and the rewrite alike (one vector past a
-    # power of two, and full)
-    from cluster_reductions_gb300 import inputs
-    from _util import assert_layernorm_close
+def test_staged_misaligned_rows(rr, oracle_mod, dtype):
+    # rows that do not start 16-byte aligned (a width that is not a vector
+    # multiple, or a misaligned base): staged with their partial first and
+    # last 16-byte chunks loaded element by element; a CTA per row and
+    # clusters, every slice offset, outputs vector-aligned or not
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     epv = 8 if dtype == torch.bfloat16 else 4
-    for i, nvec in enumerate((1025, 1536, 2048)):
-        cols = nvec * epv
-        x = _x(300, cols, dtype, 2100 + i, 1.0)
-        g, b = inputs.layernorm_params(cols, 2110 + i, "cuda")
-        mean, rstd = torch.empty(300, device="cuda"), torch.empty(300, device="cuda")
-        y = rr.layernorm(x, g, b, 1e-5, mean=mean, rstd=rstd, tier="block")
-        assert rr.last_tier() == ("block", 1) and not rr.last_staged()
-        m2, r2 = rr.layernorm_stats(x, 1e-5, tier="block")
-        assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
-        assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
-        idx = np.r_[0:5, 295:300]
-        xs = x[torch.from_numpy(idx).cuda()]
-        y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
-        assert_layernorm_close(to_np(y)[idx], y64, y16, xs.to(torch.float64).cpu().numpy(),
-                               to_np(g), to_np(b), rm, rr_)
-        assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {cols}")
+    cases = ([(sms + 5, 20001, 0), (sms + 5, 32768, 1), (sms + 3, 50257, 0), (sms + 3, 65536, 3),
+              (sms + 2, 100003, 5)] if epv == 8 else
+             [(sms + 5, 10001, 0), (sms + 5, 16384, 1), (sms + 3, 25002, 0), (sms + 2, 40003, 2)])
+    for i, (rows, cols, off) in enumerate(cases):
+        x = _x(rows, cols, dtype, 2200 + i, 2.0, off)
+        idx = np.r_[0:4, rows // 2, rows - 4:rows]
+        _check_all_row_ops(rr, oracle_mod, x, idx)
+        assert rr.last_staged(), (rows, cols, off, rr.last_tier())

@@ -183,8 +183,15 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     # not stageable: split-K over global memory
     (304, 524288, "layernorm", "bf16", True, 8, ("splitk", 8, False)),   # slices > 96 KiB
     (152, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16, False)),
-    (4096, 32767, "softmax", "bf16", True, 16, ("splitk", 2, False)),    # not a vector multiple
-    (4096, 32768, "softmax", "bf16", False, 16, ("splitk", 2, False)),   # misaligned operands
+    (4096, 32767, "softmax", "bf16", True, 16, ("block", 1, True)),      # not a vector multiple:
+    (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, True)),     # misaligned rows staged
+    (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, True)),
+    (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, True)),    # + 8 elements > 96 KiB
+    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, True)),      # misaligned rows: softmax
+    (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, False)),     # stages from 1024 vectors,
+    (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, True)),       # the statistics from 1024,
+    (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, False)),    # the rewrite from 2048
+    (4096, 16396, "layernorm", "bf16", True, 16, ("block", 1, True)),
     (4096, 32768, "softmax", "bf16", True, 1, ("block", 1, True)),       # no clusters: C = 1 fits
     (4096, 40000, "softmax", "f32", True, 1, ("block", 1, False)),       # no clusters, too long
 ])
