@@ -172,11 +172,110 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
 // CTAs of up to 8 warps, persistent over the rows.  With fewer rows than
 // 8 warps per SM take, the CTAs shrink (down to one warp) so that the warps
 // spread over every SM instead of filling a few.
-template <class In, int MODE, int L, int NV>
+// Element-wise form, for rows that are not made of aligned 16-byte vectors
+// (a width that is not a multiple of 8 bf16 / 4 fp32 elements, or a
+// misaligned operand) of up to 32 * K elements: lane `sub` of a segment of L
+// lanes holds elements k * L + sub, k < K (consecutive lanes read
+// consecutive elements), with clamped, unconditional loads and the slots
+// past the row's end left out of every fold.  Reductions, outputs and the
+// per-element arithmetic as in the vector form; stores element by element.
+template <class In, int MODE, int L, int K>
+__global__ void __launch_bounds__(kWarpRowMaxThreads)
+k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+                  float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
+                  const float *__restrict__ gamma, const float *__restrict__ beta,
+                  uint16_t *__restrict__ ybf) {
+  pdl_begin();
+  constexpr int RPW = 32 / L;
+  const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
+  for (int64_t r0 = warp * RPW; r0 < rows; r0 += stride) {  // warp-uniform trip count
+    const int64_t row = r0 + seg;
+    const int64_t rc = row < rows ? row : rows - 1;
+    const typename In::S *xr = x + rc * (int64_t)cols;
+    float v[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = k * L + sub;
+      v[k] = In::load1(xr + (i < cols ? i : cols - 1));
+    }
+    if constexpr (MODE == kModeSoftmax) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if (k * L + sub < cols) m = fmaxf(m, v[k]);
+      float s = 0.0f;
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const float p = ex2_approx(fmaf(v[k], kLog2e, -mb));
+          v[k] = p;
+          if (k * L + sub < cols) s += p;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) v[k] = 0.0f;
+      }
+      float M = m, S = s;
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1)
+        ms_combine(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
+      const float f = (m == -INFINITY) ? 0.0f : ex2_approx((m - M) * kLog2e) * (1.0f / S);
+      if (row < rows) {
+        float *yr = y + row * (int64_t)cols;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int i = k * L + sub;
+          if (i < cols) yr[i] = v[k] * f;
+        }
+      }
+    } else {
+      float s = 0.0f;
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if (k * L + sub < cols) s += v[k];
+      const float mu = warp_allreduce<SumF32, L>(s) / (float)cols;
+      float qs = 0.0f;
+#pragma unroll
+      for (int k = 0; k < K; ++k)
+        if (k * L + sub < cols) {
+          const float dlt = v[k] - mu;
+          qs = fmaf(dlt, dlt, qs);
+        }
+      const float var = warp_allreduce<SumF32, L>(qs) * (1.0f / (float)cols);
+      const float rs = 1.0f / sqrtf(var + eps);
+      if (row < rows) {
+        if constexpr (MODE == kModeLayernorm) {
+          uint16_t *yr = ybf + row * (int64_t)cols;
+#pragma unroll
+          for (int k = 0; k < K; ++k) {
+            const int i = k * L + sub;
+            if (i < cols) {
+              const __nv_bfloat16 h =
+                  __float2bfloat16_rn(fmaf((v[k] - mu) * rs, __ldg(gamma + i), __ldg(beta + i)));
+              yr[i] = *reinterpret_cast<const uint16_t *>(&h);
+            }
+          }
+        }
+        if (sub == 0) {
+          if (mean) mean[row] = mu;
+          if (rstd) rstd[row] = rs;
+        }
+      }
+    }
+  }
+}
+
+template <class In, int MODE, int L, int NV, bool EL = false>
 int launch_one(const void *x, int64_t rows, int64_t cols, float eps, float *y, float *mean,
                float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
                cudaStream_t s, const DevInfo &d) {
-  auto k = k_rowwise_warp<In, MODE, L, NV>;
+  auto k = [] {
+    if constexpr (EL) return k_rowwise_warp_el<In, MODE, L, NV>;
+    else return k_rowwise_warp<In, MODE, L, NV>;
+  }();
   constexpr int RPW = 32 / L;
   const int64_t warps = (rows + RPW - 1) / RPW;
   int wpb = kWarpRowMaxThreads / 32;
@@ -220,6 +319,31 @@ int launch_mode(int L, int nv, const void *x, int64_t rows, int64_t cols, float 
   }
 }
 
+// Element-wise form: (L, K) pairs with K >= 2, 32 * 32 elements at most.
+template <class In, int MODE>
+int launch_mode_el(int L, int K, const void *x, int64_t rows, int64_t cols, float eps, float *y,
+                   float *mean, float *rstd, const float *gamma, const float *beta,
+                   uint16_t *ybf, cudaStream_t s, const DevInfo &d) {
+#define RR_EL(LL, KK) \
+  return launch_one<In, MODE, LL, KK, true>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d)
+  if (L < 32) {
+    switch (L) {
+      case 1: RR_EL(1, 4);
+      case 2: RR_EL(2, 4);
+      case 4: RR_EL(4, 4);
+      case 8: RR_EL(8, 4);
+      default: RR_EL(16, 4);
+    }
+  }
+  switch (K) {
+    case 4: RR_EL(32, 4);
+    case 8: RR_EL(32, 8);
+    case 16: RR_EL(32, 16);
+    default: RR_EL(32, 32);
+  }
+#undef RR_EL
+}
+
 }  // namespace
 
 int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite) {
@@ -244,6 +368,43 @@ int rowwise_warp_nv(int64_t nvec, int lanes) {
   int nv = 1;
   while (nv < per) nv *= 2;
   return nv;
+}
+
+int rowwise_warp_el_lanes(int64_t cols, int lanes) {
+  if (cols < 1 || cols > (int64_t)32 * kRowWarpMaxElPerLane) return 0;
+  // 4 elements per lane up to 64 elements, then 32 lanes with 4..32 each
+  int L = 1;
+  while (L < 32 && (int64_t)L * 4 < cols) L *= 2;
+  if (lanes == 0) return L;
+  if (!(lanes == 1 || lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16 || lanes == 32)) return 0;
+  if (lanes < 32) return (int64_t)lanes * 4 >= cols ? lanes : 0;
+  return lanes;
+}
+
+int launch_rowwise_warp_el(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                           float eps, float *y, float *mean, float *rstd, const float *gamma,
+                           const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                           const DevInfo &d) {
+  if (cols > (int64_t)32 * kRowWarpMaxElPerLane) return RR_ERR_INVALID;
+  int K = 4;
+  if (lanes == 32)
+    while ((int64_t)32 * K < cols) K *= 2;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: %s warp (element-wise) rows=%lld cols=%lld L=%d K=%d\n",
+                 mode == kModeSoftmax ? "softmax" : (mode == kModeStats ? "lnstats" : "layernorm"),
+                 (long long)rows, (long long)cols, lanes, K);
+  if (in_dtype == RR_BF16) {
+    switch (mode) {
+      case kModeSoftmax: return launch_mode_el<InBF16, kModeSoftmax>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      case kModeStats: return launch_mode_el<InBF16, kModeStats>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      default: return launch_mode_el<InBF16, kModeLayernorm>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    }
+  }
+  switch (mode) {
+    case kModeSoftmax: return launch_mode_el<InF32, kModeSoftmax>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case kModeStats: return launch_mode_el<InF32, kModeStats>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_mode_el<InF32, kModeLayernorm>(lanes, K, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
 }
 
 int launch_rowwise_warp(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,

@@ -679,7 +679,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
     return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
                                                    nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return launch_rowwise_warp(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -719,7 +719,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
     return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                  nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return launch_rowwise_warp(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                                nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -762,7 +762,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
     return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                      gamma, beta, y, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return launch_rowwise_warp(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -835,7 +835,7 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     return {RR_TIER_BLOCK, 1, st};
   }
   if (tier == RR_TIER_WARP) {
-    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : 0;
+    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : rowwise_warp_el_lanes(cols, C);
     return L ? RowPlan{RR_TIER_WARP, L, false} : RowPlan{-1, 0, false};
   }
   if (tier == RR_TIER_SPLITK) {
@@ -850,8 +850,8 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     const bool st = RR_ROW_STAGED_SPLITK && stage_fits(c);
     return {RR_TIER_SPLITK, c, st};
   }
-  if (vec && rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
-    const int L = rowwise_warp_lanes(nvec, 0, rewrite);
+  if (rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
+    const int L = vec ? rowwise_warp_lanes(nvec, 0, rewrite) : rowwise_warp_el_lanes(cols, 0);
     if (L) return {RR_TIER_WARP, L, false};
   }
   if (row_vecs > staged_min) {

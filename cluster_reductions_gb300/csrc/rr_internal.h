@@ -129,6 +129,17 @@ constexpr int kRowWarpTargetNV = 4;  // automatic L: about this many vectors per
 int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite);
 // Vectors per lane for nvec vectors over `lanes` lanes (a power of two).
 int rowwise_warp_nv(int64_t nvec, int lanes);
+// Element-wise form of the warp tier, for rows that are not aligned 16-byte
+// vectors, of up to 32 * kRowWarpMaxElPerLane elements.
+constexpr int kRowWarpMaxElPerLane = 32;
+// Lanes per row of the element-wise form: `lanes` if it can hold cols (a
+// power of two; below 32, 4 elements a lane), lanes == 0 picks one; 0 when
+// the row does not fit.
+int rowwise_warp_el_lanes(int64_t cols, int lanes);
+int launch_rowwise_warp_el(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                           float eps, float *y, float *mean, float *rstd, const float *gamma,
+                           const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                           const DevInfo &d);
 // mode 0 softmax (y), 1 statistics (mean, rstd), 2 layernorm (ybf; mean /
 // rstd optional).  The caller has checked the alignment: cols a multiple
 // of the 16-byte vector, x 16-byte aligned, y as the block tier's register

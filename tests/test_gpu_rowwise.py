@@ -308,6 +308,56 @@ def test_layernorm_warp_forced(rr, oracle_mod, dtype, L):
             assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd warp L={L} {rows}x{cols}")
 
 
+# Element-wise form of the warp tier: rows that are not aligned 16-byte
+# vectors (widths that are no vector multiple, misaligned bases), lane `sub`
+# of a segment holding elements k * L + sub.  Widths: 1, ragged ones, the
+# most an L-lane segment holds (4 L below 32 lanes; 1024 at 32 lanes), one
+# width per L with more rows than the persistent grid takes in one pass.
+def _el_widths(L):
+    top = 4 * L if L < 32 else 1024
+    w = {1, 3, top - 1, top} if L < 32 else {4 * 16 + 1, 127, 250, 513, 1000, 1023, 1024}
+    return sorted(c for c in w if c <= top)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("L", [1, 2, 4, 8, 16, 32])
+def test_rowwise_warp_elementwise_forced(rr, oracle_mod, dtype, L):
+    elt = 2 if dtype == torch.bfloat16 else 4
+    widths = _el_widths(L)
+    for i, cols in enumerate(widths):
+        for off in (1, 3):
+            rows_list = (_warp_rows(L, cols, elt) if (i == len(widths) - 2 and off == 1)
+                         else [7, 300])
+            for rows in rows_list:
+                x = _x(rows, cols, dtype, 2400 + 10 * L + i, 2.0, off)
+                idx = np.r_[0:min(rows, 24), max(rows - 24, 0):rows]
+                _check_all_row_ops(rr, oracle_mod, x, np.unique(idx),
+                                   expect_tier=(("warp", L), False), tier="warp", lanes_per_row=L)
+
+
+def test_rowwise_warp_elementwise_special(rr, oracle_mod):
+    # -inf over whole lanes (elements sub, sub + L, ... of a segment), over a
+    # row's first half and over a whole row; constant rows
+    for L, cols in ((16, 60), (32, 250), (32, 1023)):
+        x = _x(9, cols, torch.bfloat16, 2500 + cols, 3.0, 1)
+        x[:, 3::L] = float("-inf")
+        x[1, : cols // 2] = float("-inf")
+        x[3, :] = float("-inf")
+        y = to_np(rr.softmax(x, tier="warp", lanes_per_row=L))
+        assert rr.last_tier() == ("warp", L)
+        ref = oracle_mod.softmax(to_np(x))
+        live = [r for r in range(9) if r != 3]
+        assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what=f"softmax -inf el L={L}")
+        assert (y[:, 3::L] == 0).all() and (y[1, : cols // 2] == 0).all()
+        assert np.isnan(ref[3]).all() and (y[3] == 0).all()
+        c = torch.full((5, cols), -2.5, dtype=torch.bfloat16, device="cuda")
+        np.testing.assert_allclose(to_np(rr.softmax(c, tier="warp", lanes_per_row=L)), 1.0 / cols,
+                                   rtol=1e-6)
+        mean, rstd = rr.layernorm_stats(c, 1e-5, tier="warp", lanes_per_row=L)
+        assert (to_np(mean) == -2.5).all()
+        np.testing.assert_allclose(to_np(rstd), 1.0 / np.sqrt(1e-5), rtol=1e-5)
+
+
 def test_warp_rowwise_special_rows(rr, oracle_mod):
     # constant rows, alternating +-a, and -inf over whole lanes of a segment
     x = torch.full((5, 512), 3.25, dtype=torch.bfloat16, device="cuda")
@@ -359,12 +409,21 @@ def test_warp_rowwise_auto_and_unsupported(rr, oracle_mod):
     check_lnstats(rr, oracle_mod, xf[:200].contiguous())
     rr.softmax(x[:8])
     assert rr.last_tier() == ("block", 1)
-    for bad in (_x(8, 512, torch.bfloat16, 1402, 1.0, 1),      # x not 16-byte aligned
-                _x(8, 100, torch.bfloat16, 1403, 1.0),         # cols not a vector multiple
+    # rows that are not aligned vectors take the element-wise form, up to
+    # 1024 elements
+    for ok, lanes in ((_x(8, 512, torch.bfloat16, 1402, 1.0, 1), 32),   # x not 16-byte aligned
+                      (_x(8, 100, torch.bfloat16, 1403, 1.0), 32),      # not a vector multiple
+                      (_x(8, 30, torch.float32, 1407, 1.0, 1), 8)):
+        rr.softmax(ok, tier="warp")
+        assert rr.last_tier() == ("warp", lanes)
+    for bad in (_x(8, 1025, torch.bfloat16, 1408, 1.0),        # > 1024 elements
                 _x(8, 4096, torch.bfloat16, 1404, 1.0)):       # 512 vectors > 8 per lane
         with pytest.raises(rr.RRError) as e:
             rr.softmax(bad, tier="warp")
         assert e.value.status == 2
+    with pytest.raises(rr.RRError) as e:                        # 100 elements > 4 x 16
+        rr.softmax(_x(8, 100, torch.bfloat16, 1409, 1.0), tier="warp", lanes_per_row=16)
+    assert e.value.status == 2
     with pytest.raises(rr.RRError) as e:
         rr.softmax(_x(8, 1024, torch.bfloat16, 1405, 1.0), tier="warp", lanes_per_row=8)
     assert e.value.status == 2                                  # 128 vectors > 8 x 8
@@ -397,7 +456,10 @@ def test_rowwise_launch_matches_host_plan(rr):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for rows, cols, dt in [(4 * sms, 256, torch.bfloat16), (4 * sms - 1, 256, torch.bfloat16),
                            (8 * sms, 1024, torch.float32), (3000, 2048, torch.bfloat16),
-                           (2000, 4096, torch.bfloat16), (40000, 16, torch.bfloat16)]:
+                           (2000, 4096, torch.bfloat16), (40000, 16, torch.bfloat16),
+                           (40000, 100, torch.bfloat16), (40000, 21, torch.float32),
+                           (4 * sms, 1001, torch.bfloat16), (4 * sms - 1, 250, torch.bfloat16),
+                           (20000, 1025, torch.float32)]:
         x = _x(rows, cols, dt, 1600 + cols, 1.0)
         g, b = inputs.layernorm_params(cols, 1601, "cuda")
         for op, call in (("softmax", lambda: rr.softmax(x)),
