@@ -53,8 +53,9 @@ AXIS_WORKLOADS = [(1, 8192, 8192), (256, 1024, 256), (32768, 256, 8), (1, 1 << 2
 # Row reductions of medium width timed beside the step (fp32, 256 MiB each).
 MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
 # Softmax / layernorm rows of medium width timed beside the step (bf16,
-# 256 MiB each): the warp tier of the two-pass row operations.
-MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048)]
+# 256 MiB each): the warp tier of the two-pass row operations; 250-element
+# rows (500 bytes) are not 16-byte aligned and take its chunked form.
+MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048), (536870, 250)]
 # Long rows timed beside the step (256 MiB each): softmax / layernorm rows
 # staged in shared memory (a CTA per row; clusters of 8 for 256K-element
 # rows), and a few long fp32 rows per SM for the block reduce.
@@ -72,17 +73,17 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1084699648, "src": ["reduce.cu", "rr_device.cuh"],
+    "splitk_sum_f32": {"bytes": 1085457408, "src": ["reduce.cu", "rr_device.cuh"],
                       "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 568142848, "src": ["combine.cu", "rr_device.cuh"],
+    "combine_p8": {"bytes": 567352320, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "e448f964a6acd0c9", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 559733760, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "83e3d82653a6eb06", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271435264, "src": ["reduce.cu", "rr_device.cuh"],
+    "softmax_bf16": {"bytes": 559430656, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "7b18d6a245fd249c", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271280128, "src": ["reduce.cu", "rr_device.cuh"],
                      "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271461888, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "83e3d82653a6eb06", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 138032384, "src": ["reduce.cu", "rr_device.cuh"],
+    "layernorm_bf16": {"bytes": 271470592, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "7b18d6a245fd249c", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 138011136, "src": ["reduce.cu", "rr_device.cuh"],
                     "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
@@ -931,6 +932,8 @@ PROFILE_CASES = {
     "medium_softmax_131072x1024_bf16": ({"shape": (131072, 1024), "op": "softmax"}, "medium", 1.0),
     "medium_layernorm_131072x1024_bf16": ({"shape": (131072, 1024), "op": "layernorm"},
                                           "medium", 1.0),
+    "medium_layernorm_536870x250_bf16": ({"shape": (536870, 250), "op": "layernorm"},
+                                         "medium", 1.0),
     # long rows staged in shared memory, automatic plan
     "long_softmax_4096x32768_bf16": ({"shape": (4096, 32768), "op": "softmax"}, "medium", 1.0),
     "long_layernorm_2048x65536_bf16": ({"shape": (2048, 65536), "op": "layernorm"}, "medium", 1.0),

@@ -169,9 +169,6 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
   }
 }
 
-// CTAs of up to 8 warps, persistent over the rows.  With fewer rows than
-// 8 warps per SM take, the CTAs shrink (down to one warp) so that the warps
-// spread over every SM instead of filling a few.
 // Element-wise form, for rows that are not made of aligned 16-byte vectors
 // (a width that is not a multiple of 8 bf16 / 4 fp32 elements, or a
 // misaligned operand) of up to 32 * K elements: lane `sub` of a segment of L
@@ -179,6 +176,9 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
 // consecutive elements), with clamped, unconditional loads and the slots
 // past the row's end left out of every fold.  Reductions, outputs and the
 // per-element arithmetic as in the vector form; stores element by element.
+// For softmax rows of 16 or more elements a lane, the next row's elements
+// are loaded (as raw bf16 / fp32) before the current row is reduced and
+// written (measured: a loss for shorter rows and for the rewrite).
 template <class In, int MODE, int L, int K>
 __global__ void __launch_bounds__(kWarpRowMaxThreads)
 k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
@@ -190,15 +190,29 @@ k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, 
   const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
-  for (int64_t r0 = warp * RPW; r0 < rows; r0 += stride) {  // warp-uniform trip count
-    const int64_t row = r0 + seg;
-    const int64_t rc = row < rows ? row : rows - 1;
+  typename In::S raw[K];
+  auto fetch = [&](int64_t r) {
+    const int64_t rc = r < rows ? r : rows - 1;
     const typename In::S *xr = x + rc * (int64_t)cols;
-    float v[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int i = k * L + sub;
-      v[k] = In::load1(xr + (i < cols ? i : cols - 1));
+      raw[k] = __ldg(xr + (i < cols ? i : cols - 1));
+    }
+  };
+  constexpr bool PF = MODE == kModeSoftmax && K >= 16;
+  int64_t r0 = warp * RPW;
+  if constexpr (PF) {
+    if (r0 < rows) fetch(r0 + seg);
+  }
+  for (; r0 < rows; r0 += stride) {  // warp-uniform trip count
+    const int64_t row = r0 + seg;
+    if constexpr (!PF) fetch(row);
+    float v[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = In::cvt(raw[k]);
+    if constexpr (PF) {
+      if (r0 + stride < rows) fetch(r0 + stride + seg);
     }
     if constexpr (MODE == kModeSoftmax) {
       float m = -INFINITY;
@@ -268,6 +282,302 @@ k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, 
   }
 }
 
+// Chunked form, for the same rows when they span a few 16-byte chunks: a
+// row is split into its head (the elements before its first 16-byte
+// boundary, fewer than EPV), its whole aligned 16-byte chunks, and its tail
+// (the elements after the last whole chunk).  The whole chunks are spread
+// over the segment as the vectors of the vector form (lane `sub` holds
+// chunks k * L + sub) and come by 16-byte loads; lane `sub` holds head and
+// tail elements i * L + sub by element loads.  Every fold takes the chunks
+// in order, then the head, then the tail elements, each slot under a
+// predicate.  Whole chunks of the outputs go as vectors when the output
+// shares x's offset within a chunk (vst: 2 for 32-byte, 1 for 16-byte
+// stores), the rest element by element.  The rewrite reads gamma and beta
+// from a copy each CTA makes in shared memory (their offset within a chunk
+// follows the row's).
+// Shared-memory image of gamma and beta for the chunked rewrite: element j
+// at j + j / 8 (a pad word after every 8), so that the lanes of a segment,
+// reading the same slot of chunks 8 elements apart, hit distinct banks.
+__host__ __device__ constexpr int gb_pitch(int cols) { return cols + (cols >> 3) + 1; }
+__device__ __forceinline__ int gb_at(int j) { return j + (j >> 3); }
+
+template <class In, int MODE, int L, int NV>
+__global__ void __launch_bounds__(kWarpRowMaxThreads)
+k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+                  float *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd,
+                  const float *__restrict__ gamma, const float *__restrict__ beta,
+                  uint16_t *__restrict__ ybf, int hx, int vst) {
+  pdl_begin();
+  using S = typename In::S;
+  constexpr int EPV = In::EPV, RPW = 32 / L, HS = (EPV - 1 + L - 1) / L;
+  const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
+  extern __shared__ float sgb[];  // rewrite: gamma, then beta, at gb_at(j)
+  if constexpr (MODE == kModeLayernorm) {
+    const int pitch = gb_pitch(cols);
+    for (int j = threadIdx.x; j < cols; j += blockDim.x) {
+      sgb[gb_at(j)] = __ldg(gamma + j);
+      sgb[pitch + gb_at(j)] = __ldg(beta + j);
+    }
+    __syncthreads();
+  }
+  // head length of row r: the elements before its first 16-byte boundary
+  auto head_of = [&](int64_t r) {
+    const int lo = (int)((hx + r * (int64_t)cols) % EPV);
+    const int hh = lo ? EPV - lo : 0;
+    return hh < cols ? hh : cols;
+  };
+  uint4 raw[NV];
+  S rh[HS], rt[HS];
+  auto fetch = [&](int64_t r) {
+    const int64_t rc = r < rows ? r : rows - 1;
+    const S *xr = x + rc * (int64_t)cols;
+    const int hh = head_of(rc), nw = (cols - hh) / EPV, te = hh + nw * EPV;
+    const uint4 *wc = reinterpret_cast<const uint4 *>(xr + hh);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      raw[k] = (k * L + sub < nw) ? ld_stream_u4(wc + k * L + sub) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < HS; ++i) {
+      const int e = i * L + sub;
+      rh[i] = e < hh ? __ldg(xr + e) : S(0);
+      rt[i] = te + e < cols ? __ldg(xr + te + e) : S(0);
+    }
+  };
+  int64_t r0 = warp * RPW;
+  if (r0 < rows) fetch(r0 + seg);
+  for (; r0 < rows; r0 += stride) {  // warp-uniform trip count
+    const int64_t row = r0 + seg;
+    const int hh = head_of(row < rows ? row : rows - 1), nw = (cols - hh) / EPV;
+    const int te = hh + nw * EPV;
+    float v[NV][EPV], h[HS], t[HS];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) In::unpack(raw[k], v[k]);
+#pragma unroll
+    for (int i = 0; i < HS; ++i) { h[i] = In::cvt(rh[i]); t[i] = In::cvt(rt[i]); }
+    if (r0 + stride < rows) fetch(r0 + stride + seg);
+    auto whole = [&](int k) { return k * L + sub < nw; };
+    auto in_head = [&](int i) { return i * L + sub < hh; };
+    auto in_tail = [&](int i) { return te + i * L + sub < cols; };
+    if constexpr (MODE == kModeSoftmax) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+        if (whole(k)) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) m = fmaxf(m, v[k][e]);
+        }
+#pragma unroll
+      for (int i = 0; i < HS; ++i) {
+        if (in_head(i)) m = fmaxf(m, h[i]);
+        if (in_tail(i)) m = fmaxf(m, t[i]);
+      }
+      float s = 0.0f;
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          float sk = 0.0f;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float p = ex2_approx(fmaf(v[k][e], kLog2e, -mb));
+            v[k][e] = p;
+            sk += p;
+          }
+          if (whole(k)) s += sk;
+        }
+#pragma unroll
+        for (int i = 0; i < HS; ++i) {
+          h[i] = ex2_approx(fmaf(h[i], kLog2e, -mb));
+          t[i] = ex2_approx(fmaf(t[i], kLog2e, -mb));
+          if (in_head(i)) s += h[i];
+        }
+#pragma unroll
+        for (int i = 0; i < HS; ++i)
+          if (in_tail(i)) s += t[i];
+      } else {
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < HS; ++i) h[i] = t[i] = 0.0f;
+      }
+      float M = m, S_ = s;
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1)
+        ms_combine(M, S_, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S_, o));
+      const float f = (m == -INFINITY) ? 0.0f : ex2_approx((m - M) * kLog2e) * (1.0f / S_);
+      if (row < rows) {
+        float *yr = y + row * (int64_t)cols;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          if (!whole(k)) continue;
+          float *p = yr + hh + (k * L + sub) * EPV;
+          float o[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) o[e] = v[k][e] * f;
+          if constexpr (EPV == 8) {
+            if (vst == 2) {
+              st_stream_v8(p, o);
+              continue;
+            }
+          }
+          if (vst) {
+#pragma unroll
+            for (int e = 0; e < EPV; e += 4) st_stream_v4(p + e, o[e], o[e + 1], o[e + 2], o[e + 3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) p[e] = o[e];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < HS; ++i) {
+          if (in_head(i)) yr[i * L + sub] = h[i] * f;
+          if (in_tail(i)) yr[te + i * L + sub] = t[i] * f;
+        }
+      }
+    } else {
+      float s = 0.0f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        float sk = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) sk += v[k][e];
+        if (whole(k)) s += sk;
+      }
+#pragma unroll
+      for (int i = 0; i < HS; ++i)
+        if (in_head(i)) s += h[i];
+#pragma unroll
+      for (int i = 0; i < HS; ++i)
+        if (in_tail(i)) s += t[i];
+      const float mu = warp_allreduce<SumF32, L>(s) / (float)cols;
+      float qs = 0.0f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        float qk = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float dlt = v[k][e] - mu;
+          qk = fmaf(dlt, dlt, qk);
+        }
+        if (whole(k)) qs += qk;
+      }
+#pragma unroll
+      for (int i = 0; i < HS; ++i)
+        if (in_head(i)) {
+          const float dlt = h[i] - mu;
+          qs = fmaf(dlt, dlt, qs);
+        }
+#pragma unroll
+      for (int i = 0; i < HS; ++i)
+        if (in_tail(i)) {
+          const float dlt = t[i] - mu;
+          qs = fmaf(dlt, dlt, qs);
+        }
+      const float var = warp_allreduce<SumF32, L>(qs) * (1.0f / (float)cols);
+      const float rs = 1.0f / sqrtf(var + eps);
+      if (row < rows) {
+        if constexpr (MODE == kModeLayernorm) {
+          uint16_t *yr = ybf + row * (int64_t)cols;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            if (!whole(k)) continue;
+            const int j0 = hh + (k * L + sub) * EPV;
+            const float *sg = sgb, *sb = sgb + gb_pitch(cols);
+            float g[EPV], b[EPV];
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              g[e] = sg[gb_at(j0 + e)];
+              b[e] = sb[gb_at(j0 + e)];
+            }
+            uint32_t pk[EPV / 2];
+#pragma unroll
+            for (int e = 0; e < EPV; e += 2)
+              pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
+                                      fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
+            if (vst) {
+              if constexpr (EPV == 8) {
+                *reinterpret_cast<uint4 *>(yr + j0) =
+                    make_uint4(pk[0], pk[1 % (EPV / 2)], pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
+              } else {
+                *reinterpret_cast<uint2 *>(yr + j0) = make_uint2(pk[0], pk[1 % (EPV / 2)]);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < EPV; e += 2) {
+                yr[j0 + e] = (uint16_t)(pk[e / 2] & 0xffffu);
+                yr[j0 + e + 1] = (uint16_t)(pk[e / 2] >> 16);
+              }
+            }
+          }
+          auto put = [&](int j, float xv) {
+            const __nv_bfloat16 o = __float2bfloat16_rn(
+                fmaf((xv - mu) * rs, sgb[gb_at(j)], sgb[gb_pitch(cols) + gb_at(j)]));
+            yr[j] = *reinterpret_cast<const uint16_t *>(&o);
+          };
+#pragma unroll
+          for (int i = 0; i < HS; ++i) {
+            if (in_head(i)) put(i * L + sub, h[i]);
+            if (in_tail(i)) put(te + i * L + sub, t[i]);
+          }
+        }
+        if (sub == 0) {
+          if (mean) mean[row] = mu;
+          if (rstd) rstd[row] = rs;
+        }
+      }
+    }
+  }
+}
+
+// CTAs of up to 8 warps, persistent over the rows.  With fewer rows than
+// 8 warps per SM take, the CTAs shrink (down to one warp) so that the warps
+// spread over every SM instead of filling a few.
+template <class K>
+int warp_row_launch(K k, int rpw, int64_t rows, cudaStream_t s, const DevInfo &d,
+                    int *grid_out, int *threads_out, size_t smem = 0) {
+  const int64_t warps = (rows + rpw - 1) / rpw;
+  int wpb = kWarpRowMaxThreads / 32;
+  if (warps < (int64_t)wpb * d.sm_count) {
+    const int64_t w = warps / d.sm_count;
+    wpb = w < 1 ? 1 : (int)w;
+  }
+  const int threads = wpb * 32;
+  const int nb = occupancy_blocks((const void *)k, threads, smem, d.device);
+  const int64_t need = (warps + wpb - 1) / wpb;
+  const int64_t cap = (int64_t)(nb > 0 ? nb : 1) * d.sm_count;
+  *grid_out = (int)(need < cap ? need : cap);
+  *threads_out = threads;
+  return 0;
+}
+
+template <class In, int MODE, int L, int NV>
+int launch_ck(const void *x, int64_t rows, int64_t cols, float eps, float *y, float *mean,
+              float *rstd, const float *gamma, const float *beta, uint16_t *ybf, cudaStream_t s,
+              const DevInfo &d) {
+  auto k = k_rowwise_warp_ck<In, MODE, L, NV>;
+  constexpr int EPV = In::EPV;
+  const int hx = (int)(((uintptr_t)x / sizeof(typename In::S)) % EPV);
+  // the output shares x's offset within a chunk: whole chunks store as
+  // vectors (softmax of bf16: 32-byte stores when y is 32-byte aligned there)
+  int vst = 0;
+  if (MODE == kModeSoftmax) {
+    const uintptr_t yo = ((uintptr_t)y / 4 + 8 - (uintptr_t)hx) % 8;
+    vst = (EPV == 8 && yo == 0) ? 2 : (yo % 4 == 0 ? 1 : 0);
+  } else if (MODE == kModeLayernorm) {
+    vst = (((uintptr_t)ybf / 2) % EPV) == (uintptr_t)hx;
+  }
+  const size_t smem = MODE == kModeLayernorm ? 2 * sizeof(float) * gb_pitch((int)cols) : 0;
+  int grid, threads;
+  warp_row_launch(k, 32 / L, rows, s, d, &grid, &threads, smem);
+  return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), smem, s, 0,
+                                   (const typename In::S *)x, rows, (int)cols, eps, y, mean,
+                                   rstd, gamma, beta, ybf, hx, vst));
+}
+
 template <class In, int MODE, int L, int NV, bool EL = false>
 int launch_one(const void *x, int64_t rows, int64_t cols, float eps, float *y, float *mean,
                float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
@@ -276,18 +586,8 @@ int launch_one(const void *x, int64_t rows, int64_t cols, float eps, float *y, f
     if constexpr (EL) return k_rowwise_warp_el<In, MODE, L, NV>;
     else return k_rowwise_warp<In, MODE, L, NV>;
   }();
-  constexpr int RPW = 32 / L;
-  const int64_t warps = (rows + RPW - 1) / RPW;
-  int wpb = kWarpRowMaxThreads / 32;
-  if (warps < (int64_t)wpb * d.sm_count) {
-    const int64_t w = warps / d.sm_count;
-    wpb = w < 1 ? 1 : (int)w;
-  }
-  const int threads = wpb * 32;
-  const int nb = occupancy_blocks((const void *)k, threads, 0, d.device);
-  const int64_t need = (warps + wpb - 1) / wpb;
-  const int64_t cap = (int64_t)(nb > 0 ? nb : 1) * d.sm_count;
-  const int grid = (int)(need < cap ? need : cap);
+  int grid, threads;
+  warp_row_launch(k, 32 / L, rows, s, d, &grid, &threads);
   return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), 0, s, 0,
                                    (const typename In::S *)x, rows, (int)cols, eps, y, mean,
                                    rstd, gamma, beta, ybf));
@@ -344,6 +644,38 @@ int launch_mode_el(int L, int K, const void *x, int64_t rows, int64_t cols, floa
 #undef RR_EL
 }
 
+template <class In, int MODE, int L>
+int launch_ck_nv(int nv, const void *x, int64_t rows, int64_t cols, float eps, float *y,
+                 float *mean, float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
+                 cudaStream_t s, const DevInfo &d) {
+  switch (nv) {
+    case 1: return launch_ck<In, MODE, L, 1>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 2: return launch_ck<In, MODE, L, 2>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 4: return launch_ck<In, MODE, L, 4>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_ck<In, MODE, L, 8>(x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
+}
+
+template <class In, int MODE>
+int launch_mode_ck(int L, int nv, const void *x, int64_t rows, int64_t cols, float eps, float *y,
+                   float *mean, float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
+                   cudaStream_t s, const DevInfo &d) {
+  switch (L) {
+    case 1: return launch_ck_nv<In, MODE, 1>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 2: return launch_ck_nv<In, MODE, 2>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 4: return launch_ck_nv<In, MODE, 4>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 8: return launch_ck_nv<In, MODE, 8>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case 16: return launch_ck_nv<In, MODE, 16>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_ck_nv<In, MODE, 32>(nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
+}
+
+// the most whole 16-byte chunks a row holds (at least 1)
+inline int64_t chunks_max(int64_t cols, int in_dtype) {
+  const int64_t c = cols / (in_dtype == RR_BF16 ? 8 : 4);
+  return c > 0 ? c : 1;
+}
+
 }  // namespace
 
 int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite) {
@@ -379,6 +711,62 @@ int rowwise_warp_el_lanes(int64_t cols, int lanes) {
   if (!(lanes == 1 || lanes == 2 || lanes == 4 || lanes == 8 || lanes == 16 || lanes == 32)) return 0;
   if (lanes < 32) return (int64_t)lanes * 4 >= cols ? lanes : 0;
   return lanes;
+}
+
+// Rows that are not aligned vectors take the chunked form while their
+// chunks fit 32 lanes x 8 and the output (if any) shares x's offset within
+// a chunk, the layernorm rewrite from RR_WARP_CHUNK_MIN_COLS_LN columns on;
+// the element-wise form otherwise.
+#ifndef RR_WARP_CHUNK_MIN_COLS_LN
+#define RR_WARP_CHUNK_MIN_COLS_LN 32
+#endif
+static bool warp_mis_chunked(int64_t cols, int in_dtype, int mode, bool out_vec) {
+  if (chunks_max(cols, in_dtype) > (int64_t)32 * kRowWarpMaxNV) return false;
+  if (mode == kModeStats) return true;
+  return out_vec && (mode == kModeSoftmax || cols >= RR_WARP_CHUNK_MIN_COLS_LN);
+}
+
+bool rowwise_warp_out_vec(int mode, int in_dtype, const void *x, const void *out) {
+  const uintptr_t elt = in_dtype == RR_BF16 ? 2 : 4, epv = 16 / elt;
+  const uintptr_t hx = ((uintptr_t)x / elt) % epv;
+  if (mode == kModeSoftmax) return ((uintptr_t)out / 4 + 8 - hx) % 4 == 0;
+  if (mode == kModeLayernorm) return ((uintptr_t)out / 2) % epv == hx;
+  return true;
+}
+
+int rowwise_warp_mis_lanes(int64_t cols, int in_dtype, int mode, bool out_vec, int lanes) {
+  if (cols < 1) return 0;
+  if (warp_mis_chunked(cols, in_dtype, mode, out_vec))
+    return rowwise_warp_lanes(chunks_max(cols, in_dtype), lanes, mode == kModeLayernorm);
+  return rowwise_warp_el_lanes(cols, lanes);
+}
+
+int launch_rowwise_warp_mis(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                            float eps, float *y, float *mean, float *rstd, const float *gamma,
+                            const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                            const DevInfo &d) {
+  const bool ov = rowwise_warp_out_vec(mode, in_dtype, x, mode == kModeSoftmax ? (const void *)y
+                                                                               : (const void *)ybf);
+  if (!warp_mis_chunked(cols, in_dtype, mode, ov))
+    return launch_rowwise_warp_el(mode, in_dtype, x, rows, cols, eps, y, mean, rstd, gamma, beta,
+                                  ybf, lanes, s, d);
+  const int nv = rowwise_warp_nv(chunks_max(cols, in_dtype), lanes);
+  if (log_enabled())
+    std::fprintf(stderr, "rr: %s warp (chunked) rows=%lld cols=%lld L=%d NV=%d\n",
+                 mode == kModeSoftmax ? "softmax" : (mode == kModeStats ? "lnstats" : "layernorm"),
+                 (long long)rows, (long long)cols, lanes, nv);
+  if (in_dtype == RR_BF16) {
+    switch (mode) {
+      case kModeSoftmax: return launch_mode_ck<InBF16, kModeSoftmax>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      case kModeStats: return launch_mode_ck<InBF16, kModeStats>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+      default: return launch_mode_ck<InBF16, kModeLayernorm>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    }
+  }
+  switch (mode) {
+    case kModeSoftmax: return launch_mode_ck<InF32, kModeSoftmax>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    case kModeStats: return launch_mode_ck<InF32, kModeStats>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+    default: return launch_mode_ck<InF32, kModeLayernorm>(lanes, nv, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, s, d);
+  }
 }
 
 int launch_rowwise_warp_el(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,

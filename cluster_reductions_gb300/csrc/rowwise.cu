@@ -654,10 +654,11 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
 // cluster: RR_MAX_CLUSTER caps it, no cluster launch makes it 1).
 template <class In>
 inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int tier, int C,
-                            const DevInfo &d, int mode) {
+                            const DevInfo &d, int mode, const void *x, const void *out) {
   const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
-  return plan_rowwise(rows, cols, In::EPV == 8 ? RR_BF16 : RR_F32, vec, mode, tier, C,
-                      d.sm_count, d.cluster_launch ? cap : 1);
+  const int dt = In::EPV == 8 ? RR_BF16 : RR_F32;
+  return plan_rowwise(rows, cols, dt, vec, mode, tier, C, d.sm_count, d.cluster_launch ? cap : 1,
+                      rowwise_warp_out_vec(mode, dt, x, out));
 }
 
 template <class In>
@@ -669,7 +670,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ax % 16 == 0 &&
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
@@ -679,7 +680,7 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
     return launch_rowwise_splitk<In, kModeSoftmax>(xv, rows, cols, 0.0f, y, nullptr, nullptr,
                                                    nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -709,7 +710,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
@@ -719,7 +720,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
     return launch_rowwise_splitk<In, kModeStats>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                  nullptr, nullptr, nullptr, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                                nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -752,7 +753,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
                    ((uintptr_t)y % (2 * In::EPV) == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm);
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.staged)
@@ -762,7 +763,7 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
     return launch_rowwise_splitk<In, kModeLayernorm>(xv, rows, cols, eps, nullptr, mean, rstd,
                                                      gamma, beta, y, pk.width, s, d);
   if (pk.tier == RR_TIER_WARP)
-    return (vec ? launch_rowwise_warp : launch_rowwise_warp_el)(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+    return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
   if (reg) {
@@ -818,7 +819,7 @@ constexpr int64_t kRowStagedMinVecMis[3] = {32, 1024, 2048};
 #endif
 
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster) {
+                     int C, int sm_count, int max_cluster, bool out_vec) {
   const bool rewrite = mode == kModeLayernorm;
   const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
   const int64_t nvec = vec ? cols * elt / 16 : 0;
@@ -835,7 +836,8 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     return {RR_TIER_BLOCK, 1, st};
   }
   if (tier == RR_TIER_WARP) {
-    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite) : rowwise_warp_el_lanes(cols, C);
+    const int L = vec ? rowwise_warp_lanes(nvec, C, rewrite)
+                      : rowwise_warp_mis_lanes(cols, in_dtype, mode, out_vec, C);
     return L ? RowPlan{RR_TIER_WARP, L, false} : RowPlan{-1, 0, false};
   }
   if (tier == RR_TIER_SPLITK) {
@@ -851,7 +853,8 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     return {RR_TIER_SPLITK, c, st};
   }
   if (rows >= (int64_t)warp_min_rows_per_sm * sm_count) {
-    const int L = vec ? rowwise_warp_lanes(nvec, 0, rewrite) : rowwise_warp_el_lanes(cols, 0);
+    const int L = vec ? rowwise_warp_lanes(nvec, 0, rewrite)
+                      : rowwise_warp_mis_lanes(cols, in_dtype, mode, out_vec, 0);
     if (L) return {RR_TIER_WARP, L, false};
   }
   if (row_vecs > staged_min) {

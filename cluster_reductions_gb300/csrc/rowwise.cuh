@@ -35,6 +35,7 @@ struct InBF16 {
   static __device__ __forceinline__ float load1(const S *p) {
     return __uint_as_float(((uint32_t)__ldg(p)) << 16);
   }
+  static __device__ __forceinline__ float cvt(S r) { return __uint_as_float(((uint32_t)r) << 16); }
 };
 struct InF32 {
   using S = float;
@@ -44,6 +45,7 @@ struct InF32 {
     o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
   }
   static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
+  static __device__ __forceinline__ float cvt(S r) { return r; }
 };
 
 // ---------------------------------------------------------------------------

@@ -92,8 +92,10 @@ struct RowPlan {
 // register forms' alignment; `mode`: 0 softmax, 1 layernorm statistics, 2
 // layernorm rewrite.  A forced split-K cluster larger than max_cluster
 // cannot run.
+// out_vec: for rows that are not aligned vectors, whether the output shares
+// x's offset within a 16-byte chunk (true for 16-byte aligned bases).
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster);
+                     int C, int sm_count, int max_cluster, bool out_vec = true);
 // Vectors per row up to which the block tier holds the row in registers
 // (256 threads x 8 vectors).
 constexpr int64_t kRowRegMaxVec = 2048;
@@ -129,12 +131,21 @@ constexpr int kRowWarpTargetNV = 4;  // automatic L: about this many vectors per
 int rowwise_warp_lanes(int64_t nvec, int lanes, bool rewrite);
 // Vectors per lane for nvec vectors over `lanes` lanes (a power of two).
 int rowwise_warp_nv(int64_t nvec, int lanes);
-// Element-wise form of the warp tier, for rows that are not aligned 16-byte
-// vectors, of up to 32 * kRowWarpMaxElPerLane elements.
+// Warp tier for rows that are not aligned 16-byte vectors: a chunked form
+// (the aligned 16-byte chunks covering the row, spread over the lanes as in
+// the vector form) and, for the narrowest rows, an element-wise form of up
+// to 32 * kRowWarpMaxElPerLane elements.
 constexpr int kRowWarpMaxElPerLane = 32;
-// Lanes per row of the element-wise form: `lanes` if it can hold cols (a
-// power of two; below 32, 4 elements a lane), lanes == 0 picks one; 0 when
-// the row does not fit.
+// Lanes per row of that tier: `lanes` if it can hold the row (a power of
+// two), lanes == 0 picks one; 0 when the row does not fit.  out_vec: the
+// output shares x's offset within a 16-byte chunk (rowwise_warp_out_vec).
+int rowwise_warp_mis_lanes(int64_t cols, int in_dtype, int mode, bool out_vec, int lanes);
+bool rowwise_warp_out_vec(int mode, int in_dtype, const void *x, const void *out);
+int launch_rowwise_warp_mis(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                            float eps, float *y, float *mean, float *rstd, const float *gamma,
+                            const float *beta, uint16_t *ybf, int lanes, cudaStream_t s,
+                            const DevInfo &d);
+// The element-wise form alone (lanes and launch).
 int rowwise_warp_el_lanes(int64_t cols, int lanes);
 int launch_rowwise_warp_el(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
                            float eps, float *y, float *mean, float *rstd, const float *gamma,

@@ -283,15 +283,25 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * Warp tier: lane j of a row's segment holds the row's 16-byte vectors j,
  * j + L, j + 2L, ... (at most 8 per lane, so rows of up to 256 vectors:
  * 2048 bf16 or 1024 fp32 elements); both reductions of a row are shuffles
- * inside the segment.  It needs cols a multiple of 8 (bf16) or 4 (fp32), x
- * 16-byte aligned, the softmax output 32-byte (bf16 input) or 16-byte
- * (fp32) aligned, and for the layernorm gamma / beta 16-byte and the output
- * 16-byte (bf16 input) or 8-byte (fp32) aligned; a forced warp tier
- * returns RR_ERR_UNSUPPORTED when these do not hold or the row does not fit
- * lanes_per_row lanes.  AUTO picks it for rows that fit when there are at
- * least 4 rows per SM (8 for rr_layernorm), with about 4 vectors per lane
- * (2 for rows of up to 8 vectors and for rr_layernorm; a lane per row for
- * rows of up to 2).
+ * inside the segment.  This vector form needs cols a multiple of 8 (bf16)
+ * or 4 (fp32), x 16-byte aligned, the softmax output 32-byte (bf16 input)
+ * or 16-byte (fp32) aligned, and for the layernorm gamma / beta 16-byte and
+ * the output 16-byte (bf16 input) or 8-byte (fp32) aligned.  Other rows
+ * take a chunked form: a row's whole aligned 16-byte chunks spread over the
+ * lanes the same way (at most 256 chunks: 2055 bf16 / 1027 fp32 elements),
+ * its head and tail elements (before its first, after its last 16-byte
+ * boundary) held by the lanes one by one; gamma / beta of the rewrite are
+ * copied into shared memory.  Softmax and the rewrite take it when their
+ * output sits at x's offset within a 16-byte chunk (always so for 16-byte
+ * aligned bases), the rewrite from 32 elements on; otherwise an
+ * element-wise form, lane j holding elements j, j + L, ... (4 per lane
+ * below 32 lanes, up to 1024 elements).  A forced warp tier returns
+ * RR_ERR_UNSUPPORTED when the row does not fit lanes_per_row lanes (or any
+ * form).  AUTO picks it for rows that fit when there are at least 4 rows
+ * per SM (8 for rr_layernorm), with about 4 vectors or chunks per lane (2
+ * for rows of up to 8 and for rr_layernorm; a lane per row for rows of up
+ * to 2).  The statistics of rr_layernorm and rr_layernorm_stats on the same
+ * x are bitwise equal when both take the same form and lanes.
  * Split-K: CTA r owns slice r of the row, and the row takes two cluster
  * combines ([CA]) on two slots without a tail sync between them: softmax
  * combines the CTA maxima, then the CTA sums rescaled to the row max (one
@@ -308,9 +318,10 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * whose slices do, each CTA staging its slice (reported as the split-K tier
  * of that cluster size); the statistics stage only up to clusters of 4.
  * Rows that are not 16-byte aligned (a width that is not a vector multiple,
- * or a misaligned operand) are staged too, beyond 32 vectors for softmax,
- * 1024 for the statistics, 2048 for rr_layernorm, with their partial first
- * and last 16-byte chunks loaded element by element.
+ * or a misaligned operand) and too few or too long for the warp tier are
+ * staged too, beyond 32 vectors for softmax, 1024 for the statistics, 2048
+ * for rr_layernorm, with their partial first and last 16-byte chunks loaded
+ * element by element.
  * Long rows that are not staged take split-K over global memory with
  * slices of at most 128 KiB.  A forced block tier stages when it applies; a
  * forced split-K tier reads from global memory.
@@ -507,7 +518,9 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * device with `sm_count` SMs whose largest co-schedulable cluster is
  * `max_cluster` CTAs.  `aligned` != 0 says every operand meets the warp
  * tier's alignment (rr_rowwise_opts); cols must also be a multiple of the
- * 16-byte vector.  Writes the tier and its width: lanes per row (warp),
+ * 16-byte vector.  Rows that are not are planned for operands whose bases
+ * are 16-byte aligned (the outputs then share x's offset within a chunk).
+ * Writes the tier and its width: lanes per row (warp),
  * cluster size (split-K) or 1 (block); *staged_out (if not NULL) 1 when the
  * block / split-K tier stages the rows in shared memory.  Touches no GPU.
  * RR_ERR_INVALID on negative sizes, sm_count or max_cluster < 1, a bad dtype

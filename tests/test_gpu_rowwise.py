@@ -308,11 +308,15 @@ def test_layernorm_warp_forced(rr, oracle_mod, dtype, L):
             assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd warp L={L} {rows}x{cols}")
 
 
-# Element-wise form of the warp tier: rows that are not aligned 16-byte
-# vectors (widths that are no vector multiple, misaligned bases), lane `sub`
-# of a segment holding elements k * L + sub.  Widths: 1, ragged ones, the
-# most an L-lane segment holds (4 L below 32 lanes; 1024 at 32 lanes), one
-# width per L with more rows than the persistent grid takes in one pass.
+# Warp tier for rows that are not aligned 16-byte vectors (widths that are no
+# vector multiple, misaligned bases): the chunked form (a row's whole
+# 16-byte chunks over the lanes, head and tail elements apart) and the
+# element-wise form (lane `sub` holding elements k * L + sub).  x at offset
+# 0 gives outputs that share its offset within a chunk (chunked softmax and
+# rewrite), offsets 1 and 3 outputs that do not (element-wise softmax and
+# rewrite); the statistics are chunked throughout.  Widths: 1, ragged ones,
+# the most an L-lane segment holds (4 L below 32 lanes; 1024 at 32 lanes),
+# one width per L with more rows than the persistent grid takes in one pass.
 def _el_widths(L):
     top = 4 * L if L < 32 else 1024
     w = {1, 3, top - 1, top} if L < 32 else {4 * 16 + 1, 127, 250, 513, 1000, 1023, 1024}
@@ -325,14 +329,50 @@ def test_rowwise_warp_elementwise_forced(rr, oracle_mod, dtype, L):
     elt = 2 if dtype == torch.bfloat16 else 4
     widths = _el_widths(L)
     for i, cols in enumerate(widths):
-        for off in (1, 3):
-            rows_list = (_warp_rows(L, cols, elt) if (i == len(widths) - 2 and off == 1)
+        for off in (0, 1, 3):
+            rows_list = (_warp_rows(L, cols, elt) if (i == len(widths) - 2 and off < 2)
                          else [7, 300])
             for rows in rows_list:
                 x = _x(rows, cols, dtype, 2400 + 10 * L + i, 2.0, off)
                 idx = np.r_[0:min(rows, 24), max(rows - 24, 0):rows]
                 _check_all_row_ops(rr, oracle_mod, x, np.unique(idx),
-                                   expect_tier=(("warp", L), False), tier="warp", lanes_per_row=L)
+                                   expect_tier=(("warp", L), False), stats_bitwise=False,
+                                   tier="warp", lanes_per_row=L)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_rowwise_warp_misaligned_operand_offsets(rr, oracle_mod, dtype):
+    # outputs, gamma and beta each at their own offset within a 16-byte
+    # chunk, matching x's or not (vector or element stores; shifted or
+    # element loads of gamma / beta); x at every element offset
+    from _util import assert_layernorm_close
+    from cluster_reductions_gb300 import inputs
+    epv = 8 if dtype == torch.bfloat16 else 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = 8 * sms + 5
+    for i, (cols, xo) in enumerate([(250, 1), (301, 2), (97, epv - 1), (1001, 0), (40, 3)]):
+        x = _x(rows, cols, dtype, 2600 + i, 2.0, xo % epv)
+        idx = np.r_[0:6, rows // 2, rows - 6:rows]
+        xs = x[torch.from_numpy(idx).cuda()]
+        ref = oracle_mod.softmax(to_np(xs))
+        for yo in (0, 1, 2, 3):
+            y = torch.empty(rows * cols + yo, device="cuda")[yo:].view(rows, cols)
+            rr.softmax(x, out=y)
+            assert rr.last_tier()[0] == "warp", (cols, xo, rr.last_tier())
+            assert_rel_close(to_np(y)[idx], ref, 1e-5, floor=1e-30, what=f"softmax {cols} x+{xo} y+{yo}")
+        g0, b0 = inputs.layernorm_params(cols + 8, 2650 + i, "cuda")
+        for go, bo, oo in ((0, 0, 0), (1, 3, 1), (2, 1, 5), (3, 2, 7)):
+            g, b = g0[go:go + cols], b0[bo:bo + cols]
+            yb = torch.empty(rows * cols + oo, dtype=torch.bfloat16, device="cuda")[oo:].view(rows, cols)
+            mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+            rr.layernorm(x, g, b, 1e-5, out=yb, mean=mean, rstd=rstd)
+            assert rr.last_tier()[0] == "warp"
+            y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
+            xf = xs.to(torch.float64).cpu().numpy()
+            assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_)
+            bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+            assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
+            assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {cols} x+{xo} out+{oo}")
 
 
 def test_rowwise_warp_elementwise_special(rr, oracle_mod):
@@ -409,20 +449,26 @@ def test_warp_rowwise_auto_and_unsupported(rr, oracle_mod):
     check_lnstats(rr, oracle_mod, xf[:200].contiguous())
     rr.softmax(x[:8])
     assert rr.last_tier() == ("block", 1)
-    # rows that are not aligned vectors take the element-wise form, up to
-    # 1024 elements
+    # rows that are not aligned vectors take the chunked or element-wise
+    # form: with 16-byte aligned bases the lanes the host plan gives many
+    # such rows, with x misaligned (the output then not sharing its offset)
+    # the element-wise form's
+    for ok in (_x(8, 100, torch.bfloat16, 1403, 1.0), _x(8, 30, torch.float32, 1407, 1.0),
+               _x(8, 3, torch.bfloat16, 1410, 1.0)):
+        rr.softmax(ok, tier="warp")
+        assert rr.last_tier() == rr.plan_rowwise(1 << 20, ok.shape[1], "softmax", 152, 16,
+                                                 dtype=ok.dtype, aligned=False)
     for ok, lanes in ((_x(8, 512, torch.bfloat16, 1402, 1.0, 1), 32),   # x not 16-byte aligned
-                      (_x(8, 100, torch.bfloat16, 1403, 1.0), 32),      # not a vector multiple
                       (_x(8, 30, torch.float32, 1407, 1.0, 1), 8)):
         rr.softmax(ok, tier="warp")
         assert rr.last_tier() == ("warp", lanes)
-    for bad in (_x(8, 1025, torch.bfloat16, 1408, 1.0),        # > 1024 elements
+    for bad in (_x(8, 4000, torch.bfloat16, 1408, 1.0, 1),     # 501 chunks > 8 per lane
                 _x(8, 4096, torch.bfloat16, 1404, 1.0)):       # 512 vectors > 8 per lane
         with pytest.raises(rr.RRError) as e:
             rr.softmax(bad, tier="warp")
         assert e.value.status == 2
-    with pytest.raises(rr.RRError) as e:                        # 100 elements > 4 x 16
-        rr.softmax(_x(8, 100, torch.bfloat16, 1409, 1.0), tier="warp", lanes_per_row=16)
+    with pytest.raises(rr.RRError) as e:                        # 14 chunks > 8 x 1
+        rr.softmax(_x(8, 100, torch.bfloat16, 1409, 1.0), tier="warp", lanes_per_row=1)
     assert e.value.status == 2
     with pytest.raises(rr.RRError) as e:
         rr.softmax(_x(8, 1024, torch.bfloat16, 1405, 1.0), tier="warp", lanes_per_row=8)
@@ -476,7 +522,7 @@ def test_rowwise_launch_matches_host_plan(rr):
 # prefetch); widths give a CTA per row, clusters of 2 and 4, ragged last
 # slices and, for fp32, 4-element tails.
 # ---------------------------------------------------------------------------
-def _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=None, **kw):
+def _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=None, stats_bitwise=True, **kw):
     from cluster_reductions_gb300 import inputs
     from _util import assert_layernorm_close
     rows, cols = x.shape
@@ -494,14 +540,17 @@ def _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=None, **kw):
     mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
     yb = rr.layernorm(x, g, b, 1e-5, mean=mean, rstd=rstd, **kw)
     m2, r2 = rr.layernorm_stats(x, 1e-5, **kw)
-    assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
-    assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
+    if stats_bitwise:
+        assert torch.equal(mean.view(torch.int32), m2.view(torch.int32))
+        assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
     y64, y16, rm, rr_ = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
     xf = xs.to(torch.float64).cpu().numpy()
     assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_)
     bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
     assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
     assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {rows}x{cols}")
+    assert (np.abs(to_np(m2)[idx].astype(np.float64) - rm) <= bound).all()
+    assert_rel_close(to_np(r2)[idx], rr_, 1e-5, what=f"stats rstd {rows}x{cols}")
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])

@@ -157,20 +157,24 @@ def test_tier_dispatch(lib, rows, cols, sms, maxc, expect):
     (1215, 256, "layernorm", "bf16", True, 16, ("block", 1)),
     (1216, 256, "layernorm", "bf16", True, 16, ("warp", 16)),
     # alignment: operands or a width that is not a vector multiple take the
-    # element-wise warp form (4 elements a lane below 32 lanes) up to 1024
-    # elements
-    (1 << 20, 128, "softmax", "bf16", False, 16, ("warp", 32)),
-    (1 << 20, 100, "softmax", "bf16", True, 16, ("warp", 32)),
-    (1 << 20, 6, "lnstats", "f32", True, 16, ("warp", 2)),
-    (1 << 20, 64, "layernorm", "bf16", False, 16, ("warp", 16)),
-    (1 << 20, 65, "layernorm", "bf16", False, 16, ("warp", 32)),
+    # chunked warp form (whole 16-byte chunks over the lanes as vectors, the
+    # rewrite at 2 a lane) up to 256 chunks, the rewrite's rows of under 32
+    # elements the element-wise form (4 elements a lane below 32 lanes)
+    (1 << 20, 128, "softmax", "bf16", False, 16, ("warp", 4)),
+    (1 << 20, 100, "softmax", "bf16", True, 16, ("warp", 4)),
+    (1 << 20, 6, "lnstats", "f32", True, 16, ("warp", 1)),
+    (1 << 20, 64, "layernorm", "bf16", False, 16, ("warp", 4)),
+    (1 << 20, 65, "layernorm", "bf16", False, 16, ("warp", 4)),
+    (1 << 20, 250, "layernorm", "bf16", False, 16, ("warp", 16)),
+    (1 << 20, 20, "layernorm", "bf16", False, 16, ("warp", 8)),
     (1 << 20, 1, "softmax", "f32", False, 16, ("warp", 1)),
-    (1 << 20, 1024, "lnstats", "f32", False, 16, ("warp", 32)),
-    (1 << 20, 1025, "lnstats", "f32", False, 16, ("block", 1)),
+    (1 << 20, 1025, "lnstats", "f32", False, 16, ("warp", 32)),
+    (1 << 20, 2055, "lnstats", "bf16", False, 16, ("warp", 32)),
+    (1 << 20, 2057, "lnstats", "bf16", False, 16, ("block", 1)),
     (607, 100, "softmax", "bf16", True, 16, ("block", 1)),
-    (608, 100, "softmax", "bf16", True, 16, ("warp", 32)),
+    (608, 100, "softmax", "bf16", True, 16, ("warp", 4)),
     (1215, 100, "layernorm", "bf16", True, 16, ("block", 1)),
-    (1216, 100, "layernorm", "bf16", True, 16, ("warp", 32)),
+    (1216, 100, "layernorm", "bf16", True, 16, ("warp", 8)),
 ])
 def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     import torch
