@@ -295,11 +295,12 @@ k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, 
 // stores), the rest element by element.  The rewrite reads gamma and beta
 // from a copy each CTA makes in shared memory (their offset within a chunk
 // follows the row's).
-// Shared-memory image of gamma and beta for the chunked rewrite: element j
-// at j + j / 8 (a pad word after every 8), so that the lanes of a segment,
-// reading the same slot of chunks 8 elements apart, hit distinct banks.
-__host__ __device__ constexpr int gb_pitch(int cols) { return cols + (cols >> 3) + 1; }
-__device__ __forceinline__ int gb_at(int j) { return j + (j >> 3); }
+// Shared-memory image of gamma and beta for the chunked rewrite: the pair
+// (gamma[j], beta[j]) at slot j + j / EPV (a pad slot after every EPV), so
+// that the lanes of a half-warp, reading the same element of chunks EPV
+// apart with 8-byte loads, hit distinct banks.  Whole chunk t of a row with
+// head hh takes its element e from slot (EPV + 1) t + hh + e + [hh + e >= EPV].
+__host__ __device__ constexpr int gb_slots(int cols, int epv) { return cols + cols / epv + 1; }
 
 template <class In, int MODE, int L, int NV>
 __global__ void __launch_bounds__(kWarpRowMaxThreads)
@@ -313,13 +314,10 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
   const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
-  extern __shared__ float sgb[];  // rewrite: gamma, then beta, at gb_at(j)
+  extern __shared__ float2 sgb[];  // rewrite: (gamma, beta) pairs, padded
   if constexpr (MODE == kModeLayernorm) {
-    const int pitch = gb_pitch(cols);
-    for (int j = threadIdx.x; j < cols; j += blockDim.x) {
-      sgb[gb_at(j)] = __ldg(gamma + j);
-      sgb[pitch + gb_at(j)] = __ldg(beta + j);
-    }
+    for (int j = threadIdx.x; j < cols; j += blockDim.x)
+      sgb[j + j / EPV] = make_float2(__ldg(gamma + j), __ldg(beta + j));
     __syncthreads();
   }
   // head length of row r: the elements before its first 16-byte boundary
@@ -482,16 +480,20 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
       if (row < rows) {
         if constexpr (MODE == kModeLayernorm) {
           uint16_t *yr = ybf + row * (int64_t)cols;
+          int de[EPV];  // slot of element e of a whole chunk, past the chunk's base
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) de[e] = hh + e + (hh + e >= EPV ? 1 : 0);
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             if (!whole(k)) continue;
             const int j0 = hh + (k * L + sub) * EPV;
-            const float *sg = sgb, *sb = sgb + gb_pitch(cols);
+            const float2 *q = sgb + (EPV + 1) * (k * L + sub);
             float g[EPV], b[EPV];
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-              g[e] = sg[gb_at(j0 + e)];
-              b[e] = sb[gb_at(j0 + e)];
+              const float2 gb = q[de[e]];
+              g[e] = gb.x;
+              b[e] = gb.y;
             }
             uint32_t pk[EPV / 2];
 #pragma unroll
@@ -514,8 +516,8 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
             }
           }
           auto put = [&](int j, float xv) {
-            const __nv_bfloat16 o = __float2bfloat16_rn(
-                fmaf((xv - mu) * rs, sgb[gb_at(j)], sgb[gb_pitch(cols) + gb_at(j)]));
+            const float2 gb = sgb[j + j / EPV];
+            const __nv_bfloat16 o = __float2bfloat16_rn(fmaf((xv - mu) * rs, gb.x, gb.y));
             yr[j] = *reinterpret_cast<const uint16_t *>(&o);
           };
 #pragma unroll
@@ -570,7 +572,7 @@ int launch_ck(const void *x, int64_t rows, int64_t cols, float eps, float *y, fl
   } else if (MODE == kModeLayernorm) {
     vst = (((uintptr_t)ybf / 2) % EPV) == (uintptr_t)hx;
   }
-  const size_t smem = MODE == kModeLayernorm ? 2 * sizeof(float) * gb_pitch((int)cols) : 0;
+  const size_t smem = MODE == kModeLayernorm ? sizeof(float2) * gb_slots((int)cols, EPV) : 0;
   int grid, threads;
   warp_row_launch(k, 32 / L, rows, s, d, &grid, &threads, smem);
   return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), smem, s, 0,
