@@ -7,14 +7,21 @@
 // A segment of L lanes of a warp owns a row (32 / L rows per warp at a
 // time; L = 1 is a thread per row) and holds it in registers: lane `sub` of
 // the segment holds vectors k * L + sub, k < NV, so each load instruction of
-// the segment covers L * 16 contiguous bytes.  Both reductions of a row are xor butterflies inside the
-// segment -- no shared memory and no barrier -- and the next row's raw
-// vectors are loaded before the current row is reduced and written, so a
-// lane keeps up to 2 * NV 16-byte loads in flight.  Vector indices past the
-// row end are clamped to the row's last vector (loaded, then left out of
-// every fold); a segment past the last row re-reads the last row and writes
-// nothing.  So every load is unconditional and every lane takes part in
-// every shuffle.
+// the segment covers L * 16 contiguous bytes.  Both reductions of a row are
+// xor butterflies inside the segment -- no shared memory and no barrier --
+// and the next row's raw vectors are loaded before the current row is
+// reduced and written, so a lane keeps up to 2 * NV 16-byte loads in flight.
+// Vector indices past the row end are clamped to the row's last vector
+// (loaded, then left out of every fold); a segment past the last row
+// re-reads the last row and writes nothing.  So every load is unconditional
+// and every lane takes part in every shuffle.
+//
+// Rows that are not aligned 16-byte vectors (a width that is not a multiple
+// of 8 bf16 / 4 fp32 elements, or a misaligned base) take a chunked form --
+// the row's whole aligned 16-byte chunks spread over the segment like the
+// vectors, its head and tail elements held one by one -- or, for outputs
+// that do not sit at x's offset within a chunk and for the rewrite's
+// narrowest rows, an element-wise form.
 #include <cstdio>
 
 #include "rr.h"
