@@ -258,6 +258,16 @@ def kernel_src_sha(files=None) -> str:
     return h.hexdigest()[:16]
 
 
+def ncu_traffic(name: str):
+    """The NCU_TRAFFIC entry of operation `name` while its kernel sources
+    still hash to the captured `src_sha`; None when there is none or the
+    kernel has changed since the counters were taken."""
+    tr = NCU_TRAFFIC.get(name)
+    if tr and tr.get("src_sha") == kernel_src_sha(tr.get("src")):
+        return tr
+    return None
+
+
 def dist_setup(n_gpus):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -528,8 +538,8 @@ def bench_ours(args):
     dname, _, dspec, _, _ = data[dom]
     dbytes = sum(algorithmic_bytes(dspec))
     achieved = dbytes / (dom_ms / 1e3) / 1e9
-    tr = NCU_TRAFFIC.get(dname)
-    traffic = tr["bytes"] if (tr and tr.get("src_sha") == kernel_src_sha(tr.get("src"))) else None
+    tr = ncu_traffic(dname)
+    traffic = tr["bytes"] if tr else None
     roofline = {"bound": "hbm", "kernel": dname, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
