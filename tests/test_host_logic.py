@@ -218,6 +218,23 @@ def test_rowwise_staged_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expe
                            staged=True) == expect
 
 
+def test_rowwise_warp_reach_for_unaligned_rows(lib):
+    # many rows that are not aligned vectors plan onto the warp tier exactly
+    # while their whole 16-byte chunks fit 32 lanes x 8 (2055 bf16 / 1027
+    # fp32 elements), with a power-of-two lane count; longer rows do not
+    import torch
+    import cluster_reductions_gb300 as rr
+    for dt, top in ((torch.bfloat16, 2055), (torch.float32, 1027)):
+        widths = list(range(1, 100)) + [250, 513, 1000, top - 8, top - 1, top, top + 1, top + 9, 4100]
+        for cols in widths:
+            for op in ("softmax", "lnstats", "layernorm"):
+                tier, width = rr.plan_rowwise(1 << 20, cols, op, 152, 16, dtype=dt, aligned=False)
+                if cols <= top:
+                    assert tier == "warp" and width in (1, 2, 4, 8, 16, 32), (dt, cols, op, tier, width)
+                else:
+                    assert tier != "warp", (dt, cols, op, tier, width)
+
+
 def test_rowwise_plan_rejects_bad_arguments(lib):
     t, w = ctypes.c_int(), ctypes.c_int()
     bt, bw = ctypes.byref(t), ctypes.byref(w)
