@@ -546,8 +546,8 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
 // 8 warps per SM take, the CTAs shrink (down to one warp) so that the warps
 // spread over every SM instead of filling a few.
 template <class K>
-int warp_row_launch(K k, int rpw, int64_t rows, cudaStream_t s, const DevInfo &d,
-                    int *grid_out, int *threads_out, size_t smem = 0) {
+void warp_row_launch(K k, int rpw, int64_t rows, const DevInfo &d, int *grid_out,
+                     int *threads_out, size_t smem = 0) {
   const int64_t warps = (rows + rpw - 1) / rpw;
   int wpb = kWarpRowMaxThreads / 32;
   if (warps < (int64_t)wpb * d.sm_count) {
@@ -560,7 +560,6 @@ int warp_row_launch(K k, int rpw, int64_t rows, cudaStream_t s, const DevInfo &d
   const int64_t cap = (int64_t)(nb > 0 ? nb : 1) * d.sm_count;
   *grid_out = (int)(need < cap ? need : cap);
   *threads_out = threads;
-  return 0;
 }
 
 template <class In, int MODE, int L, int NV>
@@ -581,7 +580,7 @@ int launch_ck(const void *x, int64_t rows, int64_t cols, float eps, float *y, fl
   }
   const size_t smem = MODE == kModeLayernorm ? sizeof(float2) * gb_slots((int)cols, EPV) : 0;
   int grid, threads;
-  warp_row_launch(k, 32 / L, rows, s, d, &grid, &threads, smem);
+  warp_row_launch(k, 32 / L, rows, d, &grid, &threads, smem);
   return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), smem, s, 0,
                                    (const typename In::S *)x, rows, (int)cols, eps, y, mean,
                                    rstd, gamma, beta, ybf, hx, vst));
@@ -596,7 +595,7 @@ int launch_one(const void *x, int64_t rows, int64_t cols, float eps, float *y, f
     else return k_rowwise_warp<In, MODE, L, NV>;
   }();
   int grid, threads;
-  warp_row_launch(k, 32 / L, rows, s, d, &grid, &threads);
+  warp_row_launch(k, 32 / L, rows, d, &grid, &threads);
   return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), 0, s, 0,
                                    (const typename In::S *)x, rows, (int)cols, eps, y, mean,
                                    rstd, gamma, beta, ybf));
