@@ -5,7 +5,7 @@ One step = one pass of every hot-path operation over its synthetic workload:
   warp tier     1,048,576 x 32 fp32 sum / max / min
   tiled tier    1,048,576 x 8 fp32 sum / max / min
   split-K tier  16 x 16,777,216 fp32 sum / max (cluster size picked by the
-                library, 8 on a 152-SM GB300)
+                library: 16 on a 152-SM GB300)
   softmax       32768 x 4096 bf16 -> fp32
   layernorm     16384 x 8192 bf16 -> mean, rstd
   combine       P = 2, 4, 8 partials of 131072 x 128 fp32 -> bf16
@@ -947,6 +947,13 @@ PROFILE_CASES = {
     # long rows staged in shared memory, automatic plan
     "long_softmax_4096x32768_bf16": ({"shape": (4096, 32768), "op": "softmax"}, "medium", 1.0),
     "long_layernorm_2048x65536_bf16": ({"shape": (2048, 65536), "op": "layernorm"}, "medium", 1.0),
+    "long_lnstats_608x262144_bf16": ({"shape": (608, 262144), "op": "lnstats"}, "medium", 1.0),
+    "long_lnstats_4096x32768_bf16": ({"shape": (4096, 32768), "op": "lnstats"}, "medium", 1.0),
+    # a few long rows: the row ops' split-K tier
+    "rowsk_softmax_16x1048576_bf16": ({"shape": (16, 1 << 20), "op": "softmax"}, "medium", 1.0),
+    "rowsk_lnstats_16x1048576_bf16": ({"shape": (16, 1 << 20), "op": "lnstats"}, "medium", 1.0),
+    "rowsk_layernorm_16x1048576_bf16": ({"shape": (16, 1 << 20), "op": "layernorm"}, "medium", 1.0),
+    "tiled_max_f32": ({}, None, 1.0),
 }
 
 
@@ -983,6 +990,10 @@ def run_case(args):
             x = inputs.normal_bf16(r, c, inputs.seed_for(5, 2), "cuda", 3.0)
             y = torch.empty((r, c), device="cuda")
             fn, nb = (lambda: rr.softmax(x, out=y)), r * c * 6
+        elif op == "lnstats":
+            x = inputs.normal_bf16(r, c, inputs.seed_for(5, 3), "cuda")
+            mu, rs = torch.empty(r, device="cuda"), torch.empty(r, device="cuda")
+            fn, nb = (lambda: rr.layernorm_stats(x, 1e-5, mean=mu, rstd=rs)), r * c * 2 + r * 8
         else:
             x = inputs.normal_bf16(r, c, inputs.seed_for(5, 3), "cuda")
             g, b = inputs.layernorm_params(c, inputs.seed_for(5, 4), "cuda")

@@ -13,6 +13,7 @@ import ctypes
 import functools
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -355,6 +356,28 @@ def cluster_allreduce_selftest_noalloc(cluster_size: int, width: int = 1, op="su
     if st not in (_lib.RR_OK, _lib.RR_ERR_MISMATCH):
         check(st, "rr_cluster_allreduce_selftest_noalloc")
     return int(n.value)
+
+
+def cluster_allreduce_selftest_dump(cluster_size: int, width: int = 1, op="sum",
+                                    dtype: torch.dtype = torch.float32, iters: int = 1000,
+                                    two_slot: bool = True, seed: int = 1,
+                                    noalloc: bool = False):
+    """rr_cluster_allreduce_selftest_ex (or its no-allocation twin, noalloc
+    = True), blocking: (mismatch count, inputs, every rank's result), the
+    arrays numpy [iters, 2, cluster_size, width] of `dtype`, for a check of
+    the run on the host."""
+    np_dt = {torch.float32: np.float32, torch.int32: np.int32}[dtype]
+    shape = (int(iters), 2, int(cluster_size), int(width))
+    vals = np.zeros(shape, np_dt)
+    res = np.zeros(shape, np_dt)
+    n = ctypes.c_int64(-1)
+    fn = (load().rr_cluster_allreduce_selftest_noalloc_ex if noalloc
+          else load().rr_cluster_allreduce_selftest_ex)
+    st = fn(int(cluster_size), int(width), _op(op), _DT[dtype], int(iters), 1 if two_slot else 0,
+            int(seed), _stream(), ctypes.byref(n), vals.ctypes.data, res.ctypes.data)
+    if st not in (_lib.RR_OK, _lib.RR_ERR_MISMATCH):
+        check(st, "rr_cluster_allreduce_selftest_ex")
+    return int(n.value), vals, res
 
 
 COMBINE_MODES = {None: 0, "auto": 0, "pull": 1, "push": 2, "generic": 3, "direct": 4}

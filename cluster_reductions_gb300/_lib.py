@@ -76,6 +76,13 @@ SIGNATURES = {
     "rr_cluster_allreduce_selftest_noalloc": (_int, [_int, _int, _int, _int, _int, _int,
                                                      ctypes.c_uint64, _vp,
                                                      ctypes.POINTER(ctypes.c_int64)]),
+    "rr_cluster_allreduce_selftest_ex": (_int, [_int, _int, _int, _int, _int, _int,
+                                                ctypes.c_uint64, _vp,
+                                                ctypes.POINTER(ctypes.c_int64), _vp, _vp]),
+    "rr_cluster_allreduce_selftest_noalloc_ex": (_int, [_int, _int, _int, _int, _int, _int,
+                                                        ctypes.c_uint64, _vp,
+                                                        ctypes.POINTER(ctypes.c_int64), _vp,
+                                                        _vp]),
     "rr_splitk_combine": (_int, [_vp, _vp, _vp, _int, _i64, _int, _f32, _vp, _vp]),
     "rr_splitk_combine_ex": (_int, [_vp, _vp, _vp, _int, _i64, _int, _f32, _vp, _vp, _int]),
     "rr_device_status": (_int, [_vp]),

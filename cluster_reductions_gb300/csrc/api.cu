@@ -735,6 +735,13 @@ int rr_cluster_allreduce(const void *vals, int clusters, int cluster_size, int w
 int rr_cluster_allreduce_selftest(int cluster_size, int width, int op, int dtype, int iters,
                                   int two_slot, uint64_t seed, void *stream,
                                   int64_t *mismatches_out) {
+  return rr_cluster_allreduce_selftest_ex(cluster_size, width, op, dtype, iters, two_slot, seed,
+                                          stream, mismatches_out, nullptr, nullptr);
+}
+
+int rr_cluster_allreduce_selftest_ex(int cluster_size, int width, int op, int dtype, int iters,
+                                     int two_slot, uint64_t seed, void *stream,
+                                     int64_t *mismatches_out, void *vals_host, void *res_host) {
   if (!mismatches_out) return RR_ERR_INVALID;
   if (iters < 1 || iters > (1 << 20)) return RR_ERR_INVALID;
   if (cluster_size < 1 || cluster_size > 16) return RR_ERR_INVALID;
@@ -762,6 +769,10 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op, int dtype
     int64_t h = -1;
     if (st == RR_OK) {
       if (cudaMemcpyAsync(&h, mism, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          (vals_host && cudaMemcpyAsync(vals_host, vals, (size_t)n * 4, cudaMemcpyDeviceToHost,
+                                        s) != cudaSuccess) ||
+          (res_host && cudaMemcpyAsync(res_host, res, (size_t)n * 4, cudaMemcpyDeviceToHost,
+                                       s) != cudaSuccess) ||
           cudaStreamSynchronize(s) != cudaSuccess)
         st = RR_ERR_CUDA;
     }

@@ -19,8 +19,9 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
 }
 
 // Iteration t, cluster cl, rank r reads vals[((t*ncl + cl)*C + r)*W + j].
-// Only thread 0's copy of the input matters (the page: the block-reduced
-// values are valid in thread 0).  With skew > 0, thread 0 of each rank first
+// Only thread 0 loads an input; the other threads start from the identity
+// ("cluster_allreduce" page, arguments: the per-CTA vector is the result of
+// a block reduction, so only its copy in thread 0 counts).  With skew > 0, thread 0 of each rank first
 // spins (hash & 7) * skew clock cycles, so ranks arrive out of step.
 template <class Op, int W>
 __global__ void __launch_bounds__(kCaThreads)

@@ -57,6 +57,15 @@ extern "C" int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width
                                                      int dtype, int iters, int two_slot,
                                                      uint64_t seed, void *stream,
                                                      int64_t *mismatches_out) {
+  return rr_cluster_allreduce_selftest_noalloc_ex(cluster_size, width, op, dtype, iters, two_slot,
+                                                  seed, stream, mismatches_out, nullptr, nullptr);
+}
+
+extern "C" int rr_cluster_allreduce_selftest_noalloc_ex(int cluster_size, int width, int op,
+                                                        int dtype, int iters, int two_slot,
+                                                        uint64_t seed, void *stream,
+                                                        int64_t *mismatches_out, void *vals_host,
+                                                        void *res_host) {
   if (!mismatches_out) return RR_ERR_INVALID;
   if (iters < 1 || cluster_size < 1 || cluster_size > 16) return RR_ERR_INVALID;
   if (!(width == 1 || width == 2 || width == 4 || width == 8)) return RR_ERR_INVALID;
@@ -89,22 +98,31 @@ extern "C" int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width
   int64_t *counter = reinterpret_cast<int64_t *>(base + 2 * (size_t)kNoAllocMaxValues * 4);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the counter must restart at 0
-  if (cudaMemsetAsync(counter, 0, sizeof(int64_t), s) != cudaSuccess) {
+  // Once anything is queued, every return waits for the stream first: work
+  // left in flight on the shared array (say a fill whose all-reduce launch
+  // was then refused) would otherwise overwrite the next caller's values
+  // after the lock is released.
+  auto finish = [&](int status) {
+    if (cudaStreamSynchronize(s) != cudaSuccess && status == RR_OK) status = RR_ERR_CUDA;
     cudaGetLastError();
-    return RR_ERR_CUDA;
-  }
+    return status;
+  };
+  // the array keeps the previous call's contents: the counter must restart at 0
+  if (cudaMemsetAsync(counter, 0, sizeof(int64_t), s) != cudaSuccess) return finish(RR_ERR_CUDA);
   st = launch_fill_selftest_values(vals, n, dtype, seed, s);
   if (st == RR_OK)
     st = launch_cluster_allreduce(vals, clusters, cluster_size, width, op, dtype, iters,
                                   two_slot ? 1 : 0, 2000, res, counter, s, d);
-  if (st != RR_OK) return st;
+  if (st != RR_OK) return finish(st);
   int64_t h = -1;
   if (cudaMemcpyAsync(&h, counter, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess) {
-    cudaGetLastError();
-    return RR_ERR_CUDA;
-  }
+      (vals_host &&
+       cudaMemcpyAsync(vals_host, vals, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+      (res_host &&
+       cudaMemcpyAsync(res_host, res, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess))
+    return finish(RR_ERR_CUDA);
+  st = finish(RR_OK);
+  if (st != RR_OK) return st;
   *mismatches_out = h;
   return h == 0 ? RR_OK : RR_ERR_MISMATCH;
 }

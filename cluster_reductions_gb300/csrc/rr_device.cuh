@@ -267,13 +267,17 @@ template <> __device__ __forceinline__ int from_bits<int>(uint32_t u) { return (
 // from where every thread of the block picks it up.  Because every CTA folds
 // the same values in the same order, every CTA gets the same bits.
 //
-// tail_sync = true retires the slot with a trailing cluster barrier, so the
-// same slot may be used again.  tail_sync = false leaves that to the caller:
-// a loop of combines must alternate between two slots (a CTA that runs
-// ahead then writes the slot its peers are not reading, and it cannot get
-// more than one combine ahead, because the next combine's barrier waits for
-// every peer), and the kernel must end with cluster_sync() so that no CTA
-// exits while a peer may still read its slot.  With C == 1 no barrier is
+// tail_sync = true ends with a second cluster barrier: once it passes, no
+// peer will read this slot again, so the next combine may reuse it.
+// tail_sync = false skips that barrier ("cluster_allreduce" page, the
+// need_tail_sync parameter) and the caller alternates two slots, A, B, A, ...
+// Why that is safe: combine k+1 writes slot B, which no peer reads during
+// combine k; and before any CTA writes slot A again in combine k+2 it has
+// passed the barrier of combine k+1, which every peer reaches only after
+// finishing its reads of slot A in combine k.  So the lead of the fastest CTA
+// over the slowest is bounded by one combine.  The kernel must still end
+// with cluster_sync(), so that no CTA exits (and its shared memory goes away)
+// while a peer may still read its last slot.  With C == 1 no barrier is
 // needed: the call only publishes thread 0's values to the block.
 // ---------------------------------------------------------------------------
 template <class Op, int W>

@@ -404,6 +404,29 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op,
                                   int64_t *mismatches_out);
 
 /*
+ * rr_cluster_allreduce_selftest_ex -- rr_cluster_allreduce_selftest that
+ * also hands the run back for a check on the host ([CA] description: every
+ * CTA folds every rank's vector in rank order, so the host can redo that
+ * fold from the inputs and compare bits with every rank's result).
+ *   vals_host  host buffer of n = iters * 2 * cluster_size * width 32-bit
+ *              values, or NULL: receives the seeded per-rank inputs, laid
+ *              out [iters][2 clusters][cluster_size][width].  Value i is
+ *              u = splitmix64(seed ^ splitmix64(i)) (splitmix64 as published
+ *              by Steele, Lea and Flood, "Fast splittable pseudorandom number
+ *              generators", 2014); int32: the high 32 bits of u; fp32:
+ *              ldexp((u >> 40) * 2^-23 - 1, (u >> 8) % 41 - 20).
+ *   res_host   host buffer of n values, or NULL: receives every rank's
+ *              combined result (thread 0's copy) in the same layout.
+ * Both are written only when the call returns RR_OK or RR_ERR_MISMATCH.
+ * Otherwise as rr_cluster_allreduce_selftest.
+ */
+int rr_cluster_allreduce_selftest_ex(int cluster_size, int width, int op,
+                                     int dtype, int iters, int two_slot,
+                                     uint64_t seed, void *stream,
+                                     int64_t *mismatches_out, void *vals_host,
+                                     void *res_host);
+
+/*
  * rr_cluster_allreduce_selftest_noalloc -- the same blocking self-test as
  * rr_cluster_allreduce_selftest (same arguments, same checks, same result),
  * but it allocates no device memory: no cudaMalloc, no cudaFree, no
@@ -421,7 +444,8 @@ int rr_cluster_allreduce_selftest(int cluster_size, int width, int op,
  *   stream capture.  Each call resets the counter it needs; the array keeps
  *   the last call's other contents.  All calls share the one array: calls
  *   from several host threads of a process run one after another (each holds
- *   a process-wide lock for its whole, blocking, duration).
+ *   a process-wide lock for its whole, blocking, duration, and waits for
+ *   its stream before it returns, on failure too).
  * Returns RR_OK, RR_ERR_MISMATCH, RR_ERR_INVALID, RR_ERR_UNSUPPORTED or
  * RR_ERR_CUDA.
  */
@@ -431,6 +455,21 @@ int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width, int op,
                                           int64_t *mismatches_out);
 
 /*
+ * rr_cluster_allreduce_selftest_noalloc_ex -- the no-allocation self-test
+ * that also copies its inputs and every rank's results out of the fixed
+ * array into caller-owned host buffers (vals_host, res_host: n 32-bit values
+ * each, or NULL; layout and values as rr_cluster_allreduce_selftest_ex), so
+ * that a caller can check the run on the host.  Allocates nothing, like
+ * rr_cluster_allreduce_selftest_noalloc; the pages have no counterpart.
+ */
+int rr_cluster_allreduce_selftest_noalloc_ex(int cluster_size, int width,
+                                             int op, int dtype, int iters,
+                                             int two_slot, uint64_t seed,
+                                             void *stream,
+                                             int64_t *mismatches_out,
+                                             void *vals_host, void *res_host);
+
+/*
  * rr_splitk_combine -- split-K attention-output combine ([FA]).
  *   O       device fp32 [P][rows][D] partial outputs (unnormalised).
  *   m, l    device fp32 [P][rows] per-partition row max (raw scores) and
@@ -438,12 +477,14 @@ int rr_cluster_allreduce_selftest_noalloc(int cluster_size, int width, int op,
  *   out_bf16 device [rows][D] bf16 bit patterns.
  * Per row: M = max_p m_p, w_p = exp2((m_p - M) * scale_log2e),
  * L = sum_p w_p l_p (rank order), out = bf16_rn(sum_p w_p O_p / L); rows
- * with M = -inf or L = 0 are written as +0.  A cluster of P CTAs handles a
- * tile of rows: CTA p stages its own partial into its shared memory,
- * publishes it with a cluster barrier, then folds the P partials of its
- * column band [p*D/P, (p+1)*D/P) in rank order through distributed shared
- * memory and stores that band.  A partition whose band is empty (D < P)
- * only stages and publishes.
+ * with M = -inf or L = 0 are written as +0.  In the page's design a cluster
+ * of P CTAs handles a tile of rows: CTA p stages its own partial into its
+ * shared memory, publishes it with a cluster barrier, then folds the P
+ * partials of its column band [p*D/P, (p+1)*D/P) in rank order through
+ * distributed shared memory and stores that band; a partition whose band is
+ * empty (D < P) only stages and publishes.  This call takes the fastest
+ * variant the arguments allow (RR_COMBINE_AUTO of rr_splitk_combine_ex);
+ * every variant returns the same bits.
  *   P in 1..16 (16 needs the non-portable cluster size), D in 1..1024.
  * Errors: RR_ERR_INVALID, RR_ERR_UNSUPPORTED (cluster of P CTAs cannot be
  * co-scheduled), RR_ERR_CUDA.  A staging copy that does not land within the
@@ -469,7 +510,7 @@ typedef enum {
     RR_COMBINE_DIRECT = 4   /* no cluster: each CTA stages the rows of all P
                                partitions itself and folds them locally;
                                same DRAM traffic, no exchange between CTAs;
-                               P in {1,2,4,8,16}, D % 4 == 0, 3*P*D*4 <= 160 KiB */
+                               P in {1,2,4,8,16}, D % 4 == 0, 2*P*D*4 <= 96 KiB */
 } rr_combine_mode;
 
 /*

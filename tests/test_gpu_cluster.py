@@ -76,3 +76,30 @@ def test_bounded_wait_reports_timeout(rr):
     assert rr.device_status() == 0          # cleared by the read
     x = torch.ones((4, 100), device="cuda")
     assert torch.equal(rr.reduce(x, "sum").cpu(), torch.full((4,), 100.0))
+
+
+@pytest.mark.parametrize("C,width,op,dtype,two_slot", [
+    (1, 1, "sum", torch.float32, True), (2, 2, "sum", torch.float32, True),
+    (4, 8, "max", torch.float32, False), (8, 4, "sum", torch.int32, True),
+    (16, 2, "min", torch.float32, True), (8, 1, "min", torch.int32, False)])
+def test_selftest_checked_on_host(rr, oracle_mod, C, width, op, dtype, two_slot):
+    # the self-test's own inputs and every rank's result, copied out and
+    # checked here: the inputs against the documented generator, each
+    # result against the oracle's rank-order fold of its iteration's inputs
+    from _util import selftest_values
+    iters, seed = 300, 4242 + C
+    try:
+        n, vals, res = rr.cluster_allreduce_selftest_dump(C, width, op, dtype, iters,
+                                                         two_slot, seed)
+    except rr.RRError as e:
+        if C == 16 and e.status == 2:
+            pytest.skip("cluster of 16 not schedulable")
+        raise
+    assert n == 0
+    np_dt = np.float32 if dtype == torch.float32 else np.int32
+    want = selftest_values(vals.size, seed, np_dt).reshape(vals.shape)
+    assert (vals.view(np.uint32) == want.view(np.uint32)).all()
+    for t in range(iters):
+        for c in range(2):
+            ref = oracle_mod.cluster_fold(vals[t, c], op).view(np.uint32)
+            assert (res[t, c].view(np.uint32) == ref[None, :]).all(), (t, c)

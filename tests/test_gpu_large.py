@@ -91,7 +91,8 @@ def test_rowwise_past_2_31(rr, oracle_mod):
     yb = rr.layernorm(xb, g, b, 1e-5, mean=mean, rstd=rstd)
     y64, y16, m64, r64 = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
     xf = xb[tail].to(torch.float64).cpu().numpy()
-    assert_layernorm_close(to_np(yb[tail]), y64, y16, xf, to_np(g), to_np(b), m64, r64)
+    assert_layernorm_close(to_np(yb[tail]), y64, y16, xf, to_np(g), to_np(b), m64, r64,
+                           to_np(mean[tail]), to_np(rstd[tail]))
     assert_rel_close(to_np(rstd[tail]), r64, 1e-5, what="layernorm rstd")
 
 
@@ -120,10 +121,12 @@ def test_rowwise_warp_past_2_31(rr, oracle_mod):
     del y
     from cluster_reductions_gb300 import inputs
     g, b = inputs.layernorm_params(cols, 9008, "cuda")
+    mean = torch.empty(rows, device="cuda")
     rstd = torch.empty(rows, device="cuda")
-    yb = rr.layernorm(xb, g, b, 1e-5, rstd=rstd)
+    yb = rr.layernorm(xb, g, b, 1e-5, mean=mean, rstd=rstd)
     assert rr.last_tier()[0] == "warp"
     y64, y16, m64, r64 = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
     xf = xb[tail].to(torch.float64).cpu().numpy()
-    assert_layernorm_close(to_np(yb[tail]), y64, y16, xf, to_np(g), to_np(b), m64, r64)
+    assert_layernorm_close(to_np(yb[tail]), y64, y16, xf, to_np(g), to_np(b), m64, r64,
+                           to_np(mean[tail]), to_np(rstd[tail]))
     assert_rel_close(to_np(rstd[tail]), r64, 1e-5, what="layernorm rstd warp")

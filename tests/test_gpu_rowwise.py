@@ -186,7 +186,8 @@ def check_layernorm(rr, oracle_mod, x, gamma, beta, **kw):
     xh = to_np(x)
     y64, y16, rm, rr_ = oracle_mod.layernorm(xh, to_np(gamma), to_np(beta), 1e-5)
     xf = x.to(torch.float64).cpu().numpy()
-    assert_layernorm_close(to_np(y), y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_)
+    assert_layernorm_close(to_np(y), y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_,
+                           to_np(mean), to_np(rstd))
     assert_rel_close(to_np(rstd), rr_, 1e-5, what="layernorm rstd")
     return y, mean, rstd
 
@@ -232,7 +233,7 @@ def test_layernorm_rewrite_workload_and_stats_agree(rr, oracle_mod):
     xs = x[idx]
     y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(gamma), to_np(beta), 1e-5)
     assert_layernorm_close(to_np(y[idx]), y64, y16, xs.to(torch.float64).cpu().numpy(),
-                           to_np(gamma), to_np(beta), rm, rr_)
+                           to_np(gamma), to_np(beta), rm, rr_, to_np(mean[idx]), to_np(rstd[idx]))
 
 
 def test_argument_errors(rr):
@@ -302,7 +303,8 @@ def test_layernorm_warp_forced(rr, oracle_mod, dtype, L):
             xs = x[torch.from_numpy(idx).cuda()]
             y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(gamma), to_np(beta), 1e-5)
             xf = xs.to(torch.float64).cpu().numpy()
-            assert_layernorm_close(to_np(y)[idx], y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_)
+            assert_layernorm_close(to_np(y)[idx], y64, y16, xf, to_np(gamma), to_np(beta), rm, rr_,
+                                   to_np(mean)[idx], to_np(rstd)[idx])
             bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
             assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
             assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd warp L={L} {rows}x{cols}")
@@ -369,7 +371,8 @@ def test_rowwise_warp_misaligned_operand_offsets(rr, oracle_mod, dtype):
             assert rr.last_tier()[0] == "warp"
             y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
             xf = xs.to(torch.float64).cpu().numpy()
-            assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_)
+            assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_,
+                                   to_np(mean)[idx], to_np(rstd)[idx])
             bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
             assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
             assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {cols} x+{xo} out+{oo}")
@@ -545,7 +548,8 @@ def _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=None, stats_bitwise=T
         assert torch.equal(rstd.view(torch.int32), r2.view(torch.int32))
     y64, y16, rm, rr_ = oracle_mod.layernorm(xh, to_np(g), to_np(b), 1e-5)
     xf = xs.to(torch.float64).cpu().numpy()
-    assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_)
+    assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm, rr_,
+                           to_np(mean)[idx], to_np(rstd)[idx])
     bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
     assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all()
     assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"rstd {rows}x{cols}")
