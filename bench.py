@@ -554,7 +554,11 @@ def bench_ours(args):
         def timed(fn, nbytes, reps=20):
             """Average device time per call of `reps` calls captured in one
             CUDA graph and replayed, so host launch overhead does not leave the
-            GPU idle between short launches."""
+            GPU idle between short launches.  Short calls get more reps (a
+            graph of at least ~0.5 ms at the copy bandwidth), so that the
+            graph's own launch and its first, unoverlapped kernel do not
+            weigh on a 36 MB call."""
+            reps = max(reps, min(256, -(-int(0.5e-3 * peak * 1e9) // max(1, int(nbytes)))))
             for _ in range(3):
                 fn()
             torch.cuda.synchronize()
@@ -825,11 +829,41 @@ def bench_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    # last key of the line: every measured fraction of the copy bandwidth in
+    # one short object, so that a reader who keeps only the line's tail
+    # still sees them all
+    line["frac_summary"] = frac_summary(line)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def frac_summary(line) -> dict:
+    """{section: "name=frac ..."}: the fraction of the measured copy
+    bandwidth of every operation timed back to back and of the extras, in
+    one short object (names shortened: "ln" = layernorm, dtype suffixes
+    dropped, fractions to two decimals)."""
+    out = {"step": round(line["value"] / line["roofline"]["peak"], 3)}
+    for sec, short in (("tiers_back_to_back", "b2b"), ("rowwise_splitk", "rowops_split"),
+                       ("long_rows", "long_rows"), ("medium_rows", "medium_rows"),
+                       ("combine_variants", "combine"), ("splitk_by_cluster", "splitk_C"),
+                       ("axis_reduce", "axis")):
+        d = line.get(sec) or {}
+        vals = []
+        for k, v in d.items():
+            if not (isinstance(v, dict) and "frac_measured" in v):
+                continue
+            if sec == "axis_reduce" and not k.endswith("_sum_f32"):
+                continue
+            kk = (k.replace("_bf16", "").replace("_f32", "").replace("layernorm", "ln")
+                  .replace("combine_", "").replace("_sum", "") if sec != "tiers_back_to_back"
+                  else k.replace("_f32", "").replace("_bf16", "").replace("layernorm", "ln"))
+            vals.append(f"{kk}={v['frac_measured']:.2f}".replace("=0.", "=.").replace("=1.", "=1."))
+        if vals:
+            out[short] = " ".join(vals)
+    return out
 
 
 def bench_e2e(args, rr, data, dev, stream, world):
@@ -954,6 +988,10 @@ PROFILE_CASES = {
     "rowsk_lnstats_16x1048576_bf16": ({"shape": (16, 1 << 20), "op": "lnstats"}, "medium", 1.0),
     "rowsk_layernorm_16x1048576_bf16": ({"shape": (16, 1 << 20), "op": "layernorm"}, "medium", 1.0),
     "tiled_max_f32": ({}, None, 1.0),
+    "long_softmax_608x262144_bf16": ({"shape": (608, 262144), "op": "softmax"}, "medium", 1.0),
+    "long_layernorm_608x262144_bf16": ({"shape": (608, 262144), "op": "layernorm"}, "medium", 1.0),
+    "ring_lnstats_8192x16392_bf16": ({"shape": (8192, 16392), "op": "lnstats"}, "medium", 1.0),
+    "rowsk_lnstats_32x524288_bf16": ({"shape": (32, 1 << 19), "op": "lnstats"}, "medium", 1.0),
 }
 
 

@@ -428,6 +428,13 @@ def last_staged() -> bool:
     return bool((int(load().rr_last_tier()) >> 16) & 1)
 
 
+def last_form() -> str:
+    """How the last row operation read its rows: "ring" (streamed through a
+    shared-memory ring), "staged" (held in shared memory) or "direct"."""
+    v = int(load().rr_last_tier())
+    return "ring" if (v >> 17) & 1 else ("staged" if (v >> 16) & 1 else "direct")
+
+
 def plan_reduce(rows: int, cols: int, sm_count: int, max_cluster: int) -> Tuple[str, int]:
     """rr_plan_reduce (host only): the tier and cluster size rr_reduce picks."""
     t, c = ctypes.c_int(), ctypes.c_int()
@@ -440,10 +447,12 @@ _ROW_OPS = {"softmax": 0, "lnstats": 1, "layernorm_stats": 1, "layernorm": 2}
 
 
 def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: int,
-                 dtype=torch.bfloat16, aligned: bool = True, staged: bool = False):
+                 dtype=torch.bfloat16, aligned: bool = True, staged: bool = False,
+                 form: bool = False):
     """rr_plan_rowwise (host only): the tier and width (lanes per row, cluster
     size or 1) that softmax / layernorm_stats / layernorm pick; with
-    staged=True also whether the rows are staged in shared memory."""
+    staged=True also whether the rows are staged in shared memory, with
+    form=True how they are read ("direct", "staged" or "ring")."""
     dt = _DT.get(dtype)
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"plan_rowwise: dtype {dtype} not supported")
@@ -452,7 +461,9 @@ def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: 
                                  int(sm_count), int(max_cluster), ctypes.byref(t),
                                  ctypes.byref(w), ctypes.byref(st)), "rr_plan_rowwise")
     if staged:
-        return TIER_NAMES[t.value], w.value, bool(st.value)
+        return TIER_NAMES[t.value], w.value, st.value == 1
+    if form:
+        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring")[st.value]
     return TIER_NAMES[t.value], w.value
 
 

@@ -255,7 +255,7 @@ int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int al
                                  max_cluster < 16 ? max_cluster : 16);
   *tier_out = p.tier;
   *width_out = p.width;
-  if (staged_out) *staged_out = p.staged ? 1 : 0;
+  if (staged_out) *staged_out = p.ring ? 2 : (p.staged ? 1 : 0);
   return RR_OK;
 }
 

@@ -673,6 +673,14 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.ring && ay % 32 == 0) {
+    int Cl = pk.width;
+    const int st = launch_rowwise_ring(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows,
+                                       cols, 0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                       pk.width, tier == RR_TIER_AUTO, &Cl, s, d);
+    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    return st;
+  }
   if (pk.staged)
     return launch_rowwise_staged(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                  0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, vec, s, d);
@@ -713,6 +721,14 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.ring) {
+    int Cl = pk.width;
+    const int st = launch_rowwise_ring(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
+                                       eps, nullptr, mean, rstd, nullptr, nullptr, nullptr,
+                                       pk.width, tier == RR_TIER_AUTO, &Cl, s, d);
+    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    return st;
+  }
   if (pk.staged)
     return launch_rowwise_staged(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                                  nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, vec, s, d);
@@ -756,6 +772,14 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  if (pk.ring && (uintptr_t)y % 16 == 0) {
+    int Cl = pk.width;
+    const int st = launch_rowwise_ring(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows,
+                                       cols, eps, nullptr, mean, rstd, gamma, beta, y, pk.width,
+                                       tier == RR_TIER_AUTO, &Cl, s, d);
+    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    return st;
+  }
   if (pk.staged)
     return launch_rowwise_staged(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                  eps, nullptr, mean, rstd, gamma, beta, y, pk.width, vec, s, d);
@@ -830,6 +854,18 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     return (rowwise_staged_chunk(cols, c) + (vec ? 0 : 8)) * elt <= kStageMaxBytes;
   };
   const int warp_min_rows_per_sm = rewrite ? kRowWarpMinRowsPerSMRewrite : kRowWarpMinRowsPerSM;
+  // the streamed ring form (rowring.cu): aligned rows of whole 8-element
+  // units; softmax and the rewrite read each slice twice, the second time
+  // from L2, so only while the rows in flight fit there
+  const bool ring_ok = vec && cols % 8 == 0;
+  auto ring_fits = [&](int64_t inflight_rows) {
+    return mode == kModeStats || inflight_rows * cols * elt <= kRingL2Bytes;
+  };
+  // a few long rows: the ring for softmax and the statistics; the rewrite
+  // keeps the global-memory split-K form, whose 16-CTA clusters spread the
+  // per-row gamma / beta reads (8 bytes an element, from L2) over more SMs
+  // (16 x 1M bf16: 35 against 48 us)
+  const bool ring_few = mode != kModeLayernorm;
   const int64_t staged_min = vec ? kRowStagedMinVec[mode] : kRowStagedMinVecMis[mode];
   if (tier == RR_TIER_BLOCK) {
     const bool st = row_vecs > staged_min && stage_fits(1);
@@ -844,11 +880,23 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
     if (C == 0) C = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
     if (C == 0) C = 2;
     if (C > 1 && C > max_cluster) return {-1, 0, false};
+    const int64_t inflight = 2 * (int64_t)sm_count / C;
+    if (ring_ok && ring_fits(rows < inflight ? rows : inflight))
+      return {RR_TIER_SPLITK, C, false, true};
     const bool st = RR_ROW_STAGED_SPLITK && stage_fits(C);
     return {RR_TIER_SPLITK, C, st};
   }
   const int c = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
   if (c > 0) {
+    // a few long rows: with the ring, a cluster of as many CTAs as there
+    // are SMs per row (any size up to 16), one CTA per SM
+    if (ring_few && ring_ok && ring_fits(rows)) {
+      int cr = (int)(sm_count / rows);
+      if (cr > 16) cr = 16;
+      if (cr > max_cluster) cr = max_cluster;
+      if (cr <= 1) return {RR_TIER_BLOCK, 1, false, true};  // a CTA per row
+      return {RR_TIER_SPLITK, cr, false, true};
+    }
     const bool st = RR_ROW_STAGED_SPLITK && stage_fits(c);
     return {RR_TIER_SPLITK, c, st};
   }
@@ -857,6 +905,12 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
                       : rowwise_warp_mis_lanes(cols, in_dtype, mode, out_vec, 0);
     if (L) return {RR_TIER_WARP, L, false};
   }
+  // the statistics of rows of 128 KiB and more: a CTA per row, streamed once
+  // through the ring (measured against staging a CTA per row: 608 x 262144
+  // bf16 0.88 against 0.49 of the copy bandwidth, 4096 x 32768 0.80 against
+  // 0.87 -- shorter rows stage)
+  if (mode == kModeStats && ring_ok && row_vecs > kRowRegMaxVec && cols * elt >= (128 << 10))
+    return {RR_TIER_BLOCK, 1, false, true};
   if (row_vecs > staged_min) {
     const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster, vec);
     if (sc == 1) return {RR_TIER_BLOCK, 1, true};

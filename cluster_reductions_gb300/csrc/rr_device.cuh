@@ -247,6 +247,13 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   return __uint_as_float(ld_dsmem_u32(addr));
 }
+// 16 bytes into the shared memory of a peer CTA (addr from map_peer, 16-byte
+// aligned); ordered before a later release-arrive of the same thread.
+__device__ __forceinline__ void st_dsmem_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 template <class T> __device__ __forceinline__ uint32_t to_bits(T v);
 template <> __device__ __forceinline__ uint32_t to_bits<float>(float v) { return __float_as_uint(v); }

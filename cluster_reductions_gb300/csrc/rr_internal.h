@@ -86,6 +86,7 @@ struct RowPlan {
   int tier;
   int width;
   bool staged;
+  bool ring = false;  // streamed through a shared-memory ring (rowring.cu)
 };
 // Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
 // cols is a multiple of the 16-byte vector and every operand meets the
@@ -120,6 +121,20 @@ int launch_rowwise_staged(int mode, int in_dtype, const void *x, int64_t rows, i
                           const float *beta, uint16_t *ybf, int C, bool aligned, cudaStream_t s,
                           const DevInfo &d);
 
+// ---- streamed row operations (rowring.cu)
+// Rows whose second pass (softmax, layernorm rewrite) re-reads them from L2:
+// the ring form takes them while the rows in flight hold at most this many
+// bytes.
+constexpr int64_t kRingL2Bytes = int64_t(64) << 20;
+// mode as launch_rowwise_warp; x 16-byte aligned, cols a multiple of 8, y
+// 32-byte aligned (softmax), ybf / gamma / beta 16-byte aligned (rewrite).
+// C: cluster size (1..16, any value); with `shrink` a C whose clusters
+// cannot all run at once is lowered (to 2 at least) until they can.  *C_out
+// receives the cluster size launched.
+int launch_rowwise_ring(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols,
+                        float eps, float *y, float *mean, float *rstd, const float *gamma,
+                        const float *beta, uint16_t *ybf, int C, bool shrink, int *C_out,
+                        cudaStream_t s, const DevInfo &d);
 // ---- warp tier of the row operations (rowwarp.cu)
 // A segment of L lanes per row holding NV 16-byte vectors per lane, NV a
 // power of two up to kRowWarpMaxNV.

@@ -532,9 +532,11 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
 int rr_device_status(void *stream);
 
 /* Tier and width of the last reduce / softmax / layernorm call made by this
- * process: (staged << 16) | (width << 8) | tier, width the cluster size (the
- * warp tier of the row operations: lanes per row), staged 1 when a row
- * operation staged its rows in shared memory. */
+ * process: (ring << 17) | (staged << 16) | (width << 8) | tier, width the
+ * cluster size (the warp tier of the row operations: lanes per row), staged
+ * 1 when a row operation staged its rows in shared memory, ring 1 when it
+ * streamed them through a shared-memory ring of bulk copies (one combine per
+ * row; the layernorm statistics as a (count, mean, M2) monoid). */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -563,7 +565,10 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * are 16-byte aligned (the outputs then share x's offset within a chunk).
  * Writes the tier and its width: lanes per row (warp),
  * cluster size (split-K) or 1 (block); *staged_out (if not NULL) 1 when the
- * block / split-K tier stages the rows in shared memory.  Touches no GPU.
+ * block / split-K tier stages the rows in shared memory, 2 when it streams
+ * them through a shared-memory ring (the split-K width is then the cluster
+ * size planned; a launch may take a smaller one, down to 2, when the device
+ * cannot co-schedule a cluster that size for every row).  Touches no GPU.
  * RR_ERR_INVALID on negative sizes, sm_count or max_cluster < 1, a bad dtype
  * or row_op.
  */

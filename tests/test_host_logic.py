@@ -134,9 +134,18 @@ def test_tier_dispatch(lib, rows, cols, sms, maxc, expect):
 
 @pytest.mark.parametrize("rows,cols,op,dtype,aligned,maxc,expect", [
     # split-K for a few long rows, the smallest C that covers the SMs
-    (16, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16)),
+    # (with rows that fit the streamed ring form: as many CTAs per row as
+    # there are SMs per row, any cluster size up to 16; one row per SM: a
+    # CTA per row)
+    (16, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 9)),
     (16, 1 << 20, "layernorm", "bf16", True, 8, ("splitk", 8)),
-    (151, 16384, "lnstats", "bf16", True, 16, ("splitk", 2)),
+    (16, 1 << 20, "layernorm", "bf16", True, 16, ("splitk", 16)),   # the rewrite: pow2 rule
+    (151, 16384, "lnstats", "bf16", True, 16, ("block", 1)),
+    (76, 16384, "lnstats", "bf16", True, 16, ("splitk", 2)),
+    (16, 1 << 20, "softmax", "f32", True, 16, ("splitk", 9)),
+    (16, 1 << 20 | 4, "softmax", "f32", True, 16, ("splitk", 16)),  # not whole 8-element units
+    (100, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 2)),     # 200 MB: beyond L2
+    (100, 1 << 20, "lnstats", "bf16", True, 16, ("block", 1)),
     (16, 1 << 20, "softmax", "bf16", True, 1, ("block", 1)),      # no clusters
     (151, 16376, "softmax", "bf16", True, 16, ("block", 1)),      # below 16384 columns
     # a CTA per row once rows fill the SMs and do not fit a warp segment
@@ -185,37 +194,44 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
 
 @pytest.mark.parametrize("rows,cols,op,dtype,aligned,maxc,expect", [
     # staged in shared memory: softmax beyond 1024 vectors, layernorm beyond 2048
-    (4096, 32768, "softmax", "bf16", True, 16, ("block", 1, True)),
-    (8192, 16384, "softmax", "bf16", True, 16, ("block", 1, True)),
-    (8192, 16384, "lnstats", "bf16", True, 16, ("block", 1, False)),     # register form
-    (16384, 8192, "softmax", "bf16", True, 16, ("block", 1, False)),
-    (4096, 16384, "layernorm", "f32", True, 16, ("block", 1, True)),     # 64 KiB rows
-    (2048, 65536, "lnstats", "bf16", True, 16, ("splitk", 2, True)),     # 2 slices of 64 KiB
-    (304, 524288, "layernorm", "bf16", True, 16, ("splitk", 16, True)),
-    (608, 262144, "softmax", "bf16", True, 16, ("splitk", 8, True)),
-    (608, 262144, "lnstats", "bf16", True, 16, ("splitk", 4, False)),    # statistics: C <= 4 staged
-    (1216, 131072, "lnstats", "bf16", True, 16, ("splitk", 4, True)),
+    (4096, 32768, "softmax", "bf16", True, 16, ("block", 1, "staged")),
+    (8192, 16384, "softmax", "bf16", True, 16, ("block", 1, "staged")),
+    (8192, 16384, "lnstats", "bf16", True, 16, ("block", 1, "direct")),   # register form
+    (16384, 8192, "softmax", "bf16", True, 16, ("block", 1, "direct")),
+    (4096, 16384, "layernorm", "f32", True, 16, ("block", 1, "staged")),  # 64 KiB rows
+    (304, 524288, "layernorm", "bf16", True, 16, ("splitk", 16, "staged")),
+    (608, 262144, "softmax", "bf16", True, 16, ("splitk", 8, "staged")),
+    # the statistics of rows beyond the register form: a CTA per row, streamed
+    (2048, 65536, "lnstats", "bf16", True, 16, ("block", 1, "ring")),
+    (608, 262144, "lnstats", "bf16", True, 16, ("block", 1, "ring")),
+    (1216, 131072, "lnstats", "bf16", True, 16, ("block", 1, "ring")),
+    (4096, 32768, "lnstats", "bf16", True, 16, ("block", 1, "staged")),   # 64 KiB rows stage
+    (4096, 32776, "lnstats", "f32", True, 16, ("block", 1, "ring")),
+    (4096, 32772, "lnstats", "f32", True, 16, ("splitk", 2, "staged")),   # not whole 8-element units
+    # a few long rows: split-K, streamed
+    (16, 1 << 20, "lnstats", "bf16", True, 16, ("splitk", 9, "ring")),
+    (16, 1 << 20, "layernorm", "bf16", True, 16, ("splitk", 16, "direct")),  # the rewrite: not
     # not stageable: split-K over global memory
-    (304, 524288, "layernorm", "bf16", True, 8, ("splitk", 8, False)),   # slices > 96 KiB
-    (152, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16, False)),
-    (4096, 32767, "softmax", "bf16", True, 16, ("block", 1, True)),      # not a vector multiple:
-    (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, True)),     # misaligned rows staged
-    (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, True)),
-    (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, True)),    # + 8 elements > 96 KiB
-    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, True)),      # misaligned rows: softmax
-    (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, False)),     # stages from 1024 vectors,
-    (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, True)),       # the statistics from 1024,
-    (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, False)),    # the rewrite from 2048
-    (4096, 16396, "layernorm", "bf16", True, 16, ("block", 1, True)),
-    (4096, 32768, "softmax", "bf16", True, 1, ("block", 1, True)),       # no clusters: C = 1 fits
-    (4096, 40000, "softmax", "f32", True, 1, ("block", 1, False)),       # no clusters, too long
+    (304, 524288, "layernorm", "bf16", True, 8, ("splitk", 8, "direct")),  # slices > 96 KiB
+    (152, 1 << 20, "softmax", "bf16", True, 16, ("splitk", 16, "direct")),
+    (4096, 32767, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # not a vector multiple:
+    (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, "staged")),   # misaligned rows staged
+    (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, "staged")),
+    (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, "staged")),  # + 8 elements > 96 KiB
+    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # misaligned rows: softmax
+    (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # stages from 1024 vectors,
+    (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # the statistics from 1024,
+    (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, "direct")),   # the rewrite from 2048
+    (4096, 16396, "layernorm", "bf16", True, 16, ("block", 1, "staged")),
+    (4096, 32768, "softmax", "bf16", True, 1, ("block", 1, "staged")),     # no clusters: C = 1 fits
+    (4096, 40000, "softmax", "f32", True, 1, ("block", 1, "direct")),      # no clusters, too long
 ])
 def test_rowwise_staged_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     import torch
     import cluster_reductions_gb300 as rr
     dt = torch.bfloat16 if dtype == "bf16" else torch.float32
     assert rr.plan_rowwise(rows, cols, op, 152, maxc, dtype=dt, aligned=aligned,
-                           staged=True) == expect
+                           form=True) == expect
 
 
 def test_rowwise_warp_reach_for_unaligned_rows(lib):
