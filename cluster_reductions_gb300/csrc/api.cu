@@ -251,8 +251,9 @@ int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int al
   if (row_op < RR_ROW_SOFTMAX || row_op > RR_ROW_LAYERNORM) return RR_ERR_INVALID;
   const int epv = in_dtype == RR_BF16 ? 8 : 4;
   const bool vec = aligned && cols % epv == 0;
+  const bool half = aligned && cols % (epv / 2) == 0;  // 8-byte vectors
   const RowPlan p = plan_rowwise(rows, cols, in_dtype, vec, row_op, RR_TIER_AUTO, 0, sm_count,
-                                 max_cluster < 16 ? max_cluster : 16);
+                                 max_cluster < 16 ? max_cluster : 16, true, half);
   *tier_out = p.tier;
   *width_out = p.width;
   if (staged_out) *staged_out = p.ring ? 2 : (p.staged ? 1 : 0);

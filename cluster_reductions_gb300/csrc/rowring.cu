@@ -63,43 +63,6 @@ static_assert(kRingStages % kRingConsWarps == 0, "one consumer warp per slot");
 // (8 elements each) a lane: 96 units per leaf round of a warp.
 constexpr uint32_t kRingPieceBig = 12288, kRingPieceSmall = 6144;
 
-// Monoid state of the layernorm statistics: count, mean and M2.
-struct Chan {
-  uint32_t n;
-  float mean, m2;
-};
-
-__device__ __forceinline__ Chan chan_merge(const Chan &a, const Chan &b) {
-  if (b.n == 0) return a;
-  if (a.n == 0) return b;
-  Chan r;
-  r.n = a.n + b.n;
-  // the weight nb / n to about 2 ulp (a reciprocal and a product): its error
-  // moves the mean by ~2^-23 |d|, far inside the statistics' tolerance
-  const float wb = __fdividef((float)b.n, (float)r.n);
-  const float d = b.mean - a.mean;
-  r.mean = fmaf(d, wb, a.mean);
-  r.m2 = (a.m2 + b.m2) + (d * d) * ((float)a.n * wb);
-  return r;
-}
-
-// Xor butterfly over a warp's lanes (SEG a power of two); the lower lane of
-// each pair is always the left operand, so both lanes of a pair compute the
-// same expression and lane 0's result depends only on the lanes' values.
-template <int SEG>
-__device__ __forceinline__ Chan chan_warp(Chan v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = SEG / 2; o > 0; o >>= 1) {
-    Chan q;
-    q.n = __shfl_xor_sync(0xffffffffu, v.n, o);
-    q.mean = __shfl_xor_sync(0xffffffffu, v.mean, o);
-    q.m2 = __shfl_xor_sync(0xffffffffu, v.m2, o);
-    v = (lane & o) ? chan_merge(q, v) : chan_merge(v, q);
-  }
-  return v;
-}
-
 template <int SEG>
 __device__ __forceinline__ void ms_warp(float &m, float &s) {
 #pragma unroll

@@ -90,13 +90,14 @@ k_softmax_reg(const typename In::S *__restrict__ x, int64_t rows, int cols,
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const uint4 *q = reinterpret_cast<const uint4 *>(x + row * (int64_t)cols);
+    using W = typename In::W;
+    const W *q = reinterpret_cast<const W *>(x + row * (int64_t)cols);
     float v[NV][EPV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int idx = k * THREADS + tid;
       if (idx < nvec) {
-        In::unpack(ld_stream_u4(q + idx), v[k]);
+        In::unpack(In::ldv(q + idx), v[k]);
       } else {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) v[k][e] = -INFINITY;
@@ -134,14 +135,17 @@ k_softmax_reg(const typename In::S *__restrict__ x, int64_t rows, int cols,
     for (int k = 0; k < NV; ++k) {
       const int idx = k * THREADS + tid;
       if (idx < nvec) {
-        if (EPV == 8) {
+        if constexpr (EPV == 8) {
           float o[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = v[k][e % EPV] * f;
           st_stream_v8(yr + (int64_t)idx * EPV, o);
-        } else {
+        } else if constexpr (EPV == 4) {
           st_stream_v4(yr + (int64_t)idx * EPV, v[k][0] * f, v[k][1 % EPV] * f,
                        v[k][2 % EPV] * f, v[k][3 % EPV] * f);
+        } else {
+          *reinterpret_cast<float2 *>(yr + (int64_t)idx * EPV) =
+              make_float2(v[k][0] * f, v[k][1 % EPV] * f);
         }
       }
     }
@@ -189,13 +193,14 @@ k_lnstats_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, floa
   const int tid = threadIdx.x;
   const int nvec = cols / EPV;
   const float inv_n = 1.0f / (float)cols;
-  uint4 raw[NV];
+  using W = typename In::W;
+  W raw[NV];
   auto fetch = [&](int64_t r) {
-    const uint4 *q = reinterpret_cast<const uint4 *>(x + r * (int64_t)cols);
+    const W *q = reinterpret_cast<const W *>(x + r * (int64_t)cols);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int idx = k * THREADS + tid;
-      if (idx < nvec) raw[k] = ld_stream_u4(q + idx);
+      if (idx < nvec) raw[k] = In::ldv(q + idx);
     }
   };
   if ((int64_t)blockIdx.x < rows) fetch(blockIdx.x);
@@ -284,13 +289,14 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
   const int nvec = cols / EPV;
   const bool gb32 = aligned32(gamma, beta);
   const float inv_n = 1.0f / (float)cols;
-  uint4 raw[NV];
+  using W = typename In::W;
+  W raw[NV];
   auto fetch = [&](int64_t r) {
-    const uint4 *q = reinterpret_cast<const uint4 *>(x + r * (int64_t)cols);
+    const W *q = reinterpret_cast<const W *>(x + r * (int64_t)cols);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int idx = k * THREADS + tid;
-      if (idx < nvec) raw[k] = ld_stream_u4(q + idx);
+      if (idx < nvec) raw[k] = In::ldv(q + idx);
     }
   };
   if ((int64_t)blockIdx.x < rows) fetch(blockIdx.x);
@@ -338,11 +344,13 @@ k_layernorm_reg(const typename In::S *__restrict__ x, int64_t rows, int cols, fl
         for (int e = 0; e < EPV; e += 2)
           pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
                                   fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
-        if (EPV == 8) {
+        if constexpr (EPV == 8) {
           *reinterpret_cast<uint4 *>(yr + idx * EPV) = make_uint4(pk[0], pk[1 % (EPV / 2)],
                                                                   pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
-        } else {
+        } else if constexpr (EPV == 4) {
           *reinterpret_cast<uint2 *>(yr + idx * EPV) = make_uint2(pk[0], pk[1 % (EPV / 2)]);
+        } else {
+          *reinterpret_cast<uint32_t *>(yr + idx * EPV) = pk[0];
         }
       }
     }
@@ -408,6 +416,10 @@ inline int pick_nv(int64_t nvec) {
 // geometry, 3-14% slower on their own, so that both fold in the same order
 // and return the same mean and rstd bits.
 constexpr int kRowWideThreads = 512;
+// Rows of 1025 to 1536 vectors take 288 or 384 threads (4 vectors each)
+// instead of 512, so that a row just past 1024 vectors does not leave half
+// the slots empty (16384 x 4100 bf16: 1025 8-byte vectors).
+inline int wide_threads(int64_t nvec) { return nvec <= 1152 ? 288 : (nvec <= 1536 ? 384 : 512); }
 
 // ---------------------------------------------------------------------------
 // Split-K tier of the two-pass row operations ("reduce" page, split-K tier;
@@ -654,12 +666,18 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
 // cluster: RR_MAX_CLUSTER caps it, no cluster launch makes it 1).
 template <class In>
 inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int tier, int C,
-                            const DevInfo &d, int mode, const void *x, const void *out) {
+                            const DevInfo &d, int mode, const void *x, const void *out,
+                            bool half = false) {
   const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
   const int dt = In::EPV == 8 ? RR_BF16 : RR_F32;
   return plan_rowwise(rows, cols, dt, vec, mode, tier, C, d.sm_count, d.cluster_launch ? cap : 1,
-                      rowwise_warp_out_vec(mode, dt, x, out));
+                      rowwise_warp_out_vec(mode, dt, x, out), half && tier == RR_TIER_AUTO);
 }
+
+// The 8-byte vector element type of an input type.
+template <class In> struct HalfOf;
+template <> struct HalfOf<InBF16> { using T = InBF16h; };
+template <> struct HalfOf<InF32> { using T = InF32h; };
 
 template <class In>
 int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStream_t s,
@@ -670,7 +688,9 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ax % 16 == 0 &&
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y);
+  using H = typename HalfOf<In>::T;
+  const bool half = cols % H::EPV == 0 && ax % 8 == 0 && ay % (H::EPV * 4) == 0;
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y, half);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.ring && ay % 32 == 0) {
@@ -691,7 +711,20 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
-  if (reg) {
+  if (pk.half) {
+#define RR_SM_REGH(T, NV)                                                      \
+  {                                                                            \
+    auto k = k_softmax_reg<T, NV, H>;                                          \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0, x, rows, (int)cols, y); \
+  }
+    switch (pick_nv(cols / H::EPV)) {
+      case 1: RR_SM_REGH(kRowThreads, 1) break;
+      case 2: RR_SM_REGH(kRowThreads, 2) break;
+      case 4: RR_SM_REGH(kRowThreads, 4) break;
+      default: RR_SM_REGH(kRowThreads, 8) break;
+    }
+#undef RR_SM_REGH
+  } else if (reg) {
 #define RR_SM_REG(T, NV)                                                       \
   {                                                                            \
     auto k = k_softmax_reg<T, NV, In>;                                         \
@@ -718,7 +751,9 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr);
+  using H = typename HalfOf<In>::T;
+  const bool half = cols % H::EPV == 0 && (uintptr_t)xv % 8 == 0;
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr, half);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.ring) {
@@ -739,7 +774,24 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                                nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
-  if (reg) {
+  if (pk.half) {
+#define RR_LN_REGH(T, NV)                                                      \
+  {                                                                            \
+    auto k = k_lnstats_reg<T, NV, H>;                                          \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0, x, rows, (int)cols, eps, mean, rstd); \
+  }
+    switch (pick_nv(cols / H::EPV)) {  // the rewrite's geometry: the same bits
+      case 1: RR_LN_REGH(kRowThreads, 1) break;
+      case 2: RR_LN_REGH(kRowThreads, 2) break;
+      case 4: RR_LN_REGH(kRowThreads, 4) break;
+      default:
+        if (wide_threads(cols / H::EPV) == 288) RR_LN_REGH(288, 4)
+        else if (wide_threads(cols / H::EPV) == 384) RR_LN_REGH(384, 4)
+        else RR_LN_REGH(kRowWideThreads, 4)
+        break;
+    }
+#undef RR_LN_REGH
+  } else if (reg) {
 #define RR_LN_REG(T, NV)                                                       \
   {                                                                            \
     auto k = k_lnstats_reg<T, NV, In>;                                         \
@@ -749,7 +801,11 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
       case 1: RR_LN_REG(kRowThreads, 1) break;
       case 2: RR_LN_REG(kRowThreads, 2) break;
       case 4: RR_LN_REG(kRowThreads, 4) break;
-      default: RR_LN_REG(kRowWideThreads, 4) break;
+      default:
+        if (wide_threads(nvec) == 288) RR_LN_REG(288, 4)
+        else if (wide_threads(nvec) == 384) RR_LN_REG(384, 4)
+        else RR_LN_REG(kRowWideThreads, 4)
+        break;
     }
 #undef RR_LN_REG
   } else {
@@ -769,7 +825,11 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0) &&
                    ((uintptr_t)gamma % 16 == 0) && ((uintptr_t)beta % 16 == 0) &&
                    ((uintptr_t)y % (2 * In::EPV) == 0);
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y);
+  using H = typename HalfOf<In>::T;
+  const bool half = cols % H::EPV == 0 && (uintptr_t)xv % 8 == 0 &&
+                    (uintptr_t)gamma % (H::EPV * 4) == 0 && (uintptr_t)beta % (H::EPV * 4) == 0 &&
+                    (uintptr_t)y % (H::EPV * 2) == 0;
+  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y, half);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
   *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
   if (pk.ring && (uintptr_t)y % 16 == 0) {
@@ -790,7 +850,25 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
   const bool reg = vec && pick_nv(nvec) > 0;
-  if (reg) {
+  if (pk.half) {
+#define RR_LNF_REGH(T, NV)                                                     \
+  {                                                                            \
+    auto k = k_layernorm_reg<T, NV, H>;                                        \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0,   \
+        x, rows, (int)cols, eps, gamma, beta, y, mean, rstd);                  \
+  }
+    switch (pick_nv(cols / H::EPV)) {
+      case 1: RR_LNF_REGH(kRowThreads, 1) break;
+      case 2: RR_LNF_REGH(kRowThreads, 2) break;
+      case 4: RR_LNF_REGH(kRowThreads, 4) break;
+      default:
+        if (wide_threads(cols / H::EPV) == 288) RR_LNF_REGH(288, 4)
+        else if (wide_threads(cols / H::EPV) == 384) RR_LNF_REGH(384, 4)
+        else RR_LNF_REGH(kRowWideThreads, 4)
+        break;
+    }
+#undef RR_LNF_REGH
+  } else if (reg) {
 #define RR_LNF_REG(T, NV)                                                      \
   {                                                                            \
     auto k = k_layernorm_reg<T, NV, In>;                                       \
@@ -801,7 +879,11 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
       case 1: RR_LNF_REG(kRowThreads, 1) break;
       case 2: RR_LNF_REG(kRowThreads, 2) break;
       case 4: RR_LNF_REG(kRowThreads, 4) break;
-      default: RR_LNF_REG(kRowWideThreads, 4) break;
+      default:
+        if (wide_threads(nvec) == 288) RR_LNF_REG(288, 4)
+        else if (wide_threads(nvec) == 384) RR_LNF_REG(384, 4)
+        else RR_LNF_REG(kRowWideThreads, 4)
+        break;
     }
 #undef RR_LNF_REG
   } else {
@@ -831,6 +913,7 @@ static int rowwise_splitk_cluster(int64_t rows, int64_t cols, int sm_count, int 
 // per thread); forced split-K stages its slices when RR_ROW_STAGED_SPLITK
 // and they fit.
 constexpr int64_t kRowStagedMinVec[3] = {1024, kRowRegMaxVec, kRowRegMaxVec};
+constexpr int64_t kRowThreadsHost = 256;  // kRowThreads, for the host plan
 // Rows that are not 16-byte aligned have no register form: they are staged
 // beyond these lengths in 16-byte vectors (softmax, statistics, rewrite),
 // shorter ones take the scalar form.  Measured against that form and the
@@ -843,7 +926,7 @@ constexpr int64_t kRowStagedMinVecMis[3] = {32, 1024, 2048};
 #endif
 
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster, bool out_vec) {
+                     int C, int sm_count, int max_cluster, bool out_vec, bool half) {
   const bool rewrite = mode == kModeLayernorm;
   const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
   const int64_t nvec = vec ? cols * elt / 16 : 0;
@@ -911,6 +994,11 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // 0.87 -- shorter rows stage)
   if (mode == kModeStats && ring_ok && row_vecs > kRowRegMaxVec && cols * elt >= (128 << 10))
     return {RR_TIER_BLOCK, 1, false, true};
+  // rows whose base is only 8-byte aligned (widths of 4k bf16 / 2k fp32
+  // elements that are not 8k / 4k): the register form read as 8-byte
+  // vectors, up to 2048 of them, rather than staging or the scalar form
+  if (!vec && half && cols / (in_dtype == RR_BF16 ? 4 : 2) <= (int64_t)kRowThreadsHost * 8)
+    return RowPlan{RR_TIER_BLOCK, 1, false, false, true};
   if (row_vecs > staged_min) {
     const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster, vec);
     if (sc == 1) return {RR_TIER_BLOCK, 1, true};

@@ -20,9 +20,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Input element types: bf16 (held as its raw 16 bits) or fp32.
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// Input element types: bf16 (held as its raw 16 bits) or fp32, read as
+// 16-byte vectors (W = uint4) -- or, for rows whose base is only 8-byte
+// aligned (InBF16h, InF32h), as 8-byte vectors (W = uint2).
 struct InBF16 {
   using S = unsigned short;
+  using W = uint4;
+  static __device__ __forceinline__ W ldv(const W *p) { return ld_stream_u4(p); }
   static constexpr int EPV = 8;  // elements per 16-byte vector
   static __device__ __forceinline__ void unpack(const uint4 &w, float (&o)[8]) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -39,10 +50,40 @@ struct InBF16 {
 };
 struct InF32 {
   using S = float;
+  using W = uint4;
+  static __device__ __forceinline__ W ldv(const W *p) { return ld_stream_u4(p); }
   static constexpr int EPV = 4;
   static __device__ __forceinline__ void unpack(const uint4 &w, float (&o)[4]) {
     o[0] = __uint_as_float(w.x); o[1] = __uint_as_float(w.y);
     o[2] = __uint_as_float(w.z); o[3] = __uint_as_float(w.w);
+  }
+  static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
+  static __device__ __forceinline__ float cvt(S r) { return r; }
+};
+struct InBF16h {
+  using S = unsigned short;
+  using W = uint2;
+  static __device__ __forceinline__ W ldv(const W *p) { return ld_stream_u2(p); }
+  static constexpr int EPV = 4;  // elements per 8-byte vector
+  static __device__ __forceinline__ void unpack(const uint2 &w, float (&o)[4]) {
+    o[0] = __uint_as_float(w.x << 16);
+    o[1] = __uint_as_float(w.x & 0xffff0000u);
+    o[2] = __uint_as_float(w.y << 16);
+    o[3] = __uint_as_float(w.y & 0xffff0000u);
+  }
+  static __device__ __forceinline__ float load1(const S *p) {
+    return __uint_as_float(((uint32_t)__ldg(p)) << 16);
+  }
+  static __device__ __forceinline__ float cvt(S r) { return __uint_as_float(((uint32_t)r) << 16); }
+};
+struct InF32h {
+  using S = float;
+  using W = uint2;
+  static __device__ __forceinline__ W ldv(const W *p) { return ld_stream_u2(p); }
+  static constexpr int EPV = 2;
+  static __device__ __forceinline__ void unpack(const uint2 &w, float (&o)[2]) {
+    o[0] = __uint_as_float(w.x);
+    o[1] = __uint_as_float(w.y);
   }
   static __device__ __forceinline__ float load1(const S *p) { return __ldg(p); }
   static __device__ __forceinline__ float cvt(S r) { return r; }
@@ -102,6 +143,50 @@ __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// ---------------------------------------------------------------------------
+// The layernorm statistics as a monoid: (count, mean, M2), M2 the sum of
+// squared deviations from the mean, merged with the update of Chan, Golub
+// and LeVeque ("Updating formulae and a pairwise algorithm for computing
+// sample variances", 1979): n = na + nb, d = mean_b - mean_a,
+// mean = mean_a + d nb / n, M2 = M2a + M2b + d^2 na nb / n.
+// ---------------------------------------------------------------------------
+// Monoid state of the layernorm statistics: count, mean and M2.
+struct Chan {
+  uint32_t n;
+  float mean, m2;
+};
+
+__device__ __forceinline__ Chan chan_merge(const Chan &a, const Chan &b) {
+  if (b.n == 0) return a;
+  if (a.n == 0) return b;
+  Chan r;
+  r.n = a.n + b.n;
+  // the weight nb / n to about 2 ulp (a reciprocal and a product): its error
+  // moves the mean by ~2^-23 |d|, far inside the statistics' tolerance
+  const float wb = __fdividef((float)b.n, (float)r.n);
+  const float d = b.mean - a.mean;
+  r.mean = fmaf(d, wb, a.mean);
+  r.m2 = (a.m2 + b.m2) + (d * d) * ((float)a.n * wb);
+  return r;
+}
+
+// Xor butterfly over a warp's lanes (SEG a power of two); the lower lane of
+// each pair is always the left operand, so both lanes of a pair compute the
+// same expression and lane 0's result depends only on the lanes' values.
+template <int SEG>
+__device__ __forceinline__ Chan chan_warp(Chan v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = SEG / 2; o > 0; o >>= 1) {
+    Chan q;
+    q.n = __shfl_xor_sync(0xffffffffu, v.n, o);
+    q.mean = __shfl_xor_sync(0xffffffffu, v.mean, o);
+    q.m2 = __shfl_xor_sync(0xffffffffu, v.m2, o);
+    v = (lane & o) ? chan_merge(q, v) : chan_merge(v, q);
+  }
+  return v;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
@@ -111,7 +196,7 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 enum { kModeSoftmax = 0, kModeStats = 1, kModeLayernorm = 2 };
 
 // gamma[off .. off+N) and beta[off .. off+N) of the layernorm rewrite
-// (N = 4 or 8, 16-byte aligned), through the read-only path and kept in L1:
+// (N = 2 with 8-byte, N = 4 or 8 with 16-byte aligned offsets), through the read-only path and kept in L1:
 // every row reads the same values.  With both 32-byte aligned (`a32`) an
 // 8-value group is one 256-bit load per array.  Lanes of a warp hold
 // adjacent groups, so a warp's load spans 32 groups either way; two 128-bit
@@ -134,6 +219,13 @@ __device__ __forceinline__ void load_gamma_beta(const float *__restrict__ gamma,
           : "l"(beta + off));
       return;
     }
+  }
+  if constexpr (N == 2) {
+    const float2 gv = __ldg(reinterpret_cast<const float2 *>(gamma + off));
+    const float2 bv = __ldg(reinterpret_cast<const float2 *>(beta + off));
+    g[0] = gv.x; g[1] = gv.y;
+    b[0] = bv.x; b[1] = bv.y;
+    return;
   }
 #pragma unroll
   for (int e = 0; e < N; e += 4) {

@@ -87,6 +87,7 @@ struct RowPlan {
   int width;
   bool staged;
   bool ring = false;  // streamed through a shared-memory ring (rowring.cu)
+  bool half = false;  // block tier, row in registers read as 8-byte vectors
 };
 // Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
 // cols is a multiple of the 16-byte vector and every operand meets the
@@ -95,8 +96,11 @@ struct RowPlan {
 // cannot run.
 // out_vec: for rows that are not aligned vectors, whether the output shares
 // x's offset within a 16-byte chunk (true for 16-byte aligned bases).
+// half: the rows are not 16-byte aligned vectors but every operand allows the
+// 8-byte vector register form (cols a multiple of 4 bf16 / 2 fp32, x and the
+// outputs 8-byte aligned, gamma / beta as that form loads them).
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster, bool out_vec = true);
+                     int C, int sm_count, int max_cluster, bool out_vec = true, bool half = false);
 // Vectors per row up to which the block tier holds the row in registers
 // (256 threads x 8 vectors).
 constexpr int64_t kRowRegMaxVec = 2048;

@@ -753,3 +753,28 @@ def test_ring_repeatable_and_huge_rows(rr, oracle_mod):
     bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / (1 << 25))
     assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
     assert_rel_close(to_np(rstd), rr_, 1e-5, what="ring rstd 2^25")
+
+
+# ---------------------------------------------------------------------------
+# Rows whose base is 8-byte but not 16-byte aligned (4k bf16 / 2k fp32
+# columns that are not 8k / 4k, or x 8 bytes past a 16-byte boundary): the
+# block tier's register form read as 8-byte vectors.  Widths give a thread
+# fewer vectors than threads, 1-8 vectors a thread, the 512-thread layernorm
+# geometry past 1024 vectors; more rows than one persistent wave.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_half_vector_rows(rr, oracle_mod, dtype):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    epv = 8 if dtype == torch.bfloat16 else 4
+    half = epv // 2
+    rows = 3 * sms + 5
+    widths = ([4100, 1028, 2052, 6148, 8188] if epv == 8 else [2050, 514, 1026, 3074, 4094])
+    for i, cols in enumerate(widths):
+        x = _x(rows, cols, dtype, 2900 + i, 2.0)
+        idx = np.r_[0:4, rows // 2, rows - 4:rows]
+        _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=(("block", 1), False))
+        assert rr.last_form() == "direct"
+    # an aligned width with x one 8-byte half-vector past a 16-byte boundary
+    cols = 2048 if epv == 8 else 1024
+    x = _x(rows, cols, dtype, 2950, 2.0, offset=half)
+    _check_all_row_ops(rr, oracle_mod, x, np.r_[0:3, rows - 3:rows], expect_tier=(("block", 1), False))

@@ -218,7 +218,9 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, "staged")),   # misaligned rows staged
     (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, "staged")),
     (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, "staged")),  # + 8 elements > 96 KiB
-    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # misaligned rows: softmax
+    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # 8-byte vector rows:
+    (16384, 8188, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # registers up to 2048
+    (16384, 8196, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # 8-byte vectors
     (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # stages from 1024 vectors,
     (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # the statistics from 1024,
     (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, "direct")),   # the rewrite from 2048
