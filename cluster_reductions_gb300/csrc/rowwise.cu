@@ -997,7 +997,10 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // rows whose base is only 8-byte aligned (widths of 4k bf16 / 2k fp32
   // elements that are not 8k / 4k): the register form read as 8-byte
   // vectors, up to 2048 of them, rather than staging or the scalar form
-  if (!vec && half && cols / (in_dtype == RR_BF16 ? 4 : 2) <= (int64_t)kRowThreadsHost * 8)
+  // (softmax up to 1024 of them: beyond, staging measured ahead, 16384 x 4100
+  // bf16 0.74 against 0.57)
+  if (!vec && half &&
+      cols / (in_dtype == RR_BF16 ? 4 : 2) <= (int64_t)kRowThreadsHost * (mode == kModeSoftmax ? 4 : 8))
     return RowPlan{RR_TIER_BLOCK, 1, false, false, true};
   if (row_vecs > staged_min) {
     const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster, vec);

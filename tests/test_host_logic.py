@@ -218,10 +218,13 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, "staged")),   # misaligned rows staged
     (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, "staged")),
     (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, "staged")),  # + 8 elements > 96 KiB
-    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # 8-byte vector rows:
-    (16384, 8188, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # registers up to 2048
-    (16384, 8196, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # 8-byte vectors
-    (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # stages from 1024 vectors,
+    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # 8-byte vector rows:
+    (16384, 4092, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # registers up to 1024
+    (16384, 8188, "layernorm", "bf16", True, 16, ("block", 1, "direct")),  # 8-byte vectors for
+    (16384, 8196, "layernorm", "bf16", True, 16, ("block", 1, "direct")),  # softmax, 2048 for the
+    (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # statistics / rewrite;
+    (16384, 4098, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # the statistics of rows
+    (16384, 4098, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # not 8-byte aligned
     (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # the statistics from 1024,
     (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, "direct")),   # the rewrite from 2048
     (4096, 16396, "layernorm", "bf16", True, 16, ("block", 1, "staged")),
