@@ -994,6 +994,8 @@ PROFILE_CASES = {
     "long_layernorm_608x262144_bf16": ({"shape": (608, 262144), "op": "layernorm"}, "medium", 1.0),
     "ring_lnstats_8192x16392_bf16": ({"shape": (8192, 16392), "op": "lnstats"}, "medium", 1.0),
     "rowsk_lnstats_32x524288_bf16": ({"shape": (32, 1 << 19), "op": "lnstats"}, "medium", 1.0),
+    # rows 8-byte but not 16-byte aligned: the register form read as 8-byte vectors
+    "medium_layernorm_16384x4100_bf16": ({"shape": (16384, 4100), "op": "layernorm"}, "medium", 1.0),
 }
 
 
