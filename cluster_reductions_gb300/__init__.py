@@ -214,19 +214,57 @@ def reduce_axis(x: torch.Tensor, op="sum", dim: int = 0, *, out: Optional[torch.
     return _deliver(o, out, x)
 
 
-def _rowwise_opts(tier, cluster_size, lanes_per_row=0):
-    if tier is None and not cluster_size and not lanes_per_row:
+def _rowwise_opts(tier, cluster_size, lanes_per_row=0, splits=0, ws=None):
+    if tier is None and not cluster_size and not lanes_per_row and not splits and ws is None:
         return None
     return ctypes.byref(_lib.rr_rowwise_opts(_TIERS[tier] if not isinstance(tier, int) else tier,
-                                             int(cluster_size), int(lanes_per_row)))
+                                             int(cluster_size), int(lanes_per_row), int(splits),
+                                             _ptr(ws),
+                                             0 if ws is None else ws.numel() * ws.element_size()))
+
+
+@functools.lru_cache(maxsize=256)
+def _row_ws_bytes(device: int, rows: int, cols: int, dt: int, row_op: int) -> int:
+    n = ctypes.c_size_t(0)
+    with torch.cuda.device(device):
+        check(load().rr_rowwise_workspace_size(rows, cols, dt, row_op, ctypes.byref(n)),
+              "rr_rowwise_workspace_size")
+    return n.value
+
+
+def _row_ws(xd: torch.Tensor, row_op: str, tier, splits: int, workspace):
+    """The workspace of a row op (the grid form's partial states): the
+    caller's tensor, none (workspace=False), or one of the size the
+    automatic plan (or a forced `splits`) asks for, allocated here on the
+    current stream."""
+    if workspace is False:
+        return None
+    if workspace is not None:
+        return workspace
+    rows, cols = xd.shape
+    if splits > 0:
+        need = rows * splits * 16
+    elif tier is None or tier == "auto":
+        if xd.data_ptr() % 16 or rows == 0:
+            return None
+        need = _row_ws_bytes(xd.device.index, rows, cols, _DT[xd.dtype], _ROW_OPS[row_op])
+    else:
+        return None
+    if not need:
+        return None
+    return torch.empty((need + 15) // 16 * 4, dtype=torch.int32, device=xd.device)
 
 
 @_on_input_device
 def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
-            cluster_size: int = 0, lanes_per_row: int = 0) -> torch.Tensor:
+            cluster_size: int = 0, lanes_per_row: int = 0, splits: int = 0,
+            workspace=None) -> torch.Tensor:
     """rr_softmax / rr_softmax_ex: row softmax of a bf16 or fp32 [rows, cols]
     tensor, fp32 out.  tier: None/"auto", "warp", "block" or "splitk";
-    cluster_size for split-K, lanes_per_row for the warp tier."""
+    cluster_size for split-K, lanes_per_row for the warp tier; splits (with
+    tier "splitk") forces the grid form with that many CTAs per row.
+    workspace: None (allocated here when the plan wants one), False (none),
+    or a device tensor."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -234,7 +272,8 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"softmax: dtype {xd.dtype} not supported (bfloat16, float32)")
     o = _out_buf(out, (rows, cols), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
+    ws = _row_ws(xd, "softmax", tier, splits, workspace)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row, splits, ws)
     if opts is None:
         st = load().rr_softmax(_ptr(xd), rows, cols, dt, _ptr(o), _stream())
     else:
@@ -247,11 +286,11 @@ def softmax(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, tier=None,
 def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
                     mean: Optional[torch.Tensor] = None,
                     rstd: Optional[torch.Tensor] = None, tier=None,
-                    cluster_size: int = 0,
-                    lanes_per_row: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+                    cluster_size: int = 0, lanes_per_row: int = 0, splits: int = 0,
+                    workspace=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """rr_layernorm_stats / rr_layernorm_stats_ex: per-row mean and
     1/sqrt(var + eps), fp32.  tier: None/"auto", "warp", "block" or
-    "splitk"."""
+    "splitk"; splits / workspace as for softmax."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -260,7 +299,8 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
         raise TypeError(f"layernorm_stats: dtype {xd.dtype} not supported")
     mu = _out_buf(mean, (rows,), torch.float32, xd.device)
     rs = _out_buf(rstd, (rows,), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
+    ws = _row_ws(xd, "lnstats", tier, splits, workspace)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row, splits, ws)
     if opts is None:
         st = load().rr_layernorm_stats(_ptr(xd), rows, cols, dt, float(eps), _ptr(mu), _ptr(rs),
                                        _stream())
@@ -275,10 +315,12 @@ def layernorm_stats(x: torch.Tensor, eps: float = 1e-5, *,
 def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
               out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
               rstd: Optional[torch.Tensor] = None, tier=None,
-              cluster_size: int = 0, lanes_per_row: int = 0) -> torch.Tensor:
+              cluster_size: int = 0, lanes_per_row: int = 0, splits: int = 0,
+              workspace=None) -> torch.Tensor:
     """rr_layernorm / rr_layernorm_ex: bf16 (x - mean) * rstd * gamma + beta per
     row of a bf16 or fp32 [rows, cols] tensor; gamma, beta fp32 [cols].
-    mean / rstd (fp32 [rows]) are filled when given."""
+    mean / rstd (fp32 [rows]) are filled when given; splits / workspace as
+    for softmax."""
     x = _as_2d(x)
     xd = _to_device(x)
     rows, cols = xd.shape
@@ -294,7 +336,8 @@ def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: flo
     o = _out_buf(out, (rows, cols), torch.bfloat16, xd.device)
     mu = None if mean is None else _out_buf(mean, (rows,), torch.float32, xd.device)
     rs = None if rstd is None else _out_buf(rstd, (rows,), torch.float32, xd.device)
-    opts = _rowwise_opts(tier, cluster_size, lanes_per_row)
+    ws = _row_ws(xd, "layernorm", tier, splits, workspace)
+    opts = _rowwise_opts(tier, cluster_size, lanes_per_row, splits, ws)
     args = (_ptr(xd), rows, cols, dt, float(eps), _ptr(gd), _ptr(bd), _ptr(o), _ptr(mu),
             _ptr(rs), _stream())
     st = load().rr_layernorm(*args) if opts is None else load().rr_layernorm_ex(*args, opts)
@@ -420,7 +463,7 @@ def device_status() -> int:
 def last_tier() -> Tuple[str, int]:
     """(tier, width) of the last reduce / softmax / layernorm call."""
     v = int(load().rr_last_tier())
-    return TIER_NAMES.get(v & 0xff, "?"), (v >> 8) & 0xff
+    return TIER_NAMES.get(v & 0xff, "?"), ((v >> 8) & 0xff) | (((v >> 19) & 0xff) << 8)
 
 
 def last_staged() -> bool:
@@ -429,9 +472,13 @@ def last_staged() -> bool:
 
 
 def last_form() -> str:
-    """How the last row operation read its rows: "ring" (streamed through a
-    shared-memory ring), "staged" (held in shared memory) or "direct"."""
+    """How the last row operation read its rows: "grid" (split-K over a
+    plain grid, partial states through the workspace), "ring" (streamed
+    through a shared-memory ring), "staged" (held in shared memory) or
+    "direct"."""
     v = int(load().rr_last_tier())
+    if (v >> 18) & 1:
+        return "grid"
     return "ring" if (v >> 17) & 1 else ("staged" if (v >> 16) & 1 else "direct")
 
 
@@ -448,22 +495,25 @@ _ROW_OPS = {"softmax": 0, "lnstats": 1, "layernorm_stats": 1, "layernorm": 2}
 
 def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: int,
                  dtype=torch.bfloat16, aligned: bool = True, staged: bool = False,
-                 form: bool = False):
+                 form: bool = False, with_workspace: bool = False):
     """rr_plan_rowwise (host only): the tier and width (lanes per row, cluster
-    size or 1) that softmax / layernorm_stats / layernorm pick; with
-    staged=True also whether the rows are staged in shared memory, with
-    form=True how they are read ("direct", "staged" or "ring")."""
+    size, CTAs per row of the grid form, or 1) that softmax / layernorm_stats
+    / layernorm pick -- with a workspace (with_workspace=True, as the
+    functions here pass one) or without; with staged=True also whether the
+    rows are staged in shared memory, with form=True how they are read
+    ("direct", "staged", "ring" or "grid")."""
     dt = _DT.get(dtype)
     if dt not in (RR_BF16, RR_F32):
         raise TypeError(f"plan_rowwise: dtype {dtype} not supported")
     t, w, st = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(load().rr_plan_rowwise(int(rows), int(cols), dt, _ROW_OPS[row_op], 1 if aligned else 0,
-                                 int(sm_count), int(max_cluster), ctypes.byref(t),
-                                 ctypes.byref(w), ctypes.byref(st)), "rr_plan_rowwise")
+                                 int(sm_count), int(max_cluster), 1 if with_workspace else 0,
+                                 ctypes.byref(t), ctypes.byref(w), ctypes.byref(st)),
+          "rr_plan_rowwise")
     if staged:
         return TIER_NAMES[t.value], w.value, st.value == 1
     if form:
-        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring")[st.value]
+        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring", "grid")[st.value]
     return TIER_NAMES[t.value], w.value
 
 

@@ -29,7 +29,8 @@ class rr_reduce_opts(ctypes.Structure):
 
 class rr_rowwise_opts(ctypes.Structure):
     _fields_ = [("tier", ctypes.c_int), ("cluster_size", ctypes.c_int),
-                ("lanes_per_row", ctypes.c_int)]
+                ("lanes_per_row", ctypes.c_int), ("splits", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class rr_axis_opts(ctypes.Structure):
@@ -88,8 +89,9 @@ SIGNATURES = {
     "rr_device_status": (_int, [_vp]),
     "rr_last_tier": (_int, []),
     "rr_status_string": (ctypes.c_char_p, [_int]),
-    "rr_plan_rowwise": (_int, [_i64, _i64, _int, _int, _int, _int, _int, ctypes.POINTER(_int),
-                               ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "rr_plan_rowwise": (_int, [_i64, _i64, _int, _int, _int, _int, _int, _int,
+                               ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "rr_rowwise_workspace_size": (_int, [_i64, _i64, _int, _int, ctypes.POINTER(ctypes.c_size_t)]),
     "rr_plan_reduce": (_int, [_i64, _i64, _int, _int, ctypes.POINTER(_int),
                               ctypes.POINTER(_int)]),
     "rr_test_wait_timeout": (_int, [_i64, _vp]),

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "rr")
 LIB = os.path.join(HERE, "librr.so")
-SOURCES = ["api.cu", "reduce.cu", "axis.cu", "rowwise.cu", "rowwarp.cu", "rowstaged.cu", "rowring.cu", "combine.cu", "cluster.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "reduce.cu", "axis.cu", "rowwise.cu", "rowwarp.cu", "rowstaged.cu", "rowring.cu", "rowgrid.cu", "combine.cu", "cluster.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <unordered_map>
 
@@ -243,8 +244,8 @@ int rr_plan_reduce(int64_t rows, int64_t cols, int sm_count, int max_cluster, in
 }
 
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int aligned,
-                    int sm_count, int max_cluster, int *tier_out, int *width_out,
-                    int *staged_out) {
+                    int sm_count, int max_cluster, int with_workspace, int *tier_out,
+                    int *width_out, int *staged_out) {
   if (rows < 0 || cols < 0 || sm_count < 1 || max_cluster < 1 || !tier_out || !width_out)
     return RR_ERR_INVALID;
   if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
@@ -253,10 +254,29 @@ int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int al
   const bool vec = aligned && cols % epv == 0;
   const bool half = aligned && cols % (epv / 2) == 0;  // 8-byte vectors
   const RowPlan p = plan_rowwise(rows, cols, in_dtype, vec, row_op, RR_TIER_AUTO, 0, sm_count,
-                                 max_cluster < 16 ? max_cluster : 16, true, half);
+                                 max_cluster < 16 ? max_cluster : 16, true, half,
+                                 with_workspace != 0 && vec);
   *tier_out = p.tier;
   *width_out = p.width;
-  if (staged_out) *staged_out = p.ring ? 2 : (p.staged ? 1 : 0);
+  if (staged_out) *staged_out = p.grid ? 3 : (p.ring ? 2 : (p.staged ? 1 : 0));
+  return RR_OK;
+}
+
+int rr_rowwise_workspace_size(int64_t rows, int64_t cols, int in_dtype, int row_op,
+                              size_t *bytes_out) {
+  if (rows < 0 || cols < 0 || !bytes_out) return RR_ERR_INVALID;
+  if (in_dtype != RR_BF16 && in_dtype != RR_F32) return RR_ERR_INVALID;
+  if (row_op < RR_ROW_SOFTMAX || row_op > RR_ROW_LAYERNORM) return RR_ERR_INVALID;
+  *bytes_out = 0;
+  int st = RR_OK;
+  const DevInfo *d = current_device(&st);
+  if (!d) return st;
+  const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
+  int tier = 0, width = 0, staged = 0;
+  st = rr_plan_rowwise(rows, cols, in_dtype, row_op, 1, d->sm_count, d->cluster_launch ? cap : 1,
+                       1, &tier, &width, &staged);
+  if (st != RR_OK) return st;
+  if (staged == 3) *bytes_out = rowgrid_ws_bytes(rows, width);
   return RR_OK;
 }
 
@@ -601,8 +621,36 @@ static bool rowwise_opts_ok(const rr_rowwise_opts *o) {
     return false;
   const int l = o->lanes_per_row;
   if (!(l == 0 || l == 1 || l == 2 || l == 4 || l == 8 || l == 16 || l == 32)) return false;
-  return o->cluster_size == 0 || o->cluster_size == 1 || o->cluster_size == 2 ||
-         o->cluster_size == 4 || o->cluster_size == 8 || o->cluster_size == 16;
+  if (!(o->cluster_size == 0 || o->cluster_size == 1 || o->cluster_size == 2 ||
+        o->cluster_size == 4 || o->cluster_size == 8 || o->cluster_size == 16))
+    return false;
+  // the grid form: forced only as split-K without a cluster, with a workspace
+  if (o->splits < 0 || o->splits > kRowGridMaxSplits) return false;
+  if (o->splits > 0 && (o->tier != RR_TIER_SPLITK || o->cluster_size > 1 || !o->workspace))
+    return false;
+  if (o->workspace && (o->workspace_bytes == 0 || (uintptr_t)o->workspace % 16 != 0)) return false;
+  return true;
+}
+
+// The caller's workspace of a row op, and whether it overlaps any operand.
+static RowWs rowwise_ws(const rr_rowwise_opts *o) {
+  RowWs w;
+  if (o) {
+    w.ws = o->workspace;
+    w.bytes = o->workspace ? o->workspace_bytes : 0;
+    w.splits = o->splits;
+  }
+  return w;
+}
+struct Span {
+  const void *p;
+  size_t n;
+};
+static bool ws_overlaps(const RowWs &w, std::initializer_list<Span> spans) {
+  if (!w.ws) return false;
+  for (const Span &sp : spans)
+    if (sp.p && overlaps(w.ws, w.bytes, sp.p, sp.n)) return true;
+  return false;
 }
 
 // The width a forced row-op tier takes: lanes per row for the warp tier, the
@@ -628,12 +676,15 @@ int rr_softmax_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, float
   const size_t es = in_dtype == RR_BF16 ? 2 : 4;
   if (overlaps(x, (size_t)(rows * cols) * es, out, (size_t)(rows * cols) * 4)) return RR_ERR_INVALID;
   if ((uintptr_t)x % es != 0 || (uintptr_t)out % 4 != 0) return RR_ERR_INVALID;
+  const RowWs w = rowwise_ws(opts);
+  if (ws_overlaps(w, {{x, (size_t)(rows * cols) * es}, {out, (size_t)(rows * cols) * 4}}))
+    return RR_ERR_INVALID;
   int st = RR_OK;
   const DevInfo *d = current_device(&st);
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
   st = launch_softmax(x, rows, cols, in_dtype, out, as_stream(stream), *d, &tier,
-                      opts ? opts->tier : RR_TIER_AUTO, rowwise_width(opts));
+                      opts ? opts->tier : RR_TIER_AUTO, rowwise_width(opts), w);
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
@@ -657,13 +708,15 @@ int rr_layernorm_stats_ex(const void *x, int64_t rows, int64_t cols, int in_dtyp
   if (overlaps(x, nx, mean, no) || overlaps(x, nx, rstd, no) || overlaps(mean, no, rstd, no))
     return RR_ERR_INVALID;
   if ((uintptr_t)x % es != 0) return RR_ERR_INVALID;
+  const RowWs w = rowwise_ws(opts);
+  if (ws_overlaps(w, {{x, nx}, {mean, no}, {rstd, no}})) return RR_ERR_INVALID;
   int st = RR_OK;
   const DevInfo *d = current_device(&st);
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
   st = launch_layernorm_stats(x, rows, cols, in_dtype, eps, mean, rstd, as_stream(stream), *d,
                               &tier, opts ? opts->tier : RR_TIER_AUTO,
-                              rowwise_width(opts));
+                              rowwise_width(opts), w);
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }
@@ -698,13 +751,16 @@ int rr_layernorm_ex(const void *x, int64_t rows, int64_t cols, int in_dtype, flo
   if ((uintptr_t)x % es != 0 || (uintptr_t)gamma % 4 || (uintptr_t)beta % 4 ||
       (uintptr_t)out_bf16 % 2)
     return RR_ERR_INVALID;
+  const RowWs w = rowwise_ws(opts);
+  if (ws_overlaps(w, {{x, nx}, {out_bf16, ny}, {gamma, ng}, {beta, ng}, {mean, no}, {rstd, no}}))
+    return RR_ERR_INVALID;
   int st = RR_OK;
   const DevInfo *d = current_device(&st);
   if (!d) return st;
   int tier = RR_TIER_BLOCK;
   st = launch_layernorm(x, rows, cols, in_dtype, eps, gamma, beta, out_bf16, mean, rstd,
                         as_stream(stream), *d, &tier, opts ? opts->tier : RR_TIER_AUTO,
-                        rowwise_width(opts));
+                        rowwise_width(opts), w);
   if (st == RR_OK) g_last_tier.store(tier);
   return st;
 }

@@ -63,16 +63,6 @@ static_assert(kRingStages % kRingConsWarps == 0, "one consumer warp per slot");
 // (8 elements each) a lane: 96 units per leaf round of a warp.
 constexpr uint32_t kRingPieceBig = 12288, kRingPieceSmall = 6144;
 
-template <int SEG>
-__device__ __forceinline__ void ms_warp(float &m, float &s) {
-#pragma unroll
-  for (int o = SEG / 2; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_combine(m, s, m2, s2);  // symmetric: both lanes get the same bits
-  }
-}
-
 // 8 elements (a "unit": 16 bytes of bf16, 32 bytes of fp32) of a ring slot.
 template <class In>
 __device__ __forceinline__ void ring_unit(const unsigned char *slot, int u, float (&e)[8]) {

@@ -667,11 +667,39 @@ int launch_rowwise_splitk(const void *xv, int64_t rows, int64_t cols, float eps,
 template <class In>
 inline RowPlan rowwise_pick(int64_t rows, int64_t cols, bool vec, int tier, int C,
                             const DevInfo &d, int mode, const void *x, const void *out,
-                            bool half = false) {
+                            bool half = false, bool grid_ok = false) {
   const int cap = cluster_cap() < 16 ? cluster_cap() : 16;
   const int dt = In::EPV == 8 ? RR_BF16 : RR_F32;
   return plan_rowwise(rows, cols, dt, vec, mode, tier, C, d.sm_count, d.cluster_launch ? cap : 1,
-                      rowwise_warp_out_vec(mode, dt, x, out), half && tier == RR_TIER_AUTO);
+                      rowwise_warp_out_vec(mode, dt, x, out), half && tier == RR_TIER_AUTO,
+                      grid_ok && tier == RR_TIER_AUTO);
+}
+
+// rr_last_tier's code: tier | (width & 0xff) << 8 | flags << 16 |
+// (width >> 8) << 19, flags 1 staged, 2 ring, 4 grid.
+inline int tier_code(int tier, int width, int flags) {
+  return tier | ((width & 0xff) << 8) | (flags << 16) | (((width >> 8) & 0xff) << 19);
+}
+constexpr int kFlagStaged = 1, kFlagRing = 2, kFlagGrid = 4;
+
+// The grid form's plan for a call: forced (w.splits), automatic with the
+// caller's workspace (falling back to the plan without one when it is too
+// small), or none.  grid_ok: the operands meet the form's alignment.
+template <class In>
+inline RowPlan rowwise_pick_ws(int64_t rows, int64_t cols, bool vec, int tier, int C,
+                               const DevInfo &d, int mode, const void *x, const void *out,
+                               bool half, bool grid_ok, const RowWs &w) {
+  grid_ok = grid_ok && w.ws != nullptr && (uintptr_t)w.ws % 16 == 0;
+  if (w.splits > 0) {
+    if (!grid_ok) return RowPlan{-1, 0, false};
+    RowPlan p{RR_TIER_SPLITK, w.splits, false};
+    p.grid = true;
+    return p;
+  }
+  RowPlan p = rowwise_pick<In>(rows, cols, vec, tier, C, d, mode, x, out, half, grid_ok);
+  if (p.grid && rowgrid_ws_bytes(rows, p.width) > w.bytes)
+    p = rowwise_pick<In>(rows, cols, vec, tier, C, d, mode, x, out, half, false);
+  return p;
 }
 
 // The 8-byte vector element type of an input type.
@@ -681,7 +709,7 @@ template <> struct HalfOf<InF32> { using T = InF32h; };
 
 template <class In>
 int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStream_t s,
-                 const DevInfo &d, int *tier_out, int tier, int C) {
+                 const DevInfo &d, int *tier_out, int tier, int C, const RowWs &w) {
   using S = typename In::S;
   const S *x = (const S *)xv;
   const uintptr_t ax = (uintptr_t)xv, ay = (uintptr_t)y;
@@ -690,15 +718,22 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
                    (In::EPV == 8 ? ay % 32 == 0 : ay % 16 == 0);
   using H = typename HalfOf<In>::T;
   const bool half = cols % H::EPV == 0 && ax % 8 == 0 && ay % (H::EPV * 4) == 0;
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y, half);
+  const RowPlan pk = rowwise_pick_ws<In>(rows, cols, vec, tier, C, d, kModeSoftmax, xv, y, half,
+                                         vec && cols % 8 == 0 && ay % 32 == 0, w);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  *tier_out = tier_code(pk.tier, pk.width, pk.staged ? kFlagStaged : 0);
+  if (pk.grid) {
+    *tier_out = tier_code(pk.tier, pk.width, kFlagGrid);
+    return launch_rowgrid(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, 0.0f, y,
+                          nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, w.ws, w.bytes, s,
+                          d);
+  }
   if (pk.ring && ay % 32 == 0) {
     int Cl = pk.width;
     const int st = launch_rowwise_ring(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows,
                                        cols, 0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr,
                                        pk.width, tier == RR_TIER_AUTO, &Cl, s, d);
-    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    *tier_out = tier_code(pk.tier, Cl, kFlagRing);
     return st;
   }
   if (pk.staged)
@@ -746,22 +781,30 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
 
 template <class In>
 int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *mean,
-                 float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
+                 float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C,
+                 const RowWs &w) {
   using S = typename In::S;
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
   const bool vec = (cols % In::EPV == 0) && ((uintptr_t)xv % 16 == 0);
   using H = typename HalfOf<In>::T;
   const bool half = cols % H::EPV == 0 && (uintptr_t)xv % 8 == 0;
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr, half);
+  const RowPlan pk = rowwise_pick_ws<In>(rows, cols, vec, tier, C, d, kModeStats, xv, nullptr,
+                                         half, vec && cols % 8 == 0, w);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  *tier_out = tier_code(pk.tier, pk.width, pk.staged ? kFlagStaged : 0);
+  if (pk.grid) {
+    *tier_out = tier_code(pk.tier, pk.width, kFlagGrid);
+    return launch_rowgrid(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+                          nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, w.ws, w.bytes,
+                          s, d);
+  }
   if (pk.ring) {
     int Cl = pk.width;
     const int st = launch_rowwise_ring(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                        eps, nullptr, mean, rstd, nullptr, nullptr, nullptr,
                                        pk.width, tier == RR_TIER_AUTO, &Cl, s, d);
-    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    *tier_out = tier_code(pk.tier, Cl, kFlagRing);
     return st;
   }
   if (pk.staged)
@@ -818,7 +861,7 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
 template <class In>
 int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const float *gamma,
                    const float *beta, uint16_t *y, float *mean, float *rstd, cudaStream_t s,
-                   const DevInfo &d, int *tier_out, int tier, int C) {
+                   const DevInfo &d, int *tier_out, int tier, int C, const RowWs &w) {
   using S = typename In::S;
   const S *x = (const S *)xv;
   const int64_t nvec = cols / In::EPV;
@@ -829,15 +872,21 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   const bool half = cols % H::EPV == 0 && (uintptr_t)xv % 8 == 0 &&
                     (uintptr_t)gamma % (H::EPV * 4) == 0 && (uintptr_t)beta % (H::EPV * 4) == 0 &&
                     (uintptr_t)y % (H::EPV * 2) == 0;
-  const RowPlan pk = rowwise_pick<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y, half);
+  const RowPlan pk = rowwise_pick_ws<In>(rows, cols, vec, tier, C, d, kModeLayernorm, xv, y, half,
+                                         vec && cols % 8 == 0 && (uintptr_t)y % 16 == 0, w);
   if (pk.tier < 0) return RR_ERR_UNSUPPORTED;
-  *tier_out = pk.tier | (pk.width << 8) | (pk.staged ? 1 << 16 : 0);
+  *tier_out = tier_code(pk.tier, pk.width, pk.staged ? kFlagStaged : 0);
+  if (pk.grid) {
+    *tier_out = tier_code(pk.tier, pk.width, kFlagGrid);
+    return launch_rowgrid(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+                          nullptr, mean, rstd, gamma, beta, y, pk.width, w.ws, w.bytes, s, d);
+  }
   if (pk.ring && (uintptr_t)y % 16 == 0) {
     int Cl = pk.width;
     const int st = launch_rowwise_ring(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows,
                                        cols, eps, nullptr, mean, rstd, gamma, beta, y, pk.width,
                                        tier == RR_TIER_AUTO, &Cl, s, d);
-    *tier_out = pk.tier | (Cl << 8) | (1 << 17);
+    *tier_out = tier_code(pk.tier, Cl, kFlagRing);
     return st;
   }
   if (pk.staged)
@@ -914,6 +963,8 @@ static int rowwise_splitk_cluster(int64_t rows, int64_t cols, int sm_count, int 
 // and they fit.
 constexpr int64_t kRowStagedMinVec[3] = {1024, kRowRegMaxVec, kRowRegMaxVec};
 constexpr int64_t kRowThreadsHost = 256;  // kRowThreads, for the host plan
+// Shortest rows the automatic plan gives the grid form (a few rows only).
+constexpr int64_t kRowGridMinCols = 16384;
 // Rows that are not 16-byte aligned have no register form: they are staged
 // beyond these lengths in 16-byte vectors (softmax, statistics, rewrite),
 // shorter ones take the scalar form.  Measured against that form and the
@@ -926,7 +977,7 @@ constexpr int64_t kRowStagedMinVecMis[3] = {32, 1024, 2048};
 #endif
 
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster, bool out_vec, bool half) {
+                     int C, int sm_count, int max_cluster, bool out_vec, bool half, bool grid_ok) {
   const bool rewrite = mode == kModeLayernorm;
   const int64_t elt = in_dtype == RR_BF16 ? 2 : 4;
   const int64_t nvec = vec ? cols * elt / 16 : 0;
@@ -968,6 +1019,13 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
       return {RR_TIER_SPLITK, C, false, true};
     const bool st = RR_ROW_STAGED_SPLITK && stage_fits(C);
     return {RR_TIER_SPLITK, C, st};
+  }
+  // a few long rows, with a workspace: the grid form (rowgrid.cu), the
+  // slices on every SM and no clusters
+  if (grid_ok && ring_ok && rows >= 1 && rows < sm_count && cols >= kRowGridMinCols) {
+    RowPlan p{RR_TIER_SPLITK, rowgrid_splits(rows, cols, sm_count), false};
+    p.grid = true;
+    return p;
   }
   const int c = rowwise_splitk_cluster(rows, cols, sm_count, max_cluster);
   if (c > 0) {
@@ -1023,27 +1081,29 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
 
 int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                      const float *gamma, const float *beta, uint16_t *y, float *mean, float *rstd,
-                     cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
+                     cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C,
+                     const RowWs &w) {
   if (in_dtype == RR_BF16)
     return layernorm_impl<InBF16>(x, rows, cols, eps, gamma, beta, y, mean, rstd, s, d, tier_out,
-                                  tier, C);
+                                  tier, C, w);
   return layernorm_impl<InF32>(x, rows, cols, eps, gamma, beta, y, mean, rstd, s, d, tier_out,
-                               tier, C);
+                               tier, C, w);
 }
 
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype, float *out,
-                   cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C) {
+                   cudaStream_t s, const DevInfo &d, int *tier_out, int tier, int C,
+                   const RowWs &w) {
   if (in_dtype == RR_BF16)
-    return softmax_impl<InBF16>(x, rows, cols, out, s, d, tier_out, tier, C);
-  return softmax_impl<InF32>(x, rows, cols, out, s, d, tier_out, tier, C);
+    return softmax_impl<InBF16>(x, rows, cols, out, s, d, tier_out, tier, C, w);
+  return softmax_impl<InF32>(x, rows, cols, out, s, d, tier_out, tier, C, w);
 }
 
 int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                            float *mean, float *rstd, cudaStream_t s, const DevInfo &d,
-                           int *tier_out, int tier, int C) {
+                           int *tier_out, int tier, int C, const RowWs &w) {
   if (in_dtype == RR_BF16)
-    return lnstats_impl<InBF16>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C);
-  return lnstats_impl<InF32>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C);
+    return lnstats_impl<InBF16>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C, w);
+  return lnstats_impl<InF32>(x, rows, cols, eps, mean, rstd, s, d, tier_out, tier, C, w);
 }
 
 }  // namespace rr

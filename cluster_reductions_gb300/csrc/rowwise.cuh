@@ -102,6 +102,18 @@ __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s
   s = a + b;
 }
 
+// Xor butterfly of (max, sum) states over segments of SEG lanes;
+// ms_combine is symmetric, so both lanes of a pair get the same bits.
+template <int SEG>
+__device__ __forceinline__ void ms_warp(float &m, float &s) {
+#pragma unroll
+  for (int o = SEG / 2; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_combine(m, s, m2, s2);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Two fp32 values in one 64-bit register (the lower element in the low
 // half) for the packed FP32 instructions of sm_100 and later

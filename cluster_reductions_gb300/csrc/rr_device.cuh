@@ -113,6 +113,26 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
+// L2 eviction policies for loads (createpolicy): evict_last keeps lines a
+// later kernel reads again ahead of other traffic; evict_first lets lines
+// read for the last time go first.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// ld_stream_u4 with an L2 eviction policy.
+__device__ __forceinline__ uint4 ld_stream_u4_hint(const void *p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+  return v;
+}
 // 32 contiguous bytes (8 x 32-bit) in one instruction; p 32-byte aligned.
 __device__ __forceinline__ void ld_stream_v8(const void *p, uint32_t (&r)[8]) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -192,6 +212,12 @@ __device__ __forceinline__ typename Op::T block_reduce(typename Op::T v,
 // nothing.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_begin() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid launch once every CTA of this one has called it or
+// exited, for a kernel one wave deep whose CTAs have issued their last
+// loads; the next grid's pdl_begin still waits for this grid to complete.
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ---------------------------------------------------------------------------
 // Thread-block cluster primitives (PTX).

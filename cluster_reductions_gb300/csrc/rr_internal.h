@@ -54,22 +54,32 @@ int launch_reduce_axis(const void *x, int64_t outer, int64_t axis, int64_t inner
                        cudaStream_t s, const DevInfo &d);
 
 // ---- softmax / layernorm statistics (rowwise.cu)
+// The caller's workspace for the grid form (rowgrid.cu): `ws` (16-byte
+// aligned, or null: no grid form) of `bytes` bytes; `splits` > 0 forces
+// the grid form with that many CTAs per row.
+struct RowWs {
+  void *ws = nullptr;
+  size_t bytes = 0;
+  int splits = 0;
+};
 // tier: RR_TIER_AUTO, RR_TIER_WARP, RR_TIER_BLOCK or RR_TIER_SPLITK; C:
 // split-K cluster size, or the warp tier's lanes per row (0 = automatic).
-// *tier_out receives (C << 8) | tier (C = lanes per row for the warp tier).
+// *tier_out receives tier | (width & 0xff) << 8 | staged << 16 | ring << 17
+// | grid << 18 | (width >> 8) << 19 (width: lanes per row for the warp
+// tier, CTAs per row for the grid form, else the cluster size).
 int launch_softmax(const void *x, int64_t rows, int64_t cols, int in_dtype,
                    float *out, cudaStream_t s, const DevInfo &d, int *tier_out,
-                   int tier, int C);
+                   int tier, int C, const RowWs &w);
 int launch_layernorm_stats(const void *x, int64_t rows, int64_t cols,
                            int in_dtype, float eps, float *mean, float *rstd,
                            cudaStream_t s, const DevInfo &d, int *tier_out,
-                           int tier, int C);
+                           int tier, int C, const RowWs &w);
 
 // Layernorm (statistics + rewrite, bf16 out); mean / rstd may be null.
 int launch_layernorm(const void *x, int64_t rows, int64_t cols, int in_dtype, float eps,
                      const float *gamma, const float *beta, uint16_t *y, float *mean,
                      float *rstd, cudaStream_t s, const DevInfo &d, int *tier_out, int tier,
-                     int C);
+                     int C, const RowWs &w);
 
 // ---- tier choice of the row operations (rowwise.cu, host only)
 // Rows per SM from which the automatic choice takes the warp tier for rows
@@ -88,6 +98,7 @@ struct RowPlan {
   bool staged;
   bool ring = false;  // streamed through a shared-memory ring (rowring.cu)
   bool half = false;  // block tier, row in registers read as 8-byte vectors
+  bool grid = false;  // split-K over a plain grid, width CTAs per row (rowgrid.cu)
 };
 // Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
 // cols is a multiple of the 16-byte vector and every operand meets the
@@ -99,8 +110,11 @@ struct RowPlan {
 // half: the rows are not 16-byte aligned vectors but every operand allows the
 // 8-byte vector register form (cols a multiple of 4 bf16 / 2 fp32, x and the
 // outputs 8-byte aligned, gamma / beta as that form loads them).
+// grid_ok: a workspace is at hand and the operands meet the grid form's
+// alignment (as the ring form's).
 RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mode, int tier,
-                     int C, int sm_count, int max_cluster, bool out_vec = true, bool half = false);
+                     int C, int sm_count, int max_cluster, bool out_vec = true, bool half = false,
+                     bool grid_ok = false);
 // Vectors per row up to which the block tier holds the row in registers
 // (256 threads x 8 vectors).
 constexpr int64_t kRowRegMaxVec = 2048;
@@ -139,6 +153,23 @@ int launch_rowwise_ring(int mode, int in_dtype, const void *x, int64_t rows, int
                         float eps, float *y, float *mean, float *rstd, const float *gamma,
                         const float *beta, uint16_t *ybf, int C, bool shrink, int *C_out,
                         cudaStream_t s, const DevInfo &d);
+// ---- grid form of the row operations (rowgrid.cu)
+// Slices of at least kRowGridMinSlice elements, at most kRowGridMaxSplits
+// CTAs per row.
+constexpr int64_t kRowGridMinSlice = 2048;
+constexpr int kRowGridMaxSplits = 1024;
+// CTAs per row for rows x cols: about 4 CTAs per SM over all rows.
+int rowgrid_splits(int64_t rows, int64_t cols, int sm_count);
+// Workspace bytes of the grid form: a 16-byte state per CTA.
+inline size_t rowgrid_ws_bytes(int64_t rows, int G) { return (size_t)rows * (size_t)G * 16; }
+// mode as launch_rowwise_warp; x 16-byte aligned, cols a multiple of 8, y
+// 32-byte aligned (softmax), ybf / gamma / beta 16-byte aligned (rewrite),
+// ws 16-byte aligned with at least rowgrid_ws_bytes(rows, G) bytes, not
+// overlapping any operand; RR_ERR_INVALID otherwise.  Two launches.
+int launch_rowgrid(int mode, int in_dtype, const void *x, int64_t rows, int64_t cols, float eps,
+                   float *y, float *mean, float *rstd, const float *gamma, const float *beta,
+                   uint16_t *ybf, int G, void *ws, size_t ws_bytes, cudaStream_t s,
+                   const DevInfo &d);
 // ---- warp tier of the row operations (rowwarp.cu)
 // A segment of L lanes per row holding NV 16-byte vectors per lane, NV a
 // power of two up to kRowWarpMaxNV.

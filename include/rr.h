@@ -325,12 +325,45 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * Long rows that are not staged take split-K over global memory with
  * slices of at most 128 KiB.  A forced block tier stages when it applies; a
  * forced split-K tier reads from global memory.
+ * Grid form (given a workspace): split-K whose G slices per row go to the
+ * CTAs of a plain grid rather than a cluster, so that a few rows cover
+ * every SM.  One kernel folds each slice into its partial state (softmax:
+ * the (max, sum) pair; layernorm: (count, mean, M2)) and stores it in the
+ * workspace; a second kernel, in stream order, folds each row's G states
+ * in one fixed order and writes the row's result (softmax and the rewrite
+ * read the slice again).  AUTO takes it, when a workspace of
+ * rr_rowwise_workspace_size bytes is given, for fewer rows than SMs of at
+ * least 16384 elements, x 16-byte aligned, cols a multiple of 8, the
+ * softmax output 32-byte and the rewrite's output, gamma and beta 16-byte
+ * aligned; G = about 4 CTAs per SM over all rows (slices of at least 2048
+ * elements, G <= 1024).  Forced with tier RR_TIER_SPLITK, cluster_size 0
+ * or 1 and splits = G.  The statistics of rr_layernorm and
+ * rr_layernorm_stats in this form are bitwise equal for the same G.
+ *   splits          0 = automatic, else G (1..1024) CTAs per row.
+ *   workspace       device scratch, 16-byte aligned, caller-owned, not
+ *                   overlapping any operand, or NULL (no grid form); its
+ *                   contents are scratch.  Calls that may run at the same
+ *                   time (other streams) need workspaces of their own.
+ *   workspace_bytes its size; at least rows * G * 16 for the grid form (a
+ *                   16-byte state per CTA).
  */
 typedef struct {
     int tier;
     int cluster_size;
     int lanes_per_row;
+    int splits;
+    void *workspace;
+    size_t workspace_bytes;
 } rr_rowwise_opts;
+
+/*
+ * rr_rowwise_workspace_size -- bytes of workspace the automatic plan of
+ * rr_softmax_ex / rr_layernorm_stats_ex / rr_layernorm_ex wants on the
+ * current device for rows x cols of in_dtype with aligned operands (0: it
+ * takes no grid form).  Queries device properties only.
+ */
+int rr_rowwise_workspace_size(int64_t rows, int64_t cols, int in_dtype,
+                              int row_op, size_t *bytes_out);
 
 /* rr_softmax with options; opts may be NULL.  RR_ERR_UNSUPPORTED if a
  * forced cluster size cannot be co-scheduled. */
@@ -532,11 +565,13 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
 int rr_device_status(void *stream);
 
 /* Tier and width of the last reduce / softmax / layernorm call made by this
- * process: (ring << 17) | (staged << 16) | (width << 8) | tier, width the
- * cluster size (the warp tier of the row operations: lanes per row), staged
- * 1 when a row operation staged its rows in shared memory, ring 1 when it
- * streamed them through a shared-memory ring of bulk copies (one combine per
- * row; the layernorm statistics as a (count, mean, M2) monoid). */
+ * process: ((width >> 8) << 19) | (grid << 18) | (ring << 17) |
+ * (staged << 16) | ((width & 0xff) << 8) | tier, width the cluster size
+ * (the warp tier of the row operations: lanes per row; the grid form: CTAs
+ * per row), staged 1 when a row operation staged its rows in shared
+ * memory, ring 1 when it streamed them through a shared-memory ring of bulk
+ * copies (one combine per row; the layernorm statistics as a (count, mean,
+ * M2) monoid), grid 1 when it took the grid form (rr_rowwise_opts). */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -568,13 +603,15 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * block / split-K tier stages the rows in shared memory, 2 when it streams
  * them through a shared-memory ring (the split-K width is then the cluster
  * size planned; a launch may take a smaller one, down to 2, when the device
- * cannot co-schedule a cluster that size for every row).  Touches no GPU.
- * RR_ERR_INVALID on negative sizes, sm_count or max_cluster < 1, a bad dtype
- * or row_op.
+ * cannot co-schedule a cluster that size for every row), 3 for the grid
+ * form (split-K, width = G CTAs per row), which the plan considers only
+ * with with_workspace != 0.  Touches no GPU.  RR_ERR_INVALID on negative
+ * sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
  */
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,
-                    int aligned, int sm_count, int max_cluster, int *tier_out,
-                    int *width_out, int *staged_out);
+                    int aligned, int sm_count, int max_cluster,
+                    int with_workspace, int *tier_out, int *width_out,
+                    int *staged_out);
 
 /*
  * rr_test_wait_timeout -- failure-detection hook: launches one CTA that

@@ -677,7 +677,7 @@ def test_ring_auto_few_rows(rr, oracle_mod, dtype):
                                       (sms // 2, 24576)]):
         x = _x(rows, cols, dtype, 2500 + i, 3.0)
         idx = np.unique(np.r_[0:3, rows - 3:rows]) if rows > 6 else np.arange(rows)
-        _ring_all_ops(rr, oracle_mod, x, idx)
+        _ring_all_ops(rr, oracle_mod, x, idx, workspace=False)  # (with one: the grid form)
         t, c = rr.last_tier()
         plan = rr.plan_rowwise(rows, cols, "lnstats", sms, 16, dtype=dtype, form=True)
         assert plan[2] == "ring" and t == plan[0], (rows, cols, plan, t, c)
@@ -721,7 +721,7 @@ def test_ring_special_rows(rr, oracle_mod):
     x[2, cols - 1] = 1.0e4
     x[3, : cols // 2 + 77] = float("-inf")
     x[4] = float("-inf")
-    y = to_np(rr.softmax(x))
+    y = to_np(rr.softmax(x, workspace=False))
     assert rr.last_form() == "ring"
     ref = oracle_mod.softmax(to_np(x))
     live = [i for i in range(rows) if i != 4]
@@ -729,7 +729,7 @@ def test_ring_special_rows(rr, oracle_mod):
     assert (y[3, : cols // 2 + 77] == 0).all()
     assert np.isnan(ref[4]).all() and (y[4] == 0).all()
     xs = x[torch.tensor([0, 1, 2] + list(range(5, rows)), device="cuda")]
-    mean, rstd = rr.layernorm_stats(xs, 1e-5)
+    mean, rstd = rr.layernorm_stats(xs, 1e-5, workspace=False)
     assert rr.last_form() == "ring"
     assert float(mean[0]) == 1.5 and float(rstd[0]) == pytest.approx(1 / np.sqrt(1e-5), rel=1e-6)
     rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xs), 1e-5)
@@ -743,21 +743,165 @@ def test_ring_repeatable_and_huge_rows(rr, oracle_mod):
     # the same call gives the same bits; a row of 2^25 elements (counts past
     # 2^24) matches the oracle
     x = _x(16, 1 << 20, torch.bfloat16, 2800, 3.0)
-    y1, y2 = rr.softmax(x), rr.softmax(x)
+    y1, y2 = rr.softmax(x, workspace=False), rr.softmax(x, workspace=False)
     assert rr.last_form() == "ring"
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
     from cluster_reductions_gb300 import inputs
     g, b = inputs.layernorm_params(1 << 20, 2801, "cuda")
-    z1, z2 = rr.layernorm(x, g, b), rr.layernorm(x, g, b)
+    z1, z2 = rr.layernorm(x, g, b, workspace=False), rr.layernorm(x, g, b, workspace=False)
     assert torch.equal(z1.view(torch.int16), z2.view(torch.int16))
     xh = _x(1, 1 << 25, torch.bfloat16, 2802, 2.0)
-    mean, rstd = rr.layernorm_stats(xh, 1e-5)
+    mean, rstd = rr.layernorm_stats(xh, 1e-5, workspace=False)
     assert rr.last_form() == "ring"
     rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xh), 1e-5)
     xf = xh.to(torch.float64).cpu().numpy()
     bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / (1 << 25))
     assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
     assert_rel_close(to_np(rstd), rr_, 1e-5, what="ring rstd 2^25")
+
+
+# ---------------------------------------------------------------------------
+# Grid form (rowgrid.cu): G CTAs per row of a plain grid, the slices' states
+# through a workspace, a second kernel folding them in one fixed order.
+# Shapes give empty slices (more CTAs than 8-element units), ragged last
+# slices, one slice, several units a thread, G past 32 (lanes fold several
+# states each) and past 255 (the width's high byte in rr_last_tier).
+# ---------------------------------------------------------------------------
+def _grid_all_ops(rr, oracle_mod, x, idx, **kw):
+    _check_all_row_ops(rr, oracle_mod, x, idx, **kw)
+    assert rr.last_form() == "grid", (x.shape, rr.last_tier(), rr.last_form())
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("G", [1, 3, 32, 77, 300])
+def test_grid_forced_splits(rr, oracle_mod, dtype, G):
+    shapes = [(1, 8), (2, 64), (3, 2056), (2, 16392), (5, 40000), (1, 131080)]
+    for i, (rows, cols) in enumerate(shapes):
+        x = _x(rows, cols, dtype, 3000 + i, 2.0)
+        _grid_all_ops(rr, oracle_mod, x, np.arange(rows), tier="splitk", splits=G)
+        assert rr.last_tier() == ("splitk", G)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_grid_auto_few_rows(rr, oracle_mod, dtype):
+    # the automatic plan with the workspace the binding allocates
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for i, (rows, cols) in enumerate([(16, 65536), (10, 100000), (3, 1 << 20), (sms - 1, 16384),
+                                      (sms // 2, 24576), (1, 40008)]):
+        x = _x(rows, cols, dtype, 3100 + i, 3.0)
+        idx = np.unique(np.r_[0:3, rows - 3:rows]) if rows > 6 else np.arange(rows)
+        _grid_all_ops(rr, oracle_mod, x, idx)
+        plan = rr.plan_rowwise(rows, cols, "lnstats", sms, 16, dtype=dtype, form=True,
+                               with_workspace=True)
+        assert plan[2] == "grid" and rr.last_tier() == plan[:2], (rows, cols, plan)
+
+
+def test_grid_special_rows(rr, oracle_mod):
+    # constant rows, a large common offset, one outlier, -inf over whole
+    # slices and an all -inf row
+    rows, cols = 16, 65536
+    x = _x(rows, cols, torch.bfloat16, 3200, 1.0)
+    x[0] = 1.5
+    x[1] = (x[1].float() + 1000.0).to(torch.bfloat16)
+    x[2] = 0.0
+    x[2, cols - 1] = 1.0e4
+    x[3, : cols // 2 + 77] = float("-inf")
+    x[4] = float("-inf")
+    y = to_np(rr.softmax(x))
+    assert rr.last_form() == "grid"
+    ref = oracle_mod.softmax(to_np(x))
+    live = [i for i in range(rows) if i != 4]
+    assert_rel_close(y[live], ref[live], 1e-5, floor=1e-30, what="grid softmax special")
+    assert (y[3, : cols // 2 + 77] == 0).all()
+    assert np.isnan(ref[4]).all() and (y[4] == 0).all()
+    xs = x[torch.tensor([0, 1, 2] + list(range(5, rows)), device="cuda")]
+    mean, rstd = rr.layernorm_stats(xs, 1e-5)
+    assert rr.last_form() == "grid"
+    assert float(mean[0]) == 1.5 and float(rstd[0]) == pytest.approx(1 / np.sqrt(1e-5), rel=1e-6)
+    rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xs), 1e-5)
+    xf = xs.to(torch.float64).cpu().numpy()
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+    assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="grid rstd special")
+
+
+def test_grid_repeatable_and_huge_rows(rr, oracle_mod):
+    # the same call gives the same bits; the statistics of the rewrite and of
+    # layernorm_stats agree bit for bit; a row of 2^25 elements (counts past
+    # 2^24) matches the oracle
+    from cluster_reductions_gb300 import inputs
+    x = _x(16, 1 << 20, torch.bfloat16, 3300, 3.0)
+    y1, y2 = rr.softmax(x), rr.softmax(x)
+    assert rr.last_form() == "grid"
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    g, b = inputs.layernorm_params(1 << 20, 3301, "cuda")
+    mu, rs = torch.empty(16, device="cuda"), torch.empty(16, device="cuda")
+    z1, z2 = rr.layernorm(x, g, b, mean=mu, rstd=rs), rr.layernorm(x, g, b)
+    assert rr.last_form() == "grid"
+    assert torch.equal(z1.view(torch.int16), z2.view(torch.int16))
+    m2, r2 = rr.layernorm_stats(x, 1e-5)
+    assert rr.last_form() == "grid"
+    assert torch.equal(mu.view(torch.int32), m2.view(torch.int32))
+    assert torch.equal(rs.view(torch.int32), r2.view(torch.int32))
+    xh = _x(1, 1 << 25, torch.bfloat16, 3302, 2.0)
+    mean, rstd = rr.layernorm_stats(xh, 1e-5)
+    assert rr.last_form() == "grid" and rr.last_tier()[1] > 255
+    rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xh), 1e-5)
+    xf = xh.to(torch.float64).cpu().numpy()
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / (1 << 25))
+    assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="grid rstd 2^25")
+
+
+def test_grid_workspace_handling(rr, oracle_mod):
+    # a workspace too small for a forced G is refused; too small for the
+    # automatic plan, the call plans without it; rows the form cannot take
+    # (x not 16-byte aligned) refuse a forced G
+    x = _x(4, 65536, torch.bfloat16, 3400, 2.0)
+    small = torch.empty(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(rr.RRError) as e:
+        rr.softmax(x, tier="splitk", splits=8, workspace=small)
+    assert e.value.status == 1
+    y = rr.softmax(x, workspace=small)
+    assert rr.last_form() != "grid"
+    assert_rel_close(to_np(y), oracle_mod.softmax(to_np(x)), 1e-5, floor=1e-30, what="no grid")
+    xm = _x(4, 65536, torch.bfloat16, 3401, 2.0, offset=4)
+    with pytest.raises(rr.RRError) as e:
+        rr.softmax(xm, tier="splitk", splits=8)
+    assert e.value.status == 2
+    big = torch.empty(4 * 8 * 4, dtype=torch.int32, device="cuda")  # a state per CTA
+    y = rr.softmax(x, tier="splitk", splits=8, workspace=big)
+    assert rr.last_tier() == ("splitk", 8) and rr.last_form() == "grid"
+    assert_rel_close(to_np(y), oracle_mod.softmax(to_np(x)), 1e-5, floor=1e-30, what="G=8")
+
+
+def test_grid_workspace_reused_across_shapes(rr, oracle_mod):
+    # one workspace, its contents scratch, through calls of different
+    # shapes, G and operations
+    from cluster_reductions_gb300 import inputs
+    ws = torch.full((1 << 16,), -1, dtype=torch.int32, device="cuda")
+    calls = [(2, 16384, "softmax"), (2, 16384, "lnstats"), (16, 65536, "softmax"),
+             (16, 65536, "lnstats"), (5, 40000, "layernorm"), (16, 65536, "layernorm"),
+             (3, 1 << 20, "lnstats"), (16, 65536, "softmax")]
+    for i, (rows, cols, op) in enumerate(calls):
+        x = _x(rows, cols, torch.bfloat16, 3500 + i, 2.0)
+        xh = to_np(x)
+        if op == "softmax":
+            y = rr.softmax(x, workspace=ws)
+            assert_rel_close(to_np(y), oracle_mod.softmax(xh), 1e-5, floor=1e-30, what=op)
+        else:
+            if op == "lnstats":
+                mean, rstd = rr.layernorm_stats(x, 1e-5, workspace=ws)
+            else:
+                g, b = inputs.layernorm_params(cols, 3600 + i, "cuda")
+                mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+                rr.layernorm(x, g, b, 1e-5, mean=mean, rstd=rstd, workspace=ws)
+            rm, _, rr_ = oracle_mod.layernorm_stats(xh, 1e-5)
+            xf = x.to(torch.float64).cpu().numpy()
+            bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+            assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all(), (rows, cols, op)
+            assert_rel_close(to_np(rstd), rr_, 1e-5, what=op)
+        assert rr.last_form() == "grid", (rows, cols, op)
 
 
 # ---------------------------------------------------------------------------

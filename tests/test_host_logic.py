@@ -239,6 +239,41 @@ def test_rowwise_staged_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expe
                            form=True) == expect
 
 
+@pytest.mark.parametrize("rows,cols,op,dtype,aligned,expect", [
+    # fewer rows than SMs, at least 16384 aligned elements whole 8-element
+    # units: the grid form, G = floor(4 * 152 / rows) CTAs per row (one
+    # wave), slices of at least 2048 elements
+    (16, 1 << 20, "softmax", "bf16", True, ("splitk", 38, "grid")),
+    (16, 1 << 20, "lnstats", "bf16", True, ("splitk", 38, "grid")),
+    (16, 1 << 20, "layernorm", "bf16", True, ("splitk", 38, "grid")),
+    (16, 1 << 20, "softmax", "f32", True, ("splitk", 38, "grid")),
+    (1, 1 << 20, "softmax", "bf16", True, ("splitk", 512, "grid")),     # slices >= 2048
+    (1, 1 << 24, "lnstats", "bf16", True, ("splitk", 608, "grid")),
+    (3, 16384, "layernorm", "bf16", True, ("splitk", 8, "grid")),
+    (151, 16384, "softmax", "bf16", True, ("splitk", 4, "grid")),
+    (64, 262144, "layernorm", "f32", True, ("splitk", 9, "grid")),
+    # not the grid form: as many rows as SMs, short rows, misaligned rows
+    (152, 16384, "softmax", "bf16", True, ("block", 1, "staged")),
+    (16, 8192, "softmax", "bf16", True, ("block", 1, "direct")),
+    (16, 65536, "softmax", "bf16", False, ("splitk", 16, "direct")),
+    (16, 65540, "softmax", "f32", True, ("splitk", 16, "direct")),       # not whole 8-element units
+])
+def test_rowwise_grid_dispatch(lib, rows, cols, op, dtype, aligned, expect):
+    import torch
+    import cluster_reductions_gb300 as rr
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    assert rr.plan_rowwise(rows, cols, op, 152, 16, dtype=dt, aligned=aligned, form=True,
+                           with_workspace=True) == expect
+
+
+def test_rowwise_grid_needs_a_workspace(lib):
+    # without a workspace the same shapes plan as before (ring or split-K)
+    import cluster_reductions_gb300 as rr
+    for op in ("softmax", "lnstats", "layernorm"):
+        assert rr.plan_rowwise(16, 1 << 20, op, 152, 16, form=True)[2] != "grid"
+        assert rr.plan_rowwise(16, 1 << 20, op, 152, 16, form=True, with_workspace=True)[2] == "grid"
+
+
 def test_rowwise_warp_reach_for_unaligned_rows(lib):
     # many rows that are not aligned vectors plan onto the warp tier exactly
     # while their whole 16-byte chunks fit 32 lanes x 8 (2055 bf16 / 1027
@@ -260,14 +295,49 @@ def test_rowwise_plan_rejects_bad_arguments(lib):
     t, w = ctypes.c_int(), ctypes.c_int()
     bt, bw = ctypes.byref(t), ctypes.byref(w)
     RR_BF16, RR_I32 = 2, 1
-    assert lib.rr_plan_rowwise(-1, 8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, -8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_I32, 0, 1, 152, 16, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 3, 1, 152, 16, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 0, 16, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 0, bt, bw, None) == 1
-    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 16, None, bw, None) == 1
-    assert lib.rr_plan_rowwise(0, 8, RR_BF16, 0, 1, 152, 16, bt, bw, None) == 0
+    assert lib.rr_plan_rowwise(-1, 8, RR_BF16, 0, 1, 152, 16, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, -8, RR_BF16, 0, 1, 152, 16, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_I32, 0, 1, 152, 16, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 3, 1, 152, 16, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 0, 16, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 0, 0, bt, bw, None) == 1
+    assert lib.rr_plan_rowwise(8, 8, RR_BF16, 0, 1, 152, 16, 0, None, bw, None) == 1
+    assert lib.rr_plan_rowwise(0, 8, RR_BF16, 0, 1, 152, 16, 0, bt, bw, None) == 0
+    n = ctypes.c_size_t(0)
+    assert lib.rr_rowwise_workspace_size(-1, 8, RR_BF16, 0, ctypes.byref(n)) == 1
+    assert lib.rr_rowwise_workspace_size(8, 8, RR_I32, 0, ctypes.byref(n)) == 1
+    assert lib.rr_rowwise_workspace_size(8, 8, RR_BF16, 3, ctypes.byref(n)) == 1
+    assert lib.rr_rowwise_workspace_size(8, 8, RR_BF16, 0, None) == 1
+
+
+def test_rowwise_grid_options_rejected_on_the_host(lib):
+    # the grid form's options: splits only as split-K without a cluster and
+    # with a workspace; a workspace 16-byte aligned, sized, not overlapping
+    from cluster_reductions_gb300._lib import rr_rowwise_opts
+    buf = (ctypes.c_float * 4096)()
+    p = ctypes.addressof(buf)
+    p = (p + 255) // 256 * 256
+    x, y, ws = p, p + 4096, p + 12288
+    SPLITK, BLOCK, AUTO, BF16 = 4, 3, 0, 2
+
+    def sm(o, xp=x, yp=y):
+        return lib.rr_softmax_ex(xp, 2, 512, BF16, yp, None, ctypes.byref(o))
+
+    assert sm(rr_rowwise_opts(AUTO, 0, 0, 4, ws, 1024)) == 1        # splits need split-K
+    assert sm(rr_rowwise_opts(BLOCK, 0, 0, 4, ws, 1024)) == 1
+    assert sm(rr_rowwise_opts(SPLITK, 2, 0, 4, ws, 1024)) == 1      # ... without a cluster
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, 4, None, 0)) == 1       # ... and a workspace
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, -1, ws, 1024)) == 1
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, 1025, ws, 1024)) == 1   # at most 1024 CTAs per row
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, 4, ws + 8, 1024)) == 1  # workspace 16-byte aligned
+    assert sm(rr_rowwise_opts(AUTO, 0, 0, 0, ws, 0)) == 1           # a workspace of no bytes
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, 4, x + 64, 1024)) == 1  # overlapping x
+    assert sm(rr_rowwise_opts(SPLITK, 0, 0, 4, y + 64, 1024)) == 1  # ... or the output
+    assert lib.rr_layernorm_stats_ex(x, 2, 512, BF16, ctypes.c_float(1e-5), y, y + 64, None,
+                                     ctypes.byref(rr_rowwise_opts(SPLITK, 0, 0, 4, y + 32, 64))) == 1
+    assert lib.rr_layernorm_ex(x, 2, 512, BF16, ctypes.c_float(1e-5), ws, ws + 2048, y, None,
+                               None, None,
+                               ctypes.byref(rr_rowwise_opts(SPLITK, 0, 0, 4, ws + 1024, 64))) == 1
 
 
 @pytest.mark.parametrize("shape,align,ws,expect", [
