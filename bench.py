@@ -677,7 +677,9 @@ def bench_ours(args):
         rowwise_sk["layernorm_16x1M_bf16"] = timed(
             lambda: rr.layernorm_stats(xs[nxt()], 1e-5, mean=mu, rstd=rs), 16 * (1 << 20) * 2 + 128,
             reps=24)
-        rowwise_sk["tier"] = "splitk C=%d" % rr.last_tier()[1]
+        _t, _w = rr.last_tier()
+        rowwise_sk["tier"] = "%s %s=%d %s" % (_t, "G" if rr.last_form() == "grid" else "C", _w,
+                                              rr.last_form())
         g16, b16 = _inp.layernorm_params(1 << 20, 778, dev)
         del ys
         yb = [torch.empty((16, 1 << 20), dtype=torch.bfloat16, device=dev) for _ in range(NR)]
