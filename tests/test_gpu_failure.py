@@ -74,6 +74,9 @@ np.save(os.path.join(sys.argv[2], "x.npy"), x.cpu().numpy())
 out["auto_tier"] = rr.last_tier()
 xb = inputs.normal_bf16(16, 1 << 16, 8202, "cuda", 3.0)
 y = rr.softmax(xb)
+out["softmax_grid"] = [rr.last_tier(), rr.last_form()]
+out["softmax_grid_rowsum_err"] = float((y.double().sum(1) - 1).abs().max())
+y = rr.softmax(xb, workspace=False)
 out["softmax_tier"] = rr.last_tier()
 out["softmax_rowsum_err"] = float((y.double().sum(1) - 1).abs().max())
 xa = inputs.normal_f32(1, 1 << 20, 8203, "cuda").view(1, 1 << 16, 16)
@@ -101,6 +104,9 @@ def test_cluster_cap(oracle_mod, tmp_path):
     assert out["auto_tier"][0] == "splitk" and out["auto_tier"][1] <= 4
     xh = np.load(tmp_path / "x.npy")
     assert_sum_close(np.array(out["sum"], np.float32), oracle_mod.reduce_rows(xh, "sum"), xh)
+    # with a workspace the few long rows take the grid form (no clusters);
+    # without one, split-K clusters within the cap
+    assert out["softmax_grid"][1] == "grid" and out["softmax_grid_rowsum_err"] < 1e-4
     assert out["softmax_tier"][0] == "splitk" and out["softmax_tier"][1] <= 4
     assert out["softmax_rowsum_err"] < 1e-4
     assert out["axis_tier"][1] <= 4
