@@ -57,7 +57,8 @@ MEDIUM_ROWS = [(1 << 20, 64), (262144, 256), (65536, 1024), (671088, 100)]
 # rows (500 bytes) are not 16-byte aligned and take its chunked form;
 # 4100-element rows (8200 bytes, every other row 8 bytes past a 16-byte
 # boundary) take the block tier's register form read as 8-byte vectors.
-MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048), (536870, 250), (16384, 4100)]
+MEDIUM_ROWOPS = [(1 << 20, 128), (131072, 1024), (65536, 2048), (536870, 250), (16384, 4100),
+                 (16384, 4099)]
 # Long rows timed beside the step (256 MiB each): softmax / layernorm rows
 # staged in shared memory (a CTA per row; clusters of 8 for 256K-element
 # rows), and a few long fp32 rows per SM for the block reduce.

@@ -474,9 +474,12 @@ def last_staged() -> bool:
 def last_form() -> str:
     """How the last row operation read its rows: "grid" (split-K over a
     plain grid, partial states through the workspace), "ring" (streamed
-    through a shared-memory ring), "staged" (held in shared memory) or
-    "direct"."""
+    through a shared-memory ring), "staged" (held in shared memory),
+    "chunked" (the statistics of a row not 16-byte aligned in registers as
+    head + vectors + tail) or "direct"."""
     v = int(load().rr_last_tier())
+    if (v >> 27) & 1:
+        return "chunked"
     if (v >> 18) & 1:
         return "grid"
     return "ring" if (v >> 17) & 1 else ("staged" if (v >> 16) & 1 else "direct")
@@ -513,7 +516,7 @@ def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: 
     if staged:
         return TIER_NAMES[t.value], w.value, st.value == 1
     if form:
-        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring", "grid")[st.value]
+        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring", "grid", "chunked")[st.value]
     return TIER_NAMES[t.value], w.value
 
 

@@ -258,7 +258,7 @@ int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int al
                                  with_workspace != 0 && vec);
   *tier_out = p.tier;
   *width_out = p.width;
-  if (staged_out) *staged_out = p.grid ? 3 : (p.ring ? 2 : (p.staged ? 1 : 0));
+  if (staged_out) *staged_out = p.chunk ? 4 : (p.grid ? 3 : (p.ring ? 2 : (p.staged ? 1 : 0)));
   return RR_OK;
 }
 

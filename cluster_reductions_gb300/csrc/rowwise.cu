@@ -395,9 +395,119 @@ k_layernorm_gen(const typename In::S *__restrict__ x, int64_t rows, int64_t cols
   }
 }
 
+// ---------------------------------------------------------------------------
+// Layernorm statistics of rows that do not start 16-byte aligned (a width
+// that is not a multiple of the 16-byte vector, or a misaligned x), a CTA
+// per row with the row in registers: its head (the elements before its first 16-byte boundary,
+// fewer than a vector), its whole 16-byte vectors spread over the threads
+// as in the register form, and its tail, one head and one tail element a
+// thread.  Each row's head length follows from its own address.
+// ---------------------------------------------------------------------------
+template <class In>
+struct ChunkRow {
+  int h, nvec, t;  // head elements, whole vectors, tail elements
+  __device__ __forceinline__ ChunkRow(const typename In::S *p, int cols) {
+    const int hh = (int)(((16u - ((uint32_t)(uintptr_t)p & 15u)) & 15u) / sizeof(typename In::S));
+    h = hh < cols ? hh : cols;
+    nvec = (cols - h) / In::EPV;
+    t = cols - h - nvec * In::EPV;
+  }
+};
+
+// The chunked row's raw vectors and its head / tail element of this thread,
+// loaded ahead of use (the next row's while the current one is reduced).
+template <int THREADS, int NV, class In>
+struct ChunkRegs {
+  uint4 raw[NV];
+  float hv, tv;
+  __device__ __forceinline__ ChunkRow<In> fetch(const typename In::S *p, int cols) {
+    const ChunkRow<In> g(p, cols);
+    const uint4 *q = reinterpret_cast<const uint4 *>(p + g.h);
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx < g.nvec) raw[k] = ld_stream_u4(q + idx);
+    }
+    hv = tid < g.h ? In::load1(p + tid) : 0.0f;
+    tv = tid < g.t ? In::load1(p + g.h + g.nvec * In::EPV + tid) : 0.0f;
+    return g;
+  }
+};
+
+// The statistics of a chunked row held in v / hv / tv: mean and 1 / sqrt(var
+// + eps), two passes over the registers (sum, then squared deviations about
+// the mean).
+template <int THREADS, int NV, int EPV>
+__device__ __forceinline__ void chunk_stats(const float (&v)[NV][EPV], float hv, float tv, int h,
+                                            int nvec, int t, int cols, float eps,
+                                            float (*red)[THREADS / 32], float &mu, float &rs) {
+  const int tid = threadIdx.x;
+  float s = hv + tv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) s += v[k][e];
+  mu = sum_block_allreduce<THREADS>(s, red[0]) / (float)cols;
+  float qs = 0.0f;
+  if (tid < h) qs = (hv - mu) * (hv - mu);
+  if (tid < t) qs = fmaf(tv - mu, tv - mu, qs);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (k * THREADS + tid < nvec) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float dlt = v[k][e] - mu;
+        qs = fmaf(dlt, dlt, qs);
+      }
+    }
+  }
+  rs = 1.0f / sqrtf(sum_block_allreduce<THREADS>(qs, red[1]) / (float)cols + eps);
+}
+
+template <int THREADS, int NV, class In>
+__device__ __forceinline__ void chunk_unpack(const ChunkRegs<THREADS, NV, In> &cr, int nvec,
+                                             float (&v)[NV][In::EPV]) {
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (k * THREADS + (int)threadIdx.x < nvec) {
+      In::unpack(cr.raw[k], v[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < In::EPV; ++e) v[k][e] = 0.0f;
+    }
+  }
+}
+
+// Layernorm statistics of chunked rows (any element-aligned x, any cols up
+// to THREADS * NV vectors).
+template <int THREADS, int NV, class In>
+__global__ void __launch_bounds__(THREADS)
+k_lnstats_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+             float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
+  __shared__ float red[2][THREADS / 32];
+  ChunkRegs<THREADS, NV, In> cr;
+  ChunkRow<In> g(x, cols);
+  if ((int64_t)blockIdx.x < rows) g = cr.fetch(x + (int64_t)blockIdx.x * cols, cols);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    float v[NV][In::EPV];
+    chunk_unpack<THREADS, NV, In>(cr, g.nvec, v);
+    const float hv = cr.hv, tv = cr.tv;
+    const ChunkRow<In> cur = g;
+    if (row + gridDim.x < rows) g = cr.fetch(x + (row + gridDim.x) * (int64_t)cols, cols);
+    float mu, rs;
+    chunk_stats<THREADS, NV, In::EPV>(v, hv, tv, cur.h, cur.nvec, cur.t, cols, eps, red, mu, rs);
+    if (threadIdx.x == 0) {
+      mean[row] = mu;
+      rstd[row] = rs;
+    }
+  }
+}
+
 template <class K>
-int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d) {
-  const int nb = occupancy_blocks((const void *)kernel, threads, 0, d.device);
+int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d, size_t smem = 0) {
+  const int nb = occupancy_blocks((const void *)kernel, threads, smem, d.device);
   const int64_t cap = (int64_t)nb * d.sm_count;
   return (int)(rows < cap ? rows : cap);
 }
@@ -681,6 +791,7 @@ inline int tier_code(int tier, int width, int flags) {
   return tier | ((width & 0xff) << 8) | (flags << 16) | (((width >> 8) & 0xff) << 19);
 }
 constexpr int kFlagStaged = 1, kFlagRing = 2, kFlagGrid = 4;
+constexpr int kChunkBit = 1 << 27;  // the statistics' chunked register form
 
 // The grid form's plan for a call: forced (w.splits), automatic with the
 // caller's workspace (falling back to the plan without one when it is too
@@ -816,6 +927,26 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
   if (pk.tier == RR_TIER_WARP)
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                                nullptr, mean, rstd, nullptr, nullptr, nullptr, pk.width, s, d);
+  if (pk.chunk) {
+    *tier_out |= kChunkBit;
+#define RR_LN_CK(T, NV)                                                        \
+  {                                                                            \
+    auto k = k_lnstats_ck<T, NV, In>;                                          \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0, x, rows, (int)cols, eps, mean, rstd); \
+  }
+    switch (pick_nv(cols / In::EPV)) {  // the rewrite's geometry: the same bits
+      case 1: RR_LN_CK(kRowThreads, 1) break;
+      case 2: RR_LN_CK(kRowThreads, 2) break;
+      case 4: RR_LN_CK(kRowThreads, 4) break;
+      default:
+        if (wide_threads(cols / In::EPV) == 288) RR_LN_CK(288, 4)
+        else if (wide_threads(cols / In::EPV) == 384) RR_LN_CK(384, 4)
+        else RR_LN_CK(kRowWideThreads, 4)
+        break;
+    }
+#undef RR_LN_CK
+    return cuda_status(cudaGetLastError());
+  }
   const bool reg = vec && pick_nv(nvec) > 0;
   if (pk.half) {
 #define RR_LN_REGH(T, NV)                                                      \
@@ -1001,8 +1132,22 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // (16 x 1M bf16: 35 against 48 us)
   const bool ring_few = mode != kModeLayernorm;
   const int64_t staged_min = vec ? kRowStagedMinVec[mode] : kRowStagedMinVecMis[mode];
+  // the statistics of rows that are not 16-byte aligned: the chunked
+  // register form (head + 16-byte vectors + tail) up to 1024 vectors, where
+  // they would otherwise take the scalar two-pass form (16384 x 4099 bf16
+  // 0.41 -> 0.58, 16384 x 4095 fp32 0.58 -> 1.00; beyond 1024 vectors
+  // staging measured ahead, 4096 x 16383 bf16 0.68 against 0.43).  The
+  // rewrite keeps the scalar form: in the chunked form its gamma / beta at
+  // any offset (shifted 16-byte windows) took 127 registers a thread and
+  // measured slower (16384 x 4099 bf16 0.39 against 0.44)
+  const bool chunk_ok = !vec && mode == kModeStats && row_vecs <= kRowStagedMinVecMis[kModeStats];
   if (tier == RR_TIER_BLOCK) {
     const bool st = row_vecs > staged_min && stage_fits(1);
+    if (!st && chunk_ok) {
+      RowPlan p{RR_TIER_BLOCK, 1, false};
+      p.chunk = true;
+      return p;
+    }
     return {RR_TIER_BLOCK, 1, st};
   }
   if (tier == RR_TIER_WARP) {
@@ -1060,6 +1205,11 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   if (!vec && half &&
       cols / (in_dtype == RR_BF16 ? 4 : 2) <= (int64_t)kRowThreadsHost * (mode == kModeSoftmax ? 4 : 8))
     return RowPlan{RR_TIER_BLOCK, 1, false, false, true};
+  if (chunk_ok) {
+    RowPlan p{RR_TIER_BLOCK, 1, false};
+    p.chunk = true;
+    return p;
+  }
   if (row_vecs > staged_min) {
     const int sc = rowwise_staged_cluster(cols, in_dtype, max_cluster, vec);
     if (sc == 1) return {RR_TIER_BLOCK, 1, true};

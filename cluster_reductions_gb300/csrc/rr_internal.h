@@ -99,6 +99,7 @@ struct RowPlan {
   bool ring = false;  // streamed through a shared-memory ring (rowring.cu)
   bool half = false;  // block tier, row in registers read as 8-byte vectors
   bool grid = false;  // split-K over a plain grid, width CTAs per row (rowgrid.cu)
+  bool chunk = false; // block tier, statistics of a row not 16-byte aligned as head + vectors + tail
 };
 // Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
 // cols is a multiple of the 16-byte vector and every operand meets the

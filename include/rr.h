@@ -565,13 +565,16 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
 int rr_device_status(void *stream);
 
 /* Tier and width of the last reduce / softmax / layernorm call made by this
- * process: ((width >> 8) << 19) | (grid << 18) | (ring << 17) |
- * (staged << 16) | ((width & 0xff) << 8) | tier, width the cluster size
+ * process: (chunked << 27) | ((width >> 8) << 19) | (grid << 18) |
+ * (ring << 17) | (staged << 16) | ((width & 0xff) << 8) | tier, width the
+ * cluster size
  * (the warp tier of the row operations: lanes per row; the grid form: CTAs
  * per row), staged 1 when a row operation staged its rows in shared
  * memory, ring 1 when it streamed them through a shared-memory ring of bulk
  * copies (one combine per row; the layernorm statistics as a (count, mean,
- * M2) monoid), grid 1 when it took the grid form (rr_rowwise_opts). */
+ * M2) monoid), grid 1 when it took the grid form (rr_rowwise_opts), chunked
+ * 1 when the layernorm statistics held a row that is not 16-byte aligned in
+ * registers as its head, whole 16-byte vectors and tail. */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -605,7 +608,8 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * size planned; a launch may take a smaller one, down to 2, when the device
  * cannot co-schedule a cluster that size for every row), 3 for the grid
  * form (split-K, width = G CTAs per row), which the plan considers only
- * with with_workspace != 0.  Touches no GPU.  RR_ERR_INVALID on negative
+ * with with_workspace != 0, 4 for the statistics' chunked register form of
+ * rows that are not 16-byte aligned (up to 1024 vectors).  Touches no GPU.  RR_ERR_INVALID on negative
  * sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
  */
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,

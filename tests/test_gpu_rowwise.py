@@ -642,6 +642,69 @@ def test_staged_misaligned_rows(rr, oracle_mod, dtype):
 
 
 # ---------------------------------------------------------------------------
+# Chunked rows at a CTA per row (rowwise.cu, k_lnstats_ck): the statistics of
+# rows that are not 16-byte aligned -- odd widths, misaligned bases -- held
+# as head + 16-byte vectors + tail up to 1024 vectors (staged beyond); the
+# rewrite of the same rows (the scalar form) beside them.  Widths from one
+# vector to the 512-thread geometry, every head length, outputs and gamma /
+# beta at their own offsets.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_chunked_rows_statistics_and_rewrite(rr, oracle_mod, dtype):
+    from _util import assert_layernorm_close
+    from cluster_reductions_gb300 import inputs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    epv = 8 if dtype == torch.bfloat16 else 4
+    widths = ([4099, 2057, 8191, 12289, 16383, 9] if epv == 8 else
+              [2051, 1029, 4095, 6145, 8191, 5])
+    for i, cols in enumerate(widths):
+        rows = sms + 3 if cols > 64 else 5
+        for xo in (0, 1):
+            x = _x(rows, cols, dtype, 4000 + 2 * i + xo, 2.0, xo)
+            idx = np.unique(np.r_[0:4, rows // 2, rows - 4:rows])
+            xs = x[torch.from_numpy(idx).cuda()]
+            mean, rstd = rr.layernorm_stats(x, 1e-5)
+            # the statistics stage rows of more than 1024 vectors
+            chunked = cols * (16 // epv) // 16 <= 1024
+            assert rr.last_tier() == ("block", 1), (cols, xo)
+            assert rr.last_form() == ("chunked" if chunked else "staged"), (cols, xo)
+            rm, _, rr_ = oracle_mod.layernorm_stats(to_np(xs), 1e-5)
+            xf = xs.to(torch.float64).cpu().numpy()
+            bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((xf ** 2).sum(axis=1)) / cols)
+            assert (np.abs(to_np(mean)[idx].astype(np.float64) - rm) <= bound).all(), (cols, xo)
+            assert_rel_close(to_np(rstd)[idx], rr_, 1e-5, what=f"chunk rstd {cols} x+{xo}")
+            g0, b0 = inputs.layernorm_params(cols + 8, 4100 + i, "cuda")
+            for go, bo, oo in ((0, 0, xo), (1, 3, 0), (4, 4, 3)):
+                g, b = g0[go:go + cols], b0[bo:bo + cols]
+                yb = torch.empty(rows * cols + oo, dtype=torch.bfloat16,
+                                 device="cuda")[oo:].view(rows, cols)
+                m2, r2 = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+                rr.layernorm(x, g, b, 1e-5, out=yb, mean=m2, rstd=r2)
+                assert rr.last_tier() == ("block", 1), (cols, xo, go, oo)
+                y64, y16, rm2, rr2 = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
+                assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm2, rr2,
+                                       to_np(m2)[idx], to_np(r2)[idx])
+
+
+def test_chunked_rows_forced_block_and_special(rr, oracle_mod):
+    # a forced block tier on a misaligned width takes the chunked form;
+    # constant rows (variance 0) and rows with a large common offset
+    x = _x(7, 5001, torch.bfloat16, 4200, 1.0, 3)
+    _check_all_row_ops(rr, oracle_mod, x, np.arange(7), tier="block")
+    c = torch.full((4, 3001), 1.25, dtype=torch.bfloat16, device="cuda")
+    mean, rstd = rr.layernorm_stats(c, 1e-5)
+    assert (to_np(mean) == 1.25).all()
+    np.testing.assert_allclose(to_np(rstd), 1 / np.sqrt(1e-5), rtol=1e-6)
+    o = (_x(4, 3001, torch.float32, 4201, 1.0, 1) + 1000.0)
+    mean, rstd = rr.layernorm_stats(o, 1e-5)
+    rm, _, rr_ = oracle_mod.layernorm_stats(to_np(o), 1e-5)
+    of = o.to(torch.float64).cpu().numpy()
+    bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((of ** 2).sum(axis=1)) / 3001)
+    assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
+    assert_rel_close(to_np(rstd), rr_, 1e-5, what="chunk rstd offset rows")
+
+
+# ---------------------------------------------------------------------------
 # Streamed ring form (rowring.cu): slices bulk-copied piece by piece through
 # a shared-memory ring, one combine per row (softmax: the (max, sum) pair;
 # layernorm: the (count, mean, M2) monoid).  Shapes give empty slices
