@@ -730,7 +730,9 @@ def bench_ours(args):
                 key = f"{mr}x{mc}_{name}_bf16"
                 medium_r[key] = timed(one_r, nb)
                 t, c = rr.last_tier()
-                medium_r[key]["tier"] = f"{t} {'L' if t == 'warp' else 'C'}={c}"
+                fm = rr.last_form()
+                medium_r[key]["tier"] = (f"{t} {'L' if t == 'warp' else 'C'}={c}"
+                                         + ("" if fm == "direct" else " " + fm))
             del xm, ym, yb
         for mr, mc in LONG_ROWOPS:
             xm = [_inp.normal_bf16(mr, mc, 830 + i, dev, 3.0) for i in range(2)]
@@ -753,7 +755,8 @@ def bench_ours(args):
                 key = f"{mr}x{mc}_{name}_bf16"
                 long_r[key] = timed(one_l, nb)
                 t, c = rr.last_tier()
-                long_r[key]["tier"] = f"{t} C={c}" + (" staged" if rr.last_staged() else "")
+                fm = rr.last_form()
+                long_r[key]["tier"] = f"{t} C={c}" + ("" if fm == "direct" else " " + fm)
             del xm, ym, yb
         for mr, mc in LONG_REDUCE:
             xm = [_inp.normal_f32(mr, mc, 840 + i, dev) for i in range(2)]
@@ -999,6 +1002,8 @@ PROFILE_CASES = {
     "rowsk_lnstats_32x524288_bf16": ({"shape": (32, 1 << 19), "op": "lnstats"}, "medium", 1.0),
     # rows 8-byte but not 16-byte aligned: the register form read as 8-byte vectors
     "medium_layernorm_16384x4100_bf16": ({"shape": (16384, 4100), "op": "layernorm"}, "medium", 1.0),
+    # odd widths: the statistics' chunked register form (head + vectors + tail)
+    "medium_lnstats_16384x4099_bf16": ({"shape": (16384, 4099), "op": "lnstats"}, "medium", 1.0),
 }
 
 
