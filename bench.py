@@ -76,18 +76,18 @@ FALLBACK_HBM_GBS = 6800.0
 # figure is low because half of its output was still in L2 when the single
 # captured launch ended.
 NCU_TRAFFIC = {
-    "splitk_sum_f32": {"bytes": 1085457408, "src": ["reduce.cu", "rr_device.cuh"],
-                      "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
-    "combine_p8": {"bytes": 567352320, "src": ["combine.cu", "rr_device.cuh"],
-                  "src_sha": "e448f964a6acd0c9", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 559430656, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "7b18d6a245fd249c", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
-    "block_sum_f32": {"bytes": 271280128, "src": ["reduce.cu", "rr_device.cuh"],
-                     "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271470592, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "7b18d6a245fd249c", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
-    "warp_sum_f32": {"bytes": 138011136, "src": ["reduce.cu", "rr_device.cuh"],
-                    "src_sha": "07f21305f8e29f0f", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
+    "splitk_sum_f32": {"bytes": 1084942336, "src": ["reduce.cu", "rr_device.cuh"],
+                      "src_sha": "200d80f613a727b2", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
+    "combine_p8": {"bytes": 566772736, "src": ["combine.cu", "rr_device.cuh"],
+                  "src_sha": "68a1353cf0e06719", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
+    "softmax_bf16": {"bytes": 558803968, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "8d9c07883fcb56a0", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "block_sum_f32": {"bytes": 271227904, "src": ["reduce.cu", "rr_device.cuh"],
+                     "src_sha": "200d80f613a727b2", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
+    "layernorm_bf16": {"bytes": 271368448, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "8d9c07883fcb56a0", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "warp_sum_f32": {"bytes": 137803776, "src": ["reduce.cu", "rr_device.cuh"],
+                    "src_sha": "200d80f613a727b2", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
 
 
