@@ -301,13 +301,19 @@ k_rowwise_warp_el(const typename In::S *__restrict__ x, int64_t rows, int cols, 
 // shares x's offset within a chunk (vst: 2 for 32-byte, 1 for 16-byte
 // stores), the rest element by element.  The rewrite reads gamma and beta
 // from a copy each CTA makes in shared memory (their offset within a chunk
-// follows the row's).
-// Shared-memory image of gamma and beta for the chunked rewrite: the pair
-// (gamma[j], beta[j]) at slot j + j / EPV (a pad slot after every EPV), so
-// that the lanes of a half-warp, reading the same element of chunks EPV
-// apart with 8-byte loads, hit distinct banks.  Whole chunk t of a row with
-// head hh takes its element e from slot (EPV + 1) t + hh + e + [hh + e >= EPV].
-__host__ __device__ constexpr int gb_slots(int cols, int epv) { return cols + cols / epv + 1; }
+// follows the row's) and computes two elements per packed fp32 instruction.
+// Shared-memory image of gamma and beta for the chunked rewrite: for each
+// column pair (j, j + 1) the float4 (gamma[j], gamma[j + 1], beta[j],
+// beta[j + 1]), so that one 16-byte load gives a pair's packed operands.
+// Pairs start at even columns in the first image and at odd ones in the
+// second (a row's chunks start at its head's parity).  Pair s of an image
+// sits at slot s + s / (EPV / 2): a pad slot after each chunk's worth, so
+// that lanes reading the same pair of consecutive chunks hit distinct banks.
+// Whole chunk t of a row whose chunks start at pair o (o < EPV / 2) of its
+// image takes its pair i from slot (EPV / 2 + 1) t + o + i + (o + i) / (EPV / 2).
+__host__ __device__ constexpr int gq_slots(int cols, int epv) {
+  return cols / 2 + (cols / 2) / (epv / 2) + 1;
+}
 
 template <class In, int MODE, int L, int NV>
 __global__ void __launch_bounds__(kWarpRowMaxThreads)
@@ -321,10 +327,18 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
   const int lane = threadIdx.x & 31, seg = lane / L, sub = lane % L;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = (((int64_t)gridDim.x * blockDim.x) >> 5) * RPW;
-  extern __shared__ float2 sgb[];  // rewrite: (gamma, beta) pairs, padded
+  constexpr int PG = EPV / 2;      // column pairs a whole chunk
+  extern __shared__ float4 sgq[];  // rewrite: the two pair images, padded
+  const int gqs = gq_slots(cols, EPV);
   if constexpr (MODE == kModeLayernorm) {
-    for (int j = threadIdx.x; j < cols; j += blockDim.x)
-      sgb[j + j / EPV] = make_float2(__ldg(gamma + j), __ldg(beta + j));
+    for (int par = 0; par < 2; ++par) {
+      const int np = (cols - par) / 2;
+      for (int q = threadIdx.x; q < np; q += blockDim.x) {
+        const int j = 2 * q + par;
+        sgq[par * gqs + q + q / PG] =
+            make_float4(__ldg(gamma + j), __ldg(gamma + j + 1), __ldg(beta + j), __ldg(beta + j + 1));
+      }
+    }
     __syncthreads();
   }
   // head length of row r: the elements before its first 16-byte boundary
@@ -487,26 +501,29 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
       if (row < rows) {
         if constexpr (MODE == kModeLayernorm) {
           uint16_t *yr = ybf + row * (int64_t)cols;
-          int de[EPV];  // slot of element e of a whole chunk, past the chunk's base
+          // the row's chunks start at column hh: pair image hh & 1, first
+          // pair o = hh / 2 of it; dq[i]: slot of pair i past the chunk's base
+          const float4 *img = sgq + (hh & 1) * gqs;
+          const int o = hh >> 1;
+          int dq[PG];
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) de[e] = hh + e + (hh + e >= EPV ? 1 : 0);
+          for (int i = 0; i < PG; ++i) dq[i] = o + i + (o + i) / PG;
+          const uint64_t mu2 = f2_pack(mu, mu), rs2 = f2_pack(rs, rs);
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             if (!whole(k)) continue;
             const int j0 = hh + (k * L + sub) * EPV;
-            const float2 *q = sgb + (EPV + 1) * (k * L + sub);
-            float g[EPV], b[EPV];
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const float2 gb = q[de[e]];
-              g[e] = gb.x;
-              b[e] = gb.y;
-            }
+            const float4 *q = img + (PG + 1) * (k * L + sub);
             uint32_t pk[EPV / 2];
 #pragma unroll
-            for (int e = 0; e < EPV; e += 2)
-              pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
-                                      fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
+            for (int i = 0; i < PG; ++i) {
+              // fmaf((x - mu) * rs, gamma, beta), two elements at a time
+              const float4 gb = q[dq[i]];
+              float lo, hi;
+              f2_unpack(f2_fma(f2_mul(f2_sub(f2_pack(v[k][2 * i], v[k][2 * i + 1]), mu2), rs2),
+                               f2_pack(gb.x, gb.y), f2_pack(gb.z, gb.w)), lo, hi);
+              pk[i] = bf16x2_bits(lo, hi);
+            }
             if (vst) {
               if constexpr (EPV == 8) {
                 *reinterpret_cast<uint4 *>(yr + j0) =
@@ -523,9 +540,9 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
             }
           }
           auto put = [&](int j, float xv) {
-            const float2 gb = sgb[j + j / EPV];
-            const __nv_bfloat16 o = __float2bfloat16_rn(fmaf((xv - mu) * rs, gb.x, gb.y));
-            yr[j] = *reinterpret_cast<const uint16_t *>(&o);
+            const __nv_bfloat16 ob =
+                __float2bfloat16_rn(fmaf((xv - mu) * rs, __ldg(gamma + j), __ldg(beta + j)));
+            yr[j] = *reinterpret_cast<const uint16_t *>(&ob);
           };
 #pragma unroll
           for (int i = 0; i < HS; ++i) {
@@ -578,7 +595,7 @@ int launch_ck(const void *x, int64_t rows, int64_t cols, float eps, float *y, fl
   } else if (MODE == kModeLayernorm) {
     vst = (((uintptr_t)ybf / 2) % EPV) == (uintptr_t)hx;
   }
-  const size_t smem = MODE == kModeLayernorm ? sizeof(float2) * gb_slots((int)cols, EPV) : 0;
+  const size_t smem = MODE == kModeLayernorm ? 2 * sizeof(float4) * gq_slots((int)cols, EPV) : 0;
   int grid, threads;
   warp_row_launch(k, 32 / L, rows, d, &grid, &threads, smem);
   return cuda_status(launch_kernel(k, dim3(grid), dim3(threads), smem, s, 0,
