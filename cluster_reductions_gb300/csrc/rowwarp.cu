@@ -458,14 +458,18 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
         }
       }
     } else {
-      float s = 0.0f;
+      // the whole chunks two elements per packed fp32 instruction (even and
+      // odd elements in the two halves), the head and tail one by one
+      uint64_t sa = 0;
 #pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        float sk = 0.0f;
+      for (int k = 0; k < NV; ++k)
+        if (whole(k)) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) sk += v[k][e];
-        if (whole(k)) s += sk;
-      }
+          for (int i = 0; i < EPV / 2; ++i) sa = f2_add(sa, f2_pack(v[k][2 * i], v[k][2 * i + 1]));
+        }
+      float slo, shi;
+      f2_unpack(sa, slo, shi);
+      float s = slo + shi;
 #pragma unroll
       for (int i = 0; i < HS; ++i)
         if (in_head(i)) s += h[i];
@@ -473,17 +477,20 @@ k_rowwise_warp_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, 
       for (int i = 0; i < HS; ++i)
         if (in_tail(i)) s += t[i];
       const float mu = warp_allreduce<SumF32, L>(s) / (float)cols;
-      float qs = 0.0f;
+      const uint64_t nmu2 = f2_pack(-mu, -mu);
+      uint64_t qa = 0;
 #pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        float qk = 0.0f;
+      for (int k = 0; k < NV; ++k)
+        if (whole(k)) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const float dlt = v[k][e] - mu;
-          qk = fmaf(dlt, dlt, qk);
+          for (int i = 0; i < EPV / 2; ++i) {
+            const uint64_t d = f2_add(f2_pack(v[k][2 * i], v[k][2 * i + 1]), nmu2);
+            qa = f2_fma(d, d, qa);
+          }
         }
-        if (whole(k)) qs += qk;
-      }
+      float qlo, qhi;
+      f2_unpack(qa, qlo, qhi);
+      float qs = qlo + qhi;
 #pragma unroll
       for (int i = 0; i < HS; ++i)
         if (in_head(i)) {
