@@ -124,29 +124,37 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
         }
       }
     } else {
-      float s = 0.0f;
+      // two elements per packed fp32 instruction (even and odd elements in
+      // the two halves)
+      uint64_t sa = 0;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
         if (k * L + sub < nvec) {
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) s += v[k][e];
+          for (int e = 0; e < EPV; e += 2) sa = f2_add(sa, f2_pack(v[k][e], v[k][e + 1]));
         }
-      const float mu = warp_allreduce<SumF32, L>(s) / (float)cols;
-      float qs = 0.0f;
+      float slo, shi;
+      f2_unpack(sa, slo, shi);
+      const float mu = warp_allreduce<SumF32, L>(slo + shi) / (float)cols;
+      const uint64_t nmu2 = f2_pack(-mu, -mu);
+      uint64_t qa = 0;
 #pragma unroll
       for (int k = 0; k < NV; ++k)
         if (k * L + sub < nvec) {
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float dlt = v[k][e] - mu;
-            qs = fmaf(dlt, dlt, qs);
+          for (int e = 0; e < EPV; e += 2) {
+            const uint64_t d = f2_add(f2_pack(v[k][e], v[k][e + 1]), nmu2);
+            qa = f2_fma(d, d, qa);
           }
         }
-      const float var = warp_allreduce<SumF32, L>(qs) * (1.0f / (float)cols);
+      float qlo, qhi;
+      f2_unpack(qa, qlo, qhi);
+      const float var = warp_allreduce<SumF32, L>(qlo + qhi) * (1.0f / (float)cols);
       const float rs = 1.0f / sqrtf(var + eps);
       if (row < rows) {
         if constexpr (MODE == kModeLayernorm) {
           uint16_t *yr = ybf + row * (int64_t)cols;
+          const uint64_t mu2 = f2_pack(mu, mu), rs2 = f2_pack(rs, rs);
 #pragma unroll
           for (int k = 0; k < NV; ++k) {
             const int idx = k * L + sub;
@@ -155,9 +163,13 @@ k_rowwise_warp(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
               load_gamma_beta<EPV>(gamma, beta, (int64_t)idx * EPV, gb32, g, b);
               uint32_t pk[EPV / 2];
 #pragma unroll
-              for (int e = 0; e < EPV; e += 2)
-                pk[e / 2] = bf16x2_bits(fmaf((v[k][e] - mu) * rs, g[e], b[e]),
-                                        fmaf((v[k][e + 1] - mu) * rs, g[e + 1], b[e + 1]));
+              for (int e = 0; e < EPV; e += 2) {
+                // fmaf((x - mu) * rs, gamma, beta), two elements at a time
+                float lo, hi;
+                f2_unpack(f2_fma(f2_mul(f2_sub(f2_pack(v[k][e], v[k][e + 1]), mu2), rs2),
+                                 f2_pack(g[e], g[e + 1]), f2_pack(b[e], b[e + 1])), lo, hi);
+                pk[e / 2] = bf16x2_bits(lo, hi);
+              }
               if constexpr (EPV == 8) {
                 *reinterpret_cast<uint4 *>(yr + idx * EPV) =
                     make_uint4(pk[0], pk[1 % (EPV / 2)], pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
