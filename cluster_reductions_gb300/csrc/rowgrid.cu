@@ -16,9 +16,9 @@
 //                          and stores it in ws[row * G + g];
 //   k_rowgrid_softmax_out  CTA (row, g) folds the row's G states and writes
 //                          slice g of the output, reading the slice again;
-//   k_rowgrid_ln_out       CTA (column block, row group) folds the states of
-//                          its rows and rewrites its columns of them, gamma
-//                          and beta read once per row group;
+//   k_rowgrid_ln_out       CTA (column block, row group; 512 threads) folds
+//                          the states of its rows and rewrites its columns of
+//                          them, gamma and beta read once per row group;
 //   k_rowgrid_stats_fin    a warp per row folds its states into mean, rstd.
 //
 // (One-launch forms -- the statistics folded by each row's last CTA in, and
@@ -371,12 +371,16 @@ k_rowgrid_softmax_out(const typename In::S *__restrict__ x, int64_t cols, int G,
   }
 }
 
-// Layernorm rewrite: CTA (bx, by) takes units bx * 256 + tid of rows
-// [by * RB, min((by + 1) * RB, rows)); ybf, gamma, beta 16-byte aligned.
-// Dynamic shared memory: RB (mean, rstd) pairs.  The CTAs of column block 0
-// write mean / rstd when given.
+// Layernorm rewrite: CTA (bx, by) of kLnThreads threads takes units
+// bx * kLnThreads + tid of rows [by * RB, min((by + 1) * RB, rows)); ybf,
+// gamma, beta 16-byte aligned.  Dynamic shared memory: RB (mean, rstd)
+// pairs.  The CTAs of column block 0 write mean / rstd when given.  512
+// threads rather than 256: twice the warps fold the rows' states at the
+// CTA's start (16 x 1M bf16: 0.55 -> 0.59 of the copy bandwidth).
+constexpr int kLnThreads = 512;
+constexpr int kLnWarps = kLnThreads / 32;
 template <class In>
-__global__ void __launch_bounds__(kGridThreads, kGridCtasPerSm)
+__global__ void __launch_bounds__(kLnThreads, 2)
 k_rowgrid_ln_out(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, int G, int RB,
                  float eps, const uint4 *__restrict__ ws, const float *__restrict__ gamma,
                  const float *__restrict__ beta, uint16_t *__restrict__ ybf,
@@ -386,13 +390,13 @@ k_rowgrid_ln_out(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t r0 = (int64_t)blockIdx.y * RB;
   const int nr = (int)(rows - r0 < RB ? rows - r0 : RB);
-  const int64_t u = (int64_t)blockIdx.x * kGridThreads + tid;
+  const int64_t u = (int64_t)blockIdx.x * kLnThreads + tid;
   const bool live = u < (cols >> 3);
   // gamma / beta of the thread's unit go out before the wait for the rows'
   // statistics
   float gv[8], bv[8];
   if (live) load_gamma_beta<8>(gamma, beta, u * 8, aligned32(gamma, beta), gv, bv);
-  for (int j = warp; j < nr; j += kGridWarps) {
+  for (int j = warp; j < nr; j += kLnWarps) {
     const Chan c = fold_row_chan(ws, r0 + j, G);
     if (lane == 0) {
       const float rs = rstd_of(c, cols, eps);
@@ -494,10 +498,10 @@ int launch_grid(int mode, const void *xv, int64_t rows, int64_t cols, float eps,
                                      dim3((unsigned)((rows + kGridWarps - 1) / kGridWarps)),
                                      dim3(kGridThreads), 0, s, 0, rows, cols, G, eps,
                                      (const uint4 *)ws, mean, rstd));
-  // the rewrite: column blocks of 256 units, row groups of RB rows, at most
-  // one wave of kGridCtasPerSm CTAs per SM
-  const int64_t cb = ((cols >> 3) + kGridThreads - 1) / kGridThreads;
-  const int64_t want = (int64_t)kGridCtasPerSm * d.sm_count;
+  // the rewrite: column blocks of kLnThreads units, row groups of RB rows,
+  // at most one wave of 2 CTAs per SM
+  const int64_t cb = ((cols >> 3) + kLnThreads - 1) / kLnThreads;
+  const int64_t want = (int64_t)2 * d.sm_count;
   int64_t groups = want / cb;
   if (groups > rows) groups = rows;
   if (groups < 1) groups = 1;
@@ -506,7 +510,7 @@ int launch_grid(int mode, const void *xv, int64_t rows, int64_t cols, float eps,
   if (RB * (int64_t)sizeof(float2) > 48 * 1024) return RR_ERR_INVALID;
   groups = (rows + RB - 1) / RB;
   return cuda_status(launch_kernel(k_rowgrid_ln_out<In>, dim3((unsigned)cb, (unsigned)groups),
-                                   dim3(kGridThreads), (size_t)RB * sizeof(float2), s, 0, x, rows,
+                                   dim3(kLnThreads), (size_t)RB * sizeof(float2), s, 0, x, rows,
                                    cols, G, (int)RB, eps, (const uint4 *)ws, gamma, beta, ybf, mean,
                                    rstd));
 }
