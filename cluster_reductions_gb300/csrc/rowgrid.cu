@@ -376,7 +376,7 @@ k_rowgrid_softmax_out(const typename In::S *__restrict__ x, int64_t cols, int G,
 // gamma, beta 16-byte aligned.  Dynamic shared memory: RB (mean, rstd)
 // pairs.  The CTAs of column block 0 write mean / rstd when given.  512
 // threads rather than 256: twice the warps fold the rows' states at the
-// CTA's start (16 x 1M bf16: 0.55 -> 0.59 of the copy bandwidth).
+// CTA's start (16 x 1M bf16: 0.50 -> 0.54 of the copy bandwidth).
 constexpr int kLnThreads = 512;
 constexpr int kLnWarps = kLnThreads / 32;
 template <class In>
