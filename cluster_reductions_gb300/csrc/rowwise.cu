@@ -505,6 +505,93 @@ k_lnstats_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, float
   }
 }
 
+// Layernorm rewrite of chunked rows: the statistics as k_lnstats_ck (the
+// same geometry and fold order, so the same mean / rstd bits), then
+// y = (x - mean) * rstd * gamma + beta -> bf16 over the row's head, whole
+// vectors and tail.  A vector's columns start at any offset, so gamma and
+// beta come from an image each CTA builds once in shared memory: the float2
+// (gamma[j], beta[j]) at slot j + j / EPV.  One pad slot per EPV columns
+// puts the 16 threads of a half warp, which read columns EPV apart, at
+// slots EPV + 1 apart (odd), on 16 distinct 8-byte bank pairs for any head
+// offset.  Two elements per packed fp32 instruction; y goes as one vector
+// a chunk where it shares x's offset within a 16-byte chunk, element by
+// element otherwise.  Dynamic shared memory: ck_image_slots(cols, EPV)
+// float2.
+__host__ __device__ constexpr int ck_image_slots(int cols, int epv) { return cols + cols / epv + 1; }
+
+template <int THREADS, int NV, class In>
+__global__ void __launch_bounds__(THREADS)
+k_layernorm_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, float eps,
+               const float *__restrict__ gamma, const float *__restrict__ beta,
+               uint16_t *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd) {
+  pdl_begin();
+  constexpr int EPV = In::EPV;
+  extern __shared__ float2 sgb[];
+  __shared__ float red[2][THREADS / 32];
+  const int tid = threadIdx.x;
+  for (int j = tid; j < cols; j += THREADS) sgb[j + j / EPV] = make_float2(__ldg(gamma + j), __ldg(beta + j));
+  ChunkRegs<THREADS, NV, In> cr;
+  ChunkRow<In> g(x, cols);
+  if ((int64_t)blockIdx.x < rows) g = cr.fetch(x + (int64_t)blockIdx.x * cols, cols);
+  __syncthreads();
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    float v[NV][EPV];
+    chunk_unpack<THREADS, NV, In>(cr, g.nvec, v);
+    const float hv = cr.hv, tv = cr.tv;
+    const ChunkRow<In> cur = g;
+    if (row + gridDim.x < rows) g = cr.fetch(x + (row + gridDim.x) * (int64_t)cols, cols);
+    float mu, rs;
+    chunk_stats<THREADS, NV, EPV>(v, hv, tv, cur.h, cur.nvec, cur.t, cols, eps, red, mu, rs);
+    if (tid == 0) {
+      if (mean) mean[row] = mu;
+      if (rstd) rstd[row] = rs;
+    }
+    uint16_t *yr = y + row * (int64_t)cols;
+    auto put = [&](int j, float xv) {
+      const float2 gb = sgb[j + j / EPV];
+      const __nv_bfloat16 ob = __float2bfloat16_rn(fmaf((xv - mu) * rs, gb.x, gb.y));
+      yr[j] = *reinterpret_cast<const uint16_t *>(&ob);
+    };
+    if (tid < cur.h) put(tid, hv);
+    if (tid < cur.t) put(cur.h + cur.nvec * EPV + tid, tv);
+    const bool vst = ((uintptr_t)(yr + cur.h) & (2 * EPV - 1)) == 0;
+    const uint64_t mu2 = f2_pack(mu, mu), rs2 = f2_pack(rs, rs);
+    // every whole vector starts at column h (mod EPV): its element e sits at
+    // slot e + dq[e] past the vector's first column's slot
+    int dq[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) dq[e] = e + (e >= EPV - cur.h ? 1 : 0);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx >= cur.nvec) continue;
+      const int j0 = cur.h + idx * EPV;
+      const float2 *q = sgb + j0 + j0 / EPV;
+      uint32_t pk[EPV / 2];
+#pragma unroll
+      for (int i = 0; i < EPV / 2; ++i) {
+        const float2 g0 = q[dq[2 * i]], g1 = q[dq[2 * i + 1]];
+        float lo, hi;
+        f2_unpack(f2_fma(f2_mul(f2_sub(f2_pack(v[k][2 * i], v[k][2 * i + 1]), mu2), rs2),
+                         f2_pack(g0.x, g1.x), f2_pack(g0.y, g1.y)),
+                  lo, hi);
+        pk[i] = bf16x2_bits(lo, hi);
+      }
+      uint16_t *p = yr + j0;
+      if (vst) {
+        if constexpr (EPV == 8) *reinterpret_cast<uint4 *>(p) = make_uint4(pk[0], pk[1 % (EPV / 2)], pk[2 % (EPV / 2)], pk[3 % (EPV / 2)]);
+        else *reinterpret_cast<uint2 *>(p) = make_uint2(pk[0], pk[1 % (EPV / 2)]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPV / 2; ++i) {
+          p[2 * i] = (uint16_t)(pk[i] & 0xffffu);
+          p[2 * i + 1] = (uint16_t)(pk[i] >> 16);
+        }
+      }
+    }
+  }
+}
+
 template <class K>
 int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d, size_t smem = 0) {
   const int nb = occupancy_blocks((const void *)kernel, threads, smem, d.device);
@@ -1029,6 +1116,31 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
   if (pk.tier == RR_TIER_WARP)
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                eps, nullptr, mean, rstd, gamma, beta, y, pk.width, s, d);
+  if (pk.chunk) {
+    *tier_out |= kChunkBit;
+    const size_t smem = (size_t)ck_image_slots((int)cols, In::EPV) * sizeof(float2);
+#define RR_LNF_CK(T, NV)                                                       \
+  {                                                                            \
+    auto k = k_layernorm_ck<T, NV, In>;                                        \
+    const cudaError_t e =                                                      \
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (e != cudaSuccess) return cuda_status(e);                               \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d, smem)), dim3(T), smem, s, 0, \
+        x, rows, (int)cols, eps, gamma, beta, y, mean, rstd);                  \
+  }
+    switch (pick_nv(cols / In::EPV)) {  // the statistics' geometry: the same bits
+      case 1: RR_LNF_CK(kRowThreads, 1) break;
+      case 2: RR_LNF_CK(kRowThreads, 2) break;
+      case 4: RR_LNF_CK(kRowThreads, 4) break;
+      default:
+        if (wide_threads(cols / In::EPV) == 288) RR_LNF_CK(288, 4)
+        else if (wide_threads(cols / In::EPV) == 384) RR_LNF_CK(384, 4)
+        else RR_LNF_CK(kRowWideThreads, 4)
+        break;
+    }
+#undef RR_LNF_CK
+    return cuda_status(cudaGetLastError());
+  }
   const bool reg = vec && pick_nv(nvec) > 0;
   if (pk.half) {
 #define RR_LNF_REGH(T, NV)                                                     \
@@ -1132,15 +1244,15 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // (16 x 1M bf16: 35 against 48 us)
   const bool ring_few = mode != kModeLayernorm;
   const int64_t staged_min = vec ? kRowStagedMinVec[mode] : kRowStagedMinVecMis[mode];
-  // the statistics of rows that are not 16-byte aligned: the chunked
-  // register form (head + 16-byte vectors + tail) up to 1024 vectors, where
-  // they would otherwise take the scalar two-pass form (16384 x 4099 bf16
-  // 0.41 -> 0.58, 16384 x 4095 fp32 0.58 -> 1.00; beyond 1024 vectors
-  // staging measured ahead, 4096 x 16383 bf16 0.68 against 0.43).  The
-  // rewrite keeps the scalar form: in the chunked form its gamma / beta at
-  // any offset (shifted 16-byte windows) took 127 registers a thread and
-  // measured slower (16384 x 4099 bf16 0.39 against 0.44)
-  const bool chunk_ok = !vec && mode == kModeStats && row_vecs <= kRowStagedMinVecMis[kModeStats];
+  // the statistics and the rewrite of rows that are not 16-byte aligned:
+  // the chunked register form (head + 16-byte vectors + tail) up to 1024
+  // vectors, where they would otherwise take the scalar two-pass form (the
+  // statistics: 16384 x 4099 bf16 0.41 -> 0.58, 16384 x 4095 fp32 0.58 ->
+  // 1.00; beyond 1024 vectors staging measured ahead, 4096 x 16383 bf16 0.68
+  // against 0.43; the rewrite, gamma / beta from a padded image in shared
+  // memory: 16384 x 4099 bf16 0.44 -> 0.60, 16384 x 8196 0.47 -> 0.65,
+  // 16384 x 4095 fp32 0.61 -> 0.80, 65536 x 1029 fp32 0.32 -> 0.39)
+  const bool chunk_ok = !vec && mode != kModeSoftmax && row_vecs <= kRowStagedMinVecMis[kModeStats];
   if (tier == RR_TIER_BLOCK) {
     const bool st = row_vecs > staged_min && stage_fits(1);
     if (!st && chunk_ok) {

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from _util import assert_rel_close, to_np
+from _util import assert_bits_equal, assert_rel_close, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -642,12 +642,13 @@ def test_staged_misaligned_rows(rr, oracle_mod, dtype):
 
 
 # ---------------------------------------------------------------------------
-# Chunked rows at a CTA per row (rowwise.cu, k_lnstats_ck): the statistics of
-# rows that are not 16-byte aligned -- odd widths, misaligned bases -- held
-# as head + 16-byte vectors + tail up to 1024 vectors (staged beyond); the
-# rewrite of the same rows (the scalar form) beside them.  Widths from one
-# vector to the 512-thread geometry, every head length, outputs and gamma /
-# beta at their own offsets.
+# Chunked rows at a CTA per row (rowwise.cu, k_lnstats_ck, k_layernorm_ck):
+# the statistics and the rewrite of rows that are not 16-byte aligned --
+# odd widths, misaligned bases -- held as head + 16-byte vectors + tail up
+# to 1024 vectors (beyond, the statistics stage and the rewrite takes the
+# scalar form).  Widths from one vector to the 512-thread geometry, every
+# head length, outputs and gamma / beta at their own offsets; where both
+# are chunked the rewrite's mean / rstd are the statistics' bits.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_chunked_rows_statistics_and_rewrite(rr, oracle_mod, dtype):
@@ -681,6 +682,10 @@ def test_chunked_rows_statistics_and_rewrite(rr, oracle_mod, dtype):
                 m2, r2 = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
                 rr.layernorm(x, g, b, 1e-5, out=yb, mean=m2, rstd=r2)
                 assert rr.last_tier() == ("block", 1), (cols, xo, go, oo)
+                assert rr.last_form() == ("chunked" if chunked else "direct"), (cols, xo, go, oo)
+                if chunked:
+                    assert_bits_equal(to_np(m2), to_np(mean))
+                    assert_bits_equal(to_np(r2), to_np(rstd))
                 y64, y16, rm2, rr2 = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
                 assert_layernorm_close(to_np(yb)[idx], y64, y16, xf, to_np(g), to_np(b), rm2, rr2,
                                        to_np(m2)[idx], to_np(r2)[idx])
@@ -702,6 +707,36 @@ def test_chunked_rows_forced_block_and_special(rr, oracle_mod):
     bound = 1e-5 * np.maximum(np.abs(rm), np.sqrt((of ** 2).sum(axis=1)) / 3001)
     assert (np.abs(to_np(mean).astype(np.float64) - rm) <= bound).all()
     assert_rel_close(to_np(rstd), rr_, 1e-5, what="chunk rstd offset rows")
+    # the rewrite of constant rows: (x - mean) * rstd = 0, so y = beta
+    from cluster_reductions_gb300 import inputs
+    g, b = inputs.layernorm_params(3001, 4202, "cuda")
+    yc = rr.layernorm(c, g, b, 1e-5)
+    assert rr.last_form() == "chunked"
+    assert_bits_equal(to_np(yc), np.broadcast_to(to_np(b.to(torch.bfloat16)), (4, 3001)))
+
+
+def test_chunked_rewrite_many_rows(rr, oracle_mod):
+    # more rows than the persistent grid holds, so that each CTA takes
+    # several rows, every head length among them (4099 = 3 mod 8), the next
+    # row's vectors loaded while the current one is rewritten
+    from _util import assert_layernorm_close
+    from cluster_reductions_gb300 import inputs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, cols = 8 * sms + 5, 4099
+    x = _x(rows, cols, torch.bfloat16, 4210, 2.0, 0)
+    g, b = inputs.layernorm_params(cols, 4211, "cuda")
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device="cuda")
+    m2, r2 = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    rr.layernorm(x, g, b, 1e-5, out=y, mean=m2, rstd=r2)
+    assert rr.last_form() == "chunked"
+    assert_bits_equal(to_np(m2), to_np(mean))
+    assert_bits_equal(to_np(r2), to_np(rstd))
+    idx = np.unique(np.r_[0:9, rows // 3:rows // 3 + 8, rows - 9:rows])
+    xs = x[torch.from_numpy(idx).cuda()]
+    y64, y16, rm2, rr2 = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
+    assert_layernorm_close(to_np(y)[idx], y64, y16, xs.to(torch.float64).cpu().numpy(), to_np(g),
+                           to_np(b), rm2, rr2, to_np(m2)[idx], to_np(r2)[idx])
 
 
 # ---------------------------------------------------------------------------

@@ -221,13 +221,17 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # 8-byte vector rows:
     (16384, 4092, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # registers up to 1024
     (16384, 8188, "layernorm", "bf16", True, 16, ("block", 1, "direct")),  # 8-byte vectors for
-    (16384, 8196, "layernorm", "bf16", True, 16, ("block", 1, "direct")),  # softmax, 2048 for the
+    (16384, 8196, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # softmax, 2048 for the
     (16384, 4100, "lnstats", "bf16", True, 16, ("block", 1, "direct")),    # statistics / rewrite;
-    (16384, 4098, "lnstats", "bf16", True, 16, ("block", 1, "chunked")),   # the statistics of rows
-    (16384, 4098, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # not 8-byte aligned
-    (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # misaligned rows: chunked
-    (8192, 8190, "lnstats", "bf16", False, 16, ("block", 1, "chunked")),   # registers to 1024 vectors
-    (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, "direct")),   # (the rewrite 2048),
+    (16384, 4098, "lnstats", "bf16", True, 16, ("block", 1, "chunked")),   # the statistics and the
+    (16384, 4098, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # rewrite of rows not
+    (16384, 4099, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # 8-byte aligned (or
+    (16384, 4095, "layernorm", "f32", True, 16, ("block", 1, "chunked")),  # past the 8-byte form):
+    (16384, 4098, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # chunked registers to
+    (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # 1024 vectors, then
+    (8192, 8190, "lnstats", "bf16", False, 16, ("block", 1, "chunked")),   # staged (the statistics)
+    (8192, 8190, "layernorm", "bf16", False, 16, ("block", 1, "chunked")), # or the scalar form
+    (8192, 8204, "layernorm", "bf16", True, 16, ("block", 1, "direct")),   # (the rewrite, to 2048),
     (4096, 16396, "layernorm", "bf16", True, 16, ("block", 1, "staged")),  # staged beyond
     (4096, 32768, "softmax", "bf16", True, 1, ("block", 1, "staged")),     # no clusters: C = 1 fits
     (4096, 40000, "softmax", "f32", True, 1, ("block", 1, "direct")),      # no clusters, too long
