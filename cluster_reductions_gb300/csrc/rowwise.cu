@@ -606,6 +606,21 @@ inline int pick_nv(int64_t nvec) {
     if ((int64_t)kRowThreads * nv >= nvec) return nv;
   return 0;
 }
+// Geometry of the chunked kernels (k_lnstats_ck, k_layernorm_ck) for rows
+// of nvec vectors: CTAs of kChunkThreads threads holding NV = 1, 2 or 4
+// vectors each up to 4 * kChunkThreads vectors, then kRowThreads x 4 (the
+// return value 8), up to 1024; 0 beyond.  128 threads rather than 256: a
+// row's two block reductions cost each thread about as much as its two
+// vectors of arithmetic, so fewer threads with more vectors each issue
+// fewer instructions a row, and one more CTA fits an SM (16384 x 4099
+// bf16 statistics / rewrite 0.57 / 0.60 -> 0.70 / 0.64, 65536 x 1029 fp32
+// 0.40 / 0.39 -> 0.59 / 0.53; rows of 513 to 1024 vectors unchanged).
+constexpr int kChunkThreads = 128;
+inline int chunk_geometry(int64_t nvec) {
+  for (int nv = 1; nv <= 4; nv <<= 1)
+    if ((int64_t)kChunkThreads * nv >= nvec) return nv;
+  return nvec <= (int64_t)kRowThreads * 4 ? 8 : 0;
+}
 // Layernorm rows of more than 4 vectors per thread (1025 to 2048 vectors)
 // run with kRowWideThreads threads and 4 vectors each instead of 256 x 8:
 // the rewrite measured 11-20% faster (at 8 vectors a thread, with gamma and
@@ -1021,15 +1036,12 @@ int lnstats_impl(const void *xv, int64_t rows, int64_t cols, float eps, float *m
     auto k = k_lnstats_ck<T, NV, In>;                                          \
     launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0, x, rows, (int)cols, eps, mean, rstd); \
   }
-    switch (pick_nv(cols / In::EPV)) {  // the rewrite's geometry: the same bits
-      case 1: RR_LN_CK(kRowThreads, 1) break;
-      case 2: RR_LN_CK(kRowThreads, 2) break;
-      case 4: RR_LN_CK(kRowThreads, 4) break;
-      default:
-        if (wide_threads(cols / In::EPV) == 288) RR_LN_CK(288, 4)
-        else if (wide_threads(cols / In::EPV) == 384) RR_LN_CK(384, 4)
-        else RR_LN_CK(kRowWideThreads, 4)
-        break;
+    switch (chunk_geometry(cols / In::EPV)) {  // the rewrite's geometry: the same bits
+      case 1: RR_LN_CK(kChunkThreads, 1) break;
+      case 2: RR_LN_CK(kChunkThreads, 2) break;
+      case 4: RR_LN_CK(kChunkThreads, 4) break;
+      case 8: RR_LN_CK(kRowThreads, 4) break;
+      default: return RR_ERR_UNSUPPORTED;
     }
 #undef RR_LN_CK
     return cuda_status(cudaGetLastError());
@@ -1128,15 +1140,12 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
     launch_kernel(k, dim3(persistent_grid(k, T, rows, d, smem)), dim3(T), smem, s, 0, \
         x, rows, (int)cols, eps, gamma, beta, y, mean, rstd);                  \
   }
-    switch (pick_nv(cols / In::EPV)) {  // the statistics' geometry: the same bits
-      case 1: RR_LNF_CK(kRowThreads, 1) break;
-      case 2: RR_LNF_CK(kRowThreads, 2) break;
-      case 4: RR_LNF_CK(kRowThreads, 4) break;
-      default:
-        if (wide_threads(cols / In::EPV) == 288) RR_LNF_CK(288, 4)
-        else if (wide_threads(cols / In::EPV) == 384) RR_LNF_CK(384, 4)
-        else RR_LNF_CK(kRowWideThreads, 4)
-        break;
+    switch (chunk_geometry(cols / In::EPV)) {  // the statistics' geometry: the same bits
+      case 1: RR_LNF_CK(kChunkThreads, 1) break;
+      case 2: RR_LNF_CK(kChunkThreads, 2) break;
+      case 4: RR_LNF_CK(kChunkThreads, 4) break;
+      case 8: RR_LNF_CK(kRowThreads, 4) break;
+      default: return RR_ERR_UNSUPPORTED;
     }
 #undef RR_LNF_CK
     return cuda_status(cudaGetLastError());
@@ -1247,11 +1256,11 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // the statistics and the rewrite of rows that are not 16-byte aligned:
   // the chunked register form (head + 16-byte vectors + tail) up to 1024
   // vectors, where they would otherwise take the scalar two-pass form (the
-  // statistics: 16384 x 4099 bf16 0.41 -> 0.58, 16384 x 4095 fp32 0.58 ->
+  // statistics: 16384 x 4099 bf16 0.41 -> 0.70, 16384 x 4095 fp32 0.58 ->
   // 1.00; beyond 1024 vectors staging measured ahead, 4096 x 16383 bf16 0.68
   // against 0.43; the rewrite, gamma / beta from a padded image in shared
-  // memory: 16384 x 4099 bf16 0.44 -> 0.60, 16384 x 8196 0.47 -> 0.65,
-  // 16384 x 4095 fp32 0.61 -> 0.80, 65536 x 1029 fp32 0.32 -> 0.39)
+  // memory: 16384 x 4099 bf16 0.44 -> 0.64, 16384 x 8196 0.47 -> 0.64,
+  // 16384 x 4095 fp32 0.61 -> 0.79, 65536 x 1029 fp32 0.32 -> 0.53)
   const bool chunk_ok = !vec && mode != kModeSoftmax && row_vecs <= kRowStagedMinVecMis[kModeStats];
   if (tier == RR_TIER_BLOCK) {
     const bool st = row_vecs > staged_min && stage_fits(1);
