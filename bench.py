@@ -80,12 +80,12 @@ NCU_TRAFFIC = {
                       "src_sha": "200d80f613a727b2", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
     "combine_p8": {"bytes": 566772736, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "68a1353cf0e06719", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 558803968, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "8d9c07883fcb56a0", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "softmax_bf16": {"bytes": 558612480, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "360e1033451eaaa8", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
     "block_sum_f32": {"bytes": 271227904, "src": ["reduce.cu", "rr_device.cuh"],
                      "src_sha": "200d80f613a727b2", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271368448, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "8d9c07883fcb56a0", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "layernorm_bf16": {"bytes": 271270144, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "360e1033451eaaa8", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
     "warp_sum_f32": {"bytes": 137803776, "src": ["reduce.cu", "rr_device.cuh"],
                     "src_sha": "200d80f613a727b2", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
@@ -1002,8 +1002,9 @@ PROFILE_CASES = {
     "rowsk_lnstats_32x524288_bf16": ({"shape": (32, 1 << 19), "op": "lnstats"}, "medium", 1.0),
     # rows 8-byte but not 16-byte aligned: the register form read as 8-byte vectors
     "medium_layernorm_16384x4100_bf16": ({"shape": (16384, 4100), "op": "layernorm"}, "medium", 1.0),
-    # odd widths: the statistics' chunked register form (head + vectors + tail)
+    # odd widths: the chunked register form (head + vectors + tail)
     "medium_lnstats_16384x4099_bf16": ({"shape": (16384, 4099), "op": "lnstats"}, "medium", 1.0),
+    "medium_layernorm_16384x4099_bf16": ({"shape": (16384, 4099), "op": "layernorm"}, "medium", 1.0),
 }
 
 
