@@ -592,6 +592,98 @@ k_layernorm_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, flo
   }
 }
 
+// Softmax of chunked rows (rows that are not 16-byte aligned, up to 1024
+// vectors): the row held as head + whole 16-byte vectors + tail as in
+// k_lnstats_ck, the next row's loaded while the current one is reduced;
+// each thread's (max, sum) over its elements, one block combine of the
+// pairs, then y = e^(x - M) / S in fp32: one 32-byte (bf16 input) or
+// 16-byte store a vector where y's offset allows, element by element
+// otherwise.  Empty slots hold -inf, so their terms are exactly 0.
+template <int THREADS, int NV, class In>
+__global__ void __launch_bounds__(THREADS)
+k_softmax_ck(const typename In::S *__restrict__ x, int64_t rows, int cols, float *__restrict__ y) {
+  pdl_begin();
+  constexpr int EPV = In::EPV;
+  __shared__ float red_m[THREADS / 32 + 1], red_s[THREADS / 32 + 1];
+  const int tid = threadIdx.x;
+  ChunkRegs<THREADS, NV, In> cr;
+  ChunkRow<In> g(x, cols);
+  if ((int64_t)blockIdx.x < rows) g = cr.fetch(x + (int64_t)blockIdx.x * cols, cols);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const ChunkRow<In> cur = g;
+    float v[NV][EPV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (k * THREADS + tid < cur.nvec) {
+        In::unpack(cr.raw[k], v[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) v[k][e] = -INFINITY;
+      }
+    }
+    float hv = tid < cur.h ? cr.hv : -INFINITY, tv = tid < cur.t ? cr.tv : -INFINITY;
+    if (row + gridDim.x < rows) g = cr.fetch(x + (row + gridDim.x) * (int64_t)cols, cols);
+    float m = fmaxf(hv, tv);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) m = fmaxf(m, v[k][e]);
+    float s = 0.0f;
+    if (m != -INFINITY) {
+      const float mb = m * kLog2e;
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float p = ex2_approx(fmaf(v[k][e], kLog2e, -mb));
+          v[k][e] = p;
+          s += p;
+        }
+      hv = ex2_approx(fmaf(hv, kLog2e, -mb));
+      tv = ex2_approx(fmaf(tv, kLog2e, -mb));
+      s += hv + tv;
+    } else {
+      // every element this thread holds is -inf: e^(x - M) = 0
+#pragma unroll
+      for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) v[k][e] = 0.0f;
+      hv = tv = 0.0f;
+    }
+    float M = m, S = s;
+    ms_block_allreduce<THREADS>(M, S, red_m, red_s);
+    const float f = (m == -INFINITY) ? 0.0f : ex2_approx((m - M) * kLog2e) * (1.0f / S);
+    float *yr = y + row * (int64_t)cols;
+    if (tid < cur.h) yr[tid] = hv * f;
+    if (tid < cur.t) yr[cur.h + cur.nvec * EPV + tid] = tv * f;
+    const uintptr_t ya = (uintptr_t)(yr + cur.h);
+    const int vw = ya % (4 * EPV) == 0 ? 2 : (ya % 16 == 0 ? 1 : 0);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int idx = k * THREADS + tid;
+      if (idx >= cur.nvec) continue;
+      float *p = yr + cur.h + (int64_t)idx * EPV;
+      float o[EPV];
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) o[e] = v[k][e] * f;
+      if constexpr (EPV == 8) {
+        if (vw == 2) {
+          st_stream_v8(p, o);
+          continue;
+        }
+      }
+      if (vw) {
+#pragma unroll
+        for (int e = 0; e < EPV; e += 4) st_stream_v4(p + e, o[e], o[e + 1], o[e + 2], o[e + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) p[e] = o[e];
+      }
+    }
+    __syncthreads();
+  }
+}
+
 template <class K>
 int persistent_grid(K kernel, int threads, int64_t rows, const DevInfo &d, size_t smem = 0) {
   const int nb = occupancy_blocks((const void *)kernel, threads, smem, d.device);
@@ -893,7 +985,7 @@ inline int tier_code(int tier, int width, int flags) {
   return tier | ((width & 0xff) << 8) | (flags << 16) | (((width >> 8) & 0xff) << 19);
 }
 constexpr int kFlagStaged = 1, kFlagRing = 2, kFlagGrid = 4;
-constexpr int kChunkBit = 1 << 27;  // the statistics' chunked register form
+constexpr int kChunkBit = 1 << 27;  // the chunked register form (k_*_ck)
 
 // The grid form's plan for a call: forced (w.splits), automatic with the
 // caller's workspace (falling back to the plan without one when it is too
@@ -958,6 +1050,23 @@ int softmax_impl(const void *xv, int64_t rows, int64_t cols, float *y, cudaStrea
   if (pk.tier == RR_TIER_WARP)
     return (vec ? launch_rowwise_warp : launch_rowwise_warp_mis)(kModeSoftmax, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols,
                                0.0f, y, nullptr, nullptr, nullptr, nullptr, nullptr, pk.width, s, d);
+  if (pk.chunk) {
+    *tier_out |= kChunkBit;
+#define RR_SM_CK(T, NV)                                                        \
+  {                                                                            \
+    auto k = k_softmax_ck<T, NV, In>;                                          \
+    launch_kernel(k, dim3(persistent_grid(k, T, rows, d)), dim3(T), 0, s, 0, x, rows, (int)cols, y); \
+  }
+    switch (chunk_geometry(cols / In::EPV)) {
+      case 1: RR_SM_CK(kChunkThreads, 1) break;
+      case 2: RR_SM_CK(kChunkThreads, 2) break;
+      case 4: RR_SM_CK(kChunkThreads, 4) break;
+      case 8: RR_SM_CK(kRowThreads, 4) break;
+      default: return RR_ERR_UNSUPPORTED;
+    }
+#undef RR_SM_CK
+    return cuda_status(cudaGetLastError());
+  }
   const bool reg = vec && pick_nv(nvec) > 0;
   if (pk.half) {
 #define RR_SM_REGH(T, NV)                                                      \
@@ -1217,12 +1326,13 @@ constexpr int64_t kRowStagedMinVec[3] = {1024, kRowRegMaxVec, kRowRegMaxVec};
 constexpr int64_t kRowThreadsHost = 256;  // kRowThreads, for the host plan
 // Shortest rows the automatic plan gives the grid form (a few rows only).
 constexpr int64_t kRowGridMinCols = 16384;
-// Rows that are not 16-byte aligned have no register form: they are staged
-// beyond these lengths in 16-byte vectors (softmax, statistics, rewrite),
-// shorter ones take the scalar form.  Measured against that form and the
-// split-K fallback: staging wins for softmax from the shortest rows tried
-// (4100 bf16: 5026 against 4315 GB/s; 8193: 6396 against 1620), for the
-// statistics from about 1024 vectors, for the rewrite from about 2048.
+// Rows that are not 16-byte aligned and not held in the chunked register
+// form (below) are staged beyond these lengths in 16-byte vectors (softmax,
+// statistics, rewrite), shorter ones take the scalar form.  Measured
+// against that form and the split-K fallback: staging wins for softmax
+// from the shortest rows tried (4100 bf16: 5026 against 4315 GB/s; 8193:
+// 6396 against 1620), for the statistics from about 1024 vectors, for the
+// rewrite from about 2048.
 constexpr int64_t kRowStagedMinVecMis[3] = {32, 1024, 2048};
 #ifndef RR_ROW_STAGED_SPLITK
 #define RR_ROW_STAGED_SPLITK 0
@@ -1261,7 +1371,14 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   // against 0.43; the rewrite, gamma / beta from a padded image in shared
   // memory: 16384 x 4099 bf16 0.44 -> 0.64, 16384 x 8196 0.47 -> 0.64,
   // 16384 x 4095 fp32 0.61 -> 0.79, 65536 x 1029 fp32 0.32 -> 0.53)
-  const bool chunk_ok = !vec && mode != kModeSoftmax && row_vecs <= kRowStagedMinVecMis[kModeStats];
+  // softmax too, up to 4096 elements (512 bf16 / 1024 fp32 vectors), when
+  // its output shares x's offset within a 16-byte chunk (vector stores),
+  // rather than staging (16384 x 4099 bf16 0.74 -> 0.90, 16384 x 2057 0.47
+  // -> 0.64, 65536 x 1029 fp32 0.40 -> 0.73; 8192 x 8191 bf16 staged 0.94
+  // against 0.80, an x base off the output's offset 0.38 against 0.27)
+  const bool chunk_ok =
+      !vec && (mode != kModeSoftmax ? row_vecs <= kRowStagedMinVecMis[kModeStats]
+                                    : out_vec && row_vecs <= (in_dtype == RR_BF16 ? 512 : 1024));
   if (tier == RR_TIER_BLOCK) {
     const bool st = row_vecs > staged_min && stage_fits(1);
     if (!st && chunk_ok) {

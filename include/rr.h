@@ -328,7 +328,9 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * shared memory, (cols + cols / 8 + 1) * 8 bytes for bf16 input, cols / 4
  * for fp32), where 8-byte aligned rows do not take the register form in
  * 8-byte vectors; rr_layernorm takes the scalar form for its rows of 1025
- * to 2048 vectors.
+ * to 2048 vectors.  rr_softmax takes the chunked form for rows of up to
+ * 4096 elements whose output shares x's offset within a 16-byte chunk
+ * (always so for a 16-byte aligned x and output), and stages the rest.
  * Long rows that are not staged take split-K over global memory with
  * slices of at most 128 KiB.  A forced block tier stages when it applies; a
  * forced split-K tier reads from global memory.
@@ -580,9 +582,8 @@ int rr_device_status(void *stream);
  * memory, ring 1 when it streamed them through a shared-memory ring of bulk
  * copies (one combine per row; the layernorm statistics as a (count, mean,
  * M2) monoid), grid 1 when it took the grid form (rr_rowwise_opts), chunked
- * 1 when the layernorm statistics or rewrite held a row that is not 16-byte
- * aligned in registers as its head, whole 16-byte vectors and tail (a CTA
- * per row). */
+ * 1 when a row operation held a row that is not 16-byte aligned in
+ * registers as its head, whole 16-byte vectors and tail (a CTA per row). */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -616,9 +617,9 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * size planned; a launch may take a smaller one, down to 2, when the device
  * cannot co-schedule a cluster that size for every row), 3 for the grid
  * form (split-K, width = G CTAs per row), which the plan considers only
- * with with_workspace != 0, 4 for the chunked register form of the
- * statistics or the rewrite of rows that are not 16-byte aligned (up to
- * 1024 vectors).  Touches no GPU.  RR_ERR_INVALID on negative
+ * with with_workspace != 0, 4 for the chunked register form of rows that
+ * are not 16-byte aligned (the statistics and the rewrite up to 1024
+ * vectors, softmax up to 4096 elements).  Touches no GPU.  RR_ERR_INVALID on negative
  * sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
  */
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,

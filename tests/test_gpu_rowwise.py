@@ -715,6 +715,51 @@ def test_chunked_rows_forced_block_and_special(rr, oracle_mod):
     assert_bits_equal(to_np(yc), np.broadcast_to(to_np(b.to(torch.bfloat16)), (4, 3001)))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_chunked_softmax_rows(rr, oracle_mod, dtype):
+    # softmax of rows that are not 16-byte aligned, up to 4096 elements, at
+    # a CTA per row (k_softmax_ck): odd widths, x at offsets 0 and 1, the
+    # output at x's offset within a 16-byte chunk (32- and 16-byte stores);
+    # an output off that offset takes another form; rows of -inf, whole and
+    # within one thread's vectors; more rows than the persistent grid holds
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    epv = 8 if dtype == torch.bfloat16 else 4
+    widths = [4099, 2057, 513, 4103] if epv == 8 else [4095, 2051, 1029, 4099]
+    for i, cols in enumerate(widths):
+        rows = 3 * sms + 7
+        for xo in (0, 1):
+            x = _x(rows, cols, dtype, 4300 + 2 * i + xo, 3.0, xo)
+            if i == 0:
+                x[1] = float("-inf")                      # a whole row
+                x[2, : cols // 3] = float("-inf")         # the first third
+                x[3, 5:12] = float("-inf")
+            idx = np.unique(np.r_[0:6, rows // 2, rows - 4:rows])
+            # the output at x's offset: elements of 4 bytes, x's of 2 or 4
+            yo = xo
+            y = torch.empty(rows * cols + yo, device="cuda")[yo:].view(rows, cols)
+            rr.softmax(x, out=y)
+            assert rr.last_tier() == ("block", 1) and rr.last_form() == "chunked", (cols, xo)
+            ref = oracle_mod.softmax(to_np(x[torch.from_numpy(idx).cuda()]))
+            got = to_np(y)[idx]
+            # an all -inf row (0/0, NaN in the oracle) is written as 0
+            live = [r for r in range(len(idx)) if not (i == 0 and idx[r] == 1)]
+            assert_rel_close(got[live], ref[live], 1e-5, floor=1e-30,
+                             what=f"chunked softmax {cols} x+{xo}")
+            np.testing.assert_allclose(got[live].astype(np.float64).sum(axis=1), 1.0, rtol=0,
+                                       atol=1e-5)
+            if i == 0:
+                assert np.isnan(ref[1]).all() and (got[1] == 0).all()
+                assert (got[2, : cols // 3] == 0).all() and (got[3, 5:12] == 0).all()
+        # an output one element off x's offset: not the chunked form
+        x = _x(rows, cols, dtype, 4320 + i, 3.0, 0)
+        y = torch.empty(rows * cols + 1, device="cuda")[1:].view(rows, cols)
+        rr.softmax(x, out=y)
+        assert rr.last_form() != "chunked", cols
+        idx = np.r_[0:3, rows - 3:rows]
+        assert_rel_close(to_np(y)[idx], oracle_mod.softmax(to_np(x[torch.from_numpy(idx).cuda()])),
+                         1e-5, floor=1e-30, what=f"softmax {cols} y+1")
+
+
 def test_chunked_rewrite_many_rows(rr, oracle_mod):
     # more rows than the persistent grid holds, so that each CTA takes
     # several rows, every head length among them (4099 = 3 mod 8), the next
@@ -1019,9 +1064,12 @@ def test_half_vector_rows(rr, oracle_mod, dtype):
     for i, cols in enumerate(widths):
         x = _x(rows, cols, dtype, 2900 + i, 2.0)
         idx = np.r_[0:4, rows // 2, rows - 4:rows]
-        # softmax keeps 8-byte vectors in registers up to 1024 of them and
-        # stages longer rows; the statistics and the rewrite up to 2048
-        sm_form = "direct" if cols // half <= 1024 else "staged"
+        # softmax keeps 8-byte vectors in registers up to 1024 of them, then
+        # holds 16-byte vectors with head and tail apart (chunked) up to 4096
+        # elements and stages longer rows; the statistics and the rewrite
+        # keep 8-byte vectors up to 2048
+        sm_form = ("direct" if cols // half <= 1024 else
+                   "chunked" if cols // epv <= (512 if epv == 8 else 1024) else "staged")
         assert rr.plan_rowwise(rows, cols, "softmax", sms, 16, dtype=dtype,
                                form=True) == ("block", 1, sm_form)
         _check_all_row_ops(rr, oracle_mod, x, idx, expect_tier=(("block", 1), sm_form))

@@ -218,7 +218,7 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     (4096, 32768, "softmax", "bf16", False, 16, ("block", 1, "staged")),   # misaligned rows staged
     (4096, 50257, "softmax", "bf16", True, 16, ("splitk", 2, "staged")),
     (4096, 49148, "softmax", "bf16", False, 16, ("splitk", 2, "staged")),  # + 8 elements > 96 KiB
-    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # 8-byte vector rows:
+    (16384, 4100, "softmax", "bf16", True, 16, ("block", 1, "chunked")),   # 8-byte vector rows:
     (16384, 4092, "softmax", "bf16", True, 16, ("block", 1, "direct")),    # registers up to 1024
     (16384, 8188, "layernorm", "bf16", True, 16, ("block", 1, "direct")),  # 8-byte vectors for
     (16384, 8196, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # softmax, 2048 for the
@@ -227,7 +227,10 @@ def test_rowwise_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expect):
     (16384, 4098, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # rewrite of rows not
     (16384, 4099, "layernorm", "bf16", True, 16, ("block", 1, "chunked")), # 8-byte aligned (or
     (16384, 4095, "layernorm", "f32", True, 16, ("block", 1, "chunked")),  # past the 8-byte form):
-    (16384, 4098, "softmax", "bf16", True, 16, ("block", 1, "staged")),    # chunked registers to
+    (16384, 4098, "softmax", "bf16", True, 16, ("block", 1, "chunked")),   # chunked registers to
+    (8192, 6148, "softmax", "bf16", True, 16, ("block", 1, "staged")),     # (softmax to 4096
+    (16384, 4095, "softmax", "f32", True, 16, ("block", 1, "chunked")),    # elements: 512 bf16 /
+    (8192, 4105, "softmax", "f32", True, 16, ("block", 1, "staged")),      # 1024 fp32 vectors)
     (8192, 8204, "lnstats", "bf16", True, 16, ("block", 1, "staged")),     # 1024 vectors, then
     (8192, 8190, "lnstats", "bf16", False, 16, ("block", 1, "chunked")),   # staged (the statistics)
     (8192, 8190, "layernorm", "bf16", False, 16, ("block", 1, "chunked")), # or the scalar form
