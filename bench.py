@@ -1005,6 +1005,7 @@ PROFILE_CASES = {
     # odd widths: the chunked register form (head + vectors + tail)
     "medium_lnstats_16384x4099_bf16": ({"shape": (16384, 4099), "op": "lnstats"}, "medium", 1.0),
     "medium_layernorm_16384x4099_bf16": ({"shape": (16384, 4099), "op": "layernorm"}, "medium", 1.0),
+    "medium_softmax_16384x4099_bf16": ({"shape": (16384, 4099), "op": "softmax"}, "medium", 1.0),
 }
 
 
