@@ -233,7 +233,8 @@ def _row_ws_bytes(device: int, rows: int, cols: int, dt: int, row_op: int) -> in
 
 
 def _row_ws(xd: torch.Tensor, row_op: str, tier, splits: int, workspace):
-    """The workspace of a row op (the grid form's partial states): the
+    """The workspace of a row op (the grid form's partial states, the
+    layernorm two-pass form's statistics): the
     caller's tensor, none (workspace=False), or one of the size the
     automatic plan (or a forced `splits`) asks for, allocated here on the
     current stream."""
@@ -475,9 +476,13 @@ def last_form() -> str:
     """How the last row operation read its rows: "grid" (split-K over a
     plain grid, partial states through the workspace), "ring" (streamed
     through a shared-memory ring), "staged" (held in shared memory),
-    "chunked" (the statistics of a row not 16-byte aligned in registers as
-    head + vectors + tail) or "direct"."""
+    "chunked" (a row not 16-byte aligned in registers as head + vectors +
+    tail), "twopass" (the layernorm rewrite of many long rows: the
+    statistics streamed through the ring, then x read again for the
+    rewrite) or "direct"."""
     v = int(load().rr_last_tier())
+    if (v >> 28) & 1:
+        return "twopass"
     if (v >> 27) & 1:
         return "chunked"
     if (v >> 18) & 1:
@@ -516,7 +521,7 @@ def plan_rowwise(rows: int, cols: int, row_op: str, sm_count: int, max_cluster: 
     if staged:
         return TIER_NAMES[t.value], w.value, st.value == 1
     if form:
-        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring", "grid", "chunked")[st.value]
+        return TIER_NAMES[t.value], w.value, ("direct", "staged", "ring", "grid", "chunked", "twopass")[st.value]
     return TIER_NAMES[t.value], w.value
 
 

@@ -258,7 +258,8 @@ int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op, int al
                                  with_workspace != 0 && vec);
   *tier_out = p.tier;
   *width_out = p.width;
-  if (staged_out) *staged_out = p.chunk ? 4 : (p.grid ? 3 : (p.ring ? 2 : (p.staged ? 1 : 0)));
+  if (staged_out)
+    *staged_out = p.twopass ? 5 : (p.chunk ? 4 : (p.grid ? 3 : (p.ring ? 2 : (p.staged ? 1 : 0))));
   return RR_OK;
 }
 
@@ -277,6 +278,7 @@ int rr_rowwise_workspace_size(int64_t rows, int64_t cols, int in_dtype, int row_
                        1, &tier, &width, &staged);
   if (st != RR_OK) return st;
   if (staged == 3) *bytes_out = rowgrid_ws_bytes(rows, width);
+  if (staged == 5) *bytes_out = rowtwopass_ws_bytes(rows);
   return RR_OK;
 }
 

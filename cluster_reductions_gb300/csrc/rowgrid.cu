@@ -380,7 +380,9 @@ k_rowgrid_softmax_out(const typename In::S *__restrict__ x, int64_t cols, int G,
 // Layernorm rewrite: CTA (bx, by) of kLnThreads threads takes units
 // bx * kLnThreads + tid of rows [by * RB, min((by + 1) * RB, rows)); ybf,
 // gamma, beta 16-byte aligned.  Dynamic shared memory: RB (mean, rstd)
-// pairs.  The CTAs of column block 0 write mean / rstd when given.  512
+// pairs, folded from the rows' G states in ws, or read from mean_in /
+// rstd_in when those are given (a row's statistics computed beforehand).
+// The CTAs of column block 0 write mean / rstd when given.  512
 // threads rather than 256: twice the warps fold the rows' states at the
 // CTA's start (16 x 1M bf16: 0.50 -> 0.54 of the copy bandwidth).
 constexpr int kLnThreads = 512;
@@ -388,7 +390,8 @@ constexpr int kLnWarps = kLnThreads / 32;
 template <class In>
 __global__ void __launch_bounds__(kLnThreads, 2)
 k_rowgrid_ln_out(const typename In::S *__restrict__ x, int64_t rows, int64_t cols, int G, int RB,
-                 float eps, const uint4 *__restrict__ ws, const float *__restrict__ gamma,
+                 float eps, const uint4 *__restrict__ ws, const float *__restrict__ mean_in,
+                 const float *__restrict__ rstd_in, const float *__restrict__ gamma,
                  const float *__restrict__ beta, uint16_t *__restrict__ ybf,
                  float *__restrict__ mean, float *__restrict__ rstd) {
   pdl_begin();
@@ -402,7 +405,10 @@ k_rowgrid_ln_out(const typename In::S *__restrict__ x, int64_t rows, int64_t col
   // statistics
   float gv[8], bv[8];
   if (live) load_gamma_beta<8>(gamma, beta, u * 8, aligned32(gamma, beta), gv, bv);
-  for (int j = warp; j < nr; j += kLnWarps) {
+  if (mean_in) {
+    for (int j = tid; j < nr; j += kLnThreads) rowst[j] = make_float2(mean_in[r0 + j], rstd_in[r0 + j]);
+  }
+  for (int j = warp; !mean_in && j < nr; j += kLnWarps) {
     const Chan c = fold_row_chan(ws, r0 + j, G);
     if (lane == 0) {
       const float rs = rstd_of(c, cols, eps);
@@ -475,6 +481,28 @@ k_rowgrid_stats_fin(int64_t rows, int64_t cols, int G, float eps, const uint4 *_
   }
 }
 
+// The rewrite launch: column blocks of kLnThreads units, row groups of RB
+// rows, at most one wave of 2 CTAs per SM.
+template <class In>
+int launch_ln_out(const typename In::S *x, int64_t rows, int64_t cols, int G, float eps,
+                  const uint4 *ws, const float *mean_in, const float *rstd_in, const float *gamma,
+                  const float *beta, uint16_t *ybf, float *mean, float *rstd, cudaStream_t s,
+                  const DevInfo &d) {
+  const int64_t cb = ((cols >> 3) + kLnThreads - 1) / kLnThreads;
+  const int64_t want = (int64_t)2 * d.sm_count;
+  int64_t groups = want / cb;
+  if (groups > rows) groups = rows;
+  if (groups < 1) groups = 1;
+  int64_t RB = (rows + groups - 1) / groups;
+  if (RB < (rows + 65534) / 65535) RB = (rows + 65534) / 65535;
+  if (RB * (int64_t)sizeof(float2) > 48 * 1024) return RR_ERR_INVALID;
+  groups = (rows + RB - 1) / RB;
+  return cuda_status(launch_kernel(k_rowgrid_ln_out<In>, dim3((unsigned)cb, (unsigned)groups),
+                                   dim3(kLnThreads), (size_t)RB * sizeof(float2), s, 0, x, rows,
+                                   cols, G, (int)RB, eps, ws, mean_in, rstd_in, gamma, beta, ybf,
+                                   mean, rstd));
+}
+
 template <class In>
 int launch_grid(int mode, const void *xv, int64_t rows, int64_t cols, float eps, float *y,
                 float *mean, float *rstd, const float *gamma, const float *beta, uint16_t *ybf,
@@ -504,21 +532,8 @@ int launch_grid(int mode, const void *xv, int64_t rows, int64_t cols, float eps,
                                      dim3((unsigned)((rows + kGridWarps - 1) / kGridWarps)),
                                      dim3(kGridThreads), 0, s, 0, rows, cols, G, eps,
                                      (const uint4 *)ws, mean, rstd));
-  // the rewrite: column blocks of kLnThreads units, row groups of RB rows,
-  // at most one wave of 2 CTAs per SM
-  const int64_t cb = ((cols >> 3) + kLnThreads - 1) / kLnThreads;
-  const int64_t want = (int64_t)2 * d.sm_count;
-  int64_t groups = want / cb;
-  if (groups > rows) groups = rows;
-  if (groups < 1) groups = 1;
-  int64_t RB = (rows + groups - 1) / groups;
-  if (RB < (rows + 65534) / 65535) RB = (rows + 65534) / 65535;
-  if (RB * (int64_t)sizeof(float2) > 48 * 1024) return RR_ERR_INVALID;
-  groups = (rows + RB - 1) / RB;
-  return cuda_status(launch_kernel(k_rowgrid_ln_out<In>, dim3((unsigned)cb, (unsigned)groups),
-                                   dim3(kLnThreads), (size_t)RB * sizeof(float2), s, 0, x, rows,
-                                   cols, G, (int)RB, eps, (const uint4 *)ws, gamma, beta, ybf, mean,
-                                   rstd));
+  return launch_ln_out<In>(x, rows, cols, G, eps, ws, nullptr, nullptr, gamma, beta, ybf, mean,
+                           rstd, s, d);
 }
 
 }  // namespace
@@ -554,6 +569,23 @@ int launch_rowgrid(int mode, int in_dtype, const void *x, int64_t rows, int64_t 
                                (uint4 *)ws, s, d);
   return launch_grid<InF32>(mode, x, rows, cols, eps, y, mean, rstd, gamma, beta, ybf, G,
                             (uint4 *)ws, s, d);
+}
+
+int launch_ln_apply(int in_dtype, const void *x, int64_t rows, int64_t cols, const float *mean_in,
+                    const float *rstd_in, const float *gamma, const float *beta, uint16_t *ybf,
+                    cudaStream_t s, const DevInfo &d) {
+  if (cols % 8 != 0 || cols / 8 > INT_MAX || (uintptr_t)x % 16 != 0 || !mean_in || !rstd_in ||
+      (uintptr_t)ybf % 16 != 0 || (uintptr_t)gamma % 16 != 0 || (uintptr_t)beta % 16 != 0)
+    return RR_ERR_INVALID;
+  if (rows == 0 || cols == 0) return RR_OK;
+  if (log_enabled())
+    std::fprintf(stderr, "rr: layernorm apply rows=%lld cols=%lld\n", (long long)rows,
+                 (long long)cols);
+  if (in_dtype == RR_BF16)
+    return launch_ln_out<InBF16>((const InBF16::S *)x, rows, cols, 0, 0.0f, nullptr, mean_in,
+                                 rstd_in, gamma, beta, ybf, nullptr, nullptr, s, d);
+  return launch_ln_out<InF32>((const InF32::S *)x, rows, cols, 0, 0.0f, nullptr, mean_in, rstd_in,
+                              gamma, beta, ybf, nullptr, nullptr, s, d);
 }
 
 }  // namespace rr

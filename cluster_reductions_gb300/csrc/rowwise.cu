@@ -986,6 +986,7 @@ inline int tier_code(int tier, int width, int flags) {
 }
 constexpr int kFlagStaged = 1, kFlagRing = 2, kFlagGrid = 4;
 constexpr int kChunkBit = 1 << 27;  // the chunked register form (k_*_ck)
+constexpr int kTwoPassBit = 1 << 28;  // the rewrite's two-pass form
 
 // The grid form's plan for a call: forced (w.splits), automatic with the
 // caller's workspace (falling back to the plan without one when it is too
@@ -1002,7 +1003,8 @@ inline RowPlan rowwise_pick_ws(int64_t rows, int64_t cols, bool vec, int tier, i
     return p;
   }
   RowPlan p = rowwise_pick<In>(rows, cols, vec, tier, C, d, mode, x, out, half, grid_ok);
-  if (p.grid && rowgrid_ws_bytes(rows, p.width) > w.bytes)
+  if ((p.grid && rowgrid_ws_bytes(rows, p.width) > w.bytes) ||
+      (p.twopass && rowtwopass_ws_bytes(rows) > w.bytes))
     p = rowwise_pick<In>(rows, cols, vec, tier, C, d, mode, x, out, half, false);
   return p;
 }
@@ -1219,6 +1221,18 @@ int layernorm_impl(const void *xv, int64_t rows, int64_t cols, float eps, const 
     *tier_out = tier_code(pk.tier, pk.width, kFlagGrid);
     return launch_rowgrid(kModeLayernorm, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
                           nullptr, mean, rstd, gamma, beta, y, pk.width, w.ws, w.bytes, s, d);
+  }
+  if (pk.twopass) {
+    // the statistics into mean / rstd where asked for, else the workspace
+    float *mu = mean ? mean : (float *)w.ws;
+    float *rs = rstd ? rstd : (float *)w.ws + rows;
+    int Cl = 1;
+    int st = launch_rowwise_ring(kModeStats, In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, eps,
+                                 nullptr, mu, rs, nullptr, nullptr, nullptr, 1, true, &Cl, s, d);
+    if (st != RR_OK) return st;
+    *tier_out = tier_code(RR_TIER_BLOCK, 1, 0) | kTwoPassBit;
+    return launch_ln_apply(In::EPV == 8 ? RR_BF16 : RR_F32, xv, rows, cols, mu, rs, gamma, beta, y,
+                           s, d);
   }
   if (pk.ring && (uintptr_t)y % 16 == 0) {
     int Cl = pk.width;
@@ -1446,6 +1460,16 @@ RowPlan plan_rowwise(int64_t rows, int64_t cols, int in_dtype, bool vec, int mod
   if (chunk_ok) {
     RowPlan p{RR_TIER_BLOCK, 1, false};
     p.chunk = true;
+    return p;
+  }
+  // the rewrite of many long rows, with a workspace: the statistics through
+  // the ring (a CTA per row), then a rewrite pass that reads x again with
+  // gamma / beta held over a group of rows (rowgrid.cu), rather than staging
+  // the rows, whose rewrite reloads gamma / beta (8 bytes an element) for
+  // every row
+  if (rewrite && grid_ok && ring_ok && rows >= sm_count && cols * elt >= kRowTwoPassMinBytes) {
+    RowPlan p{RR_TIER_BLOCK, 1, false};
+    p.twopass = true;
     return p;
   }
   if (row_vecs > staged_min) {

@@ -100,6 +100,7 @@ struct RowPlan {
   bool half = false;  // block tier, row in registers read as 8-byte vectors
   bool grid = false;  // split-K over a plain grid, width CTAs per row (rowgrid.cu)
   bool chunk = false; // block tier, statistics of a row not 16-byte aligned as head + vectors + tail
+  bool twopass = false;  // rewrite of many long rows: ring statistics, then launch_ln_apply
 };
 // Forced (tier, C) or automatic choice for rows x cols of `in_dtype`; `vec`:
 // cols is a multiple of the 16-byte vector and every operand meets the
@@ -171,6 +172,19 @@ int launch_rowgrid(int mode, int in_dtype, const void *x, int64_t rows, int64_t 
                    float *y, float *mean, float *rstd, const float *gamma, const float *beta,
                    uint16_t *ybf, int G, void *ws, size_t ws_bytes, cudaStream_t s,
                    const DevInfo &d);
+// The layernorm rewrite of rows whose (mean, rstd) are already in mean_in /
+// rstd_in: x read again, y = (x - mean) rstd gamma + beta in bf16, gamma /
+// beta loaded once per column block of a group of rows.  x 16-byte aligned,
+// cols a multiple of 8, ybf / gamma / beta 16-byte aligned; RR_ERR_INVALID
+// otherwise.  One launch.
+int launch_ln_apply(int in_dtype, const void *x, int64_t rows, int64_t cols, const float *mean_in,
+                    const float *rstd_in, const float *gamma, const float *beta, uint16_t *ybf,
+                    cudaStream_t s, const DevInfo &d);
+// Rows from which rr_layernorm, given a workspace, takes the two-pass form
+// when there are at least as many rows as SMs (bytes of x a row).
+constexpr int64_t kRowTwoPassMinBytes = 256 << 10;
+// Workspace bytes of the two-pass form: a row's mean and rstd.
+inline size_t rowtwopass_ws_bytes(int64_t rows) { return (size_t)rows * 8; }
 // ---- warp tier of the row operations (rowwarp.cu)
 // A segment of L lanes per row holding NV 16-byte vectors per lane, NV a
 // power of two up to kRowWarpMaxNV.

@@ -348,13 +348,24 @@ int rr_layernorm_stats(const void *x, int64_t rows, int64_t cols, int in_dtype,
  * elements, G <= 1024).  Forced with tier RR_TIER_SPLITK, cluster_size 0
  * or 1 and splits = G.  The statistics of rr_layernorm and
  * rr_layernorm_stats in this form are bitwise equal for the same G.
+ * Two-pass form of rr_layernorm (given a workspace): for at least as many
+ * rows as SMs, rows of at least 256 KiB of x, aligned as for the grid form,
+ * the statistics are streamed through the shared-memory ring (a CTA per
+ * row, as rr_layernorm_stats takes them, so their bits are the same) into
+ * mean / rstd where asked for, else into the workspace; a second kernel
+ * reads x again and writes y, each thread holding gamma / beta for its 8
+ * columns over a group of rows.  Two HBM reads of x, against the staged
+ * form's one, but gamma / beta are no longer reloaded (8 bytes an element)
+ * for every row.
  *   splits          0 = automatic, else G (1..1024) CTAs per row.
  *   workspace       device scratch, 16-byte aligned, caller-owned, not
  *                   overlapping any operand, or NULL (no grid form); its
  *                   contents are scratch.  Calls that may run at the same
  *                   time (other streams) need workspaces of their own.
  *   workspace_bytes its size; at least rows * G * 16 for the grid form (a
- *                   16-byte state per CTA).
+ *                   16-byte state per CTA), rows * 8 for the two-pass form
+ *                   (a row's mean and rstd); the automatic plan does
+ *                   without either form when it is smaller.
  */
 typedef struct {
     int tier;
@@ -369,7 +380,8 @@ typedef struct {
  * rr_rowwise_workspace_size -- bytes of workspace the automatic plan of
  * rr_softmax_ex / rr_layernorm_stats_ex / rr_layernorm_ex wants on the
  * current device for rows x cols of in_dtype with aligned operands (0: it
- * takes no grid form).  Queries device properties only.
+ * takes neither the grid nor the two-pass form).  Queries device
+ * properties only.
  */
 int rr_rowwise_workspace_size(int64_t rows, int64_t cols, int in_dtype,
                               int row_op, size_t *bytes_out);
@@ -574,7 +586,7 @@ int rr_splitk_combine_ex(const float *O, const float *m, const float *l, int P,
 int rr_device_status(void *stream);
 
 /* Tier and width of the last reduce / softmax / layernorm call made by this
- * process: (chunked << 27) | ((width >> 8) << 19) | (grid << 18) |
+ * process: (twopass << 28) | (chunked << 27) | ((width >> 8) << 19) | (grid << 18) |
  * (ring << 17) | (staged << 16) | ((width & 0xff) << 8) | tier, width the
  * cluster size
  * (the warp tier of the row operations: lanes per row; the grid form: CTAs
@@ -583,7 +595,8 @@ int rr_device_status(void *stream);
  * copies (one combine per row; the layernorm statistics as a (count, mean,
  * M2) monoid), grid 1 when it took the grid form (rr_rowwise_opts), chunked
  * 1 when a row operation held a row that is not 16-byte aligned in
- * registers as its head, whole 16-byte vectors and tail (a CTA per row). */
+ * registers as its head, whole 16-byte vectors and tail (a CTA per row),
+ * twopass 1 when rr_layernorm took its two-pass form. */
 int rr_last_tier(void);
 
 /* Static English name of a status code. */
@@ -619,7 +632,8 @@ typedef enum { RR_ROW_SOFTMAX = 0, RR_ROW_LNSTATS = 1, RR_ROW_LAYERNORM = 2 } rr
  * form (split-K, width = G CTAs per row), which the plan considers only
  * with with_workspace != 0, 4 for the chunked register form of rows that
  * are not 16-byte aligned (the statistics and the rewrite up to 1024
- * vectors, softmax up to 4096 elements).  Touches no GPU.  RR_ERR_INVALID on negative
+ * vectors, softmax up to 4096 elements), 5 for rr_layernorm's two-pass
+ * form (with_workspace != 0 only).  Touches no GPU.  RR_ERR_INVALID on negative
  * sizes, sm_count or max_cluster < 1, a bad dtype or row_op.
  */
 int rr_plan_rowwise(int64_t rows, int64_t cols, int in_dtype, int row_op,

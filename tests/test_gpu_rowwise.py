@@ -1018,6 +1018,48 @@ def test_grid_workspace_handling(rr, oracle_mod):
     assert_rel_close(to_np(y), oracle_mod.softmax(to_np(x)), 1e-5, floor=1e-30, what="G=8")
 
 
+@pytest.mark.parametrize("dtype,shape", [(torch.bfloat16, (160, 131072)), (torch.float32, (152, 65536))],
+                         ids=["bf16", "f32"])
+def test_twopass_rewrite(rr, oracle_mod, dtype, shape):
+    # at least as many rows as SMs, rows of 256 KiB, a workspace: the
+    # statistics through the ring, then the rewrite pass; its mean / rstd
+    # are the statistics' bits whether they go to the caller or to the
+    # workspace; a constant row gives y = beta; without a workspace (or with
+    # one too small) another form
+    from _util import assert_layernorm_close
+    from cluster_reductions_gb300 import inputs
+    rows, cols = shape
+    x = _x(rows, cols, dtype, 3700, 2.0)
+    x[5] = 0.75
+    g, b = inputs.layernorm_params(cols, 3701, "cuda")
+    mean, rstd = rr.layernorm_stats(x, 1e-5)
+    assert rr.last_form() == "ring"
+    m1, r1 = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    y1 = rr.layernorm(x, g, b, 1e-5, mean=m1, rstd=r1)
+    assert rr.last_tier() == ("block", 1) and rr.last_form() == "twopass"
+    assert_bits_equal(to_np(m1), to_np(mean))
+    assert_bits_equal(to_np(r1), to_np(rstd))
+    y2 = rr.layernorm(x, g, b, 1e-5)                        # statistics in the workspace
+    assert rr.last_form() == "twopass"
+    assert_bits_equal(to_np(y2), to_np(y1))
+    m3 = torch.full((rows,), -1.0, device="cuda")
+    y3 = rr.layernorm(x, g, b, 1e-5, mean=m3)               # only the mean asked for
+    assert_bits_equal(to_np(m3), to_np(mean))
+    assert_bits_equal(to_np(y3), to_np(y1))
+    assert_bits_equal(to_np(y1)[5], to_np(b.to(torch.bfloat16)))
+    idx = np.r_[0:8, rows // 2, rows - 3:rows]
+    xs = x[torch.from_numpy(idx).cuda()]
+    y64, y16, rm, rr_ = oracle_mod.layernorm(to_np(xs), to_np(g), to_np(b), 1e-5)
+    assert_layernorm_close(to_np(y1)[idx], y64, y16, xs.to(torch.float64).cpu().numpy(), to_np(g),
+                           to_np(b), rm, rr_, to_np(m1)[idx], to_np(r1)[idx])
+    for ws in (False, torch.empty(4, dtype=torch.int32, device="cuda")):
+        m4, r4 = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+        y4 = rr.layernorm(x, g, b, 1e-5, mean=m4, rstd=r4, workspace=ws)
+        assert rr.last_form() != "twopass"
+        assert_layernorm_close(to_np(y4)[idx], y64, y16, xs.to(torch.float64).cpu().numpy(),
+                               to_np(g), to_np(b), rm, rr_, to_np(m4)[idx], to_np(r4)[idx])
+
+
 def test_grid_workspace_reused_across_shapes(rr, oracle_mod):
     # one workspace, its contents scratch, through calls of different
     # shapes, G and operations

@@ -265,6 +265,16 @@ def test_rowwise_staged_dispatch(lib, rows, cols, op, dtype, aligned, maxc, expe
     (16, 8192, "softmax", "bf16", True, ("block", 1, "direct")),
     (16, 65536, "softmax", "bf16", False, ("splitk", 16, "direct")),
     (16, 65540, "softmax", "f32", True, ("splitk", 16, "direct")),       # not whole 8-element units
+    # the rewrite of at least as many rows as SMs, rows of 256 KiB and more:
+    # ring statistics, then a rewrite pass (two passes); the statistics and
+    # softmax of the same rows, shorter rows, misaligned rows: not
+    (608, 262144, "layernorm", "bf16", True, ("block", 1, "twopass")),
+    (152, 131072, "layernorm", "bf16", True, ("block", 1, "twopass")),
+    (1000, 65536, "layernorm", "f32", True, ("block", 1, "twopass")),
+    (608, 262144, "lnstats", "bf16", True, ("block", 1, "ring")),
+    (608, 262144, "softmax", "bf16", True, ("splitk", 8, "staged")),
+    (2048, 65536, "layernorm", "bf16", True, ("splitk", 2, "staged")),    # 128 KiB rows
+    (608, 262148, "layernorm", "bf16", True, ("splitk", 8, "staged")),    # not whole units
 ])
 def test_rowwise_grid_dispatch(lib, rows, cols, op, dtype, aligned, expect):
     import torch
