@@ -80,12 +80,12 @@ NCU_TRAFFIC = {
                       "src_sha": "200d80f613a727b2", "profile": "profiles/k_splitk_sum_16x4M_f32.md"},
     "combine_p8": {"bytes": 566772736, "src": ["combine.cu", "rr_device.cuh"],
                   "src_sha": "68a1353cf0e06719", "profile": "profiles/k_combine_direct_p8_32768x128.md"},
-    "softmax_bf16": {"bytes": 559105024, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                    "src_sha": "74c39b733b88e12f", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
+    "softmax_bf16": {"bytes": 559710208, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                    "src_sha": "acc28fce14c4253a", "profile": "profiles/k_softmax_reg_8192x4096_bf16.md"},
     "block_sum_f32": {"bytes": 271227904, "src": ["reduce.cu", "rr_device.cuh"],
                      "src_sha": "200d80f613a727b2", "profile": "profiles/k_block_sum_8192x8192_f32.md"},
-    "layernorm_bf16": {"bytes": 271249920, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
-                      "src_sha": "74c39b733b88e12f", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
+    "layernorm_bf16": {"bytes": 271349760, "src": ["rowwise.cu", "rowwise.cuh", "rr_device.cuh"],
+                      "src_sha": "acc28fce14c4253a", "profile": "profiles/k_lnstats_reg_16384x8192_bf16.md"},
     "warp_sum_f32": {"bytes": 137803776, "src": ["reduce.cu", "rr_device.cuh"],
                     "src_sha": "200d80f613a727b2", "profile": "profiles/k_warp_vec_sum_1Mx32_f32.md"},
 }
