@@ -442,3 +442,25 @@ def test_two_rank_replica_timing_gloo():
         assert slowest == 20.0
         # both replicas' bytes over the slowest rank's time: 2 * 10 GB / 20 ms
         assert abs(gbs - 2 * 10 / 0.020) < 1e-9
+
+
+@pytest.mark.parametrize("epv", [8, 4], ids=["bf16", "f32"])
+def test_chunk_image_slots_conflict_free(epv):
+    # k_layernorm_ck's gamma / beta image: column j at slot j + j // EPV,
+    # 8-byte slots.  A half warp's 16 lanes read one column each, EPV apart
+    # (lane t: h + EPV (c0 + t) + e, h the row's head length), so the slots
+    # are EPV + 1 apart: 16 distinct 8-byte bank pairs (slot % 16) for every
+    # head length, element and starting vector; and every slot stays below
+    # the image's cols + cols // EPV + 1.
+    for cols in (9, 1029, 2057, 4095, 4099, 8191, 8199):
+        nslots = cols + cols // epv + 1
+        for h in range(min(epv, cols)):
+            nvec = (cols - h) // epv
+            for c0 in range(0, max(1, nvec - 15), 16):
+                for e in range(epv):
+                    js = [h + epv * (c0 + t) + e for t in range(16) if c0 + t < nvec]
+                    if not js:
+                        continue
+                    slots = [j + j // epv for j in js]
+                    assert max(slots) < nslots
+                    assert len({s % 16 for s in slots}) == len(slots), (cols, h, c0, e)
